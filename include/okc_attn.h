@@ -1,0 +1,210 @@
+/*
+ * okc_attn.h — C ABI of the GB300 (sm_103a) paged-FP8 gated attention block.
+ *
+ * The block is the part of a MuseSpark-style decoder layer that sits between
+ * the QKV projection and the output projection ("012-attention-local-splits.py",
+ * the docstring of the problem file: FusedQKNorm, set_kv_buffer/store_cache,
+ * q.to(float8_e4m3fn), flash_attn_with_kvcache, rms_norm_gate). One step of it:
+ *
+ *   okc_attn_plan              host, once per decode step, shared by all layers
+ *   okc_prepare_qkv            steps 1-3: q/k RMSNorm (+RoPE), K/V E4M3 scatter, q E4M3
+ *   okc_attn_decode            step 4: split-KV paged causal GQA attention
+ *   okc_attn_combine_normgate  split merge fused with step 5, RMSNorm x sigmoid(gate)
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers unless the name ends in _host. Every buffer is
+ *    owned by the caller; the library never frees or retains one past the call,
+ *    except that a plan remembers the workspace it was uploaded into.
+ *  - The kernel launches are asynchronous on `stream`. Entry points that launch
+ *    kernels allocate nothing (no cudaMalloc, no host allocation).
+ *  - Argument errors are detected on the host before any launch and return
+ *    OKC_ERR_INVALID / OKC_ERR_UNSUPPORTED without touching the GPU. A failed
+ *    launch returns OKC_ERR_CUDA. Nothing throws and nothing exits.
+ *  - Errors that only the device can see (a cache row, page id or position out
+ *    of range) never fault: the kernel skips the access, reads zeros where a
+ *    key was expected, and ORs an OKC_DEVERR_* bit into the plan's device error
+ *    word, which okc_attn_plan_read_errors returns.
+ *  - Layouts (the problem file's `class Inputs`):
+ *      qkv        bf16  [T, (2*Hq + 2*Hkv)*64]  per token: q | k | v | gate logits
+ *      k_cache    e4m3  [num_pages, page_size, Hkv, 64]  flat row = page*page_size + offset
+ *      v_cache    e4m3  same as k_cache
+ *      page_table int32 [B, max_pages]  physical page of each logical page (-1 unused)
+ *      out        bf16  [B, L, Hq*64]
+ *    with T = B*L tokens, token t = b*L + i at position seq_lens[b] + i.
+ */
+#ifndef OKC_ATTN_H
+#define OKC_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that C callers need no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st* okc_stream;
+
+typedef enum okc_status {
+  OKC_OK = 0,
+  OKC_ERR_INVALID = 1,      /* a bad argument: null pointer, size, shape or range */
+  OKC_ERR_UNSUPPORTED = 2,  /* valid for the problem, but not a shape this library runs */
+  OKC_ERR_CUDA = 3,         /* a CUDA runtime call or a kernel launch failed */
+  OKC_ERR_WORKSPACE = 4     /* the workspace or a scratch buffer is too small or misaligned */
+} okc_status;
+
+/* Bits of the device error word (okc_attn_plan_read_errors). */
+#define OKC_DEVERR_CACHE_LOC 0x1u  /* a cache_loc row outside the pool: that K/V row was not written */
+#define OKC_DEVERR_POSITION 0x2u   /* a position outside the RoPE table: that token's q/k were written unrotated */
+#define OKC_DEVERR_PAGE 0x4u       /* a page_table entry outside [0, num_pages) for a visible key: key read as zeros */
+#define OKC_DEVERR_LENGTHS 0x8u    /* device lengths disagree with the plan (cache_seqlens, cu_seqlens_q, seq_lens) */
+
+/*
+ * Mirrors the problem file's `class Config`. The library runs the per-GPU shape
+ * of Muse Spark under TP8: num_q_heads = 16, num_kv_heads = 2, head_dim = 64
+ * (anything else returns OKC_ERR_UNSUPPORTED), q_len in [1, 16], page_size a
+ * power of two in [1, 256].
+ */
+typedef struct okc_attn_config {
+  int32_t batch;           /* B: requests in the step */
+  int32_t q_len;           /* L: 1 for decode, 8 for a speculative verify block (causal inside it) */
+  int32_t num_q_heads;     /* Hq */
+  int32_t num_kv_heads;    /* Hkv; each serves Hq/Hkv query heads */
+  int32_t head_dim;        /* 64 */
+  int32_t page_size;       /* cache rows per page */
+  int32_t window;          /* 0 = all keys; else a token sees itself and the window-1 keys before it */
+  int32_t max_pages;       /* columns of page_table */
+  int32_t num_pages;       /* pages in each of k_cache and v_cache (bounds every device access) */
+  float rope_theta;        /* 0 = no RoPE (full-attention layers) */
+  float qk_scale_factor;   /* folded into the softmax scale */
+  float sm_scale;          /* softmax scale before the factor, 1/8 */
+  float kv_scale;          /* != 1 selects the scaled cache path (K/V divided by k/v_scale on write) */
+} okc_attn_config;
+
+/* Optional plan knobs. Pass NULL for the defaults (all zero). */
+typedef struct okc_plan_options {
+  int32_t chunk_keys;      /* keys per split work item; 0 = the built-in heuristic, else >= 16 */
+  int32_t flags;           /* OKC_PLAN_NO_PDL: launch the kernels without programmatic dependent launch */
+  int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
+  int32_t reserved;
+} okc_plan_options;
+#define OKC_PLAN_NO_PDL 0x1
+
+/* Sizes of the buffers a plan needs. All byte counts are multiples of 256. */
+typedef struct okc_attn_sizes {
+  size_t workspace_bytes;    /* device workspace the plan is uploaded into (okc_attn_plan) */
+  size_t q_fp8_bytes;        /* scratch: E4M3 q [T, Hq, 64], written by prepare, read by decode */
+  size_t o_partial_bytes;    /* scratch: f32 per-split outputs [num_work, L*Hq, 64] */
+  size_t lse_partial_bytes;  /* scratch: f32 per-split base-2 log-sum-exp [num_work, L*Hq] */
+  int32_t num_work;          /* split work items of this step */
+  int32_t num_tokens;        /* T = B*L */
+  int32_t max_chunks;        /* largest number of splits of one request */
+  int32_t reserved;
+} okc_attn_sizes;
+
+typedef struct okc_attn_plan_s* okc_attn_plan_t;
+
+/*
+ * Sizes for a step (host only, no GPU work). seq_lens_host: int32 [B], cached
+ * tokens per request before this step (the problem file's `Inputs.seq_lens`).
+ */
+okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                               const okc_plan_options* opts, okc_attn_sizes* sizes);
+
+/*
+ * okc_attn_plan — the per-step plan ("Differs from SGLang" note of the problem
+ * file: positions, cache rows, lengths and the attention schedule are built once
+ * per step for all layers). Validates cfg, splits every request's visible keys
+ * into work items (the split count grows with the parallelism B*Hkv leaves idle
+ * on the GPU and shrinks with the window, as the problem file's local-splits
+ * bound does for H200), and copies the work list into `workspace` with an
+ * asynchronous host-to-device copy on `stream`; it also zeroes the device error
+ * word. Run it outside CUDA-graph capture. The workspace must stay allocated and
+ * unmodified while kernels of this plan may run. Kernels read every per-request
+ * length from device memory; a captured graph stays valid for any later step
+ * whose lengths still fit this plan's splits (otherwise OKC_DEVERR_LENGTHS).
+ * workspace: device, >= okc_attn_sizes.workspace_bytes, 256-byte aligned.
+ * On success *plan_out owns host memory released by okc_attn_plan_destroy.
+ */
+okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                         const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
+                         okc_stream stream, okc_attn_plan_t* plan_out);
+okc_status okc_attn_plan_destroy(okc_attn_plan_t plan);
+okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
+/* Synchronizes `stream`, then reads and returns the OKC_DEVERR_* bits seen so far. */
+okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, uint32_t* flags_host);
+
+/*
+ * RoPE cos|sin table, built once per theta like the problem file's `_cos_sin`:
+ * table[pos][0:32] = cos(pos * inv_freq), table[pos][32:64] = sin(pos * inv_freq),
+ * inv_freq[i] = 1 / theta^(2i/64), all as float32 with the products and the
+ * power rounded to float32 and cos/sin the float32 rounding of the exact value.
+ * table: device float32 [num_positions, 64]; num_positions in [1, 2^21].
+ */
+okc_status okc_rope_table_init(float rope_theta, int32_t num_positions, float* table,
+                               okc_stream stream);
+
+/*
+ * Steps 1-3 (the problem file's `_prepare_qkv` kernel). For every token and
+ * every q and k head: float32 RMSNorm of the bf16 head (eps 1e-5), rounded to
+ * bf16; if rope_theta != 0, interleaved RoPE on pairs (2i, 2i+1) at the token's
+ * position, rounded to bf16. q is stored as E4M3 (no scale). k, and the raw v
+ * heads, are divided by k_scale / v_scale and rounded to bf16 when the config is
+ * scaled, then stored as E4M3 (round to nearest even, saturating to +-448) in
+ * the cache row cache_loc[t].
+ *  qkv        bf16 [T, (2Hq+2Hkv)*64], row stride (2Hq+2Hkv)*64, 16-byte aligned
+ *  positions  int64 [T]; cache_loc int64 [T] (flat cache row)
+ *  k_cache/v_cache  e4m3 pool, written in place at the cache_loc rows only
+ *  k_scale/v_scale  device float32 scalars; read only when the config is scaled
+ *  rope_table float32 [rope_positions, 64] from okc_rope_table_init, or NULL
+ *             when rope_theta == 0
+ *  q_fp8      scratch, >= okc_attn_sizes.q_fp8_bytes
+ * T == 0 returns OKC_OK without a launch.
+ */
+okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t* positions,
+                           const int64_t* cache_loc, uint8_t* k_cache, uint8_t* v_cache,
+                           const float* k_scale, const float* v_scale, const float* rope_table,
+                           int32_t rope_positions, uint8_t* q_fp8, okc_stream stream);
+
+/*
+ * Step 4 (the problem file's flash_attn_with_kvcache call: paged, causal,
+ * window_size (window-1, 0) or (-1,-1), softmax_scale = sm_scale*qk_scale_factor,
+ * k/v descale when scaled). Query i of request b sits at position
+ * cache_seqlens[b] - q_len_b + i and sees keys j with max(0, p-window+1) <= j <= p
+ * (window 0: 0 <= j <= p); query head h reads KV head h / (Hq/Hkv). Each work item
+ * of the plan covers a key range of one request for all its query rows and both
+ * KV heads, and writes a normalized f32 partial output (already times v_scale)
+ * and its base-2 log-sum-exp.
+ *  q_fp8          from okc_prepare_qkv
+ *  page_table     int32 [B, max_pages]
+ *  cache_seqlens  int32 [B] = seq_lens + L; cu_seqlens_q int32 [B+1] = 0, L, 2L, ...
+ *  seq_lens       int32 [B] (checked against cache_seqlens; may be NULL)
+ *  o_partial/lse_partial  scratch, >= the plan's sizes
+ */
+okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uint8_t* k_cache,
+                           const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* page_table, const int32_t* cache_seqlens,
+                           const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                           float* o_partial, float* lse_partial, okc_stream stream);
+
+/*
+ * Split merge fused with step 5 (the problem file's rms_norm_gate call, weight
+ * None, has_norm, eps 1e-5). Per token and q head: o = log-sum-exp merge of the
+ * request's splits, ob = bf16(o), out = bf16(ob * rsqrt(mean(ob^2) + eps) * w *
+ * sigmoid(gate)) with gate = qkv[t, (Hq+2Hkv)*64 + h*64 + c] read in place.
+ *  norm_weight  bf16 [64] or NULL (NULL = the problem file's weight None)
+ *  out          bf16 [B, L, Hq*64]
+ */
+okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partial,
+                                     const float* lse_partial, const void* qkv,
+                                     const void* norm_weight, float eps, void* out,
+                                     okc_stream stream);
+
+const char* okc_status_string(okc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OKC_ATTN_H */
