@@ -1,0 +1,409 @@
+"""Benchmark of the paged-FP8 gated attention block on GB300.
+
+One step = the whole block (okc_prepare_qkv -> okc_attn_decode ->
+okc_attn_combine_normgate) over one batch of the sliding-window decode
+workload: B=64, L=1, Hq=16, Hkv=2, d=64, seq_lens uniform in [1024, 8192],
+page_size 1, window 2048, RoPE theta 5e5, kv_scale 1 (synthetic, seeded).
+
+Timing: W warm-up steps, then exactly K steps, replayed from CUDA graphs of
+the three launches; consecutive steps rotate over independent copies of the
+inputs (cache pools, page tables, qkv) whose total exceeds 3x the L2 cache, so
+every step streams its KV rows from HBM. CUDA events on the launching stream,
+a device synchronize and a barrier on both sides, max over ranks. The decode
+kernel is then timed alone (K launches, no programmatic overlap) for the
+roofline. `e2e` repeats the step through the public API from pinned host
+buffers: per step the plan, the host-to-device copies of the step's inputs,
+the three calls and the device-to-host copy of the output.
+
+--impl reference times the CPU oracle (the only other implementation of the
+block here) on the host cores, on a bounded sample of the same workload.
+Multi-GPU: replicas only (each rank runs its own independent batch).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per step"
+WORKLOAD = "sliding_decode"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kv_bytes(cfg, seq_lens) -> int:
+    """Algorithmic KV-stream bytes of one step: each request's visible keys (the
+    union over its L queries) read once, K and V rows of Hkv x 64 E4M3 bytes."""
+    L, w = cfg["q_len"], cfg["window"]
+    n = seq_lens.astype(np.int64) + L
+    if w > 0:
+        n = np.minimum(n, w + L - 1)
+    return int(n.sum()) * cfg["num_kv_heads"] * cfg["head_dim"] * 2
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l.split(", ") for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.15]
+        if not rows:  # a short timed region: use every sample of the run
+            rows = [l.split(", ") for (_, l) in self.lines]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(mx)) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_run(cfg, inp, budget_s: float, max_steps: int | None = None):
+    """Time the oracle (as it stands) on a bounded sample: whole requests of the
+    workload, as many as fit the budget. Returns (tokens/s, sample text, tokens)."""
+    import oracle
+    B, L = cfg["batch"], cfg["q_len"]
+    # one request first to size the sample
+    def sub(bs):
+        c = dict(cfg, batch=len(bs))
+        rows = np.concatenate([np.arange(b * L, (b + 1) * L) for b in bs])
+        d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows],
+                 cache_loc=inp["cache_loc"][rows], cache_seqlens=inp["cache_seqlens"][bs],
+                 seq_lens=inp["seq_lens"][bs], page_table=inp["page_table"][bs],
+                 cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
+        return c, d
+    t0 = time.perf_counter()
+    c1, d1 = sub([0])
+    oracle.step(c1, d1)
+    per_req = max(time.perf_counter() - t0, 1e-4)
+    nreq = int(max(1, min(B, budget_s / per_req)))
+    reps = 1
+    if nreq == B:
+        reps = int(max(1, budget_s / (per_req * B)))
+        if max_steps is not None:
+            reps = max(1, min(reps, max_steps))
+    c, d = sub(list(range(nreq)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.step(c, d)
+    el = time.perf_counter() - t0
+    toks = nreq * L * reps
+    sample = f"{nreq} of {B} requests x {reps} pass(es) of {cfg['name']}, single-threaded C oracle"
+    return toks / el, sample, toks, el
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores, each of
+    the K steps one bounded sample (whole requests) of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    cfg = W.config(args.workload)
+    inp = W.generate(cfg)
+    B, L = cfg["batch"], cfg["q_len"]
+
+    def sub(bs):
+        c = dict(cfg, batch=len(bs))
+        rows = np.concatenate([np.arange(b * L, (b + 1) * L) for b in bs])
+        d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows],
+                 cache_loc=inp["cache_loc"][rows], cache_seqlens=inp["cache_seqlens"][bs],
+                 seq_lens=inp["seq_lens"][bs], page_table=inp["page_table"][bs],
+                 cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
+        return c, d
+
+    t0 = time.perf_counter()
+    oracle.step(*sub([0]))
+    per_req = max(time.perf_counter() - t0, 1e-4)
+    total_budget = 90.0  # seconds of oracle work for the whole run
+    nreq = int(max(1, min(B, total_budget / (per_req * max(1, args.steps + args.warmup)))))
+    c, d = sub(list(range(nreq)))
+    for _ in range(args.warmup):
+        oracle.step(c, d)
+    el = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.step(c, d)
+        el += time.perf_counter() - t0
+    value = nreq * L * args.steps / el
+    sample = f"{nreq} of {B} requests of {args.workload} per step, single-threaded C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps * B / nreq,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "batch": B, "q_len": L, "page_size": cfg["page_size"],
+                   "window": cfg["window"], "rope_theta": cfg["rope_theta"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", default="okc", choices=["okc", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import fp8_kv_paged_gb300 as okc
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    okc.build()
+
+    cfg = W.config(args.workload)
+    inp = W.generate(cfg, seed=cfg["seed"] + 7919 * rank)
+    T = cfg["batch"] * cfg["q_len"]
+    kvb = kv_bytes(cfg, inp["seq_lens"])
+
+    # independent input sets so that consecutive steps miss in L2
+    base = W.to_torch(inp, dev)
+    if cfg["rope_theta"] != 0.0:
+        npos = int(inp["positions"].max()) + 1
+        base["rope_table"] = torch.empty((npos, 64), dtype=torch.float32, device=dev)
+        okc.okc_rope_table_init(cfg["rope_theta"], npos, base["rope_table"])
+    set_bytes = sum(t.numel() * t.element_size() for k, t in base.items()
+                    if t is not None and k not in ("rope_table",))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, math.ceil(3 * l2 / set_bytes))
+    sets = [base] + [{k: (None if t is None else (t if k in ("rope_table", "k_scale", "v_scale", "norm_weight")
+                                                   else t.clone())) for k, t in base.items()}
+                     for _ in range(n_sets - 1)]
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(nsteps, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step.run(sets[offset % n_sets], eps=inp["eps"], stream=stream)  # warm the launch path
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                step.run(sets[(offset + i) % n_sets], eps=inp["eps"], stream=stream)
+        return g
+
+    R = n_sets * max(1, 48 // n_sets)          # steps per graph replay
+    g_main = capture(R)
+    reps, rem = divmod(args.steps, R)
+    g_rem = capture(rem) if rem else None
+    g_warm = capture(max(3, min(args.warmup, R)))
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    warm_left = args.warmup
+    while warm_left > 0:
+        g_warm.replay()
+        warm_left -= max(3, min(args.warmup, R))
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    # the decode kernel alone (the dominant kernel), K launches, no programmatic overlap
+    step_np = okc.AttnStep(cfg, inp["seq_lens"], opts={"flags": okc.PLAN_NO_PDL})
+    for s_ in sets:
+        step_np.run(s_, eps=inp["eps"], stream=stream)
+    stream.synchronize()
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=stream):
+        for i in range(R):
+            s_ = sets[i % n_sets]
+            okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
+                                s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
+                                s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
+    gd.replay()
+    stream.synchronize()
+    dreps = max(1, reps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(dreps):
+            gd.replay()
+        e1.record(stream)
+    stream.synchronize()
+    decode_us = 1000.0 * e0.elapsed_time(e1) / (dreps * R)
+    clk = clocks.stop(t_wall0, t_wall1)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(args.steps, 200))
+
+    peak, peak_kind = measured_peak_hbm()
+    achieved = kvb / (decode_us * 1e-6) / 1e9
+    value = T * world / (ms_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3/f16->f32",
+        "data": "synthetic (seeded), L2 defeated by rotating %d input sets > 3x L2" % n_sets,
+        "config": {"workload": args.workload, "batch": cfg["batch"], "q_len": cfg["q_len"],
+                   "page_size": cfg["page_size"], "window": cfg["window"],
+                   "rope_theta": cfg["rope_theta"], "kv_bytes_per_step": kvb,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
+        "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
+        "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_kind, "avg_launch_us": decode_us},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, toks, el = cpu_oracle_run(cfg, inp, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": sample, "seconds": el}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int):
+    """Per step: plan from host seq_lens, pinned host->device copies of the step's
+    inputs, the three calls, device->host copy of the output; K steps timed."""
+    names = ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table")
+    host = W.to_torch({**inp, "k_cache": inp["k_cache"][:1], "v_cache": inp["v_cache"][:1]}, "cpu")
+    pinned = {k: host[k].pin_memory() for k in names}
+    dev_in = W.to_torch(inp, dev)
+    if cfg["rope_theta"] != 0.0:
+        npos = int(inp["positions"].max()) + 1
+        dev_in["rope_table"] = torch.empty((npos, 64), dtype=torch.float32, device=dev)
+        okc.okc_rope_table_init(cfg["rope_theta"], npos, dev_in["rope_table"], stream)
+    T = cfg["batch"] * cfg["q_len"]
+    out_host = torch.empty((T, cfg["num_q_heads"] * cfg["head_dim"]), dtype=torch.bfloat16).pin_memory()
+    sizes = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"])
+    ws = torch.empty(sizes["workspace_bytes"], dtype=torch.uint8, device=dev)
+    q8 = torch.empty(sizes["q_fp8_bytes"], dtype=torch.uint8, device=dev)
+    op = torch.empty(sizes["o_partial_bytes"] // 4, dtype=torch.float32, device=dev)
+    lp = torch.empty(sizes["lse_partial_bytes"] // 4, dtype=torch.float32, device=dev)
+    out = torch.empty_like(out_host, device=dev)
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names) + \
+        sizes["workspace_bytes"] - 256
+    d2h = out_host.numel() * 2
+
+    def one():
+        plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
+        for k in names:
+            dev_in[k].copy_(pinned[k], non_blocking=True)
+        okc.okc_prepare_qkv(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
+                            dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
+                            q8, stream)
+        okc.okc_attn_decode(plan, q8, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
+                            dev_in["v_scale"], dev_in["page_table"], dev_in["cache_seqlens"],
+                            dev_in["cu_seqlens_q"], dev_in["seq_lens"], op, lp, stream)
+        okc.okc_attn_combine_normgate(plan, op, lp, dev_in["qkv"], dev_in["norm_weight"], inp["eps"], out, stream)
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+        plan.close()
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            one()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        el = time.perf_counter() - t0
+    return {"value": T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / steps, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

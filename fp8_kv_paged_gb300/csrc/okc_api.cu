@@ -1,0 +1,360 @@
+// okc_api.cu — the C ABI declared in okc_attn.h: argument validation, the
+// per-step plan (split work list, workspace layout), and the launches.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "okc_common.cuh"
+#include "okc_internal.h"
+
+using okc::ReqInfo;
+using okc::WorkItem;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+okc_status check_config(const okc_attn_config* c) {
+  if (!c) return OKC_ERR_INVALID;
+  if (c->batch < 0 || c->q_len < 1 || c->q_len > 16) return OKC_ERR_INVALID;
+  if (c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return OKC_ERR_INVALID;
+  if (c->num_q_heads % c->num_kv_heads != 0) return OKC_ERR_INVALID;
+  if (c->window < 0 || c->max_pages < 1 || c->num_pages < 1 || c->page_size < 1) return OKC_ERR_INVALID;
+  if (!(c->rope_theta >= 0.f) || !std::isfinite(c->rope_theta)) return OKC_ERR_INVALID;
+  if (!(c->sm_scale > 0.f) || !(c->qk_scale_factor > 0.f) || !(c->kv_scale > 0.f)) return OKC_ERR_INVALID;
+  if (!std::isfinite(c->sm_scale) || !std::isfinite(c->qk_scale_factor) || !std::isfinite(c->kv_scale))
+    return OKC_ERR_INVALID;
+  if (c->head_dim != okc::kHeadDim || c->num_q_heads != okc::kNumQHeads ||
+      c->num_kv_heads != okc::kNumKvHeads)
+    return OKC_ERR_UNSUPPORTED;
+  if (!is_pow2(c->page_size) || c->page_size > 256) return OKC_ERR_UNSUPPORTED;
+  // every flat cache row and page-table index must fit the kernels' int32 key math
+  if ((int64_t)c->max_pages * c->page_size > (int64_t)1 << 30) return OKC_ERR_UNSUPPORTED;
+  return OKC_OK;
+}
+
+int page_shift(int P) {
+  int s = 0;
+  while ((1 << s) < P) s++;
+  return s;
+}
+
+struct SplitResult {
+  std::vector<WorkItem> work;
+  std::vector<ReqInfo> req;
+  int max_chunks = 0;
+};
+
+// Split every request's visible keys into work items. Visible keys of request b:
+// [lo, seq+L) with lo = max(0, seq - window + 1) on window layers (the union of
+// its L queries' windows). The split count follows the parallelism the batch
+// leaves idle: aim for one item per resident CTA slot on the GPU (SMs x CTAs per
+// SM), never below 128 keys per item unless the request is shorter, so short or
+// windowed requests get few splits and long ones many (the problem file's H200
+// bound cdiv(132, B*Hkv) plays the same role with a fixed SM count).
+okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
+                       int slots, SplitResult* r) {
+  const int B = c->batch, L = c->q_len;
+  std::vector<int64_t> nvis(B);
+  int64_t total = 0;
+  for (int b = 0; b < B; b++) {
+    if (seq[b] < 0) return OKC_ERR_INVALID;
+    const int64_t hi = (int64_t)seq[b] + L;
+    if (hi > (int64_t)c->max_pages * c->page_size) return OKC_ERR_INVALID;
+    const int64_t lo = c->window > 0 ? std::max<int64_t>(0, (int64_t)seq[b] - c->window + 1) : 0;
+    nvis[b] = hi - lo;
+    total += nvis[b];
+  }
+  const int64_t min_chunk = 128;
+  int64_t ideal = slots > 0 ? (total + slots - 1) / slots : total;
+  ideal = std::max<int64_t>(ideal, min_chunk);
+  r->req.assign(B, ReqInfo{0, 0, 0, 0});
+  std::vector<std::pair<int64_t, int>> sizes;  // (chunk keys, request) per request
+  int64_t wbase = 0;
+  for (int b = 0; b < B; b++) {
+    int64_t chunk;
+    if (o && o->chunk_keys > 0) {
+      chunk = o->chunk_keys;
+    } else {
+      int64_t k = std::max<int64_t>(1, (nvis[b] + ideal / 2) / ideal);
+      chunk = (nvis[b] + k - 1) / k;
+      chunk = (chunk + 15) / 16 * 16;
+    }
+    const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
+    if (nch > (1 << 20) || wbase + nch > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
+    r->req[b] = ReqInfo{(int32_t)wbase, (int32_t)nch, (int32_t)chunk, 0};
+    r->max_chunks = std::max<int>(r->max_chunks, (int)nch);
+    wbase += nch;
+  }
+  r->work.clear();
+  r->work.reserve((size_t)wbase);
+  for (int b = 0; b < B; b++)
+    for (int k = 0; k < r->req[b].nchunks; k++) r->work.push_back(WorkItem{b, k, r->req[b].wbase + k, 0});
+  // launch the largest items first (the last chunk of a request may be short)
+  auto keys = [&](const WorkItem& w) {
+    const ReqInfo& q = r->req[w.b];
+    const int64_t start = (int64_t)w.chunk * q.chunk_keys;
+    return std::min<int64_t>(q.chunk_keys, nvis[w.b] - start);
+  };
+  std::stable_sort(r->work.begin(), r->work.end(),
+                   [&](const WorkItem& x, const WorkItem& y) { return keys(x) > keys(y); });
+  return OKC_OK;
+}
+
+okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {
+  const int64_t T = (int64_t)c->batch * c->q_len;
+  const int64_t W = (int64_t)s.work.size();
+  const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
+  std::memset(z, 0, sizeof *z);
+  z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo));
+  z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
+  z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
+  z->lse_partial_bytes = round_up(W * rows * sizeof(float));
+  z->num_work = (int32_t)W;
+  z->num_tokens = (int32_t)T;
+  z->max_chunks = s.max_chunks;
+  return OKC_OK;
+}
+
+int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count_out) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : okc::decode_ctas_per_sm(c->q_len);
+  if (per_sm <= 0) return -1;
+  if (sm_count_out) *sm_count_out = sms;
+  return sms * per_sm;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* okc_status_string(okc_status s) {
+  switch (s) {
+    case OKC_OK: return "ok";
+    case OKC_ERR_INVALID: return "invalid argument";
+    case OKC_ERR_UNSUPPORTED: return "unsupported shape";
+    case OKC_ERR_CUDA: return "CUDA error";
+    case OKC_ERR_WORKSPACE: return "workspace or scratch too small or misaligned";
+  }
+  return "unknown status";
+}
+
+okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                               const okc_plan_options* opts, okc_attn_sizes* sizes) {
+  okc_status st = check_config(cfg);
+  if (st != OKC_OK) return st;
+  if (!sizes || (cfg->batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
+  const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
+  if (slots < 0) return OKC_ERR_CUDA;
+  SplitResult s;
+  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  if (st != OKC_OK) return st;
+  return compute_sizes(cfg, s, sizes);
+}
+
+okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                         const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
+                         okc_stream stream, okc_attn_plan_t* plan_out) {
+  okc_status st = check_config(cfg);
+  if (st != OKC_OK) return st;
+  if (!plan_out || (cfg->batch > 0 && !seq_lens_host) || !workspace) return OKC_ERR_INVALID;
+  *plan_out = nullptr;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return OKC_ERR_WORKSPACE;
+  int sms = 0;
+  const int slots = slots_for(cfg, opts, &sms);
+  if (slots < 0) return OKC_ERR_CUDA;
+  SplitResult s;
+  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  if (st != OKC_OK) return st;
+  okc_attn_sizes z;
+  compute_sizes(cfg, s, &z);
+  if (workspace_bytes < z.workspace_bytes) return OKC_ERR_WORKSPACE;
+
+  okc_attn_plan_s* p = new (std::nothrow) okc_attn_plan_s();
+  if (!p) return OKC_ERR_INVALID;
+  p->cfg = *cfg;
+  if (opts) p->opts = *opts; else std::memset(&p->opts, 0, sizeof p->opts);
+  p->sizes = z;
+  p->work = std::move(s.work);
+  p->req = std::move(s.req);
+  p->workspace = workspace;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->d_err = reinterpret_cast<unsigned*>(ws);
+  p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
+  p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
+  cudaGetDevice(&p->device);
+  p->sm_count = sms;
+  p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
+  // softmax scale: the float32 value of sm_scale * qk_scale_factor, in base 2
+  const float scale = (float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
+  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+
+  cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, okc::kWsHeader, str);
+  if (e == cudaSuccess && !p->work.empty())
+    e = cudaMemcpyAsync(p->d_work, p->work.data(), p->work.size() * sizeof(WorkItem), cudaMemcpyHostToDevice, str);
+  if (e == cudaSuccess && !p->req.empty())
+    e = cudaMemcpyAsync(p->d_req, p->req.data(), p->req.size() * sizeof(ReqInfo), cudaMemcpyHostToDevice, str);
+  if (e != cudaSuccess) {
+    delete p;
+    return OKC_ERR_CUDA;
+  }
+  *plan_out = p;
+  return OKC_OK;
+}
+
+okc_status okc_attn_plan_destroy(okc_attn_plan_t plan) {
+  delete plan;
+  return OKC_OK;
+}
+
+okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes) {
+  if (!plan || !sizes) return OKC_ERR_INVALID;
+  *sizes = plan->sizes;
+  return OKC_OK;
+}
+
+okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, uint32_t* flags_host) {
+  if (!plan || !flags_host) return OKC_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, plan->d_err, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return OKC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OKC_ERR_CUDA;
+  *flags_host = v;
+  return OKC_OK;
+}
+
+okc_status okc_rope_table_init(float rope_theta, int32_t num_positions, float* table, okc_stream stream) {
+  if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !table) return OKC_ERR_INVALID;
+  if (num_positions < 1 || num_positions > okc::kRopePositionsMax) return OKC_ERR_INVALID;
+  if (!aligned16(table)) return OKC_ERR_INVALID;
+  // inv_freq = 1 / theta^(arange(0, 64, 2)/64): the power rounded once to float32
+  // (computed in double), then a float32 division.
+  float inv[okc::kHeadDim / 2];
+  for (int i = 0; i < okc::kHeadDim / 2; i++) {
+    const float e = (float)(2 * i) / (float)okc::kHeadDim;
+    const float pw = (float)std::pow((double)rope_theta, (double)e);
+    volatile float one = 1.0f;  // keep the division in float32
+    inv[i] = one / pw;
+  }
+  cudaError_t err = okc::launch_rope_table(rope_theta, inv, num_positions, table,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+}
+
+okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t* positions,
+                           const int64_t* cache_loc, uint8_t* k_cache, uint8_t* v_cache,
+                           const float* k_scale, const float* v_scale, const float* rope_table,
+                           int32_t rope_positions, uint8_t* q_fp8, okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  const okc_attn_config& c = plan->cfg;
+  const int T = plan->sizes.num_tokens;
+  if (T == 0) return OKC_OK;
+  if (!qkv || !cache_loc || !k_cache || !v_cache || !q_fp8) return OKC_ERR_INVALID;
+  if (!aligned16(qkv) || !aligned16(q_fp8)) return OKC_ERR_INVALID;
+  const bool rope = c.rope_theta != 0.f;
+  const bool scaled = c.kv_scale != 1.f;
+  if (rope && (!positions || !rope_table || !aligned16(rope_table) || rope_positions < 1 ||
+               rope_positions > okc::kRopePositionsMax))
+    return OKC_ERR_INVALID;
+  if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
+  okc::PrepareArgs a;
+  a.qkv = static_cast<const uint16_t*>(qkv);
+  a.positions = positions;
+  a.cache_loc = cache_loc;
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.rope_table = rope ? rope_table : nullptr;
+  a.q8 = q_fp8;
+  a.err = plan->d_err;
+  a.num_rows = (int64_t)c.num_pages * c.page_size;
+  a.T = T;
+  a.rope_positions = rope ? rope_positions : 0;
+  a.rope = rope;
+  a.scaled = scaled;
+  cudaError_t e = okc::launch_prepare(a, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+}
+
+okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uint8_t* k_cache,
+                           const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* page_table, const int32_t* cache_seqlens,
+                           const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                           float* o_partial, float* lse_partial, okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  const okc_attn_config& c = plan->cfg;
+  if (plan->sizes.num_work == 0) return OKC_OK;
+  if (!q_fp8 || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q ||
+      !o_partial || !lse_partial)
+    return OKC_ERR_INVALID;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_partial) || !aligned16(q_fp8))
+    return OKC_ERR_INVALID;
+  const bool scaled = c.kv_scale != 1.f;
+  if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
+  okc::DecodeArgs a;
+  a.q8 = q_fp8;
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.page_table = page_table;
+  a.cache_seqlens = cache_seqlens;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.seq_lens = seq_lens;
+  a.work = plan->d_work;
+  a.req = plan->d_req;
+  a.o_part = o_partial;
+  a.lse_part = lse_partial;
+  a.err = plan->d_err;
+  a.batch = c.batch;
+  a.L = c.q_len;
+  a.window = c.window;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
+  a.page_shift = page_shift(c.page_size);
+  a.scaled = scaled;
+  a.T = plan->sizes.num_tokens;
+  a.scale_log2 = plan->scale_log2;  // the kernel multiplies in *k_scale when scaled
+  cudaError_t e = okc::launch_decode(a, plan->sizes.num_work, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+}
+
+okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partial,
+                                     const float* lse_partial, const void* qkv,
+                                     const void* norm_weight, float eps, void* out,
+                                     okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  const int T = plan->sizes.num_tokens;
+  if (T == 0) return OKC_OK;
+  if (!o_partial || !lse_partial || !qkv || !out) return OKC_ERR_INVALID;
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(o_partial) ||
+      (norm_weight && !aligned16(norm_weight)))
+    return OKC_ERR_INVALID;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return OKC_ERR_INVALID;
+  okc::CombineArgs a;
+  a.o_part = o_partial;
+  a.lse_part = lse_partial;
+  a.qkv = static_cast<const uint16_t*>(qkv);
+  a.weight = static_cast<const uint16_t*>(norm_weight);
+  a.out = static_cast<uint16_t*>(out);
+  a.req = plan->d_req;
+  a.err = plan->d_err;
+  a.T = T;
+  a.L = plan->cfg.q_len;
+  a.eps = eps;
+  cudaError_t e = okc::launch_combine(a, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+}
+
+}  // extern "C"

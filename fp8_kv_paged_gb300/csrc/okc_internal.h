@@ -1,0 +1,104 @@
+// okc_internal.h — what the library's translation units share: the plan
+// object, the kernel argument blocks and the launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "okc_attn.h"
+
+namespace okc {
+
+// Workspace layout (device, caller-owned): [error word | work list | request table]
+constexpr size_t kWsHeader = 256;
+
+// One split work item: request b, chunk c of its visible keys, output slot.
+struct WorkItem {
+  int32_t b, chunk, slot, pad;
+};
+// Per request: first output slot, number of chunks, keys per chunk.
+struct ReqInfo {
+  int32_t wbase, nchunks, chunk_keys, pad;
+};
+
+struct PrepareArgs {
+  const uint16_t* qkv;  // bf16 bits [T, width]
+  const int64_t* positions;
+  const int64_t* cache_loc;
+  uint8_t* kc;
+  uint8_t* vc;
+  const float* k_scale;
+  const float* v_scale;
+  const float* rope_table;  // [rope_positions, 64] or null
+  uint8_t* q8;              // [T, Hq, 64]
+  unsigned* err;
+  int64_t num_rows;  // num_pages * page_size
+  int32_t T;
+  int32_t rope_positions;
+  int32_t rope;
+  int32_t scaled;
+};
+
+struct DecodeArgs {
+  const uint8_t* q8;
+  const uint8_t* kc;
+  const uint8_t* vc;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* cache_seqlens;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  const WorkItem* work;
+  const ReqInfo* req;
+  float* o_part;
+  float* lse_part;
+  unsigned* err;
+  int32_t batch, L, window, max_pages, num_pages, page_shift, scaled, T;
+  float scale_log2;  // f32(sm_scale * qk_scale_factor) * log2(e)
+};
+
+struct CombineArgs {
+  const float* o_part;
+  const float* lse_part;
+  const uint16_t* qkv;
+  const uint16_t* weight;  // bf16 [64] or null
+  uint16_t* out;
+  const ReqInfo* req;
+  unsigned* err;
+  int32_t T, L;
+  float eps;
+};
+
+}  // namespace okc
+
+struct okc_attn_plan_s {
+  okc_attn_config cfg;
+  okc_plan_options opts;
+  okc_attn_sizes sizes;
+  std::vector<okc::WorkItem> work;
+  std::vector<okc::ReqInfo> req;
+  void* workspace;
+  unsigned* d_err;
+  okc::WorkItem* d_work;
+  okc::ReqInfo* d_req;
+  int device;
+  int sm_count;
+  bool pdl;
+  float scale_log2;
+};
+
+namespace okc {
+
+// Kernel launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_prepare(const PrepareArgs& a, bool pdl, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
+cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, float* table,
+                              cudaStream_t s);
+// Resident CTAs per SM of the decode kernel chosen for q_len L (0 on error).
+int decode_ctas_per_sm(int L);
+
+}  // namespace okc

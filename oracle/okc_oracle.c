@@ -235,6 +235,8 @@ int64_t orc_attention(const orc_cfg* cfg, const uint8_t* q8, const uint8_t* k_ca
   const double ks = scaled ? (double)k_scale : 1.0, vs = scaled ? (double)v_scale : 1.0;
   const double scale = (double)(float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
   int64_t bad = 0;
+  double val[256]; /* decoded E4M3 codes, so the loops below are plain multiply-adds */
+  for (int c = 0; c < 256; c++) val[c] = orc_e4m3_value((uint8_t)c);
 
   for (int b = 0; b < cfg->batch; b++) {
     const int64_t n = cache_seqlens[b];
@@ -248,7 +250,7 @@ int64_t orc_attention(const orc_cfg* cfg, const uint8_t* q8, const uint8_t* k_ca
         if (mask && !mask[t * hq + h]) continue;
         const int g = h / group;
         double qv[ORC_D];
-        for (int c = 0; c < ORC_D; c++) qv[c] = orc_e4m3_value(q8[(t * hq + h) * ORC_D + c]);
+        for (int c = 0; c < ORC_D; c++) qv[c] = val[q8[(t * hq + h) * ORC_D + c]];
         double* s = (double*)malloc((size_t)(nk > 0 ? nk : 1) * sizeof(double));
         int64_t* rowid = (int64_t*)malloc((size_t)(nk > 0 ? nk : 1) * sizeof(int64_t));
         double mx = -INFINITY;
@@ -263,7 +265,7 @@ int64_t orc_attention(const orc_cfg* cfg, const uint8_t* q8, const uint8_t* k_ca
           double dot = 0.0;
           if (r >= 0)
             for (int c = 0; c < ORC_D; c++)
-              dot += qv[c] * (orc_e4m3_value(k_cache[(r * hkv + g) * ORC_D + c]) * ks);
+              dot += qv[c] * (val[k_cache[(r * hkv + g) * ORC_D + c]] * ks);
           s[j - lo] = dot * scale;
           if (s[j - lo] > mx) mx = s[j - lo];
         }
@@ -274,7 +276,7 @@ int64_t orc_attention(const orc_cfg* cfg, const uint8_t* q8, const uint8_t* k_ca
           denom += w;
           if (rowid[j] >= 0)
             for (int c = 0; c < ORC_D; c++)
-              acc[c] += w * (orc_e4m3_value(v_cache[(rowid[j] * hkv + g) * ORC_D + c]) * vs);
+              acc[c] += w * (val[v_cache[(rowid[j] * hkv + g) * ORC_D + c]] * vs);
         }
         for (int c = 0; c < ORC_D; c++) o[(t * hq + h) * ORC_D + c] = acc[c] / denom;
         if (lse) lse[t * hq + h] = mx + log(denom);

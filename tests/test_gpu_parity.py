@@ -1,0 +1,107 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, on seeded
+inputs of the five workloads' shapes at sizes the oracle finishes in seconds
+(several tiles, ragged tails), plus edge cases and forced split counts."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity_util import full_check, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+SMALL = {
+    "tiny_sliding_decode": {},
+    "sliding_decode": dict(batch=8, seq=("uniform", 1024, 3000)),
+    "full_decode_32k": dict(batch=4, seq=("const", 5000)),
+    "verify_block": dict(batch=4, seq=("uniform", 2100, 4000)),
+    "mixed_full_decode": dict(batch=16, seq=("loguniform", 1, 20000)),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_shapes_small(name):
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    rep = full_check(cfg, inp)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("chunk", [16, 64, 100, 448, 100000])
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block"])
+def test_forced_split_sizes(name, chunk):
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    full_check(cfg, inp, opts={"chunk_keys": chunk})
+
+
+@pytest.mark.parametrize("seq,L,window,P", [
+    ([0, 1, 2, 3], 1, 2048, 1),             # empty history (padded slots)
+    ([0, 5, 70, 129], 8, 2048, 64),         # verify block from position 0
+    ([2046, 2047, 2048, 2049], 1, 2048, 1),  # window edge
+    ([2040, 2041, 2047, 2055], 8, 2048, 1),  # window edge inside the block
+    ([4097], 1, 0, 1),                       # B = 1
+    ([300, 17, 1000], 2, 0, 4),
+    ([300, 17, 1000], 4, 256, 16),
+    ([900, 33], 16, 512, 256),
+    ([63, 64, 65, 127, 128, 129], 1, 64, 64),
+])
+def test_edge_shapes(seq, L, window, P):
+    cfg = W.config("tiny_sliding_decode", batch=len(seq), q_len=L, window=window, page_size=P,
+                   seq=("list", seq))
+    inp = W.generate(cfg)
+    full_check(cfg, inp)
+    full_check(cfg, inp, opts={"chunk_keys": 32})
+
+
+def test_norm_weight_none_and_no_rope_scaled():
+    cfg = W.config("verify_block", batch=3, seq=("uniform", 100, 900), norm_weight=False,
+                   rope_theta=0.0, kv_scale=0.75)
+    inp = W.generate(cfg)
+    assert inp["norm_weight"] is None
+    full_check(cfg, inp)
+
+
+def test_rope_table_matches_oracle_rows():
+    import fp8_kv_paged_gb300 as okc
+    n = 140000
+    tab = torch.empty((n, 64), dtype=torch.float32, device="cuda")
+    okc.okc_rope_table_init(5e5, n, tab)
+    host = tab.cpu().numpy()
+    rng = np.random.default_rng(2)
+    for pos in list(rng.integers(0, n, 200)) + [0, 1, n - 1]:
+        c, s = oracle.rope_row(5e5, int(pos))
+        assert np.array_equal(host[pos, :32], c) and np.array_equal(host[pos, 32:], s), pos
+
+
+def test_bad_inputs_flag_errors_without_faulting():
+    """Host-made bad inputs that the kernels bound-check: an out-of-pool page id,
+    an out-of-pool cache row, a position past the RoPE table, inconsistent
+    lengths. Each sets its error bit; nothing is read or written out of range."""
+    import fp8_kv_paged_gb300 as okc
+    cfg = W.config("sliding_decode", batch=4, seq=("uniform", 500, 900))
+    inp = W.generate(cfg)
+    # 1) a page id past the pool for a visible key of request 2: read as zeros
+    bad = dict(inp, page_table=inp["page_table"].copy())
+    bad["page_table"][2, 10] = cfg["num_pages"] + 5
+    full_check(cfg, bad, expect_errors=okc.DEVERR_PAGE)
+    # 2) a cache row past the pool: not written
+    bad = dict(inp, cache_loc=inp["cache_loc"].copy())
+    bad["cache_loc"][1] = cfg["num_pages"] * cfg["page_size"] + 3
+    gpu = run_gpu(cfg, bad)
+    assert gpu["errors"] & okc.DEVERR_CACHE_LOC
+    # 3) a position past the RoPE table
+    d = to_device(cfg, inp, rope_positions=int(inp["positions"].max()))  # one short
+    gpu = run_gpu(cfg, inp, dev_inp=d)
+    assert gpu["errors"] & okc.DEVERR_POSITION
+    # 4) device seq_lens inconsistent with cache_seqlens (the plan keeps the true ones)
+    d = to_device(cfg, dict(inp, seq_lens=inp["seq_lens"] + 1))
+    gpu = run_gpu(cfg, inp, dev_inp=d)
+    assert gpu["errors"] & okc.DEVERR_LENGTHS

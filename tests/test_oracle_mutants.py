@@ -42,7 +42,7 @@ MUTANTS = [
      [lambda: TA.test_matches_dense_brute_force(1, 1, 0, (5, 11), 1.0)]),
     ("softmax_scale_dropped", "s[j - lo] = dot * scale;", "s[j - lo] = dot;",
      [lambda: TA.test_matches_dense_brute_force(1, 1, 0, (5, 11), 1.0)]),
-    ("v_scale_dropped", "ORC_D + c]) * vs);", "ORC_D + c]));",
+    ("v_scale_dropped", "ORC_D + c]] * vs);", "ORC_D + c]]);",
      [lambda: TA.test_matches_dense_brute_force(8, 4, 5, (0, 13), 0.5)]),
     ("page_offset_transposed", "r = page * P + j % P;", "r = page * P + (j / P) % P;",
      [lambda: TA.test_matches_dense_brute_force(1, 4, 3, (6, 16), 0.5)]),

@@ -118,3 +118,19 @@ def generate(cfg: dict, seed: int | None = None) -> dict:
         norm_weight=weight, eps=float(cfg["eps"]),
     )
 
+
+
+def to_torch(inp: dict, device) -> dict:
+    """Copy one step's inputs to torch tensors on `device` (bf16 as bfloat16,
+    E4M3 caches as uint8). Pure copies; the RoPE table is the caller's."""
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    d = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).to(device)
+         for k in ("positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table",
+                   "k_cache", "v_cache")}
+    d["qkv"] = bf16(inp["qkv"])
+    d["k_scale"] = torch.tensor(float(inp["k_scale"]), dtype=torch.float32, device=device)
+    d["v_scale"] = torch.tensor(float(inp["v_scale"]), dtype=torch.float32, device=device)
+    d["norm_weight"] = None if inp.get("norm_weight") is None else bf16(inp["norm_weight"])
+    d["rope_table"] = None
+    return d
