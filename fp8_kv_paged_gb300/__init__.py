@@ -18,6 +18,7 @@ from . import build as _build_mod
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
+           "okc_attn_decode_combine_noalloc",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS",
            "PLAN_NO_PDL", "EXPORTED_SYMBOLS"]
 
@@ -28,7 +29,7 @@ PLAN_NO_PDL = 0x1
 EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
-    "okc_attn_combine_normgate", "okc_status_string",
+    "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
 ]
 
 
@@ -100,6 +101,8 @@ def load(path: str | None = None):
     lib.okc_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.okc_attn_combine_normgate.restype = st
     lib.okc_attn_combine_normgate.argtypes = [P, P, P, P, P, f32, P, P]
+    lib.okc_attn_decode_combine_noalloc.restype = st
+    lib.okc_attn_decode_combine_noalloc.argtypes = [ctypes.POINTER(_Config), P] + [P] * 11 + [f32, P, P]
     _lib = lib
     return lib
 
@@ -220,6 +223,19 @@ def okc_attn_combine_normgate(plan: Plan, o_partial, lse_partial, qkv, norm_weig
                                             _ptr(qkv), _ptr(norm_weight), eps, _ptr(out),
                                             _stream(stream)),
            "okc_attn_combine_normgate")
+
+
+def okc_attn_decode_combine_noalloc(cfg: dict, seq_lens_host, q_fp8, k_cache, v_cache, k_scale,
+                                    v_scale, page_table, cache_seqlens, cu_seqlens_q, seq_lens, qkv,
+                                    norm_weight, eps, out, stream=None):
+    """Decode + merge + norm-gate without any caller-provided scratch, for
+    callers that cannot allocate device memory (see the header)."""
+    seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    _check(load().okc_attn_decode_combine_noalloc(
+        ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _ptr(q_fp8), _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(cache_seqlens),
+        _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(qkv), _ptr(norm_weight), eps, _ptr(out),
+        _stream(stream)), "okc_attn_decode_combine_noalloc")
 
 
 class AttnStep:

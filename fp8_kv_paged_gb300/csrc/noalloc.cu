@@ -1,0 +1,178 @@
+// noalloc.cu — okc_attn_decode_combine_noalloc: split-KV decode plus the merge
+// and norm-gate for callers that cannot allocate device memory.
+//
+// Some callers can't call cudaMalloc: an op hosted inside a framework that owns
+// every device allocation and hands the op only its input and output buffers
+// (a plugin or custom-op interface with no workspace), or code that must not
+// trigger the device synchronisation cudaMalloc/cudaFree may cause. For them the
+// split partials, the work list and the per-request table live in one
+// file-scope device array instead of caller buffers. The array is fixed at
+// kNoAllocScratchBytes (8 MiB); every GPU that loads this library holds it until
+// the process exits.
+//
+// The decode and combine kernels are the library's own, launched with pointers
+// into the array. The array's device address is looked up once per device with
+// cudaGetSymbolAddress (host code may not use the symbol's name as an address).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "okc_common.cuh"
+#include "okc_internal.h"
+
+namespace okc {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+constexpr int kMaxWork = 4096;     // work items per call (host stack arrays below)
+constexpr int kMaxBatch = 2048;    // requests per call
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Device address of g_noalloc_scratch on the current device (set up on first use).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace okc
+
+extern "C" okc_status okc_attn_decode_combine_noalloc(
+    const okc_attn_config* cfg, const int32_t* seq_lens_host, const uint8_t* q_fp8,
+    const uint8_t* k_cache, const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+    const int32_t* page_table, const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+    const int32_t* seq_lens, const void* qkv, const void* norm_weight, float eps, void* out,
+    okc_stream stream) {
+  using namespace okc;
+  if (!cfg || !seq_lens_host) return OKC_ERR_INVALID;
+  const okc_attn_config& c = *cfg;
+  if (c.batch < 1 || c.q_len < 1 || c.q_len > 16 || c.window < 0 || c.max_pages < 1 ||
+      c.num_pages < 1 || !(c.sm_scale > 0.f) || !(c.qk_scale_factor > 0.f) || !(c.kv_scale > 0.f) ||
+      !std::isfinite(c.sm_scale) || !std::isfinite(c.qk_scale_factor) || !std::isfinite(c.kv_scale) ||
+      !(eps >= 0.f) || !std::isfinite(eps))
+    return OKC_ERR_INVALID;
+  if (c.head_dim != kHeadDim || c.num_q_heads != kNumQHeads || c.num_kv_heads != kNumKvHeads ||
+      c.page_size < 1 || c.page_size > 256 || (c.page_size & (c.page_size - 1)) ||
+      (int64_t)c.max_pages * c.page_size > (int64_t)1 << 30)
+    return OKC_ERR_UNSUPPORTED;
+  if (!q_fp8 || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q || !qkv || !out)
+    return OKC_ERR_INVALID;
+  const bool scaled = c.kv_scale != 1.f;
+  if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!al16(q_fp8) || !al16(k_cache) || !al16(v_cache) || !al16(qkv) || !al16(out) ||
+      (norm_weight && !al16(norm_weight)))
+    return OKC_ERR_INVALID;
+  if (c.batch > kMaxBatch) return OKC_ERR_WORKSPACE;
+
+  // Work list on the stack (no heap): the same split rule as okc_attn_plan.
+  const int B = c.batch, L = c.q_len;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return OKC_ERR_CUDA;
+  const int per_sm = decode_ctas_per_sm(L);
+  if (per_sm <= 0) return OKC_ERR_CUDA;
+  int64_t nvis[kMaxBatch];
+  int64_t total = 0;
+  for (int b = 0; b < B; b++) {
+    if (seq_lens_host[b] < 0) return OKC_ERR_INVALID;
+    const int64_t hi = (int64_t)seq_lens_host[b] + L;
+    if (hi > (int64_t)c.max_pages * c.page_size) return OKC_ERR_INVALID;
+    const int64_t lo = c.window > 0 ? std::max<int64_t>(0, (int64_t)seq_lens_host[b] - c.window + 1) : 0;
+    nvis[b] = hi - lo;
+    total += nvis[b];
+  }
+  const int64_t slots = (int64_t)sms * per_sm;
+  const int64_t ideal = std::max<int64_t>(128, (total + slots - 1) / slots);
+  WorkItem work[kMaxWork];  // ~100 KB of stack in all, no heap
+  ReqInfo req[kMaxBatch];
+  int64_t W = 0;
+  for (int b = 0; b < B; b++) {
+    const int64_t k = std::max<int64_t>(1, (nvis[b] + ideal / 2) / ideal);
+    const int64_t chunk = ((nvis[b] + k - 1) / k + 15) / 16 * 16;
+    const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
+    if (W + nch > kMaxWork) return OKC_ERR_WORKSPACE;
+    req[b] = ReqInfo{(int32_t)W, (int32_t)nch, (int32_t)chunk, 0};
+    for (int64_t i = 0; i < nch; i++) work[W + i] = WorkItem{b, (int32_t)i, (int32_t)(W + i), 0};
+    W += nch;
+  }
+  // Scratch layout in the static array: work list | request table | LSE | partial outputs.
+  const int64_t rows = (int64_t)L * kNumQHeads;
+  const size_t off_req = up256((size_t)W * sizeof(WorkItem));
+  const size_t off_lse = off_req + up256((size_t)B * sizeof(ReqInfo));
+  const size_t off_o = off_lse + up256((size_t)W * rows * sizeof(float));
+  const size_t need = off_o + (size_t)W * rows * kHeadDim * sizeof(float);
+  if (need > kNoAllocScratchBytes) return OKC_ERR_WORKSPACE;
+
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return OKC_ERR_CUDA;
+  uint8_t* s8 = static_cast<uint8_t*>(base);
+  cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  // pageable sources are staged before cudaMemcpyAsync returns
+  if (cudaMemcpyAsync(s8, work, (size_t)W * sizeof(WorkItem), cudaMemcpyHostToDevice, str) != cudaSuccess ||
+      cudaMemcpyAsync(s8 + off_req, req, (size_t)B * sizeof(ReqInfo), cudaMemcpyHostToDevice, str) != cudaSuccess)
+    return OKC_ERR_CUDA;
+
+  int shift = 0;
+  while ((1 << shift) < c.page_size) shift++;
+  DecodeArgs d;
+  d.q8 = q_fp8;
+  d.kc = k_cache;
+  d.vc = v_cache;
+  d.k_scale = k_scale;
+  d.v_scale = v_scale;
+  d.page_table = page_table;
+  d.cache_seqlens = cache_seqlens;
+  d.cu_seqlens_q = cu_seqlens_q;
+  d.seq_lens = seq_lens;
+  d.work = reinterpret_cast<const WorkItem*>(s8);
+  d.req = reinterpret_cast<const ReqInfo*>(s8 + off_req);
+  d.o_part = reinterpret_cast<float*>(s8 + off_o);
+  d.lse_part = reinterpret_cast<float*>(s8 + off_lse);
+  d.err = nullptr;  // out-of-range accesses are still skipped, just not reported
+  d.batch = B;
+  d.L = L;
+  d.window = c.window;
+  d.max_pages = c.max_pages;
+  d.num_pages = c.num_pages;
+  d.page_shift = shift;
+  d.scaled = scaled;
+  d.T = B * L;
+  const float scale = (float)((double)c.sm_scale * (double)c.qk_scale_factor);
+  d.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  if (launch_decode(d, (int)W, false, str) != cudaSuccess) return OKC_ERR_CUDA;
+
+  CombineArgs m;
+  m.o_part = d.o_part;
+  m.lse_part = d.lse_part;
+  m.qkv = static_cast<const uint16_t*>(qkv);
+  m.weight = static_cast<const uint16_t*>(norm_weight);
+  m.out = static_cast<uint16_t*>(out);
+  m.req = d.req;
+  m.err = nullptr;
+  m.T = B * L;
+  m.L = L;
+  m.eps = eps;
+  if (launch_combine(m, false, str) != cudaSuccess) return OKC_ERR_CUDA;
+  return OKC_OK;
+}

@@ -203,6 +203,41 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
 
 const char* okc_status_string(okc_status status);
 
+/*
+ * okc_attn_decode_combine_noalloc — okc_attn_decode followed by
+ * okc_attn_combine_normgate, for callers that cannot allocate device memory.
+ * The paper has no counterpart of this entry point.
+ *
+ * Who needs it: an op hosted inside a framework that owns every device
+ * allocation and hands the op only its input and output buffers (a plugin or
+ * custom-op interface with no workspace), or code that must not trigger the
+ * device-wide synchronisation that cudaMalloc/cudaFree can cause. This call
+ * takes no plan, workspace or scratch buffer: the work list, the per-request
+ * table and the split partials live in one static device array of 8 MiB inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments are those of okc_attn_plan (cfg, seq_lens_host), okc_attn_decode and
+ * okc_attn_combine_normgate; q_fp8 must already hold okc_prepare_qkv's output.
+ * The result equals the three-call path's `out` for the same inputs.
+ * Limits: at most 2048 requests and 4096 split work items, and the partials
+ * (work items x q_len*16 rows x 260 bytes, plus the tables) must fit in 8 MiB;
+ * larger steps return OKC_ERR_WORKSPACE before any GPU work. Device-side range
+ * errors are skipped as in okc_attn_decode but not reported (there is no plan
+ * error word).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture. All calls share the one array, which keeps the last call's contents:
+ * calls that may overlap on the GPU (different streams without ordering, or
+ * several host threads) race on it, so serialise them on one stream.
+ */
+okc_status okc_attn_decode_combine_noalloc(
+    const okc_attn_config* cfg, const int32_t* seq_lens_host, const uint8_t* q_fp8,
+    const uint8_t* k_cache, const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+    const int32_t* page_table, const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+    const int32_t* seq_lens, const void* qkv, const void* norm_weight, float eps, void* out,
+    okc_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,81 @@
+"""okc_attn_decode_combine_noalloc: decode + merge + norm-gate for callers that
+cannot allocate device memory (an op inside a framework that owns every device
+allocation and passes the op only its inputs and outputs, or code that must not
+trigger the synchronisation cudaMalloc/cudaFree can cause). Its scratch is a
+static device array inside the library, so its output must equal the
+three-call path's output for the same inputs, call after call, although every
+call reuses (and leaves behind) the same array.
+
+This file is collected last on purpose: a run that stops at the first failure
+has run every other test before this one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from parity_util import OUT_MAX_ABS, OUT_MEAN_ABS, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _three_call(okc, cfg, inp, d):
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    out = step.run(d, eps=inp["eps"]).clone()
+    torch.cuda.synchronize()
+    assert step.errors() == 0
+    return step, out
+
+
+def _noalloc(okc, cfg, inp, d, q_fp8):
+    out = torch.full((inp["qkv"].shape[0], 16 * 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    okc.okc_attn_decode_combine_noalloc(
+        cfg, inp["seq_lens"], q_fp8, d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+        d["page_table"], d["cache_seqlens"], d["cu_seqlens_q"], d["seq_lens"], d["qkv"],
+        d["norm_weight"], inp["eps"], out)
+    torch.cuda.synchronize()
+    return out
+
+
+def _compare(out, ref):
+    a = out.float().cpu().numpy()
+    b = ref.float().cpu().numpy()
+    assert np.all(np.isfinite(a))
+    err = np.abs(a - b)
+    assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS, (err.max(), err.mean())
+    return float(np.mean(a == b))
+
+
+def test_noalloc_matches_three_call_path(cuda_lib):
+    okc = cuda_lib
+    cases = [
+        W.config("sliding_decode", batch=8, seq=("uniform", 1024, 3000)),
+        W.config("verify_block", batch=4, seq=("uniform", 2100, 4000)),
+    ]
+    prepared = []
+    for cfg in cases:
+        inp = W.generate(cfg)
+        d = to_device(cfg, inp)
+        step, ref = _three_call(okc, cfg, inp, d)  # also runs okc_prepare_qkv into step.q_fp8
+        prepared.append((cfg, inp, d, step, ref))
+    # two calls in a row on different steps, then the first again: each one must
+    # match the three-call output whatever the previous call left in the array
+    for cfg, inp, d, step, ref in prepared + prepared[:1]:
+        out = _noalloc(okc, cfg, inp, d, step.q_fp8)
+        exact = _compare(out, ref)
+        assert exact == 1.0  # same kernels, same merge order: bit-identical
+
+
+def test_noalloc_rejects_steps_beyond_its_scratch(cuda_lib):
+    okc = cuda_lib
+    # 200 requests x a 16-token block: 200 work items x 256 rows of partials
+    # need ~13 MB, more than the 8 MiB static array
+    cfg = dict(W.config("verify_block"), batch=200, q_len=16, max_pages=4, num_pages=1000)
+    dummy = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    f = torch.zeros(1 << 14, dtype=torch.float32, device="cuda")
+    i32 = torch.zeros(1 << 14, dtype=torch.int32, device="cuda")
+    bf = torch.zeros(1 << 15, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(okc.OkcError) as e:
+        okc.okc_attn_decode_combine_noalloc(cfg, np.full(200, 100, np.int32), dummy, dummy, dummy, f, f,
+                                            i32, i32, i32, i32, bf, None, 1e-5, bf)
+    assert e.value.status == okc.ERR_WORKSPACE
