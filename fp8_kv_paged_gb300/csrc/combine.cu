@@ -45,20 +45,40 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   const ReqInfo rq = a.req[b];
   const int rows = a.L * kNumQHeads;
   const int row = i * kNumQHeads + h;
+  const float* lse = a.lse_part + (int64_t)rq.wbase * rows + row;
+  const float* op = a.o_part + ((int64_t)rq.wbase * rows + row) * kHeadDim + c0;
+  const int64_t ostride = (int64_t)rows * kHeadDim;
+  // splits are visited in batches of kB with every load of a batch in flight at once
+  constexpr int kB = 8;
   float M = -INFINITY;
-  for (int s = 0; s < rq.nchunks; s++) M = fmaxf(M, a.lse_part[(int64_t)(rq.wbase + s) * rows + row]);
+  for (int s0 = 0; s0 < rq.nchunks; s0 += kB) {
+    float ls[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) ls[u] = s0 + u < rq.nchunks ? lse[(int64_t)(s0 + u) * rows] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kB; u++) M = fmaxf(M, ls[u]);
+  }
   const float Mu = M == -INFINITY ? 0.f : M;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
-  for (int s = 0; s < rq.nchunks; s++) {
-    const int64_t slot = rq.wbase + s;
-    const float ls = a.lse_part[slot * rows + row];
-    const float wt = ls == -INFINITY ? 0.f : exp2f(ls - Mu);
-    const float4* src = reinterpret_cast<const float4*>(a.o_part + (slot * rows + row) * kHeadDim + c0);
-    const float4 x0 = src[0], x1 = src[1];
-    wsum += wt;
-    acc[0] += wt * x0.x; acc[1] += wt * x0.y; acc[2] += wt * x0.z; acc[3] += wt * x0.w;
-    acc[4] += wt * x1.x; acc[5] += wt * x1.y; acc[6] += wt * x1.z; acc[7] += wt * x1.w;
+  for (int s0 = 0; s0 < rq.nchunks; s0 += kB) {
+    float ls[kB];
+    float4 x0[kB], x1[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const bool live = s0 + u < rq.nchunks;
+      ls[u] = live ? lse[(int64_t)(s0 + u) * rows] : -INFINITY;
+      const float4* src = reinterpret_cast<const float4*>(op + (int64_t)(live ? s0 + u : 0) * ostride);
+      x0[u] = live ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+      x1[u] = live ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - Mu);
+      wsum += wt;
+      acc[0] += wt * x0[u].x; acc[1] += wt * x0[u].y; acc[2] += wt * x0[u].z; acc[3] += wt * x0[u].w;
+      acc[4] += wt * x1[u].x; acc[5] += wt * x1[u].y; acc[6] += wt * x1[u].z; acc[7] += wt * x1[u].w;
+    }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   float ob[8];

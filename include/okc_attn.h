@@ -59,6 +59,7 @@ typedef enum okc_status {
 #define OKC_DEVERR_POSITION 0x2u   /* a position outside the RoPE table: that token's q/k were written unrotated */
 #define OKC_DEVERR_PAGE 0x4u       /* a page_table entry outside [0, num_pages) for a visible key: key read as zeros */
 #define OKC_DEVERR_LENGTHS 0x8u    /* device lengths disagree with the plan (cache_seqlens, cu_seqlens_q, seq_lens) */
+#define OKC_DEVERR_TIMEOUT 0x10u   /* a bounded in-kernel wait gave up (a copy never completed); the step's output is void */
 
 /*
  * Mirrors the problem file's `class Config`. The library runs the per-GPU shape
