@@ -52,7 +52,22 @@ constexpr int kTileKeys = 64;
 constexpr int kRowPitch = kRowBytes + 16;          // 144: conflict-free ldmatrix rows
 constexpr int kTileSmem = kTileKeys * kRowPitch;   // one tensor's tile
 constexpr int kStageSmem = 2 * kTileSmem;          // K + V
-constexpr int kStages = 4;
+// Build-time tuning knobs (the defaults are the measured best on GB300).
+#ifndef OKC_DECODE_STAGES
+#define OKC_DECODE_STAGES 4
+#endif
+#ifndef OKC_DECODE_PRODUCERS
+#define OKC_DECODE_PRODUCERS 4  // producer warps per CTA (1, 2 or 4)
+#endif
+#ifndef OKC_DECODE_KS_L1
+#define OKC_DECODE_KS_L1 2  // q_len 1: key shares per KV head (consumer warps = 2 x this)
+#endif
+#ifndef OKC_DECODE_MINBLOCKS_L1
+#define OKC_DECODE_MINBLOCKS_L1 3  // residency hint for the q_len 1 variant
+#endif
+constexpr int kStages = OKC_DECODE_STAGES;
+constexpr int kProducers = OKC_DECODE_PRODUCERS;
+static_assert(kProducers == 1 || kProducers == 2 || kProducers == 4, "1, 2 or 4 producer warps");
 constexpr int kBarOffset = kStages * kStageSmem;
 constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8;
 constexpr uint32_t kWaitLimit = 1u << 25;          // polls of mbarrier.try_wait before giving up
@@ -63,7 +78,8 @@ struct DecodeCfg {
 };
 
 template <int KS, int NTW, int NCW>
-__global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_MINBLOCKS_L1 : 1)
+    decode_kernel(DecodeArgs a) {
   using C = DecodeCfg<KS, NTW, NCW>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -73,7 +89,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
-      mbar_init(full_bar(s), 32);  // one cp.async-tracked arrival per producer lane
+      mbar_init(full_bar(s), 32 * kProducers);  // one cp.async-tracked arrival per producer lane
       mbar_init(empty_bar(s), NCW);
     }
     fence_mbar_init();
@@ -102,12 +118,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
   const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
   __syncthreads();  // barriers initialised
 
-  if (warp == NCW) {
+  if (warp >= NCW) {
     // ================================================================ producer
-    // Lane (rr, ch) = (lane >> 3, lane & 7) copies 16-byte chunk ch of tile rows
-    // rr, rr+4, ..., rr+60 of K and of V; eight lanes cover one 128-byte row, so
-    // each warp instruction fetches four whole rows. Page ids: lane l loads the
-    // ids of tile keys l and l+32 and the row owners read them by shuffle.
+    // Producer warp pw owns keys [pw*kKeysPW, (pw+1)*kKeysPW) of every tile.
+    // Lane (rr, ch) = (lane >> 3, lane & 7) copies 16-byte chunk ch of the owned
+    // rows rr, rr+4, ...; eight lanes cover one 128-byte row, so each warp
+    // instruction fetches four whole rows. Page ids: lane l loads the ids of owned
+    // keys l, l+32, ... and the row owners read them by shuffle.
+    constexpr int kKeysPW = kTileKeys / kProducers;  // keys per producer warp per tile
+    constexpr int kIds = kKeysPW >= 32 ? kKeysPW / 32 : 1;  // page ids per lane per tile
+    const int pw = warp - NCW, kbase = pw * kKeysPW;
     const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
     const int pmask = P - 1;
     const int newk = n - ql;  // keys >= newk are written by the prepare kernel
@@ -117,7 +137,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       const int j = j0 + tile * kTileKeys + r;
       return (tile < ntiles && j < j1) ? __ldg(pt + (j >> a.page_shift)) : -1;
     };
-    auto issue = [&](int k, int ida, int idb) {
+    auto load_ids = [&](int (&dst)[kIds], int tile) {
+#pragma unroll
+      for (int q = 0; q < kIds; q++) dst[q] = (32 * q + lane < kKeysPW) ? page_of(tile, kbase + 32 * q + lane) : -1;
+    };
+    auto issue = [&](int k, const int (&id)[kIds]) {
       const int s = k % kStages;
       const uint32_t sK = sbase + s * kStageSmem, sV = sK + kTileSmem;
       const int tj = j0 + k * kTileKeys;
@@ -126,9 +150,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
         dep = true;
       }
 #pragma unroll
-      for (int i = 0; i < kTileKeys / 4; i++) {
-        const int r = rr + 4 * i;
-        const int pg = __shfl_sync(0xffffffffu, i < 8 ? ida : idb, r & 31);
+      for (int i = 0; i < kKeysPW / 4; i++) {
+        const int rl = rr + 4 * i;  // row within this warp's keys
+        const int r = kbase + rl;
+        const int pg = __shfl_sync(0xffffffffu, id[rl >> 5], rl & 31);
         const int j = tj + r;
         int64_t row = 0;
         int bytes = 0;  // 0: zero-fill, read nothing (masked key or invalid page)
@@ -147,20 +172,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       cp_async_mbar_arrive(full_bar(s));
     };
 
-    int pA[kStages], pB[kStages];
+    // Page ids live in a register ring one slot per stage: the ids of tile k are
+    // loaded when tile k - kStages is issued, so their latency hides behind a
+    // whole ring of copies.
+    int ids[kStages][kIds];
 #pragma unroll
-    for (int t = 0; t < kStages; t++) { pA[t] = page_of(t, lane); pB[t] = page_of(t, lane + 32); }
+    for (int t = 0; t < kStages; t++) load_ids(ids[t], t);
 #pragma unroll
-    for (int t = 0; t < kStages; t++)
-      if (t < ntiles) issue(t, pA[t], pB[t]);
-    int nA = page_of(kStages, lane), nB = page_of(kStages, lane + 32);
+    for (int t = 0; t < kStages; t++) {
+      if (t < ntiles) issue(t, ids[t]);
+      load_ids(ids[t], t + kStages);
+    }
     bool ok = true;
-    for (int k = kStages; k < ntiles; k++) {
-      if (!mbar_wait(empty_bar(k % kStages), ((k / kStages) & 1) ^ 1, kWaitLimit)) { ok = false; break; }
-      const int ca = nA, cb = nB;
-      nA = page_of(k + 1, lane);
-      nB = page_of(k + 1, lane + 32);
-      issue(k, ca, cb);
+    for (int k0 = kStages; k0 < ntiles && ok; k0 += kStages) {
+#pragma unroll
+      for (int u = 0; u < kStages; u++) {  // tile k = k0 + u uses ring slot u
+        const int k = k0 + u;
+        if (k >= ntiles) break;
+        if (!mbar_wait(empty_bar(u), ((k / kStages) & 1) ^ 1, kWaitLimit)) { ok = false; break; }
+        issue(k, ids[u]);
+        load_ids(ids[u], k + kStages);
+      }
     }
     if (bad_page && ch == 0) set_error(a.err, OKC_DEVERR_PAGE);
     if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
@@ -171,8 +203,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
   // ================================================================ consumers
   const int g = warp & 1;                       // KV head of this warp
   const int sub = warp >> 1;
-  const int ks = (KS == 2) ? sub : 0;           // key share (L = 1 mode)
-  const int tok0 = (KS == 2) ? 0 : sub * NTW;   // first query token of this warp
+  const int ks = (KS > 1) ? sub : 0;            // key share (L = 1 mode)
+  const int tok0 = (KS > 1) ? 0 : sub * NTW;    // first query token of this warp
   const int gq = lane >> 2, tq = lane & 3;      // mma fragment coordinates
   // logit scale in base 2; on the scaled path every key is its E4M3 value times k_scale
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
@@ -227,7 +259,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       float sc[C::kMTiles][NTW][4];
 #pragma unroll
       for (int mi = 0; mi < C::kMTiles; mi++) {
-        const int mt = (KS == 2) ? ks * 2 + mi : mi;
+        const int mt = ks * C::kMTiles + mi;
         uint32_t a0[4], a1[4];
         const uint32_t ra = ks_base + (mt * 16 + k_row) * kRowPitch;
         ldsm_x4(a0, ra + k_ch * 16);
@@ -241,7 +273,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       }
 #pragma unroll
       for (int mi = 0; mi < C::kMTiles; mi++) {
-        const int mt = (KS == 2) ? ks * 2 + mi : mi;
+        const int mt = ks * C::kMTiles + mi;
 #pragma unroll
         for (int nt = 0; nt < NTW; nt++) {
 #pragma unroll
@@ -295,7 +327,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       }
 #pragma unroll
       for (int mi = 0; mi < C::kMTiles; mi++) {
-        const int mt = (KS == 2) ? ks * 2 + mi : mi;
+        const int mt = ks * C::kMTiles + mi;
         const uint32_t rv = vs_base + (mt * 16 + v_row) * kRowPitch;
 #pragma unroll
         for (int half = 0; half < 2; half++) {  // d in [32*half, 32*half+32)
@@ -329,12 +361,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
       l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 8);
       l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], 16);
     }
-  if constexpr (KS == 2) {
-    named_bar_sync(1, NCW * 32);  // every consumer is past its last tile: reuse stage 0
+  if constexpr (KS > 1) {
+    // warps with ks > 0 park (o, m, l) in shared memory; ks == 0 merges them
+    named_bar_sync(1, NCW * 32);  // every consumer is past its last tile: reuse the ring
     float* xs = reinterpret_cast<float*>(smem);
     constexpr int kPer = 4 * NTW * 4 + NTW * 4;  // o + (m, l) per lane
-    if (ks == 1) {
-      float* dst = xs + (g * 32 + lane) * kPer;
+    if (ks > 0) {
+      float* dst = xs + (((ks - 1) * 2 + g) * 32 + lane) * kPer;
       int q = 0;
 #pragma unroll
       for (int dt = 0; dt < 4; dt++)
@@ -348,32 +381,35 @@ __global__ void __launch_bounds__((NCW + 1) * 32) decode_kernel(DecodeArgs a) {
         for (int c = 0; c < 2; c++) { dst[q++] = m[nt][c]; dst[q++] = l[nt][c]; }
     }
     named_bar_sync(1, NCW * 32);
-    if (ks == 1) return;
-    const float* src = xs + (g * 32 + lane) * kPer;
-    float o2[4][NTW][4];
-    int q = 0;
+    if (ks > 0) return;
+#pragma unroll 1
+    for (int other = 1; other < KS; other++) {
+      const float* src = xs + (((other - 1) * 2 + g) * 32 + lane) * kPer;
+      float o2[4][NTW][4];
+      int q = 0;
 #pragma unroll
-    for (int dt = 0; dt < 4; dt++)
+      for (int dt = 0; dt < 4; dt++)
+#pragma unroll
+        for (int nt = 0; nt < NTW; nt++)
+#pragma unroll
+          for (int e = 0; e < 4; e++) o2[dt][nt][e] = src[q++];
 #pragma unroll
       for (int nt = 0; nt < NTW; nt++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) o2[dt][nt][e] = src[q++];
+        for (int c = 0; c < 2; c++) {
+          const float m2 = src[q++], l2 = src[q++];
+          const float mm = fmaxf(m[nt][c], m2);
+          const float mu = mm == -INFINITY ? 0.f : mm;
+          const float f1 = fast_exp2(m[nt][c] - mu), f2 = fast_exp2(m2 - mu);
+          m[nt][c] = mm;
+          l[nt][c] = l[nt][c] * f1 + l2 * f2;
 #pragma unroll
-    for (int nt = 0; nt < NTW; nt++)
-#pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const float m2 = src[q++], l2 = src[q++];
-        const float mm = fmaxf(m[nt][c], m2);
-        const float mu = mm == -INFINITY ? 0.f : mm;
-        const float f1 = fast_exp2(m[nt][c] - mu), f2 = fast_exp2(m2 - mu);
-        m[nt][c] = mm;
-        l[nt][c] = l[nt][c] * f1 + l2 * f2;
-#pragma unroll
-        for (int dt = 0; dt < 4; dt++) {
-          o[dt][nt][c] = o[dt][nt][c] * f1 + o2[dt][nt][c] * f2;
-          o[dt][nt][c + 2] = o[dt][nt][c + 2] * f1 + o2[dt][nt][c + 2] * f2;
+          for (int dt = 0; dt < 4; dt++) {
+            o[dt][nt][c] = o[dt][nt][c] * f1 + o2[dt][nt][c] * f2;
+            o[dt][nt][c + 2] = o[dt][nt][c + 2] * f1 + o2[dt][nt][c + 2] * f2;
+          }
         }
-      }
+    }
   }
 
   const float vscale = a.scaled ? *a.v_scale : 1.0f;
@@ -411,7 +447,7 @@ cudaError_t launch_variant(const DecodeArgs& a, int num_work, bool pdl, cudaStre
   auto kern = decode_kernel<KS, NTW, NCW>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_work);
-  cfg.blockDim = dim3((NCW + 1) * 32);
+  cfg.blockDim = dim3((NCW + kProducers) * 32);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -428,7 +464,7 @@ int occupancy_variant() {
   auto kern = decode_kernel<KS, NTW, NCW>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, (NCW + 1) * 32, kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, (NCW + kProducers) * 32, kSmemBytes) != cudaSuccess)
     return 0;
   return nb;
 }
@@ -439,7 +475,7 @@ int occupancy_variant() {
 // q_len 2..16: one consumer warp per KV head per pair of tokens (n-tiles of 8 heads).
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
-  if (a.L == 1) return launch_variant<2, 1, 4>(a, num_work, pdl, s);
+  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1>(a, num_work, pdl, s);
   if (a.L <= 2) return launch_variant<1, 2, 2>(a, num_work, pdl, s);
   if (a.L <= 4) return launch_variant<1, 2, 4>(a, num_work, pdl, s);
   if (a.L <= 8) return launch_variant<1, 2, 8>(a, num_work, pdl, s);
@@ -447,7 +483,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStrea
 }
 
 int decode_ctas_per_sm(int L) {
-  if (L == 1) return occupancy_variant<2, 1, 4>();
+  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1>();
   if (L <= 2) return occupancy_variant<1, 2, 2>();
   if (L <= 4) return occupancy_variant<1, 2, 4>();
   if (L <= 8) return occupancy_variant<1, 2, 8>();

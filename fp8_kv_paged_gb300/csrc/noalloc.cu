@@ -102,14 +102,48 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     nvis[b] = hi - lo;
     total += nvis[b];
   }
+  // The key budget of okc_attn_plan: for m = 1..4 waves of the resident CTA slots,
+  // the smallest C whose items fit m waves, scored as max(largest item,
+  // ceil(items / slots) * mean item) with kItemCost keys added per item.
   const int64_t slots = (int64_t)sms * per_sm;
-  const int64_t ideal = std::max<int64_t>(128, (total + slots - 1) / slots);
+  const int64_t kItemCost = 128;
+  int64_t nmax = 1;
+  for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
+  auto items = [&](int64_t C) {
+    int64_t w = 0;
+    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, (nvis[b] + C - 1) / C);
+    return w;
+  };
+  int64_t budget = std::max<int64_t>(128, nmax);
+  double best = -1.0;
+  for (int m = 1; m <= 4; m++) {
+    int64_t lo_c = 128, hi_c = std::max<int64_t>(128, nmax);
+    while (lo_c < hi_c) {
+      const int64_t mid = (lo_c + hi_c) / 2;
+      if (items(mid) <= (int64_t)m * slots) hi_c = mid; else lo_c = mid + 1;
+    }
+    const int64_t C = lo_c, Wc = items(C);
+    int64_t biggest = 0;
+    for (int b = 0; b < B; b++) {
+      const int64_t k = std::max<int64_t>(1, (nvis[b] + C - 1) / C);
+      biggest = std::max(biggest, (nvis[b] + k - 1) / k);
+    }
+    const double mean = (double)(total + Wc * kItemCost) / (double)Wc;
+    const double waves = (double)((Wc + slots - 1) / slots);
+    const double score = std::max((double)(biggest + kItemCost), waves * mean);
+    if (best < 0.0 || score < best) {
+      best = score;
+      budget = C;
+    }
+    if (C == 128) break;
+  }
+  (void)total;
   WorkItem work[kMaxWork];  // ~100 KB of stack in all, no heap
   ReqInfo req[kMaxBatch];
   int64_t W = 0;
   for (int b = 0; b < B; b++) {
-    const int64_t k = std::max<int64_t>(1, (nvis[b] + ideal / 2) / ideal);
-    const int64_t chunk = ((nvis[b] + k - 1) / k + 15) / 16 * 16;
+    const int64_t k = std::max<int64_t>(1, (nvis[b] + budget - 1) / budget);
+    const int64_t chunk = std::max<int64_t>(16, ((nvis[b] + k - 1) / k + 15) / 16 * 16);
     const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (W + nch > kMaxWork) return OKC_ERR_WORKSPACE;
     req[b] = ReqInfo{(int32_t)W, (int32_t)nch, (int32_t)chunk, 0};

@@ -53,10 +53,11 @@ struct SplitResult {
 // Split every request's visible keys into work items. Visible keys of request b:
 // [lo, seq+L) with lo = max(0, seq - window + 1) on window layers (the union of
 // its L queries' windows). The split count follows the parallelism the batch
-// leaves idle: aim for one item per resident CTA slot on the GPU (SMs x CTAs per
-// SM), never below 128 keys per item unless the request is shorter, so short or
-// windowed requests get few splits and long ones many (the problem file's H200
-// bound cdiv(132, B*Hkv) plays the same role with a fixed SM count).
+// leaves idle: as many items as the GPU has resident CTA slots (SMs x CTAs per
+// SM, both read at run time), never below 128 keys per item unless the request
+// is shorter, so short or windowed requests get few splits and long ones many
+// (the H200 bound cdiv(132, B*Hkv) of "012-attention-local-splits.py" plays the
+// same role with a fixed SM count).
 okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
                        int slots, SplitResult* r) {
   const int B = c->batch, L = c->q_len;
@@ -70,20 +71,57 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
     nvis[b] = hi - lo;
     total += nvis[b];
   }
-  const int64_t min_chunk = 128;
-  int64_t ideal = slots > 0 ? (total + slots - 1) / slots : total;
-  ideal = std::max<int64_t>(ideal, min_chunk);
+  // Choose one key budget C for every request (a request's keys are then split
+  // into ceil(n_b / C) equal chunks). For m = 1..4 waves of the `slots` resident
+  // CTA slots, take the smallest C whose items fit m waves and score it as
+  //   max(largest item, ceil(items / slots) * mean item),
+  // each item costing kItemCost keys on top of its own (start-up, the split's
+  // partial output and its merge). The lowest score wins (ties: fewer waves).
+  // Skewed batches pick more waves of smaller items; uniform ones one wave.
+  const int64_t min_chunk = 128, kItemCost = 128;
+  int64_t nmax = 1;
+  for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
+  auto items = [&](int64_t C) {
+    int64_t w = 0;
+    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, (nvis[b] + C - 1) / C);
+    return w;
+  };
+  int64_t Cbud = std::max<int64_t>(min_chunk, nmax);
+  if (slots > 0 && B > 0) {
+    double best = -1.0;
+    for (int m = 1; m <= 4; m++) {
+      int64_t lo_c = min_chunk, hi_c = std::max<int64_t>(min_chunk, nmax);
+      while (lo_c < hi_c) {  // smallest C with items(C) <= m * slots (items(nmax) = B)
+        const int64_t mid = (lo_c + hi_c) / 2;
+        if (items(mid) <= (int64_t)m * slots) hi_c = mid; else lo_c = mid + 1;
+      }
+      const int64_t C = lo_c, W = items(C);
+      int64_t biggest = 0;
+      for (int b = 0; b < B; b++) {
+        const int64_t k = std::max<int64_t>(1, (nvis[b] + C - 1) / C);
+        biggest = std::max(biggest, (nvis[b] + k - 1) / k);
+      }
+      const double mean = (double)(total + W * kItemCost) / (double)W;
+      const double waves = (double)((W + slots - 1) / slots);
+      const double score = std::max((double)(biggest + kItemCost), waves * mean);
+      if (best < 0.0 || score < best) {
+        best = score;
+        Cbud = C;
+      }
+      if (C == min_chunk) break;  // smaller items are not allowed
+    }
+  }
+  (void)total;
   r->req.assign(B, ReqInfo{0, 0, 0, 0});
-  std::vector<std::pair<int64_t, int>> sizes;  // (chunk keys, request) per request
   int64_t wbase = 0;
   for (int b = 0; b < B; b++) {
     int64_t chunk;
     if (o && o->chunk_keys > 0) {
       chunk = o->chunk_keys;
     } else {
-      int64_t k = std::max<int64_t>(1, (nvis[b] + ideal / 2) / ideal);
+      const int64_t k = std::max<int64_t>(1, (nvis[b] + Cbud - 1) / Cbud);
       chunk = (nvis[b] + k - 1) / k;
-      chunk = (chunk + 15) / 16 * 16;
+      chunk = std::max<int64_t>(16, (chunk + 15) / 16 * 16);
     }
     const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (nch > (1 << 20) || wbase + nch > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
