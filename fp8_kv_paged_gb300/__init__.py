@@ -18,7 +18,7 @@ from . import build as _build_mod
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
-           "okc_attn_decode_combine_noalloc",
+           "okc_attn_decode_combine_noalloc", "okc_attn_step",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "EXPORTED_SYMBOLS"]
 
@@ -30,6 +30,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
+    "okc_attn_step",
 ]
 
 
@@ -101,6 +102,8 @@ def load(path: str | None = None):
     lib.okc_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.okc_attn_combine_normgate.restype = st
     lib.okc_attn_combine_normgate.argtypes = [P, P, P, P, P, f32, P, P]
+    lib.okc_attn_step.restype = st
+    lib.okc_attn_step.argtypes = [P] * 9 + [i32] + [P] * 5 + [f32, P, P, P, P]
     lib.okc_attn_decode_combine_noalloc.restype = st
     lib.okc_attn_decode_combine_noalloc.argtypes = [ctypes.POINTER(_Config), P] + [P] * 11 + [f32, P, P]
     _lib = lib
@@ -225,6 +228,19 @@ def okc_attn_combine_normgate(plan: Plan, o_partial, lse_partial, qkv, norm_weig
            "okc_attn_combine_normgate")
 
 
+def okc_attn_step(plan: Plan, qkv, positions, cache_loc, k_cache, v_cache, k_scale, v_scale,
+                  rope_table, page_table, cache_seqlens, cu_seqlens_q, seq_lens, norm_weight, eps,
+                  o_partial, lse_partial, out, stream=None):
+    """The whole block in one launch (see the header)."""
+    npos = 0 if rope_table is None else rope_table.shape[0]
+    _check(load().okc_attn_step(plan.handle, _ptr(qkv), _ptr(positions), _ptr(cache_loc), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(rope_table), npos,
+                                _ptr(page_table), _ptr(cache_seqlens), _ptr(cu_seqlens_q), _ptr(seq_lens),
+                                _ptr(norm_weight), eps, _ptr(o_partial), _ptr(lse_partial), _ptr(out),
+                                _stream(stream)),
+           "okc_attn_step")
+
+
 def okc_attn_decode_combine_noalloc(cfg: dict, seq_lens_host, q_fp8, k_cache, v_cache, k_scale,
                                     v_scale, page_table, cache_seqlens, cu_seqlens_q, seq_lens, qkv,
                                     norm_weight, eps, out, stream=None):
@@ -274,6 +290,15 @@ class AttnStep:
                         inp.get("seq_lens"), self.o_partial, self.lse_partial, stream)
         okc_attn_combine_normgate(self.plan, self.o_partial, self.lse_partial, inp["qkv"],
                                   inp.get("norm_weight"), eps, out, stream)
+        return out
+
+    def run_fused(self, inp: dict, eps: float = 1e-5, out=None, stream=None):
+        """The same step through okc_attn_step (one launch)."""
+        out = self.out if out is None else out
+        okc_attn_step(self.plan, inp["qkv"], inp["positions"], inp["cache_loc"], inp["k_cache"],
+                      inp["v_cache"], inp["k_scale"], inp["v_scale"], inp.get("rope_table"),
+                      inp["page_table"], inp["cache_seqlens"], inp["cu_seqlens_q"], inp.get("seq_lens"),
+                      inp.get("norm_weight"), eps, self.o_partial, self.lse_partial, out, stream)
         return out
 
     def errors(self, stream=None) -> int:

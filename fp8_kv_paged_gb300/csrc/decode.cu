@@ -41,6 +41,7 @@
 //        movmatrix transpose per 8x8 block.
 // Epilogue: warps that split the keys of a tile merge (m, l, O) through shared
 // memory; the item writes O/l (times v_scale) and its base-2 log-sum-exp.
+#include "normgate.cuh"
 #include "okc_common.cuh"
 #include "okc_internal.h"
 
@@ -69,15 +70,109 @@ constexpr int kStages = OKC_DECODE_STAGES;
 constexpr int kProducers = OKC_DECODE_PRODUCERS;
 static_assert(kProducers == 1 || kProducers == 2 || kProducers == 4, "1, 2 or 4 producer warps");
 constexpr int kBarOffset = kStages * kStageSmem;
-constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8;
+constexpr int kFlagOffset = kBarOffset + 2 * kStages * 8;  // one int: "this CTA merges"
+constexpr int kSmemBytes = kFlagOffset + 16;
 constexpr uint32_t kWaitLimit = 1u << 25;          // polls of mbarrier.try_wait before giving up
+
+// ---- the fused step: steps 1-3 inside the decode CTA (the arithmetic of the
+// prepare kernel: RMS inverse from the exact sum of squares in double, each
+// float32 product and sum rounded separately, bf16 roundings, E4M3 RNE satfinite).
+
+// This lane's q fragment of token t, q head `head`: dims kk*32 + jj*16 + 4*tq + e
+// (e = 0..3) land in byte e of q[kk][jj]. The four lanes tq = 0..3 that share the
+// head reduce its sum of squares; `live` false makes this lane contribute zeros.
+__device__ __forceinline__ void fused_q_frag(const DecodeArgs& a, int64_t t, int head, int tq, bool live,
+                                             uint32_t (&q)[2][2], bool& pos_err) {
+  float x[16];
+  const uint16_t* row = a.qkv + t * kQkvWidth + head * kHeadDim;
+#pragma unroll
+  for (int grp = 0; grp < 4; grp++) {  // grp = kk*2 + jj
+    const uint2 raw = live ? *reinterpret_cast<const uint2*>(row + (grp >> 1) * 32 + (grp & 1) * 16 + 4 * tq)
+                           : make_uint2(0u, 0u);
+    x[grp * 4 + 0] = bf16_bits_to_f32(raw.x & 0xFFFFu);
+    x[grp * 4 + 1] = bf16_bits_to_f32(raw.x >> 16);
+    x[grp * 4 + 2] = bf16_bits_to_f32(raw.y & 0xFFFFu);
+    x[grp * 4 + 3] = bf16_bits_to_f32(raw.y >> 16);
+  }
+  double ss = 0.0;
+#pragma unroll
+  for (int i = 0; i < 16; i++) ss = fma((double)x[i], (double)x[i], ss);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  const float inv = (float)(1.0 / sqrt(ss / (double)kHeadDim + (double)kRmsEps));
+  float y[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
+  if (a.rope && live) {
+    const int64_t pos = a.positions[t];
+    if (pos >= 0 && pos < a.rope_positions) {
+      const float* tab = a.rope_table + pos * kHeadDim;
+#pragma unroll
+      for (int grp = 0; grp < 4; grp++) {
+        const int p0 = (grp >> 1) * 16 + (grp & 1) * 8 + 2 * tq;  // pair index of dims 4*... and +1
+        const float2 c = *reinterpret_cast<const float2*>(tab + p0);
+        const float2 sn = *reinterpret_cast<const float2*>(tab + kHeadDim / 2 + p0);
+        const float cc[2] = {c.x, c.y}, sv[2] = {sn.x, sn.y};
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+          const float e = y[grp * 4 + 2 * u], o = y[grp * 4 + 2 * u + 1];
+          y[grp * 4 + 2 * u] = bf16_round(__fsub_rn(__fmul_rn(e, cc[u]), __fmul_rn(o, sv[u])));
+          y[grp * 4 + 2 * u + 1] = bf16_round(__fadd_rn(__fmul_rn(o, cc[u]), __fmul_rn(e, sv[u])));
+        }
+      }
+    } else {
+      pos_err = true;
+    }
+  }
+#pragma unroll
+  for (int grp = 0; grp < 4; grp++)
+    q[grp >> 1][grp & 1] = (uint32_t)f32x2_to_e4m3x2(y[grp * 4], y[grp * 4 + 1]) |
+                           ((uint32_t)f32x2_to_e4m3x2(y[grp * 4 + 2], y[grp * 4 + 3]) << 16);
+}
+
+// The new key row of token t for KV head g: this lane's dims 2*lane, 2*lane+1 of
+// K (RMSNorm + RoPE, / k_scale on the scaled path) and of V (raw, / v_scale),
+// as two E4M3 pairs. All 32 lanes take part (the head's reduction).
+__device__ __forceinline__ void fused_new_kv(const DecodeArgs& a, int64_t t, int g, int lane, uint16_t& k8,
+                                             uint16_t& v8, bool& pos_err) {
+  const uint16_t* row = a.qkv + t * kQkvWidth;
+  const uint32_t kr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + g) * kHeadDim + 2 * lane);
+  const uint32_t vr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + kNumKvHeads + g) * kHeadDim + 2 * lane);
+  const float x0 = bf16_bits_to_f32(kr & 0xFFFFu), x1 = bf16_bits_to_f32(kr >> 16);
+  double ss = fma((double)x1, (double)x1, (double)x0 * (double)x0);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = (float)(1.0 / sqrt(ss / (double)kHeadDim + (double)kRmsEps));
+  float y0 = bf16_round(__fmul_rn(x0, inv)), y1 = bf16_round(__fmul_rn(x1, inv));
+  if (a.rope) {
+    const int64_t pos = a.positions[t];
+    if (pos >= 0 && pos < a.rope_positions) {
+      const float c = a.rope_table[pos * kHeadDim + lane], sn = a.rope_table[pos * kHeadDim + kHeadDim / 2 + lane];
+      const float e = y0, o = y1;
+      y0 = bf16_round(__fsub_rn(__fmul_rn(e, c), __fmul_rn(o, sn)));
+      y1 = bf16_round(__fadd_rn(__fmul_rn(o, c), __fmul_rn(e, sn)));
+    } else {
+      pos_err = true;
+    }
+  }
+  float v0 = bf16_bits_to_f32(vr & 0xFFFFu), v1 = bf16_bits_to_f32(vr >> 16);
+  if (a.scaled) {
+    const float ks = *a.k_scale, vs = *a.v_scale;
+    y0 = bf16_round(__fdiv_rn(y0, ks));
+    y1 = bf16_round(__fdiv_rn(y1, ks));
+    v0 = bf16_round(__fdiv_rn(v0, vs));
+    v1 = bf16_round(__fdiv_rn(v1, vs));
+  }
+  k8 = f32x2_to_e4m3x2(y0, y1);
+  v8 = f32x2_to_e4m3x2(v0, v1);
+}
 
 template <int KS, int NTW, int NCW>
 struct DecodeCfg {
   static constexpr int kMTiles = 4 / KS;  // 16-key m-tiles per consumer warp per tile
 };
 
-template <int KS, int NTW, int NCW>
+template <int KS, int NTW, int NCW, bool FUSED>
 __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_MINBLOCKS_L1 : 1)
     decode_kernel(DecodeArgs a) {
   using C = DecodeCfg<KS, NTW, NCW>;
@@ -95,6 +190,10 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     fence_mbar_init();
   }
 
+  if constexpr (FUSED) {  // the first kernel of the step: its predecessor may write any input
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   // ---- the work item and the request's lengths (caller inputs)
   const WorkItem wk = a.work[blockIdx.x];
   const int b = wk.b;
@@ -130,9 +229,9 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     const int pw = warp - NCW, kbase = pw * kKeysPW;
     const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
     const int pmask = P - 1;
-    const int newk = n - ql;  // keys >= newk are written by the prepare kernel
+    const int newk = n - ql;  // keys >= newk are written by the prepare kernel (three-call path)
     const int rr = lane >> 3, ch = lane & 7;
-    bool dep = false, bad_page = false;
+    bool dep = FUSED, bad_page = false;  // the fused step has waited already
     auto page_of = [&](int tile, int r) {
       const int j = j0 + tile * kTileKeys + r;
       return (tile < ntiles && j < j1) ? __ldg(pt + (j >> a.page_shift)) : -1;
@@ -209,18 +308,26 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   // logit scale in base 2; on the scaled path every key is its E4M3 value times k_scale
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
 
-  pdl_wait();  // q_fp8 is the prepare kernel's output
-  pdl_launch_dependents();
-
+  bool pos_err = false;
   uint32_t qf[NTW][2][2];
+  if constexpr (FUSED) {
 #pragma unroll
-  for (int nt = 0; nt < NTW; nt++) {
-    const int tok = tok0 + nt;
-    const uint8_t* qrow = a.q8 + ((int64_t)(qb + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
+    for (int nt = 0; nt < NTW; nt++) {
+      const int tok = tok0 + nt;
+      fused_q_frag(a, (int64_t)qb + (tok < ql ? tok : 0), g * kGroup + gq, tq, tok < ql, qf[nt], pos_err);
+    }
+  } else {
+    pdl_wait();  // q_fp8 is the prepare kernel's output
+    pdl_launch_dependents();
 #pragma unroll
-    for (int kk = 0; kk < 2; kk++) {
-      qf[nt][kk][0] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + tq * 4) : 0u;
-      qf[nt][kk][1] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + 16 + tq * 4) : 0u;
+    for (int nt = 0; nt < NTW; nt++) {
+      const int tok = tok0 + nt;
+      const uint8_t* qrow = a.q8 + ((int64_t)(qb + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
+#pragma unroll
+      for (int kk = 0; kk < 2; kk++) {
+        qf[nt][kk][0] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + tq * 4) : 0u;
+        qf[nt][kk][1] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + 16 + tq * 4) : 0u;
+      }
     }
   }
 
@@ -250,6 +357,33 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     const uint32_t ks_base = sbase + s * kStageSmem;
     const uint32_t vs_base = ks_base + kTileSmem;
     const int tile_j = j0 + k * kTileKeys;
+    if constexpr (FUSED) {
+      // The step's new keys in this warp's rows of the tile: computed here from
+      // qkv, put in place of the gathered row, and written to the cache (once,
+      // by the warp that owns the row in its key share / the first token group).
+      const int wlo = tile_j + ks * C::kMTiles * 16;
+      const int whi = min(j1, wlo + C::kMTiles * 16);
+      const bool writer = (KS > 1) || sub == 0;
+      for (int j = max(wlo, pbase); j < whi; j++) {
+        const int64_t t = (int64_t)qb + (j - pbase);
+        uint16_t k8, v8;
+        fused_new_kv(a, t, g, lane, k8, v8, pos_err);
+        const int r = j - tile_j;
+        uint8_t* srow = smem + s * kStageSmem + r * kRowPitch + g * kHeadDim + 2 * lane;
+        *reinterpret_cast<uint16_t*>(srow) = k8;
+        *reinterpret_cast<uint16_t*>(srow + kTileSmem) = v8;
+        if (writer) {
+          const int64_t slot = a.cache_loc[t];
+          if (slot >= 0 && slot < a.num_rows) {
+            *reinterpret_cast<uint16_t*>(a.kc_w + slot * kRowBytes + g * kHeadDim + 2 * lane) = k8;
+            *reinterpret_cast<uint16_t*>(a.vc_w + slot * kRowBytes + g * kHeadDim + 2 * lane) = v8;
+          } else if (lane == 0) {
+            set_error(a.err, OKC_DEVERR_CACHE_LOC);
+          }
+        }
+      }
+      __syncwarp();
+    }
     if (tok_last >= tok0) {
       const int key_hi = tile_j + kTileKeys - 1;
       const int p_lo = pbase + tok0, p_hi = pbase + tok_last;
@@ -381,7 +515,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
         for (int c = 0; c < 2; c++) { dst[q++] = m[nt][c]; dst[q++] = l[nt][c]; }
     }
     named_bar_sync(1, NCW * 32);
-    if (ks > 0) return;
+    if (ks == 0) {
 #pragma unroll 1
     for (int other = 1; other < KS; other++) {
       const float* src = xs + (((other - 1) * 2 + g) * 32 + lane) * kPer;
@@ -410,6 +544,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
           }
         }
     }
+    }  // ks == 0
   }
 
   const float vscale = a.scaled ? *a.v_scale : 1.0f;
@@ -418,6 +553,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   float* lbase = a.lse_part + (int64_t)wk.slot * rows;
 #pragma unroll
   for (int nt = 0; nt < NTW; nt++) {
+    if (ks > 0) break;  // key shares were merged into ks == 0
     const int tok = tok0 + nt;
     if (tok >= ql) continue;
 #pragma unroll
@@ -439,12 +575,40 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       if (gq == 0) lbase[row] = lv > 0.f ? m[nt][c] + log2f(lv) : -INFINITY;
     }
   }
+
+  if constexpr (FUSED) {
+    // Last CTA of the request merges every split and applies the norm-gate: each
+    // CTA publishes its partials (fence), then takes a ticket; the CTA that draws
+    // the last ticket reads all partials (fence, L2 loads) and resets the counter
+    // for the next launch. Nothing waits on another CTA.
+    volatile int& s_last = *reinterpret_cast<int*>(smem + kFlagOffset);
+    if (pos_err && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
+    __threadfence();
+    named_bar_sync(1, NCW * 32);
+    if (tid == 0) s_last = atomicAdd(a.tickets + b, 1) == rq.nchunks - 1;
+    named_bar_sync(1, NCW * 32);
+    if (s_last) {
+      __threadfence();
+      const int64_t base_lse = (int64_t)rq.wbase * rows;
+      for (int rowi = tid >> 3; rowi < ql * kNumQHeads; rowi += NCW * 4) {  // 8 lanes per row
+        const int tok = rowi / kNumQHeads, h = rowi % kNumQHeads;
+        const int64_t t = (int64_t)qb + tok;
+        const int c0 = (tid & 7) * 8;
+        float gg[8], ww[8];
+        load_gate_weight(a.qkv, a.weight, (int)t, h, c0, gg, ww);
+        merge_normgate(a.lse_part + base_lse + rowi, rows,
+                       a.o_part + (base_lse + rowi) * kHeadDim + c0, (int64_t)rows * kHeadDim, rq.nchunks, gg,
+                       ww, a.eps, a.out + t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
+      }
+      if (tid == 0) a.tickets[b] = 0;
+    }
+  }
 }
 
-template <int KS, int NTW, int NCW>
+template <int KS, int NTW, int NCW, bool FUSED>
 cudaError_t launch_variant(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   // the dynamic shared-memory limit was raised when the plan was made (occupancy query)
-  auto kern = decode_kernel<KS, NTW, NCW>;
+  auto kern = decode_kernel<KS, NTW, NCW, FUSED>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_work);
   cfg.blockDim = dim3((NCW + kProducers) * 32);
@@ -458,10 +622,10 @@ cudaError_t launch_variant(const DecodeArgs& a, int num_work, bool pdl, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int KS, int NTW, int NCW>
+template <int KS, int NTW, int NCW, bool FUSED>
 int occupancy_variant() {
   int nb = 0;
-  auto kern = decode_kernel<KS, NTW, NCW>;
+  auto kern = decode_kernel<KS, NTW, NCW, FUSED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, (NCW + kProducers) * 32, kSmemBytes) != cudaSuccess)
@@ -469,25 +633,40 @@ int occupancy_variant() {
   return nb;
 }
 
+template <bool FUSED>
+cudaError_t launch_any(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  if (num_work == 0) return cudaSuccess;
+  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, FUSED>(a, num_work, pdl, s);
+  if (a.L <= 2) return launch_variant<1, 2, 2, FUSED>(a, num_work, pdl, s);
+  if (a.L <= 4) return launch_variant<1, 2, 4, FUSED>(a, num_work, pdl, s);
+  if (a.L <= 8) return launch_variant<1, 2, 8, FUSED>(a, num_work, pdl, s);
+  return launch_variant<1, 2, 16, FUSED>(a, num_work, pdl, s);
+}
+
+template <bool FUSED>
+int occupancy_any(int L) {
+  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, FUSED>();
+  if (L <= 2) return occupancy_variant<1, 2, 2, FUSED>();
+  if (L <= 4) return occupancy_variant<1, 2, 4, FUSED>();
+  if (L <= 8) return occupancy_variant<1, 2, 8, FUSED>();
+  return occupancy_variant<1, 2, 16, FUSED>();
+}
+
 }  // namespace
 
-// q_len 1: 4 consumer warps (2 KV heads x 2 key shares), one n-tile of 8 heads each.
-// q_len 2..16: one consumer warp per KV head per pair of tokens (n-tiles of 8 heads).
+// q_len 1: 2*KS consumer warps (2 KV heads x KS key shares), one n-tile of 8 heads
+// each; q_len 2..16: one consumer warp per KV head per pair of tokens.
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  if (num_work == 0) return cudaSuccess;
-  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1>(a, num_work, pdl, s);
-  if (a.L <= 2) return launch_variant<1, 2, 2>(a, num_work, pdl, s);
-  if (a.L <= 4) return launch_variant<1, 2, 4>(a, num_work, pdl, s);
-  if (a.L <= 8) return launch_variant<1, 2, 8>(a, num_work, pdl, s);
-  return launch_variant<1, 2, 16>(a, num_work, pdl, s);
+  return launch_any<false>(a, num_work, pdl, s);
+}
+
+cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  return launch_any<true>(a, num_work, pdl, s);
 }
 
 int decode_ctas_per_sm(int L) {
-  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1>();
-  if (L <= 2) return occupancy_variant<1, 2, 2>();
-  if (L <= 4) return occupancy_variant<1, 2, 4>();
-  if (L <= 8) return occupancy_variant<1, 2, 8>();
-  return occupancy_variant<1, 2, 16>();
+  const int a = occupancy_any<false>(L), b = occupancy_any<true>(L);
+  return a < b ? a : b;
 }
 
 }  // namespace okc

@@ -149,7 +149,8 @@ okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_att
   const int64_t W = (int64_t)s.work.size();
   const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
-  z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo));
+  z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo)) +
+                      round_up(c->batch * sizeof(int32_t));  // + the fused step's arrival counters
   z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
   z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
   z->lse_partial_bytes = round_up(W * rows * sizeof(float));
@@ -229,6 +230,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   p->d_err = reinterpret_cast<unsigned*>(ws);
   p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
   p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
+  p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
@@ -238,6 +240,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
 
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws, 0, okc::kWsHeader, str);
+  if (e == cudaSuccess && cfg->batch > 0) e = cudaMemsetAsync(p->d_tickets, 0, cfg->batch * sizeof(int32_t), str);
   if (e == cudaSuccess && !p->work.empty())
     e = cudaMemcpyAsync(p->d_work, p->work.data(), p->work.size() * sizeof(WorkItem), cudaMemcpyHostToDevice, str);
   if (e == cudaSuccess && !p->req.empty())
@@ -392,6 +395,69 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
   a.L = plan->cfg.q_len;
   a.eps = eps;
   cudaError_t e = okc::launch_combine(a, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+}
+
+okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* positions,
+                         const int64_t* cache_loc, uint8_t* k_cache, uint8_t* v_cache, const float* k_scale,
+                         const float* v_scale, const float* rope_table, int32_t rope_positions,
+                         const int32_t* page_table, const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                         const int32_t* seq_lens, const void* norm_weight, float eps, float* o_partial,
+                         float* lse_partial, void* out, okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  const okc_attn_config& c = plan->cfg;
+  if (plan->sizes.num_work == 0) return OKC_OK;
+  if (!qkv || !cache_loc || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q ||
+      !o_partial || !lse_partial || !out)
+    return OKC_ERR_INVALID;
+  if (!aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_partial) ||
+      !aligned16(out) || (norm_weight && !aligned16(norm_weight)))
+    return OKC_ERR_INVALID;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return OKC_ERR_INVALID;
+  const bool rope = c.rope_theta != 0.f;
+  const bool scaled = c.kv_scale != 1.f;
+  if (rope && (!positions || !rope_table || !aligned16(rope_table) || rope_positions < 1 ||
+               rope_positions > okc::kRopePositionsMax))
+    return OKC_ERR_INVALID;
+  if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
+  okc::DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.kc = k_cache;
+  a.vc = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.page_table = page_table;
+  a.cache_seqlens = cache_seqlens;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.seq_lens = seq_lens;
+  a.work = plan->d_work;
+  a.req = plan->d_req;
+  a.o_part = o_partial;
+  a.lse_part = lse_partial;
+  a.err = plan->d_err;
+  a.batch = c.batch;
+  a.L = c.q_len;
+  a.window = c.window;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
+  a.page_shift = page_shift(c.page_size);
+  a.scaled = scaled;
+  a.T = plan->sizes.num_tokens;
+  a.scale_log2 = plan->scale_log2;
+  a.qkv = static_cast<const uint16_t*>(qkv);
+  a.positions = positions;
+  a.cache_loc = cache_loc;
+  a.kc_w = k_cache;
+  a.vc_w = v_cache;
+  a.rope_table = rope ? rope_table : nullptr;
+  a.rope_positions = rope ? rope_positions : 0;
+  a.rope = rope;
+  a.num_rows = (int64_t)c.num_pages * c.page_size;
+  a.tickets = plan->d_tickets;
+  a.weight = static_cast<const uint16_t*>(norm_weight);
+  a.out = static_cast<uint16_t*>(out);
+  a.eps = eps;
+  cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }
 

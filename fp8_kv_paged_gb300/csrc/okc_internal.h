@@ -58,6 +58,20 @@ struct DecodeArgs {
   unsigned* err;
   int32_t batch, L, window, max_pages, num_pages, page_shift, scaled, T;
   float scale_log2;  // f32(sm_scale * qk_scale_factor) * log2(e)
+  // ---- the fused step only (okc_attn_step): steps 1-3 and 5 inside the kernel
+  const uint16_t* qkv;      // bf16 bits [T, width]
+  const int64_t* positions;
+  const int64_t* cache_loc;
+  uint8_t* kc_w;            // the caches again, written at the new tokens' rows
+  uint8_t* vc_w;
+  const float* rope_table;  // [rope_positions, 64] or null
+  int32_t rope_positions;
+  int32_t rope;
+  int64_t num_rows;         // num_pages * page_size
+  int32_t* tickets;         // [B] arrival counters, zero between launches
+  const uint16_t* weight;   // norm-gate weight bf16 [64] or null
+  uint16_t* out;            // bf16 [T, Hq*64]
+  float eps;
 };
 
 struct CombineArgs {
@@ -84,6 +98,7 @@ struct okc_attn_plan_s {
   unsigned* d_err;
   okc::WorkItem* d_work;
   okc::ReqInfo* d_req;
+  int32_t* d_tickets;  // the fused step's per-request arrival counters
   int device;
   int sm_count;
   bool pdl;
@@ -95,10 +110,13 @@ namespace okc {
 // Kernel launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_prepare(const PrepareArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
+// The whole step in one launch (q from qkv, new K/V rows, attention, last-CTA merge).
+cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, float* table,
                               cudaStream_t s);
-// Resident CTAs per SM of the decode kernel chosen for q_len L (0 on error).
+// Resident CTAs per SM of the decode kernels chosen for q_len L, the lower of
+// the three-call and the fused variant (0 on error).
 int decode_ctas_per_sm(int L);
 
 }  // namespace okc

@@ -202,6 +202,27 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
                                      const void* norm_weight, float eps, void* out,
                                      okc_stream stream);
 
+/*
+ * okc_attn_step — the whole block in ONE launch: steps 1-3 (the
+ * `_prepare_qkv` arithmetic, bit-identical to okc_prepare_qkv), step 4 and the
+ * split merge with step 5 (bit-identical to okc_attn_combine_normgate). Each
+ * decode CTA derives its q heads from qkv; the CTA whose key range holds a new
+ * token's key computes that K/V row, uses it in place and writes it to the
+ * cache at cache_loc; the last CTA of each request to finish (an atomic ticket
+ * in the plan workspace, reset after use; no CTA waits on another) merges the
+ * request's splits and writes `out`. The "one fused kernel" of the survey's
+ * next steps; the three-call path stays the reference decomposition.
+ * Arguments: those of the three calls, minus q_fp8. cache_loc[t] must be the
+ * page-table row of token t's position (the kernel uses the computed row
+ * directly instead of reading it back).
+ */
+okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* positions,
+                         const int64_t* cache_loc, uint8_t* k_cache, uint8_t* v_cache, const float* k_scale,
+                         const float* v_scale, const float* rope_table, int32_t rope_positions,
+                         const int32_t* page_table, const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                         const int32_t* seq_lens, const void* norm_weight, float eps, float* o_partial,
+                         float* lse_partial, void* out, okc_stream stream);
+
 const char* okc_status_string(okc_status status);
 
 /*

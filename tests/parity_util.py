@@ -28,11 +28,13 @@ def to_device(cfg: dict, inp: dict, device="cuda", rope_positions: int | None = 
     return d
 
 
-def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None = None) -> dict:
+def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None = None,
+            fused: bool = False) -> dict:
+    """One step through the three calls (fused=False) or okc_attn_step (fused=True)."""
     import fp8_kv_paged_gb300 as okc
     d = dev_inp if dev_inp is not None else to_device(cfg, inp)
     step = okc.AttnStep(cfg, inp["seq_lens"], opts=opts)
-    out = step.run(d, eps=inp["eps"])
+    out = step.run_fused(d, eps=inp["eps"]) if fused else step.run(d, eps=inp["eps"])
     torch.cuda.synchronize()
     T = inp["qkv"].shape[0]
     return {
@@ -90,12 +92,13 @@ def check_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, rows_mask: np.ndarray 
     return {"max_abs": mx, "mean_abs": mean, "exact": float(np.mean(g == r))}
 
 
-def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, expect_errors: int = 0):
-    gpu = run_gpu(cfg, inp, opts)
+def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, expect_errors: int = 0,
+               fused: bool = False):
+    gpu = run_gpu(cfg, inp, opts, fused=fused)
     k = inp["k_cache"].copy()
     v = inp["v_cache"].copy()
     q8, _ = oracle.prepare(cfg, inp, k, v)
-    rep = {"q8": check_fp8(gpu["q8"], q8, "q8")}
+    rep = {} if fused else {"q8": check_fp8(gpu["q8"], q8, "q8")}
     rep.update(check_caches(inp, gpu, k, v))
     o, _ = oracle.attention(cfg, inp, q8, k, v, rows_mask)
     ref = oracle.normgate(cfg, o, inp["qkv"], inp.get("norm_weight"), inp["eps"], rows_mask)

@@ -1,0 +1,75 @@
+"""GPU parity of okc_attn_step, the whole block in one launch: against the
+oracle under the acceptance bounds, and bit for bit against the three-call
+path (same arithmetic, same merge order), on the workloads' shapes, edge cases
+and forced split counts; consecutive launches reuse the plan's arrival counters."""
+import numpy as np
+import pytest
+
+import workloads as W
+from parity_util import full_check, run_gpu, to_device
+from test_gpu_parity import SMALL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+def _same_as_three_call(cfg, inp, opts=None):
+    a = run_gpu(cfg, inp, opts)
+    b = run_gpu(cfg, inp, opts, fused=True)
+    assert b["errors"] == 0
+    assert np.array_equal(a["out"], b["out"])
+    assert np.array_equal(a["k_cache"], b["k_cache"]) and np.array_equal(a["v_cache"], b["v_cache"])
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_fused_workload_shapes(name):
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    rep = full_check(cfg, inp, fused=True)
+    print(name, rep)
+    _same_as_three_call(cfg, inp)
+
+
+@pytest.mark.parametrize("chunk", [16, 100, 100000])
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block"])
+def test_fused_forced_splits(name, chunk):
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    full_check(cfg, inp, opts={"chunk_keys": chunk}, fused=True)
+    _same_as_three_call(cfg, inp, {"chunk_keys": chunk})
+
+
+@pytest.mark.parametrize("seq,L,window,P", [
+    ([0, 1, 2, 3], 1, 2048, 1),
+    ([0, 5, 70, 129], 8, 2048, 64),
+    ([2046, 2047, 2048, 2049], 1, 2048, 1),
+    ([2040, 2041, 2047, 2055], 8, 2048, 1),
+    ([300, 17, 1000], 4, 256, 16),
+    ([900, 33], 16, 512, 256),
+])
+def test_fused_edge_shapes(seq, L, window, P):
+    cfg = W.config("tiny_sliding_decode", batch=len(seq), q_len=L, window=window, page_size=P,
+                   seq=("list", seq))
+    inp = W.generate(cfg)
+    full_check(cfg, inp, fused=True)
+    full_check(cfg, inp, opts={"chunk_keys": 32}, fused=True)
+
+
+def test_fused_repeated_launches_reuse_tickets():
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    cfg = W.config("sliding_decode", batch=6, seq=("uniform", 1500, 2600))
+    inp = W.generate(cfg)
+    d = to_device(cfg, inp)
+    step = okc.AttnStep(cfg, inp["seq_lens"], opts={"chunk_keys": 256})
+    outs = []
+    for _ in range(3):
+        outs.append(step.run_fused(d, eps=inp["eps"]).clone())
+    torch.cuda.synchronize()
+    assert step.errors() == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
