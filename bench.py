@@ -1,19 +1,22 @@
 """Benchmark of the paged-FP8 gated attention block on GB300.
 
-One step = the whole block (okc_prepare_qkv -> okc_attn_decode ->
-okc_attn_combine_normgate) over one batch of the sliding-window decode
+One step = the whole block over one batch of the sliding-window decode
 workload: B=64, L=1, Hq=16, Hkv=2, d=64, seq_lens uniform in [1024, 8192],
 page_size 1, window 2048, RoPE theta 5e5, kv_scale 1 (synthetic, seeded).
 
+The timed step is okc_attn_step (the whole block in one launch; --path
+three_call times okc_prepare_qkv -> okc_attn_decode -> okc_attn_combine_normgate
+instead, and the line's "compare" entry times the other path the same way).
+
 Timing: W warm-up steps, then exactly K steps, replayed from CUDA graphs of
-the three launches; consecutive steps rotate over independent copies of the
+the step's launches; consecutive steps rotate over independent copies of the
 inputs (cache pools, page tables, qkv) whose total exceeds 3x the L2 cache, so
 every step streams its KV rows from HBM. CUDA events on the launching stream,
-a device synchronize and a barrier on both sides, max over ranks. The decode
-kernel is then timed alone (K launches, no programmatic overlap) for the
-roofline. `e2e` repeats the step through the public API from pinned host
+a device synchronize and a barrier on both sides, max over ranks. The step's
+dominant kernel is then timed alone (launches without programmatic overlap)
+for the roofline. `e2e` repeats the step through the public API from pinned host
 buffers: per step the plan, the host-to-device copies of the step's inputs,
-the three calls and the device-to-host copy of the output.
+the step's calls and the device-to-host copy of the output.
 
 --impl reference times the CPU oracle (the only other implementation of the
 block here) on the host cores, on a bounded sample of the same workload.
@@ -212,6 +215,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="fused", choices=["fused", "three_call"],
+                    help="okc_attn_step (one launch) or okc_prepare_qkv + okc_attn_decode + okc_attn_combine_normgate")
+    ap.add_argument("--no-compare", action="store_true", help="skip timing the other path")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -247,22 +253,55 @@ def main():
                      for _ in range(n_sets - 1)]
     step = okc.AttnStep(cfg, inp["seq_lens"])
     stream = torch.cuda.Stream(device=dev)
+    fused = args.path == "fused"
 
-    def capture(nsteps, offset=0):
+    def run_step(st, s_):
+        if fused:
+            st.run_fused(s_, eps=inp["eps"], stream=stream)
+        else:
+            st.run(s_, eps=inp["eps"], stream=stream)
+
+    def capture(fn, nsteps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            step.run(sets[offset % n_sets], eps=inp["eps"], stream=stream)  # warm the launch path
+            fn(0)  # warm the launch path
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for i in range(nsteps):
-                step.run(sets[(offset + i) % n_sets], eps=inp["eps"], stream=stream)
+                fn(i)
         return g
 
-    R = n_sets * max(1, 48 // n_sets)          # steps per graph replay
-    g_main = capture(R)
+    R = n_sets * max(1, 48 // n_sets)  # steps per graph replay
     reps, rem = divmod(args.steps, R)
-    g_rem = capture(rem) if rem else None
-    g_warm = capture(max(3, min(args.warmup, R)))
+
+    def timed(fn, steps_total, warm):
+        """ms per step of `steps_total` steps replayed from graphs (exact count)."""
+        r_, m_ = divmod(steps_total, R)
+        g_main = capture(fn, R)
+        g_rem = capture(fn, m_) if m_ else None
+        g_warm = capture(fn, max(3, min(warm, R)))
+        left = warm
+        while left > 0:
+            g_warm.replay()
+            left -= max(3, min(warm, R))
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.time()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(r_):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        barrier()
+        w1 = time.time()
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t_ = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t_.item())
+        return ms / steps_total, w0, w1
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -272,59 +311,51 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    warm_left = args.warmup
-    while warm_left > 0:
-        g_warm.replay()
-        warm_left -= max(3, min(args.warmup, R))
-    barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(reps):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
-    barrier()
-    t_wall1 = time.time()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
-    ms_step = ms_total / args.steps
+    ms_step, t_wall0, t_wall1 = timed(lambda i: run_step(step, sets[i % n_sets]), args.steps, args.warmup)
 
-    # the decode kernel alone (the dominant kernel), K launches, no programmatic overlap
+    # the step's dominant kernel alone, K launches, no programmatic overlap: the
+    # fused step kernel, or the decode kernel of the three-call path
     step_np = okc.AttnStep(cfg, inp["seq_lens"], opts={"flags": okc.PLAN_NO_PDL})
     for s_ in sets:
         step_np.run(s_, eps=inp["eps"], stream=stream)
     stream.synchronize()
-    gd = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gd, stream=stream):
-        for i in range(R):
+    if fused:
+        def one_kernel(i):
+            s_ = sets[i % n_sets]
+            okc.okc_attn_step(step_np.plan, s_["qkv"], s_["positions"], s_["cache_loc"], s_["k_cache"],
+                              s_["v_cache"], s_["k_scale"], s_["v_scale"], s_["rope_table"], s_["page_table"],
+                              s_["cache_seqlens"], s_["cu_seqlens_q"], s_["seq_lens"], s_["norm_weight"],
+                              inp["eps"], step_np.o_partial, step_np.lse_partial, step_np.out, stream)
+        kname = "decode_kernel<fused step>"
+    else:
+        def one_kernel(i):
             s_ = sets[i % n_sets]
             okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
                                 s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
                                 s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
-    gd.replay()
-    stream.synchronize()
-    dreps = max(1, reps)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(dreps):
-            gd.replay()
-        e1.record(stream)
-    stream.synchronize()
-    decode_us = 1000.0 * e0.elapsed_time(e1) / (dreps * R)
+        kname = "decode_kernel"
+    kernel_ms, _, _ = timed(one_kernel, max(R, min(args.steps, 20 * R)), 3)
+    kernel_us = 1000.0 * kernel_ms
     clk = clocks.stop(t_wall0, t_wall1)
 
+    # the other path, for comparison (same timing method)
+    other = {}
+    if not args.no_compare:
+        other_fused = not fused
+        def run_other(i):
+            if other_fused:
+                step.run_fused(sets[i % n_sets], eps=inp["eps"], stream=stream)
+            else:
+                step.run(sets[i % n_sets], eps=inp["eps"], stream=stream)
+        oms, _, _ = timed(run_other, max(R, min(args.steps, 20 * R)), 3)
+        other = {"path": "fused" if other_fused else "three_call", "ms_per_step": oms,
+                 "value": T * world / (oms * 1e-3)}
+
     # end to end through the public API with host buffers
-    e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(args.steps, 200))
+    e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(args.steps, 200), fused=fused)
 
     peak, peak_kind = measured_peak_hbm()
-    achieved = kvb / (decode_us * 1e-6) / 1e9
+    achieved = kvb / (kernel_us * 1e-6) / 1e9
     value = T * world / (ms_step * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -334,17 +365,20 @@ def main():
         "config": {"workload": args.workload, "batch": cfg["batch"], "q_len": cfg["q_len"],
                    "page_size": cfg["page_size"], "window": cfg["window"],
                    "rope_theta": cfg["rope_theta"], "kv_bytes_per_step": kvb,
+                   "path": "okc_attn_step (one launch)" if fused else "three calls",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
         "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
         "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
-        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                     "peak_source": peak_kind, "avg_launch_us": decode_us},
+                     "peak_source": peak_kind, "avg_launch_us": kernel_us},
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 if fused else 3) * args.steps,
     }
+    if other:
+        line["compare"] = other
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, toks, el = cpu_oracle_run(cfg, inp, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -355,9 +389,10 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int):
+def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
     """Per step: plan from host seq_lens, pinned host->device copies of the step's
-    inputs, the three calls, device->host copy of the output; K steps timed."""
+    inputs, the step (okc_attn_step, or the three calls), device->host copy of the
+    output; K steps timed on the host clock."""
     names = ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table")
     host = W.to_torch({**inp, "k_cache": inp["k_cache"][:1], "v_cache": inp["v_cache"][:1]}, "cpu")
     pinned = {k: host[k].pin_memory() for k in names}
@@ -382,13 +417,20 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int):
         plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
         for k in names:
             dev_in[k].copy_(pinned[k], non_blocking=True)
-        okc.okc_prepare_qkv(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
-                            dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
-                            q8, stream)
-        okc.okc_attn_decode(plan, q8, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
-                            dev_in["v_scale"], dev_in["page_table"], dev_in["cache_seqlens"],
-                            dev_in["cu_seqlens_q"], dev_in["seq_lens"], op, lp, stream)
-        okc.okc_attn_combine_normgate(plan, op, lp, dev_in["qkv"], dev_in["norm_weight"], inp["eps"], out, stream)
+        if fused:
+            okc.okc_attn_step(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
+                              dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
+                              dev_in["page_table"], dev_in["cache_seqlens"], dev_in["cu_seqlens_q"],
+                              dev_in["seq_lens"], dev_in["norm_weight"], inp["eps"], op, lp, out, stream)
+        else:
+            okc.okc_prepare_qkv(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
+                                dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
+                                q8, stream)
+            okc.okc_attn_decode(plan, q8, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
+                                dev_in["v_scale"], dev_in["page_table"], dev_in["cache_seqlens"],
+                                dev_in["cu_seqlens_q"], dev_in["seq_lens"], op, lp, stream)
+            okc.okc_attn_combine_normgate(plan, op, lp, dev_in["qkv"], dev_in["norm_weight"], inp["eps"], out,
+                                          stream)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
         plan.close()
@@ -402,7 +444,8 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int):
             one()
         el = time.perf_counter() - t0
     return {"value": T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / steps, "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / steps, "steps": steps,
+            "api": "okc_attn_plan + okc_attn_step" if fused else "okc_attn_plan + three calls"}
 
 
 if __name__ == "__main__":

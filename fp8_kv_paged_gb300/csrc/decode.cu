@@ -75,8 +75,9 @@ constexpr int kSmemBytes = kFlagOffset + 16;
 constexpr uint32_t kWaitLimit = 1u << 25;          // polls of mbarrier.try_wait before giving up
 
 // ---- the fused step: steps 1-3 inside the decode CTA (the arithmetic of the
-// prepare kernel: RMS inverse from the exact sum of squares in double, each
-// float32 product and sum rounded separately, bf16 roundings, E4M3 RNE satfinite).
+// prepare kernel: correctly rounded RMS inverse (rms_inverse), each float32
+// product and sum of the rotation rounded separately, bf16 roundings, E4M3 RNE
+// satfinite).
 
 // This lane's q fragment of token t, q head `head`: dims kk*32 + jj*16 + 4*tq + e
 // (e = 0..3) land in byte e of q[kk][jj]. The four lanes tq = 0..3 that share the
@@ -94,12 +95,7 @@ __device__ __forceinline__ void fused_q_frag(const DecodeArgs& a, int64_t t, int
     x[grp * 4 + 2] = bf16_bits_to_f32(raw.y & 0xFFFFu);
     x[grp * 4 + 3] = bf16_bits_to_f32(raw.y >> 16);
   }
-  double ss = 0.0;
-#pragma unroll
-  for (int i = 0; i < 16; i++) ss = fma((double)x[i], (double)x[i], ss);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  const float inv = (float)(1.0 / sqrt(ss / (double)kHeadDim + (double)kRmsEps));
+  const float inv = rms_inverse<4, 16>(x, kRmsEps);
   float y[16];
 #pragma unroll
   for (int i = 0; i < 16; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
@@ -139,10 +135,8 @@ __device__ __forceinline__ void fused_new_kv(const DecodeArgs& a, int64_t t, int
   const uint32_t kr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + g) * kHeadDim + 2 * lane);
   const uint32_t vr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + kNumKvHeads + g) * kHeadDim + 2 * lane);
   const float x0 = bf16_bits_to_f32(kr & 0xFFFFu), x1 = bf16_bits_to_f32(kr >> 16);
-  double ss = fma((double)x1, (double)x1, (double)x0 * (double)x0);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = (float)(1.0 / sqrt(ss / (double)kHeadDim + (double)kRmsEps));
+  const float xs[2] = {x0, x1};
+  const float inv = rms_inverse<32, 2>(xs, kRmsEps);
   float y0 = bf16_round(__fmul_rn(x0, inv)), y1 = bf16_round(__fmul_rn(x1, inv));
   if (a.rope) {
     const int64_t pos = a.positions[t];

@@ -155,6 +155,75 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ------------------------------------------------------------ RMS inverse
+// inv = float32 rounding of 1 / sqrt(sum(x^2) / 64 + eps) for one head of 64
+// bf16 values spread over LPH lanes (N values each; the LPH lanes of a head are
+// consecutive and LPH-aligned). Float32 arithmetic, exact in the result:
+//  - squares of bf16 values are exact in float32; the sum is accumulated
+//    error-free into a float pair (hi, lo) (TwoSum), relative error <= ~2^-42;
+//  - inv = rsqrtf seed + one float-float Newton correction, rounded once;
+//  - if the correction leaves the value within 2^-40 (relative) of a float32
+//    rounding midpoint, or anything overflowed, the whole warp recomputes in
+//    double precision (sum of squares exact in double, IEEE sqrt and divide),
+//    so the result is the correctly rounded value in every case. The double
+//    path runs for about one head in 2^15.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+template <int LPH, int N>
+__device__ __forceinline__ float rms_inverse(const float (&x)[N], float eps) {
+  float h = 0.f, l = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; i++) {
+    float s, e;
+    two_sum(h, __fmul_rn(x[i], x[i]), s, e);
+    h = s;
+    l = __fadd_rn(l, e);
+  }
+#pragma unroll
+  for (int o = 1; o < LPH; o <<= 1) {
+    const float ho = __shfl_xor_sync(0xffffffffu, h, o), lo = __shfl_xor_sync(0xffffffffu, l, o);
+    float s, e;
+    two_sum(h, ho, s, e);
+    h = s;
+    l = __fadd_rn(__fadd_rn(l, lo), e);
+  }
+  // m = S/64 + eps as a float pair (the scalings by 1/64 are exact)
+  float mh, ml;
+  {
+    float s, e;
+    two_sum(__fmul_rn(h, 1.f / 64.f), eps, s, e);
+    mh = s;
+    ml = __fadd_rn(__fmul_rn(l, 1.f / 64.f), e);
+    const float t = __fadd_rn(mh, ml);  // renormalise
+    ml = __fsub_rn(ml, __fsub_rn(t, mh));
+    mh = t;
+  }
+  const float y0 = rsqrtf(mh);
+  // e = 1 - m*y0^2 with products split exactly (fma), corrections in float
+  const float a = __fmul_rn(y0, y0), b = __fmaf_rn(y0, y0, -a);
+  const float c = __fmul_rn(mh, a), d = __fmaf_rn(mh, a, -c);
+  const float e = __fsub_rn(__fsub_rn(__fsub_rn(__fsub_rn(1.f, c), d), __fmul_rn(mh, b)), __fmul_rn(ml, a));
+  // 1/sqrt(m) = y0 * (1 - e)^(-1/2) = y0 * (1 + e/2 + 3e^2/8 + ...)
+  const float corr = __fmul_rn(y0, __fmaf_rn(__fmul_rn(0.375f, e), e, __fmul_rn(0.5f, e)));
+  const float r = __fadd_rn(y0, corr);
+  const float z = __fsub_rn(corr, __fsub_rn(r, y0));  // what the rounding dropped
+  const float nb = z >= 0.f ? __int_as_float(__float_as_int(r) + 1) : __int_as_float(__float_as_int(r) - 1);
+  const float half = 0.5f * fabsf(__fsub_rn(nb, r));
+  const bool amb = !(mh > 0x1p-100f) || !isfinite(mh) || !isfinite(r) ||
+                   fabsf(__fsub_rn(fabsf(z), half)) <= __fmul_rn(r, 0x1p-40f);
+  if (!__any_sync(0xffffffffu, amb)) return r;
+  double ss = 0.0;
+#pragma unroll
+  for (int i = 0; i < N; i++) ss = fma((double)x[i], (double)x[i], ss);
+#pragma unroll
+  for (int o = 1; o < LPH; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  return (float)(1.0 / sqrt(ss / 64.0 + (double)eps));
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }

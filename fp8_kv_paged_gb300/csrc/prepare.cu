@@ -11,9 +11,9 @@
 // 8 lanes of a head cover the head's 64-byte segment of the row.
 //
 // Numerics (the reading the oracle also takes): the RMS inverse is the float32
-// rounding of 1/sqrt(sum(x^2)/64 + eps) computed in double (squares of bf16
-// values are exact in double and the 64-term sum is exact for any practical
-// exponent spread, so the result does not depend on summation order); every
+// rounding of 1/sqrt(sum(x^2)/64 + eps) (rms_inverse: float32 arithmetic with a
+// double-precision fallback near rounding boundaries, so the rounding does not
+// depend on summation order); every
 // float32 product and sum of the rotation is rounded separately (explicit
 // __fmul_rn / __fadd_rn, no contraction); the scaled path divides with
 // IEEE division (__fdiv_rn).
@@ -54,21 +54,15 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_kernel(PrepareArgs a) {
       x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
     }
   }
-  // Sum of squares over the head's 64 columns (all lanes take part so the
-  // 8-lane shuffles see full groups; the v heads ignore the result).
-  double ss = 0.0;
-#pragma unroll
-  for (int i = 0; i < 8; i++) ss = fma((double)x[i], (double)x[i], ss);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  // RMS inverse of the head (all lanes take part so the 8-lane shuffles see
+  // full groups; the v heads ignore the result)
+  const float inv = rms_inverse<8, 8>(x, kRmsEps);
 
   const int64_t slot = a.cache_loc[t];
   const bool slot_ok = slot >= 0 && slot < a.num_rows;
   if (!slot_ok && threadIdx.x == 0) set_error(a.err, OKC_DEVERR_CACHE_LOC);
 
   if (h < kNumQHeads + kNumKvHeads) {
-    const float inv = (float)(1.0 / sqrt(ss / (double)kHeadDim + (double)kRmsEps));
     float y[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
