@@ -627,23 +627,21 @@ int occupancy_variant() {
   return nb;
 }
 
-template <bool FUSED>
 cudaError_t launch_any(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
-  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, FUSED>(a, num_work, pdl, s);
-  if (a.L <= 2) return launch_variant<1, 2, 2, FUSED>(a, num_work, pdl, s);
-  if (a.L <= 4) return launch_variant<1, 2, 4, FUSED>(a, num_work, pdl, s);
-  if (a.L <= 8) return launch_variant<1, 2, 8, FUSED>(a, num_work, pdl, s);
-  return launch_variant<1, 2, 16, FUSED>(a, num_work, pdl, s);
+  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>(a, num_work, pdl, s);
+  if (a.L <= 2) return launch_variant<1, 2, 2, false>(a, num_work, pdl, s);
+  if (a.L <= 4) return launch_variant<1, 2, 4, false>(a, num_work, pdl, s);
+  if (a.L <= 8) return launch_variant<1, 2, 8, false>(a, num_work, pdl, s);
+  return launch_variant<1, 2, 16, false>(a, num_work, pdl, s);
 }
 
-template <bool FUSED>
 int occupancy_any(int L) {
-  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, FUSED>();
-  if (L <= 2) return occupancy_variant<1, 2, 2, FUSED>();
-  if (L <= 4) return occupancy_variant<1, 2, 4, FUSED>();
-  if (L <= 8) return occupancy_variant<1, 2, 8, FUSED>();
-  return occupancy_variant<1, 2, 16, FUSED>();
+  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>();
+  if (L <= 2) return occupancy_variant<1, 2, 2, false>();
+  if (L <= 4) return occupancy_variant<1, 2, 4, false>();
+  if (L <= 8) return occupancy_variant<1, 2, 8, false>();
+  return occupancy_variant<1, 2, 16, false>();
 }
 
 }  // namespace
@@ -651,15 +649,22 @@ int occupancy_any(int L) {
 // q_len 1: 2*KS consumer warps (2 KV heads x KS key shares), one n-tile of 8 heads
 // each; q_len 2..16: one consumer warp per KV head per pair of tokens.
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  return launch_any<false>(a, num_work, pdl, s);
+  return launch_any(a, num_work, pdl, s);
 }
 
+// The single-launch step is built for q_len 1 only: for a verify block the
+// three kernels are faster (one CTA per SM at the fused variant's registers,
+// and every split recomputing the block's new K/V rows).
 cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  return launch_any<true>(a, num_work, pdl, s);
+  if (a.L != 1) return cudaErrorInvalidValue;
+  if (num_work == 0) return cudaSuccess;
+  return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>(a, num_work, pdl, s);
 }
 
 int decode_ctas_per_sm(int L) {
-  const int a = occupancy_any<false>(L), b = occupancy_any<true>(L);
+  const int a = occupancy_any(L);
+  if (L != 1) return a;
+  const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>();
   return a < b ? a : b;
 }
 

@@ -150,7 +150,8 @@ okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_att
   const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
   z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo)) +
-                      round_up(c->batch * sizeof(int32_t));  // + the fused step's arrival counters
+                      round_up(c->batch * sizeof(int32_t)) +  // + the fused step's arrival counters
+                      (c->q_len > 1 ? round_up(T * c->num_q_heads * c->head_dim) : 0);  // + its q (q_len > 1)
   z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
   z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
   z->lse_partial_bytes = round_up(W * rows * sizeof(float));
@@ -231,6 +232,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
   p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
   p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
+  p->d_q8 = cfg->q_len > 1 ? reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(cfg->batch * sizeof(int32_t)) : nullptr;
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
@@ -457,8 +459,20 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.weight = static_cast<const uint16_t*>(norm_weight);
   a.out = static_cast<uint16_t*>(out);
   a.eps = eps;
-  cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+  cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  if (c.q_len == 1) {
+    cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, str);
+    return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
+  }
+  // q_len > 1: the three kernels (measured faster than the single launch for a
+  // verify block), with q in the plan workspace
+  okc_status st = okc_prepare_qkv(plan, qkv, positions, cache_loc, k_cache, v_cache, k_scale, v_scale, rope_table,
+                                  rope_positions, plan->d_q8, stream);
+  if (st != OKC_OK) return st;
+  st = okc_attn_decode(plan, plan->d_q8, k_cache, v_cache, k_scale, v_scale, page_table, cache_seqlens,
+                       cu_seqlens_q, seq_lens, o_partial, lse_partial, stream);
+  if (st != OKC_OK) return st;
+  return okc_attn_combine_normgate(plan, o_partial, lse_partial, qkv, norm_weight, eps, out, stream);
 }
 
 }  // extern "C"

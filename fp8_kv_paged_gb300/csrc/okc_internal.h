@@ -99,6 +99,7 @@ struct okc_attn_plan_s {
   okc::WorkItem* d_work;
   okc::ReqInfo* d_req;
   int32_t* d_tickets;  // the fused step's per-request arrival counters
+  uint8_t* d_q8;       // the fused step's q for q_len > 1 (three launches)
   int device;
   int sm_count;
   bool pdl;

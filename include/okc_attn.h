@@ -210,8 +210,9 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
  * token's key computes that K/V row, uses it in place and writes it to the
  * cache at cache_loc; the last CTA of each request to finish (an atomic ticket
  * in the plan workspace, reset after use; no CTA waits on another) merges the
- * request's splits and writes `out`. The "one fused kernel" of the survey's
- * next steps; the three-call path stays the reference decomposition.
+ * request's splits and writes `out`. For q_len > 1 (a verify block) the call
+ * runs the three kernels instead (measured faster there), keeping q in the
+ * plan workspace; either way the results equal the three calls' bit for bit.
  * Arguments: those of the three calls, minus q_fp8. cache_loc[t] must be the
  * page-table row of token t's position (the kernel uses the computed row
  * directly instead of reading it back).
