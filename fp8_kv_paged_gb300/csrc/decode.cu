@@ -16,8 +16,9 @@
 // (cp.async.mbarrier.arrive); consumer warps release a stage through its
 // "empty" mbarrier. Keys that are masked, or whose page id is invalid, are
 // zero-filled without a read (an invalid page reads as zeros). Every mbarrier
-// wait is bounded: a wait that gives up flags OKC_DEVERR_TIMEOUT, and the
-// producer still waits for its own copies before it returns.
+// wait is bounded in time (mbar_wait): a wait that gives up flags
+// OKC_DEVERR_TIMEOUT, and the producer still waits for its own copies before
+// it returns.
 // (One TMA bulk copy per 128-byte row was measured slower: the copy engine's
 // per-request cost caps a small-row gather well below HBM bandwidth.)
 //
@@ -69,10 +70,9 @@ constexpr int kStageSmem = 2 * kTileSmem;          // K + V
 constexpr int kStages = OKC_DECODE_STAGES;
 constexpr int kProducers = OKC_DECODE_PRODUCERS;
 static_assert(kProducers == 1 || kProducers == 2 || kProducers == 4, "1, 2 or 4 producer warps");
-constexpr int kBarOffset = kStages * kStageSmem;
-constexpr int kFlagOffset = kBarOffset + 2 * kStages * 8;  // one int: "this CTA merges"
+constexpr int kBarOffset = kStages * kStageSmem;             // full[kStages], empty[kStages]
+constexpr int kFlagOffset = kBarOffset + 2 * kStages * 8;    // one int: "this CTA merges"
 constexpr int kSmemBytes = kFlagOffset + 16;
-constexpr uint32_t kWaitLimit = 1u << 25;          // polls of mbarrier.try_wait before giving up
 
 // ---- the fused step: steps 1-3 inside the decode CTA (the arithmetic of the
 // prepare kernel: correctly rounded RMS inverse (rms_inverse), each float32
@@ -166,6 +166,8 @@ struct DecodeCfg {
   static constexpr int kMTiles = 4 / KS;  // 16-key m-tiles per consumer warp per tile
 };
 
+// FUSED false: the decode kernel of the three-call path (q from q_fp8, partials
+// out); true: the whole step (okc_attn_step), last-CTA merge through tickets.
 template <int KS, int NTW, int NCW, bool FUSED>
 __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_MINBLOCKS_L1 : 1)
     decode_kernel(DecodeArgs a) {
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       for (int u = 0; u < kStages; u++) {  // tile k = k0 + u uses ring slot u
         const int k = k0 + u;
         if (k >= ntiles) break;
-        if (!mbar_wait(empty_bar(u), ((k / kStages) & 1) ^ 1, kWaitLimit)) { ok = false; break; }
+        if (!mbar_wait(empty_bar(u), ((k / kStages) & 1) ^ 1)) { ok = false; break; }
         issue(k, ids[u]);
         load_ids(ids[u], k + kStages);
       }
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 
   for (int k = 0; k < ntiles; k++) {
     const int s = k % kStages;
-    if (!mbar_wait(full_bar(s), (k / kStages) & 1, kWaitLimit)) {
+    if (!mbar_wait(full_bar(s), (k / kStages) & 1)) {
       if (lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
       break;
     }

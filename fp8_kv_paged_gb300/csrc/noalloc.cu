@@ -169,7 +169,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
 
   int shift = 0;
   while ((1 << shift) < c.page_size) shift++;
-  DecodeArgs d;
+  DecodeArgs d = {};
   d.q8 = q_fp8;
   d.kc = k_cache;
   d.vc = v_cache;

@@ -38,43 +38,26 @@ __device__ __forceinline__ void load_gate_weight(const uint16_t* qkv, const uint
   }
 }
 
-// lse: the row's base-2 LSE of split 0, consecutive splits `lse_stride` floats
-// apart; op: this lane's 8 columns of split 0, splits `o_stride` floats apart.
-// Loads bypass L1 (partials written by other CTAs of the same grid).
-__device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_stride, const float* op,
-                                               int64_t o_stride, int nchunks, const float (&g)[8],
+// Splits are visited in batches of kMergeBatch with every load of a batch in
+// flight: M = max lse (first pass), then the weighted sums (second pass).
+constexpr int kMergeBatch = 8;
+
+__device__ __forceinline__ void merge_accumulate(const float (&ls)[kMergeBatch], const float4 (&x0)[kMergeBatch],
+                                                 const float4 (&x1)[kMergeBatch], float Mu, float (&acc)[8],
+                                                 float& wsum) {
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; u++) {
+    const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - Mu);
+    wsum += wt;
+    acc[0] += wt * x0[u].x; acc[1] += wt * x0[u].y; acc[2] += wt * x0[u].z; acc[3] += wt * x0[u].w;
+    acc[4] += wt * x1[u].x; acc[5] += wt * x1[u].y; acc[6] += wt * x1[u].z; acc[7] += wt * x1[u].w;
+  }
+}
+
+// o = acc / wsum rounded to bf16, then the row's RMS over its 8 lanes and the
+// gated, weighted bf16 output (8 columns, one 16-byte store).
+__device__ __forceinline__ void normgate_store(const float (&acc)[8], float wsum, const float (&g)[8],
                                                const float (&w)[8], float eps, uint16_t* dst) {
-  constexpr int kB = 8;  // splits visited in batches with every load of a batch in flight
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < nchunks; s0 += kB) {
-    float ls[kB];
-#pragma unroll
-    for (int u = 0; u < kB; u++) ls[u] = s0 + u < nchunks ? __ldcg(lse + (int64_t)(s0 + u) * lse_stride) : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kB; u++) M = fmaxf(M, ls[u]);
-  }
-  const float Mu = M == -INFINITY ? 0.f : M;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float wsum = 0.f;
-  for (int s0 = 0; s0 < nchunks; s0 += kB) {
-    float ls[kB];
-    float4 x0[kB], x1[kB];
-#pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const bool live = s0 + u < nchunks;
-      ls[u] = live ? __ldcg(lse + (int64_t)(s0 + u) * lse_stride) : -INFINITY;
-      const float4* src = reinterpret_cast<const float4*>(op + (int64_t)(live ? s0 + u : 0) * o_stride);
-      x0[u] = live ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x1[u] = live ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < kB; u++) {
-      const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - Mu);
-      wsum += wt;
-      acc[0] += wt * x0[u].x; acc[1] += wt * x0[u].y; acc[2] += wt * x0[u].z; acc[3] += wt * x0[u].w;
-      acc[4] += wt * x1[u].x; acc[5] += wt * x1[u].y; acc[6] += wt * x1[u].z; acc[7] += wt * x1[u].w;
-    }
-  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   float ob[8];
   float ss = 0.f;
@@ -100,6 +83,41 @@ __device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_str
     outw[k] = *reinterpret_cast<const uint32_t*>(&p);
   }
   *reinterpret_cast<uint4*>(dst) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+}
+
+// Splits in global memory. lse: the row's base-2 LSE of split 0, consecutive
+// splits `lse_stride` floats apart; op: this lane's 8 columns of split 0, splits
+// `o_stride` floats apart. Loads bypass L1 (partials written by other CTAs of
+// the same grid).
+__device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_stride, const float* op,
+                                               int64_t o_stride, int nchunks, const float (&g)[8],
+                                               const float (&w)[8], float eps, uint16_t* dst) {
+  constexpr int kB = kMergeBatch;
+  float M = -INFINITY;
+  for (int s0 = 0; s0 < nchunks; s0 += kB) {
+    float ls[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) ls[u] = s0 + u < nchunks ? __ldcg(lse + (int64_t)(s0 + u) * lse_stride) : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kB; u++) M = fmaxf(M, ls[u]);
+  }
+  const float Mu = M == -INFINITY ? 0.f : M;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  for (int s0 = 0; s0 < nchunks; s0 += kB) {
+    float ls[kB];
+    float4 x0[kB], x1[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const bool live = s0 + u < nchunks;
+      ls[u] = live ? __ldcg(lse + (int64_t)(s0 + u) * lse_stride) : -INFINITY;
+      const float4* src = reinterpret_cast<const float4*>(op + (int64_t)(live ? s0 + u : 0) * o_stride);
+      x0[u] = live ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x1[u] = live ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    merge_accumulate(ls, x0, x1, Mu, acc, wsum);
+  }
+  normgate_store(acc, wsum, g, w, eps, dst);
 }
 
 }  // namespace okc

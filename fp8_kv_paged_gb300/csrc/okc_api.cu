@@ -165,8 +165,10 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : okc::decode_ctas_per_sm(c->q_len);
-  if (per_sm <= 0) return -1;
+  // the occupancy query also raises the kernels' shared-memory limit: always run it
+  const int occ = okc::decode_ctas_per_sm(c->q_len);
+  if (occ <= 0) return -1;
+  const int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : occ;
   if (sm_count_out) *sm_count_out = sms;
   return sms * per_sm;
 }
@@ -345,7 +347,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
     return OKC_ERR_INVALID;
   const bool scaled = c.kv_scale != 1.f;
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
-  okc::DecodeArgs a;
+  okc::DecodeArgs a = {};
   a.q8 = q_fp8;
   a.kc = k_cache;
   a.vc = v_cache;
@@ -422,7 +424,7 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
                rope_positions > okc::kRopePositionsMax))
     return OKC_ERR_INVALID;
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
-  okc::DecodeArgs a;
+  okc::DecodeArgs a = {};
   std::memset(&a, 0, sizeof a);
   a.kc = k_cache;
   a.vc = v_cache;

@@ -74,11 +74,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of parity `parity` to complete; false after `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; i++)
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of parity `parity` to complete. Bounded in time: a poll of
+// try_wait may suspend the thread for a hardware-defined while, so a poll count
+// alone does not bound the wait; it gives up (returns false) once it has polled
+// kWaitMinPolls times and kWaitNs have passed since its first failed poll (the
+// poll count keeps a kernel that was preempted mid-wait from giving up early).
+constexpr uint32_t kWaitMinPolls = 1u << 12;
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s; a tile lands within microseconds
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; i++) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if (i >= kWaitMinPolls && global_ns() - t0 > kWaitNs) return false;
+  }
 }
 // Arrive on mbarrier `bar` once every cp.async this thread has issued so far has
 // completed (the arrival counts toward the barrier's expected count).

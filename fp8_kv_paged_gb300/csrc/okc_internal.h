@@ -111,7 +111,8 @@ namespace okc {
 // Kernel launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_prepare(const PrepareArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
-// The whole step in one launch (q from qkv, new K/V rows, attention, last-CTA merge).
+// The whole step in one launch for q_len 1 (q from qkv, new K/V rows,
+// attention, last-CTA merge).
 cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, float* table,
