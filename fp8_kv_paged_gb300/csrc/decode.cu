@@ -178,6 +178,9 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   auto full_bar = [&](int s) { return sbase + kBarOffset + 8 * s; };
   auto empty_bar = [&](int s) { return sbase + kBarOffset + 8 * (kStages + s); };
 
+  // The work item is plan data (written when the plan was made): it is read
+  // before the programmatic-dependency wait, overlapping the previous kernel.
+  const WorkItem wk = a.work[blockIdx.x];
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(full_bar(s), 32 * kProducers);  // one cp.async-tracked arrival per producer lane
@@ -185,15 +188,47 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     }
     fence_mbar_init();
   }
+  const int b = wk.b;
 
   if constexpr (FUSED) {  // the first kernel of the step: its predecessor may write any input
     pdl_wait();
     pdl_launch_dependents();
+    // the gate logits and norm weight the merge reads at the end: into L2 now
+    // (token b*L is the request's first token for the usual cu_seqlens_q)
+    if (tid < 16) prefetch_l2(a.qkv + (int64_t)b * a.L * kQkvWidth + kGateCol + tid * 64);
+    if (tid == 16 && a.weight) prefetch_l2(a.weight);
   }
-  // ---- the work item and the request's lengths (caller inputs)
-  const WorkItem wk = a.work[blockIdx.x];
-  const int b = wk.b;
-  const ReqInfo rq = a.req[b];
+
+  // ---- producer set-up: page ids of the first kStages tiles, loaded with the
+  // item's key range under the plan's lengths while the request's lengths
+  // (caller inputs) are still in flight; checked against them below.
+  // Producer warp pw owns keys [pw*kKeysPW, (pw+1)*kKeysPW) of every tile.
+  // Lane (rr, ch) = (lane >> 3, lane & 7) copies 16-byte chunk ch of the owned
+  // rows rr, rr+4, ...; eight lanes cover one 128-byte row, so each warp
+  // instruction fetches four whole rows. Page ids: lane l loads the ids of owned
+  // keys l, l+32, ... and the row owners read them by shuffle.
+  constexpr int kKeysPW = kTileKeys / kProducers;  // keys per producer warp per tile
+  constexpr int kIds = kKeysPW >= 32 ? kKeysPW / 32 : 1;  // page ids per lane per tile
+  const int pw = warp - NCW, kbase = pw * kKeysPW;
+  const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
+  // ids of tile `tile` of key range [jb, je)
+  auto load_ids = [&](int (&dst)[kIds], int tile, int jb, int je) {
+#pragma unroll
+    for (int q = 0; q < kIds; q++) {
+      const int j = jb + tile * kTileKeys + kbase + 32 * q + lane;
+      dst[q] = (32 * q + lane < kKeysPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+    }
+  };
+  // Page ids live in a register ring one slot per stage: the ids of tile k are
+  // loaded when tile k - kStages is issued, so their latency hides behind a
+  // whole ring of copies.
+  int ids[kStages][kIds];
+  if (warp >= NCW) {
+#pragma unroll
+    for (int t = 0; t < kStages; t++) load_ids(ids[t], t, wk.j0, wk.j1);
+  }
+
+  // ---- the request's lengths (caller inputs)
   int n = a.cache_seqlens[b];
   const int qb = a.cu_seqlens_q[b];
   int ql = a.cu_seqlens_q[b + 1] - qb;
@@ -206,36 +241,23 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     n = max(ql, min(n, a.max_pages * P));
   }
   const int lo = a.window > 0 ? max(0, n - ql - a.window + 1) : 0;  // first key any query sees
-  const int j0 = lo + wk.chunk * rq.chunk_keys;
-  const int j1 = min(n, j0 + rq.chunk_keys);
-  if (wk.chunk == rq.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
+  const int j0 = lo + wk.chunk * wk.chunk_keys;
+  const int j1 = min(n, j0 + wk.chunk_keys);
+  if (wk.chunk == wk.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
   const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
   __syncthreads();  // barriers initialised
 
   if (warp >= NCW) {
     // ================================================================ producer
-    // Producer warp pw owns keys [pw*kKeysPW, (pw+1)*kKeysPW) of every tile.
-    // Lane (rr, ch) = (lane >> 3, lane & 7) copies 16-byte chunk ch of the owned
-    // rows rr, rr+4, ...; eight lanes cover one 128-byte row, so each warp
-    // instruction fetches four whole rows. Page ids: lane l loads the ids of owned
-    // keys l, l+32, ... and the row owners read them by shuffle.
-    constexpr int kKeysPW = kTileKeys / kProducers;  // keys per producer warp per tile
-    constexpr int kIds = kKeysPW >= 32 ? kKeysPW / 32 : 1;  // page ids per lane per tile
-    const int pw = warp - NCW, kbase = pw * kKeysPW;
-    const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
+    if (j0 != wk.j0 || j1 != wk.j1) {  // the lengths differ from the plan's: reload
+#pragma unroll
+      for (int t = 0; t < kStages; t++) load_ids(ids[t], t, j0, j1);
+    }
     const int pmask = P - 1;
     const int newk = n - ql;  // keys >= newk are written by the prepare kernel (three-call path)
     const int rr = lane >> 3, ch = lane & 7;
     bool dep = FUSED, bad_page = false;  // the fused step has waited already
-    auto page_of = [&](int tile, int r) {
-      const int j = j0 + tile * kTileKeys + r;
-      return (tile < ntiles && j < j1) ? __ldg(pt + (j >> a.page_shift)) : -1;
-    };
-    auto load_ids = [&](int (&dst)[kIds], int tile) {
-#pragma unroll
-      for (int q = 0; q < kIds; q++) dst[q] = (32 * q + lane < kKeysPW) ? page_of(tile, kbase + 32 * q + lane) : -1;
-    };
     auto issue = [&](int k, const int (&id)[kIds]) {
       const int s = k % kStages;
       const uint32_t sK = sbase + s * kStageSmem, sV = sK + kTileSmem;
@@ -267,16 +289,10 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       cp_async_mbar_arrive(full_bar(s));
     };
 
-    // Page ids live in a register ring one slot per stage: the ids of tile k are
-    // loaded when tile k - kStages is issued, so their latency hides behind a
-    // whole ring of copies.
-    int ids[kStages][kIds];
-#pragma unroll
-    for (int t = 0; t < kStages; t++) load_ids(ids[t], t);
 #pragma unroll
     for (int t = 0; t < kStages; t++) {
       if (t < ntiles) issue(t, ids[t]);
-      load_ids(ids[t], t + kStages);
+      load_ids(ids[t], t + kStages, j0, j1);
     }
     bool ok = true;
     for (int k0 = kStages; k0 < ntiles && ok; k0 += kStages) {
@@ -286,7 +302,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
         if (k >= ntiles) break;
         if (!mbar_wait(empty_bar(u), ((k / kStages) & 1) ^ 1)) { ok = false; break; }
         issue(k, ids[u]);
-        load_ids(ids[u], k + kStages);
+        load_ids(ids[u], k + kStages, j0, j1);
       }
     }
     if (bad_page && ch == 0) set_error(a.err, OKC_DEVERR_PAGE);
@@ -573,19 +589,23 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   }
 
   if constexpr (FUSED) {
-    // Last CTA of the request merges every split and applies the norm-gate: each
-    // CTA publishes its partials (fence), then takes a ticket; the CTA that draws
-    // the last ticket reads all partials (fence, L2 loads) and resets the counter
-    // for the next launch. Nothing waits on another CTA.
+    // Last CTA of the request merges every split and applies the norm-gate: once
+    // the CTA's partials are written (barrier), one thread publishes them (fence)
+    // and takes a ticket; the CTA that draws the last ticket fences again, then
+    // reads all partials (L2 loads) and resets the counter for the next launch.
+    // Nothing waits on another CTA.
     volatile int& s_last = *reinterpret_cast<int*>(smem + kFlagOffset);
     if (pos_err && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
-    __threadfence();
     named_bar_sync(1, NCW * 32);
-    if (tid == 0) s_last = atomicAdd(a.tickets + b, 1) == rq.nchunks - 1;
+    if (tid == 0) {
+      __threadfence();
+      const bool last = atomicAdd(a.tickets + b, 1) == wk.nchunks - 1;
+      if (last) __threadfence();
+      s_last = last;
+    }
     named_bar_sync(1, NCW * 32);
     if (s_last) {
-      __threadfence();
-      const int64_t base_lse = (int64_t)rq.wbase * rows;
+      const int64_t base_lse = (int64_t)wk.wbase * rows;
       for (int rowi = tid >> 3; rowi < ql * kNumQHeads; rowi += NCW * 4) {  // 8 lanes per row
         const int tok = rowi / kNumQHeads, h = rowi % kNumQHeads;
         const int64_t t = (int64_t)qb + tok;
@@ -593,7 +613,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
         float gg[8], ww[8];
         load_gate_weight(a.qkv, a.weight, (int)t, h, c0, gg, ww);
         merge_normgate(a.lse_part + base_lse + rowi, rows,
-                       a.o_part + (base_lse + rowi) * kHeadDim + c0, (int64_t)rows * kHeadDim, rq.nchunks, gg,
+                       a.o_part + (base_lse + rowi) * kHeadDim + c0, (int64_t)rows * kHeadDim, wk.nchunks, gg,
                        ww, a.eps, a.out + t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
       }
       if (tid == 0) a.tickets[b] = 0;

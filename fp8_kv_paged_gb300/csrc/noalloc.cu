@@ -138,7 +138,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     if (C == 128) break;
   }
   (void)total;
-  WorkItem work[kMaxWork];  // ~100 KB of stack in all, no heap
+  WorkItem work[kMaxWork];  // ~180 KB of stack in all, no heap
   ReqInfo req[kMaxBatch];
   int64_t W = 0;
   for (int b = 0; b < B; b++) {
@@ -147,7 +147,12 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (W + nch > kMaxWork) return OKC_ERR_WORKSPACE;
     req[b] = ReqInfo{(int32_t)W, (int32_t)nch, (int32_t)chunk, 0};
-    for (int64_t i = 0; i < nch; i++) work[W + i] = WorkItem{b, (int32_t)i, (int32_t)(W + i), 0};
+    const int64_t n = (int64_t)seq_lens_host[b] + L, lo = n - nvis[b];
+    for (int64_t i = 0; i < nch; i++) {
+      const int64_t j0 = lo + i * chunk, j1 = std::min<int64_t>(n, j0 + chunk);
+      work[W + i] = WorkItem{b, (int32_t)i, (int32_t)(W + i), (int32_t)j0,
+                             (int32_t)j1, (int32_t)chunk, (int32_t)nch, (int32_t)W};
+    }
     W += nch;
   }
   // Scratch layout in the static array: work list | request table | LSE | partial outputs.

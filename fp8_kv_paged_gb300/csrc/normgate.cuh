@@ -39,15 +39,28 @@ __device__ __forceinline__ void load_gate_weight(const uint16_t* qkv, const uint
 }
 
 // Splits are visited in batches of kMergeBatch with every load of a batch in
-// flight: M = max lse (first pass), then the weighted sums (second pass).
+// flight (one round trip per batch). Online over batches: the running sums are
+// rescaled by 2^(M_old - M_new) when a batch raises the maximum; with at most
+// kMergeBatch splits this is the plain two-pass merge (M = max of all lse).
 constexpr int kMergeBatch = 8;
 
 __device__ __forceinline__ void merge_accumulate(const float (&ls)[kMergeBatch], const float4 (&x0)[kMergeBatch],
-                                                 const float4 (&x1)[kMergeBatch], float Mu, float (&acc)[8],
+                                                 const float4 (&x1)[kMergeBatch], float& M, float (&acc)[8],
                                                  float& wsum) {
+  float bm = M;
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; u++) bm = fmaxf(bm, ls[u]);
+  const float bmu = bm == -INFINITY ? 0.f : bm;
+  if (M != -INFINITY && bm != M) {  // an earlier batch: rescale its sums to the new maximum
+    const float sc = exp2f(M - bmu);
+    wsum *= sc;
+#pragma unroll
+    for (int k = 0; k < 8; k++) acc[k] *= sc;
+  }
+  M = bm;
 #pragma unroll
   for (int u = 0; u < kMergeBatch; u++) {
-    const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - Mu);
+    const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - bmu);
     wsum += wt;
     acc[0] += wt * x0[u].x; acc[1] += wt * x0[u].y; acc[2] += wt * x0[u].z; acc[3] += wt * x0[u].w;
     acc[4] += wt * x1[u].x; acc[5] += wt * x1[u].y; acc[6] += wt * x1[u].z; acc[7] += wt * x1[u].w;
@@ -94,14 +107,6 @@ __device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_str
                                                const float (&w)[8], float eps, uint16_t* dst) {
   constexpr int kB = kMergeBatch;
   float M = -INFINITY;
-  for (int s0 = 0; s0 < nchunks; s0 += kB) {
-    float ls[kB];
-#pragma unroll
-    for (int u = 0; u < kB; u++) ls[u] = s0 + u < nchunks ? __ldcg(lse + (int64_t)(s0 + u) * lse_stride) : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kB; u++) M = fmaxf(M, ls[u]);
-  }
-  const float Mu = M == -INFINITY ? 0.f : M;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
   for (int s0 = 0; s0 < nchunks; s0 += kB) {
@@ -115,7 +120,7 @@ __device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_str
       x0[u] = live ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
       x1[u] = live ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    merge_accumulate(ls, x0, x1, Mu, acc, wsum);
+    merge_accumulate(ls, x0, x1, M, acc, wsum);
   }
   normgate_store(acc, wsum, g, w, eps, dst);
 }

@@ -131,8 +131,14 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   }
   r->work.clear();
   r->work.reserve((size_t)wbase);
-  for (int b = 0; b < B; b++)
-    for (int k = 0; k < r->req[b].nchunks; k++) r->work.push_back(WorkItem{b, k, r->req[b].wbase + k, 0});
+  for (int b = 0; b < B; b++) {
+    const ReqInfo& q = r->req[b];
+    const int64_t n = (int64_t)seq[b] + L, lo = n - nvis[b];
+    for (int k = 0; k < q.nchunks; k++) {
+      const int64_t j0 = lo + (int64_t)k * q.chunk_keys, j1 = std::min<int64_t>(n, j0 + q.chunk_keys);
+      r->work.push_back(WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)j1, q.chunk_keys, q.nchunks, q.wbase});
+    }
+  }
   // launch the largest items first (the last chunk of a request may be short)
   auto keys = [&](const WorkItem& w) {
     const ReqInfo& q = r->req[w.b];

@@ -14,9 +14,14 @@ namespace okc {
 // Workspace layout (device, caller-owned): [error word | work list | request table]
 constexpr size_t kWsHeader = 256;
 
-// One split work item: request b, chunk c of its visible keys, output slot.
+// One split work item: request b, chunk `chunk` of its visible keys, output
+// slot; [j0, j1) is the chunk's key range under the plan's lengths (the kernel
+// starts loading page ids with it and checks it against the device lengths);
+// chunk_keys, nchunks and wbase repeat the request's ReqInfo so that a CTA
+// needs one 32-byte load to start.
 struct WorkItem {
-  int32_t b, chunk, slot, pad;
+  int32_t b, chunk, slot, j0;
+  int32_t j1, chunk_keys, nchunks, wbase;
 };
 // Per request: first output slot, number of chunks, keys per chunk.
 struct ReqInfo {

@@ -29,11 +29,12 @@ def to_device(cfg: dict, inp: dict, device="cuda", rope_positions: int | None = 
 
 
 def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None = None,
-            fused: bool = False) -> dict:
-    """One step through the three calls (fused=False) or okc_attn_step (fused=True)."""
+            fused: bool = False, plan_seq=None) -> dict:
+    """One step through the three calls (fused=False) or okc_attn_step (fused=True).
+    plan_seq: host lengths the plan is made with (default: the inputs' own)."""
     import fp8_kv_paged_gb300 as okc
     d = dev_inp if dev_inp is not None else to_device(cfg, inp)
-    step = okc.AttnStep(cfg, inp["seq_lens"], opts=opts)
+    step = okc.AttnStep(cfg, inp["seq_lens"] if plan_seq is None else plan_seq, opts=opts)
     out = step.run_fused(d, eps=inp["eps"]) if fused else step.run(d, eps=inp["eps"])
     torch.cuda.synchronize()
     T = inp["qkv"].shape[0]
@@ -93,8 +94,8 @@ def check_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, rows_mask: np.ndarray 
 
 
 def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, expect_errors: int = 0,
-               fused: bool = False):
-    gpu = run_gpu(cfg, inp, opts, fused=fused)
+               fused: bool = False, plan_seq=None):
+    gpu = run_gpu(cfg, inp, opts, fused=fused, plan_seq=plan_seq)
     k = inp["k_cache"].copy()
     v = inp["v_cache"].copy()
     q8, _ = oracle.prepare(cfg, inp, k, v)

@@ -105,3 +105,19 @@ def test_bad_inputs_flag_errors_without_faulting():
     d = to_device(cfg, dict(inp, seq_lens=inp["seq_lens"] + 1))
     gpu = run_gpu(cfg, inp, dev_inp=d)
     assert gpu["errors"] & okc.DEVERR_LENGTHS
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_plan_lengths_longer_than_device_lengths(fused):
+    """A plan made for longer requests than the step's device lengths still
+    covers every key: the kernels start from the plan's key ranges, find that
+    the device lengths differ, reload the page ids and follow the device
+    lengths (results equal the oracle's on the device lengths)."""
+    cfg = W.config("sliding_decode", batch=6, seq=("uniform", 500, 3000))
+    inp = W.generate(cfg)
+    pad = np.full((cfg["batch"], 64), -1, np.int32)  # room in the page table for the plan's lengths
+    inp["page_table"] = np.concatenate([inp["page_table"], pad], axis=1)
+    cfg["max_pages"] += 64
+    plan_seq = inp["seq_lens"] + 37
+    full_check(cfg, inp, plan_seq=plan_seq, fused=fused)
+    full_check(cfg, inp, opts={"chunk_keys": 96}, plan_seq=plan_seq, fused=fused)
