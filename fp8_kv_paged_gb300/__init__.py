@@ -20,11 +20,12 @@ __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_attn_step",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
-           "PLAN_NO_PDL", "EXPORTED_SYMBOLS"]
+           "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "EXPORTED_SYMBOLS"]
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
 DEVERR_CACHE_LOC, DEVERR_POSITION, DEVERR_PAGE, DEVERR_LENGTHS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 PLAN_NO_PDL = 0x1
+PLAN_NO_TCGEN05 = 0x2
 
 EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libokc_attn.so")
-SOURCES = ["okc_api.cu", "prepare.cu", "decode.cu", "combine.cu", "noalloc.cu"]
+SOURCES = ["okc_api.cu", "prepare.cu", "decode.cu", "decode_tc.cu", "combine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

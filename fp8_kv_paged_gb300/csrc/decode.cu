@@ -671,6 +671,7 @@ int occupancy_any(int L) {
 // q_len 1: 2*KS consumer warps (2 KV heads x KS key shares), one n-tile of 8 heads
 // each; q_len 2..16: one consumer warp per KV head per pair of tokens.
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  if (a.tc && a.L >= 2 && a.L <= 8) return launch_decode_tc(a, num_work, pdl, s);
   return launch_any(a, num_work, pdl, s);
 }
 
@@ -683,7 +684,8 @@ cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaS
   return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>(a, num_work, pdl, s);
 }
 
-int decode_ctas_per_sm(int L) {
+int decode_ctas_per_sm(int L, bool tc) {
+  if (tc && L >= 2 && L <= 8) return decode_tc_ctas_per_sm();
   const int a = occupancy_any(L);
   if (L != 1) return a;
   const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>();

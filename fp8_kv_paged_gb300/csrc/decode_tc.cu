@@ -1,0 +1,520 @@
+// decode_tc.cu — step 4 for a speculative verify block (2 <= q_len <= 8) on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory): the
+// flash_attn_with_kvcache call of "012-attention-local-splits.py" with the
+// block's L queries, paged, causal within the block, window (window-1, 0).
+//
+// One CTA per work item (request b, chunk of its visible keys), as in
+// decode.cu; the CTA holds all 128 q rows of the request (L tokens x 16 heads,
+// rows g*64 + i*8 + hh for KV head g, token i, head g*8 + hh; rows of tokens
+// past q_len are zero and ignored) as ONE M = 128 operand:
+//   S [128 x 64 keys]  = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
+//   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16)
+// where column 128 of the B operand is all ones, so O's column 128 is the row
+// sum of P as the tensor core saw it (f16 P, f32 sums): the softmax
+// denominator, consistent with the numerator and kept by the same rescales.
+// GQA without splitting the MMA by KV head: a q row of KV head g carries its 64
+// dims at K positions [64g, 64g+64) and zeros elsewhere, against K rows that
+// hold both heads' 64 dims (the cache row as stored), so S = q . k_g exactly;
+// for PV every row gets both heads' 64 output dims and keeps its own half.
+//
+// Warps: 0-3 and 4-7 are two softmax warpgroups that take alternate tiles
+// (thread r of a group owns q row r), 8 issues the MMAs (one thread) and owns
+// the TMEM allocation, 9-10 gather (the cp.async producer of decode.cu; K rows
+// land in the MMA's canonical layout, V rows in a staging tile). Each group j
+// has its own S and O in TMEM and its own P and V^T tiles in shared memory, so
+// one group's softmax overlaps the other group's MMAs. Per tile k of group j:
+//   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
+//   group j: wait s_ready_j -> S row from TMEM -> arrive(s_free_j) -> mask; row
+//            max; P = 2^(s - m) (f16) into shared memory; V tile E4M3 -> f16
+//            transposed (ldmatrix, exact conversion, stmatrix.trans)
+//            -> arrive(p_ready_j)
+//   MMA:     wait p_ready_j -> free the stage -> O_j += P V -> commit(pv_done_j)
+// O accumulates in TMEM against a reference max m per row that moves only when
+// the row's max grows past m + 8 (in log2 units; P stays <= 2^8): then the
+// row's O is rescaled in TMEM (tcgen05.ld / st) before the next PV. At the end
+// group 0 merges both groups' (m, l, O) and writes O/l (times v_scale) and the
+// base-2 LSE per row, as decode.cu does; the combine kernel merges the splits.
+//
+// Shared-memory operands use the no-swizzle K-major layout (8-row x 16-byte
+// core matrices; core matrices 128 bytes apart along K, 8-row groups 1024
+// bytes apart for 128-byte rows). Every wait is bounded (mbar_wait); on a
+// timeout the kernel flags OKC_DEVERR_TIMEOUT, waits for the MMAs it issued
+// and frees its TMEM before it returns.
+#include "okc_common.cuh"
+#include "okc_internal.h"
+
+namespace okc {
+
+namespace {
+
+constexpr int kTcTileKeys = 64;
+constexpr int kTcStages = 6;
+constexpr int kTcProducers = 2;   // producer warps
+constexpr int kTcRows = 128;      // q rows per CTA (M)
+constexpr int kTcGroups = 2;      // softmax warpgroups
+constexpr int kTcMmaWarp = 4 * kTcGroups;  // warps 0-7 softmax, 8 MMA, 9-10 producers
+constexpr int kTcThreads = (kTcMmaWarp + 1 + kTcProducers) * 32;
+constexpr int kTcVPitch = 144;    // V staging row pitch: conflict-free ldmatrix
+constexpr uint32_t kTcLbo = 128;  // next core matrix along K
+constexpr uint32_t kTcSbo = 1024; // next 8-row group (rows of 128 bytes)
+#ifndef OKC_TC_RESCALE
+#define OKC_TC_RESCALE 0
+#endif
+constexpr float kTcRescale = OKC_TC_RESCALE;  // log2 headroom of the reference max (0: exact max)
+// shared memory
+constexpr int kTcQ = 0;                                              // Q E4M3 [128 x 128 B]
+constexpr int kTcK = kTcQ + kTcRows * 128;                           // K E4M3 [stage][64 x 128 B]
+constexpr int kTcV = kTcK + kTcStages * kTcTileKeys * 128;           // V E4M3 [stage][64 x 144 B]
+constexpr int kTcP = kTcV + kTcStages * kTcTileKeys * kTcVPitch;     // P f16 [group][128 x 64]
+constexpr int kTcPvN = 144;                                          // PV's N: 128 dims + the ones column
+constexpr int kTcVTBytes = kTcPvN * 128;
+constexpr int kTcVT = kTcP + kTcGroups * kTcRows * 128;              // [V | 1]^T f16 [group][144 x 64 keys]
+constexpr int kTcX = kTcVT + kTcGroups * kTcVTBytes;                 // group 1's reference max per row
+constexpr int kTcBar = kTcX + kTcRows * 8;
+// barriers: full[S], empty[S], s_ready[2], p_ready[2], pv_done[2], s_free[2], mma_done
+constexpr int kTcTmemSlot = kTcBar + (2 * kTcStages + 4 * kTcGroups + 1) * 8;
+constexpr int kTcSmem = kTcTmemSlot + 16 + 2048;  // + slack past the last operand
+constexpr uint32_t kTcCols = 512;  // TMEM columns: S_j at 64 j (64), O_j at 128 + 160 j (144)
+__host__ __device__ constexpr uint32_t tc_col_s(int j) { return 64u * j; }
+__host__ __device__ constexpr uint32_t tc_col_o(int j) { return 128u + 160u * j; }
+static_assert(tc_col_o(1) + kTcPvN <= kTcCols, "TMEM columns");
+static_assert(kTcQ % 1024 == 0 && kTcK % 1024 == 0 && kTcP % 1024 == 0 && kTcVT % 1024 == 0, "operand alignment");
+
+// Byte offset of (row r, byte kb) in a canonical tile of 128-byte rows.
+__device__ __forceinline__ uint32_t canon(int r, int kb) {
+  return (uint32_t)((r >> 3) * kTcSbo + (kb >> 4) * kTcLbo + (r & 7) * 16 + (kb & 15));
+}
+
+__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sb = smem_u32(smem);
+  auto full_bar = [&](int s) { return sb + kTcBar + 8 * s; };
+  auto empty_bar = [&](int s) { return sb + kTcBar + 8 * (kTcStages + s); };
+  auto s_ready = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + j); };
+  auto p_ready = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + kTcGroups + j); };
+  auto pv_done = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + 2 * kTcGroups + j); };
+  auto s_free = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + 3 * kTcGroups + j); };
+  const uint32_t mma_done = sb + kTcBar + 8 * (2 * kTcStages + 4 * kTcGroups);
+
+  const WorkItem wk = a.work[blockIdx.x];  // plan data
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; s++) {
+      mbar_init(full_bar(s), 32 * kTcProducers);  // one cp.async-tracked arrival per producer lane
+      mbar_init(empty_bar(s), 1);                  // the MMA thread frees a stage
+    }
+    for (int j = 0; j < kTcGroups; j++) {
+      mbar_init(s_ready(j), 1);
+      mbar_init(p_ready(j), kTcRows);
+      mbar_init(pv_done(j), 1);
+      mbar_init(s_free(j), kTcRows);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kTcMmaWarp) tmem_alloc(sb + kTcTmemSlot, kTcCols);
+  const int b = wk.b;
+
+  // ---- producer set-up (as decode.cu): page ids of the first tiles with the
+  // plan's key range while the device lengths load. Producer warp pw owns keys
+  // [pw kKeysPW, (pw + 1) kKeysPW) of every tile; lane l < kKeysPW loads the id
+  // of its key l.
+  constexpr int kKeysPW = kTcTileKeys / kTcProducers;
+  static_assert(kKeysPW == 16 || kKeysPW == 32, "at most one page id per producer lane per tile");
+  const int pw = warp - (kTcMmaWarp + 1), kbase = pw * kKeysPW;
+  const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
+  auto load_ids = [&](int& dst, int tile, int jb, int je) {
+    const int j = jb + tile * kTcTileKeys + kbase + lane;
+    dst = (lane < kKeysPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+  };
+  int ids[kTcStages];
+  if (warp > kTcMmaWarp) {
+#pragma unroll
+    for (int t = 0; t < kTcStages; t++) load_ids(ids[t], t, wk.j0, wk.j1);
+  }
+
+  // ---- the request's lengths (caller inputs)
+  int n = a.cache_seqlens[b];
+  const int qb = a.cu_seqlens_q[b];
+  int ql = a.cu_seqlens_q[b + 1] - qb;
+  const int P = 1 << a.page_shift;
+  bool bad_len = ql < 0 || ql > a.L || qb < 0 || qb + ql > a.T || n < ql ||
+                 (a.seq_lens && a.seq_lens[b] != n - ql) || (int64_t)n > (int64_t)a.max_pages * P;
+  if (bad_len) {  // keep every access in range; the result of this request is void
+    ql = max(0, min(ql, a.L));
+    if (qb < 0 || qb + ql > a.T) ql = 0;
+    n = max(ql, min(n, a.max_pages * P));
+  }
+  const int lo = a.window > 0 ? max(0, n - ql - a.window + 1) : 0;
+  const int j0 = lo + wk.chunk * wk.chunk_keys;
+  const int j1 = min(n, j0 + wk.chunk_keys);
+  if (wk.chunk == wk.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
+  if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
+  const int ntiles = j1 > j0 ? (j1 - j0 + kTcTileKeys - 1) / kTcTileKeys : 0;
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, TMEM address in shared memory
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTcTmemSlot);
+
+  if (warp > kTcMmaWarp) {
+    // ================================================================ producer
+    if (j0 != wk.j0 || j1 != wk.j1) {  // the lengths differ from the plan's: reload
+#pragma unroll
+      for (int t = 0; t < kTcStages; t++) load_ids(ids[t], t, j0, j1);
+    }
+    const int pmask = P - 1;
+    const int newk = n - ql;  // keys >= newk are written by the prepare kernel
+    const int rr = lane >> 3, ch = lane & 7;
+    bool dep = false, bad_page = false;
+    auto issue = [&](int k, int id) {
+      const int s = k % kTcStages;
+      const uint32_t sK = sb + kTcK + s * (kTcTileKeys * 128), sV = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
+      const int tj = j0 + k * kTcTileKeys;
+      if (!dep && min(j1, tj + kTcTileKeys) > newk) {  // this tile holds a key prepare writes
+        pdl_wait();
+        dep = true;
+      }
+#pragma unroll
+      for (int i = 0; i < kKeysPW / 4; i++) {
+        const int rl = rr + 4 * i;
+        const int r = kbase + rl;
+        const int pg = __shfl_sync(0xffffffffu, id, rl);
+        const int j = tj + r;
+        int64_t row = 0;
+        int bytes = 0;
+        if (j < j1) {
+          if (pg >= 0 && pg < a.num_pages) {
+            row = ((int64_t)pg << a.page_shift) | (j & pmask);
+            bytes = 16;
+          } else {
+            bad_page = true;
+          }
+        }
+        cp_async_16(sK + canon(r, ch * 16), a.kc + row * kRowBytes + ch * 16, bytes);
+        cp_async_16(sV + r * kTcVPitch + ch * 16, a.vc + row * kRowBytes + ch * 16, bytes);
+      }
+      cp_async_mbar_arrive(full_bar(s));
+    };
+#pragma unroll
+    for (int t = 0; t < kTcStages; t++) {
+      if (t < ntiles) issue(t, ids[t]);
+      load_ids(ids[t], t + kTcStages, j0, j1);
+    }
+    bool ok = true;
+    for (int k0 = kTcStages; k0 < ntiles && ok; k0 += kTcStages) {
+#pragma unroll
+      for (int u = 0; u < kTcStages; u++) {
+        const int k = k0 + u;
+        if (k >= ntiles) break;
+        if (!mbar_wait(empty_bar(u), ((k / kTcStages) & 1) ^ 1)) { ok = false; break; }
+        issue(k, ids[u]);
+        load_ids(ids[u], k + kTcStages, j0, j1);
+      }
+    }
+    if (bad_page && ch == 0) set_error(a.err, OKC_DEVERR_PAGE);
+    if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
+    cp_async_wait<0>();
+    return;
+  }
+
+  if (warp == kTcMmaWarp) {
+    // ================================================================ MMA issue
+    named_bar_sync(1, (kTcMmaWarp + 1) * 32);  // Q is in shared memory
+    if (lane == 0) {
+      constexpr uint32_t id_qk = umma_idesc(0, kTcRows, kTcTileKeys);  // E4M3 x E4M3 -> f32, 128 x 64
+      constexpr uint32_t id_pv = umma_idesc(0, kTcRows, kTcPvN);       // f16 x f16 -> f32, 128 x 144
+      // S_j = Q K_k^T for tile k (group j = k & 1)
+      auto qk = [&](int k) -> bool {
+        const int s = k % kTcStages, j = k & 1;
+        if (!mbar_wait(full_bar(s), (k / kTcStages) & 1)) return false;
+        fence_proxy_async();  // the gathered tile, written through the generic proxy
+        tc_fence_after();
+        const uint32_t kt = sb + kTcK + s * (kTcTileKeys * 128);
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++)  // 128 bytes of K: 32 per instruction (two core matrices)
+          umma_f8(tmem + tc_col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
+                  umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_qk, kk > 0);
+        umma_commit(s_ready(j));
+        return true;
+      };
+      // O_j (+)= P_j V_k once group j has written P and V^T of tile k
+      auto pv = [&](int k) -> bool {
+        const int j = k & 1;
+        if (!mbar_wait(p_ready(j), (k >> 1) & 1)) return false;
+        fence_proxy_async();
+        tc_fence_after();
+        mbar_arrive(empty_bar(k % kTcStages));  // K read (S_k consumed), V converted: the stage is free
+        const uint32_t pa = sb + kTcP + j * (kTcRows * 128), va = sb + kTcVT + j * kTcVTBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++)  // 64 keys: 16 per instruction
+          umma_f16(tmem + tc_col_o(j), umma_desc(pa + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
+                   umma_desc(va + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_pv, (k >= kTcGroups || kk > 0) ? 1u : 0u);
+        umma_commit(pv_done(j));
+        return true;
+      };
+      // Issue order follows readiness: QK of tile t (S_j free: group j has read
+      // S of tile t-2; tile t landed) and PV of tile t (P_j written) are
+      // polled without blocking and issued as soon as their inputs are ready,
+      // so a late tile never holds back a PV. Bounded: gives up after kWaitNs
+      // without progress.
+      bool ok = true;
+      int nq = 0, np = 0;  // next QK / PV to issue
+      uint64_t t_idle = 0;
+      while (np < ntiles) {
+        bool did = false;
+        if (nq < ntiles && (nq < kTcGroups || mbar_test_wait(s_free(nq & 1), ((nq - kTcGroups) >> 1) & 1)) &&
+            mbar_test_wait(full_bar(nq % kTcStages), (nq / kTcStages) & 1)) {
+          tc_fence_after();
+          ok = qk(nq);  // its waits succeed at once
+          nq++;
+          did = true;
+        }
+        if (ok && np < nq && mbar_test_wait(p_ready(np & 1), (np >> 1) & 1)) {
+          ok = pv(np);
+          np++;
+          did = true;
+        }
+        if (!ok) break;
+        if (did) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_ns();
+        } else if (global_ns() - t_idle > kWaitNs) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) set_error(a.err, OKC_DEVERR_TIMEOUT);
+      umma_commit(mma_done);  // arrives once every MMA issued above has completed
+      if (!mbar_wait(mma_done, 0)) set_error(a.err, OKC_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+    tc_fence_before();
+    named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // the softmax warps are done with TMEM
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcCols);
+    return;
+  }
+
+  // ================================================================== softmax
+  const int jw = warp >> 2;  // this thread's group: tiles jw, jw + 2, ...
+  const int r = tid & (kTcRows - 1);  // q row
+  const int g = r >> 6, ti = (r >> 3) & 7, hh = r & 7;
+  const int head = g * kGroup + hh;
+  const bool live = ti < ql;
+  pdl_wait();  // q_fp8 is the prepare kernel's output
+  pdl_launch_dependents();
+  {
+    // Q row r: the 64 E4M3 dims of (token ti, head) at K bytes [64g, 64g+64),
+    // zeros elsewhere; group jw writes chunks [4 jw, 4 jw + 4) of the row
+    const uint4* src = reinterpret_cast<const uint4*>(a.q8 + ((int64_t)(qb + (live ? ti : 0)) * kNumQHeads + head) *
+                                                                 kHeadDim);
+#pragma unroll
+    for (int c = 4 * jw; c < 4 * jw + 4; c++) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (live && (c >> 2) == g) v = src[c & 3];
+      *reinterpret_cast<uint4*>(smem + kTcQ + canon(r, c * 16)) = v;
+    }
+  }
+  {
+    // rows 128..143 of both groups' [V | 1]^T: row 128 ones, the rest zeros
+    // (never rewritten; the V conversion writes rows 0..127)
+    const int gj = tid >> 7, rr2 = 128 + ((tid >> 3) & 15), c = tid & 7;
+    const uint32_t one2 = rr2 == 128 ? 0x3C003C00u : 0u;  // f16 1.0 pairs
+    *reinterpret_cast<uint4*>(smem + kTcVT + gj * kTcVTBytes + canon(rr2, c * 16)) = make_uint4(one2, one2, one2, one2);
+  }
+  fence_proxy_async();
+  named_bar_sync(1, (kTcMmaWarp + 1) * 32);
+
+  const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
+  const int pos = n - ql + ti;  // this row's query position
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint32_t tS = t_lane + tc_col_s(jw);              // this row's S
+  const uint32_t tO = t_lane + tc_col_o(jw) + 64 * g;      // this row's O half
+  const uint32_t tL = t_lane + tc_col_o(jw) + 128;         // this row's P sum
+  const uint32_t sP = kTcP + jw * (kTcRows * 128), sVT = kTcVT + jw * kTcVTBytes;
+  float m = -INFINITY;  // reference max (log2 units)
+  bool ok = true;
+  int last = -1;  // this group's last tile
+  for (int k = jw; k < ntiles; k += kTcGroups) {
+    const int s = k % kTcStages;
+    const bool w = mbar_wait(s_ready(jw), (k >> 1) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
+    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+    tc_fence_after();
+    const int tile_j = j0 + k * kTcTileKeys;
+    float s0[32], s1[32];
+    tmem_ld32(tS, s0);
+    tmem_ld32(tS + 32, s1);
+    tc_fence_before();
+    mbar_arrive(s_free(jw));  // S of this tile is in registers: the next QK may overwrite it
+    // ---- mask: this row's valid keys of the tile are [klo, khi) (window,
+    // causal, chunk end; none for a dead row); row max on the raw scores
+    int klo = 0, khi = 0;
+    if (live) {
+      klo = a.window > 0 ? max(0, pos - a.window + 1 - tile_j) : 0;
+      khi = min(kTcTileKeys, min(j1, pos + 1) - tile_j);
+    }
+    const uint32_t kn = khi > klo ? (uint32_t)(khi - klo) : 0u;
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (__all_sync(0xffffffffu, klo == 0 && khi == kTcTileKeys)) {  // every key valid for the warp's rows
+#pragma unroll
+      for (int c = 0; c < 32; c++) mx4[c & 3] = fmaxf(mx4[c & 3], fmaxf(s0[c], s1[c]));
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        s0[c] = (uint32_t)(c - klo) < kn ? s0[c] : -INFINITY;
+        s1[c] = (uint32_t)(32 + c - klo) < kn ? s1[c] : -INFINITY;
+        mx4[c & 3] = fmaxf(mx4[c & 3], fmaxf(s0[c], s1[c]));
+      }
+    }
+    // in log2 units (the scale is positive)
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+    // ---- P, V^T and O of this group are free once its previous PV completed
+    if (k >= kTcGroups) {
+      const bool w2 = mbar_wait(pv_done(jw), ((k - kTcGroups) >> 1) & 1);
+      if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+      tc_fence_after();
+    }
+    // ---- reference max: moves when the row max passes it by more than 2^8
+    const float m_new = (m == -INFINITY || mx > m + kTcRescale) ? fmaxf(m, mx) : m;
+    const float alpha = m_new == m ? 1.f : (m == -INFINITY ? 0.f : fast_exp2(m - m_new));
+    if (k >= kTcGroups && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
+      float ov[32];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; h2++) {
+        tmem_ld32(tO + 32 * h2, ov);
+#pragma unroll
+        for (int d = 0; d < 32; d++) ov[d] *= alpha;
+        tmem_st32(tO + 32 * h2, ov);
+      }
+      tmem_st1(tL, tmem_ld1(tL) * alpha);
+    }
+    m = m_new;
+    const float m_use = m == -INFINITY ? 0.f : m;
+    // ---- P row (f16) into this group's canonical A tile, 8 keys per 16-byte
+    // chunk: p = 2^(s * scale - m) in f32, rounded to f16
+#pragma unroll
+    for (int c8 = 0; c8 < 8; c8++) {
+      uint32_t pw4[4];
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const int c = c8 * 8 + 2 * e;
+        const float x0 = c < 32 ? s0[c] : s1[c - 32], x1 = c + 1 < 32 ? s0[c + 1] : s1[c - 31];
+        pw4[e] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
+      }
+      *reinterpret_cast<uint4*>(smem + sP + canon(r, c8 * 16)) = make_uint4(pw4[0], pw4[1], pw4[2], pw4[3]);
+    }
+    // ---- V tile E4M3 -> f16, transposed into this group's canonical B tile
+    // (dims x keys). Warp w of the group converts key groups 2w, 2w+1 (8 keys
+    // each) x 8 groups of 16 dims.
+    {
+      const int wg = warp & 3;
+      const uint32_t vs = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
+#pragma unroll
+      for (int it = 0; it < 4; it++) {
+        const int a8 = 2 * wg + (it >> 1);   // key group
+        const int cbase = (it & 1) * 4;      // first 16-dim group of this x4
+        uint32_t rg[4];
+        // matrix mi = lane >> 3: keys a8*8 + (lane & 7), bytes 16 (cbase + mi) .. +15
+        ldsm_x4(rg, vs + (a8 * 8 + (lane & 7)) * kTcVPitch + (cbase + (lane >> 3)) * 16);
+        // rg[mi]: key a8*8 + lane/4, dims 16 (cbase+mi) + 4 (lane%4) + {0,1,2,3}
+        uint32_t lo4[4], hi4[4];
+#pragma unroll
+        for (int mi = 0; mi < 4; mi++) {
+          lo4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] & 0xFFFFu));  // dims +0, +1
+          hi4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] >> 16));      // dims +2, +3
+        }
+        // stored matrix jm (lanes 8jm..8jm+7 give its rows): {lo, hi} of block 2*half + (jm >> 1);
+        // its row cc holds dim 16 c16 + 4 (cc >> 1) + 2 (jm & 1) + (cc & 1) for the 8 keys
+        const int jm = lane >> 3, cc = lane & 7;
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          const int c16 = cbase + half * 2 + (jm >> 1);
+          const int d = 16 * c16 + 4 * (cc >> 1) + 2 * (jm & 1) + (cc & 1);
+          stsm_x4_trans(sb + sVT + canon(d, a8 * 16), lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1],
+                        hi4[half * 2 + 1]);
+        }
+      }
+    }
+    fence_proxy_async();  // P and V^T, written through the generic proxy, for the MMA
+    tc_fence_before();
+    mbar_arrive(p_ready(jw));
+    last = k;
+  }
+  // this group's O is complete once its last PV has
+  if (ok && last >= 0) {
+    const bool w3 = mbar_wait(pv_done(jw), (last >> 1) & 1);
+    if (!__all_sync(0xffffffffu, w3)) ok = false;
+    tc_fence_after();
+  }
+  if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
+
+  // ---- merge the two groups (group 1 hands (m, l) over), write the split
+  float* xml = reinterpret_cast<float*>(smem + kTcX);
+  if (jw == 1) xml[r] = m;
+  tc_fence_before();
+  named_bar_sync(3, kTcGroups * kTcRows);
+  tc_fence_after();
+  if (jw == 0) {
+    const bool has0 = ok && ntiles >= 1, has1 = ok && ntiles >= 2;  // groups that ran a PV
+    const float m1 = xml[r];
+    const float l = has0 ? tmem_ld1(t_lane + tc_col_o(0) + 128) : 0.f;
+    const float l1 = has1 ? tmem_ld1(t_lane + tc_col_o(1) + 128) : 0.f;
+    const float M = fmaxf(m, m1);
+    const float f0 = m == -INFINITY ? 0.f : fast_exp2(m - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+    const float L = l * f0 + l1 * f1;
+    const float vscale = a.scaled ? *a.v_scale : 1.0f;
+    const float inv = L > 0.f ? vscale / L : 0.f;
+    const int rows = a.L * kNumQHeads;
+    const int row = ti * kNumQHeads + head;
+    float* orow = a.o_part + ((int64_t)wk.slot * rows + row) * kHeadDim;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; h2++) {
+      float o0[32], o1[32];
+      if (has0) tmem_ld32(t_lane + tc_col_o(0) + 64 * g + 32 * h2, o0);
+      if (has1) tmem_ld32(t_lane + tc_col_o(1) + 64 * g + 32 * h2, o1);
+      if (live) {
+#pragma unroll
+        for (int d = 0; d < 32; d += 4) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; e++)
+            v[e] = ((has0 ? o0[d + e] * f0 : 0.f) + (has1 ? o1[d + e] * f1 : 0.f)) * inv;
+          *reinterpret_cast<float4*>(orow + 32 * h2 + d) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+      }
+    }
+    if (live) a.lse_part[(int64_t)wk.slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
+  }
+  tc_fence_before();
+  named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // TMEM reads done: the MMA warp may free it
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  if (num_work == 0) return cudaSuccess;
+  if (a.L < 2 || a.L > 8) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_work);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a);
+}
+
+int decode_tc_ctas_per_sm() {
+  int nb = 0;
+  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_tc_kernel, kTcThreads, kTcSmem) != cudaSuccess)
+    return 0;
+  return nb;
+}
+
+}  // namespace okc

@@ -90,7 +90,8 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return OKC_ERR_CUDA;
-  const int per_sm = decode_ctas_per_sm(L);
+  const bool use_tc = L >= 2 && L <= 8;  // the default plan's kernel choice
+  const int per_sm = decode_ctas_per_sm(L, use_tc);
   if (per_sm <= 0) return OKC_ERR_CUDA;
   int64_t nvis[kMaxBatch];
   int64_t total = 0;
@@ -175,6 +176,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   int shift = 0;
   while ((1 << shift) < c.page_size) shift++;
   DecodeArgs d = {};
+  d.tc = use_tc ? 1 : 0;
   d.q8 = q_fp8;
   d.kc = k_cache;
   d.vc = v_cache;

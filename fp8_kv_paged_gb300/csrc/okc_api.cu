@@ -167,12 +167,17 @@ okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_att
   return OKC_OK;
 }
 
+// Step 4 of a 2..8-token block runs on the tcgen05 kernel unless the plan says not to.
+bool use_tc(const okc_attn_config* c, const okc_plan_options* o) {
+  return c->q_len >= 2 && c->q_len <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
+}
+
 int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count_out) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
   // the occupancy query also raises the kernels' shared-memory limit: always run it
-  const int occ = okc::decode_ctas_per_sm(c->q_len);
+  const int occ = okc::decode_ctas_per_sm(c->q_len, use_tc(c, o));
   if (occ <= 0) return -1;
   const int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : occ;
   if (sm_count_out) *sm_count_out = sms;
@@ -244,6 +249,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
+  p->tc = use_tc(cfg, opts);
   // softmax scale: the float32 value of sm_scale * qk_scale_factor, in base 2
   const float scale = (float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
   p->scale_log2 = (float)((double)scale * 1.4426950408889634);
@@ -354,6 +360,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
   const bool scaled = c.kv_scale != 1.f;
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
   okc::DecodeArgs a = {};
+  a.tc = plan->tc ? 1 : 0;
   a.q8 = q_fp8;
   a.kc = k_cache;
   a.vc = v_cache;

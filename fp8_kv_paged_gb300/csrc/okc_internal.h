@@ -77,6 +77,7 @@ struct DecodeArgs {
   const uint16_t* weight;   // norm-gate weight bf16 [64] or null
   uint16_t* out;            // bf16 [T, Hq*64]
   float eps;
+  int32_t tc;               // 1: q_len 2..8 runs on the tcgen05 kernel (decode_tc.cu)
 };
 
 struct CombineArgs {
@@ -105,6 +106,7 @@ struct okc_attn_plan_s {
   okc::ReqInfo* d_req;
   int32_t* d_tickets;  // the fused step's per-request arrival counters
   uint8_t* d_q8;       // the fused step's q for q_len > 1 (three launches)
+  bool tc;             // decode on the tcgen05 kernel (q_len 2..8)
   int device;
   int sm_count;
   bool pdl;
@@ -122,8 +124,12 @@ cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaS
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, float* table,
                               cudaStream_t s);
-// Resident CTAs per SM of the decode kernels chosen for q_len L, the lower of
-// the three-call and the fused variant (0 on error).
-int decode_ctas_per_sm(int L);
+// Resident CTAs per SM of the decode kernels chosen for q_len L (tc: the
+// tcgen05 kernel for q_len 2..8), the lower of the three-call and the fused
+// variant (0 on error).
+int decode_ctas_per_sm(int L, bool tc);
+// The tcgen05 decode kernel for q_len 2..8 (decode_tc.cu).
+cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
+int decode_tc_ctas_per_sm();
 
 }  // namespace okc

@@ -86,11 +86,14 @@ typedef struct okc_attn_config {
 /* Optional plan knobs. Pass NULL for the defaults (all zero). */
 typedef struct okc_plan_options {
   int32_t chunk_keys;      /* keys per split work item; 0 = the built-in heuristic, else >= 16 */
-  int32_t flags;           /* OKC_PLAN_NO_PDL: launch the kernels without programmatic dependent launch */
+  int32_t flags;           /* OKC_PLAN_NO_PDL: launch the kernels without programmatic dependent launch;
+                              OKC_PLAN_NO_TCGEN05: q_len 2..8 decodes with the warp-level MMA kernel
+                              instead of the tcgen05 one */
   int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
   int32_t reserved;
 } okc_plan_options;
 #define OKC_PLAN_NO_PDL 0x1
+#define OKC_PLAN_NO_TCGEN05 0x2
 
 /* Sizes of the buffers a plan needs. All byte counts are multiples of 256. */
 typedef struct okc_attn_sizes {

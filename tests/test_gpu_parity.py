@@ -121,3 +121,22 @@ def test_plan_lengths_longer_than_device_lengths(fused):
     plan_seq = inp["seq_lens"] + 37
     full_check(cfg, inp, plan_seq=plan_seq, fused=fused)
     full_check(cfg, inp, opts={"chunk_keys": 96}, plan_seq=plan_seq, fused=fused)
+
+
+@pytest.mark.parametrize("seq,L,P,kv_scale", [
+    ([100, 300], 8, 64, 0.5),
+    ([2100, 2600, 4000, 70], 8, 64, 0.5),
+    ([50, 900, 2047, 2048, 2049], 2, 1, 1.0),
+    ([0, 1, 63, 64, 65], 4, 16, 1.0),
+    ([5000, 3], 6, 64, 0.5),
+])
+def test_verify_block_both_decode_kernels(seq, L, P, kv_scale):
+    """Blocks of 2..8 tokens decode on the tcgen05 kernel by default and on the
+    warp-level MMA kernel with OKC_PLAN_NO_TCGEN05: both within the bounds
+    against the oracle, with forced split sizes too."""
+    import fp8_kv_paged_gb300 as okc
+    cfg = W.config("verify_block", batch=len(seq), q_len=L, page_size=P, kv_scale=kv_scale, seq=("list", seq))
+    inp = W.generate(cfg)
+    for flags in (0, okc.PLAN_NO_TCGEN05):
+        full_check(cfg, inp, opts={"flags": flags} if flags else None)
+        full_check(cfg, inp, opts={"flags": flags, "chunk_keys": 100})
