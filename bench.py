@@ -319,7 +319,7 @@ def main():
     for s_ in sets:
         step_np.run(s_, eps=inp["eps"], stream=stream)
     stream.synchronize()
-    one_launch = fused and cfg["q_len"] == 1  # okc_attn_step runs the three kernels for q_len > 1
+    one_launch = fused and step.sizes["step_kernels"] == 1  # the form okc_attn_step takes for this plan
     if one_launch:
         def one_kernel(i):
             s_ = sets[i % n_sets]

@@ -20,12 +20,15 @@ __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_attn_step",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
-           "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "EXPORTED_SYMBOLS"]
+           "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
+           "EXPORTED_SYMBOLS"]
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
 DEVERR_CACHE_LOC, DEVERR_POSITION, DEVERR_PAGE, DEVERR_LENGTHS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 PLAN_NO_PDL = 0x1
 PLAN_NO_TCGEN05 = 0x2
+PLAN_STEP_ONE_LAUNCH = 0x4
+PLAN_STEP_THREE_LAUNCHES = 0x8
 
 EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
@@ -58,7 +61,7 @@ class _Sizes(ctypes.Structure):
     _fields_ = [("workspace_bytes", ctypes.c_size_t), ("q_fp8_bytes", ctypes.c_size_t),
                 ("o_partial_bytes", ctypes.c_size_t), ("lse_partial_bytes", ctypes.c_size_t),
                 ("num_work", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
-                ("max_chunks", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_chunks", ctypes.c_int32), ("step_kernels", ctypes.c_int32)]
 
 
 _lib = None
@@ -142,7 +145,7 @@ def _options(opts: dict | None):
 
 
 def _sizes_dict(z: _Sizes) -> dict:
-    return {f: getattr(z, f) for f, _ in _Sizes._fields_ if f != "reserved"}
+    return {f: getattr(z, f) for f, _ in _Sizes._fields_}
 
 
 def okc_attn_plan_sizes(cfg: dict, seq_lens_host, opts: dict | None = None) -> dict:

@@ -150,20 +150,37 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   return OKC_OK;
 }
 
+// Kernels okc_attn_step launches: 1 (the fused step kernel, q_len 1) when the
+// work list fills at least half of the resident CTA slots with chunks of at
+// most 2048 keys (measured faster there: the merge tail is short against the
+// step), else 3 (prepare, decode, combine: faster for very small batches,
+// where the kernels' latencies overlap under programmatic launch, and for long
+// chunks, where the separate merge overlaps the decode's tail).
+int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_options* o, int slots) {
+  if (c->q_len != 1) return 3;
+  const int flags = o ? o->flags : 0;
+  if (flags & OKC_PLAN_STEP_THREE_LAUNCHES) return 3;
+  if (flags & OKC_PLAN_STEP_ONE_LAUNCH) return 1;
+  int64_t max_chunk = 0;
+  for (const ReqInfo& q : s.req) max_chunk = std::max<int64_t>(max_chunk, q.chunk_keys);
+  return (2 * (int64_t)s.work.size() >= slots && max_chunk <= 2048) ? 1 : 3;
+}
+
 okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {
   const int64_t T = (int64_t)c->batch * c->q_len;
   const int64_t W = (int64_t)s.work.size();
   const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
   z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo)) +
-                      round_up(c->batch * sizeof(int32_t)) +  // + the fused step's arrival counters
-                      (c->q_len > 1 ? round_up(T * c->num_q_heads * c->head_dim) : 0);  // + its q (q_len > 1)
+                      round_up(c->batch * sizeof(int32_t)) +  // + the one-launch step's arrival counters
+                      round_up(T * c->num_q_heads * c->head_dim);  // + q for the three-launch step
   z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
   z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
   z->lse_partial_bytes = round_up(W * rows * sizeof(float));
   z->num_work = (int32_t)W;
   z->num_tokens = (int32_t)T;
   z->max_chunks = s.max_chunks;
+  z->step_kernels = 3;
   return OKC_OK;
 }
 
@@ -211,7 +228,9 @@ okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_le
   SplitResult s;
   st = make_splits(cfg, seq_lens_host, opts, slots, &s);
   if (st != OKC_OK) return st;
-  return compute_sizes(cfg, s, sizes);
+  st = compute_sizes(cfg, s, sizes);
+  sizes->step_kernels = step_kernels(cfg, s, opts, slots);
+  return st;
 }
 
 okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
@@ -230,6 +249,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   if (st != OKC_OK) return st;
   okc_attn_sizes z;
   compute_sizes(cfg, s, &z);
+  z.step_kernels = step_kernels(cfg, s, opts, slots);
   if (workspace_bytes < z.workspace_bytes) return OKC_ERR_WORKSPACE;
 
   okc_attn_plan_s* p = new (std::nothrow) okc_attn_plan_s();
@@ -245,7 +265,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
   p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
   p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
-  p->d_q8 = cfg->q_len > 1 ? reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(cfg->batch * sizeof(int32_t)) : nullptr;
+  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(cfg->batch * sizeof(int32_t));
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
@@ -475,12 +495,11 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.out = static_cast<uint16_t*>(out);
   a.eps = eps;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
-  if (c.q_len == 1) {
+  if (plan->sizes.step_kernels == 1) {
     cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, str);
     return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
   }
-  // q_len > 1: the three kernels (measured faster than the single launch for a
-  // verify block), with q in the plan workspace
+  // the three kernels, with q in the plan workspace
   okc_status st = okc_prepare_qkv(plan, qkv, positions, cache_loc, k_cache, v_cache, k_scale, v_scale, rope_table,
                                   rope_positions, plan->d_q8, stream);
   if (st != OKC_OK) return st;

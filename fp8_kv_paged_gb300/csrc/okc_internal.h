@@ -105,7 +105,7 @@ struct okc_attn_plan_s {
   okc::WorkItem* d_work;
   okc::ReqInfo* d_req;
   int32_t* d_tickets;  // the fused step's per-request arrival counters
-  uint8_t* d_q8;       // the fused step's q for q_len > 1 (three launches)
+  uint8_t* d_q8;       // q of okc_attn_step when it runs the three kernels
   bool tc;             // decode on the tcgen05 kernel (q_len 2..8)
   int device;
   int sm_count;

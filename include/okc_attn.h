@@ -88,12 +88,16 @@ typedef struct okc_plan_options {
   int32_t chunk_keys;      /* keys per split work item; 0 = the built-in heuristic, else >= 16 */
   int32_t flags;           /* OKC_PLAN_NO_PDL: launch the kernels without programmatic dependent launch;
                               OKC_PLAN_NO_TCGEN05: q_len 2..8 decodes with the warp-level MMA kernel
-                              instead of the tcgen05 one */
+                              instead of the tcgen05 one;
+                              OKC_PLAN_STEP_ONE_LAUNCH / OKC_PLAN_STEP_THREE_LAUNCHES: force the form
+                              of okc_attn_step at q_len 1 (default: chosen by the plan) */
   int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
   int32_t reserved;
 } okc_plan_options;
 #define OKC_PLAN_NO_PDL 0x1
 #define OKC_PLAN_NO_TCGEN05 0x2
+#define OKC_PLAN_STEP_ONE_LAUNCH 0x4
+#define OKC_PLAN_STEP_THREE_LAUNCHES 0x8
 
 /* Sizes of the buffers a plan needs. All byte counts are multiples of 256. */
 typedef struct okc_attn_sizes {
@@ -104,7 +108,8 @@ typedef struct okc_attn_sizes {
   int32_t num_work;          /* split work items of this step */
   int32_t num_tokens;        /* T = B*L */
   int32_t max_chunks;        /* largest number of splits of one request */
-  int32_t reserved;
+  int32_t step_kernels;      /* kernels okc_attn_step launches: 1 (one fused kernel, q_len 1 only)
+                                or 3 (prepare, decode, combine) */
 } okc_attn_sizes;
 
 typedef struct okc_attn_plan_s* okc_attn_plan_t;
@@ -213,9 +218,12 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
  * token's key computes that K/V row, uses it in place and writes it to the
  * cache at cache_loc; the last CTA of each request to finish (an atomic ticket
  * in the plan workspace, reset after use; no CTA waits on another) merges the
- * request's splits and writes `out`. For q_len > 1 (a verify block) the call
- * runs the three kernels instead (measured faster there), keeping q in the
- * plan workspace; either way the results equal the three calls' bit for bit.
+ * request's splits and writes `out`. The plan chooses this one-kernel form for
+ * q_len 1 when its work list fills at least half of the GPU's resident CTA
+ * slots with chunks of at most 2048 keys (sizes.step_kernels == 1, or forced by
+ * OKC_PLAN_STEP_ONE_LAUNCH); otherwise, and always for q_len > 1, the call runs
+ * the three kernels, keeping q in the plan workspace. Either way the results
+ * equal the three calls' bit for bit.
  * Arguments: those of the three calls, minus q_fp8. cache_loc[t] must be the
  * page-table row of token t's position (the kernel uses the computed row
  * directly instead of reading it back).

@@ -34,6 +34,8 @@ def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None
     plan_seq: host lengths the plan is made with (default: the inputs' own)."""
     import fp8_kv_paged_gb300 as okc
     d = dev_inp if dev_inp is not None else to_device(cfg, inp)
+    if fused:  # the one-kernel form wherever it exists (q_len 1), whatever the plan would choose
+        opts = dict(opts or {}, flags=(opts or {}).get("flags", 0) | okc.PLAN_STEP_ONE_LAUNCH)
     step = okc.AttnStep(cfg, inp["seq_lens"] if plan_seq is None else plan_seq, opts=opts)
     out = step.run_fused(d, eps=inp["eps"]) if fused else step.run(d, eps=inp["eps"])
     torch.cuda.synchronize()

@@ -65,7 +65,8 @@ def test_fused_repeated_launches_reuse_tickets():
     cfg = W.config("sliding_decode", batch=6, seq=("uniform", 1500, 2600))
     inp = W.generate(cfg)
     d = to_device(cfg, inp)
-    step = okc.AttnStep(cfg, inp["seq_lens"], opts={"chunk_keys": 256})
+    step = okc.AttnStep(cfg, inp["seq_lens"], opts={"chunk_keys": 256, "flags": okc.PLAN_STEP_ONE_LAUNCH})
+    assert step.sizes["step_kernels"] == 1
     outs = []
     for _ in range(3):
         outs.append(step.run_fused(d, eps=inp["eps"]).clone())
@@ -73,3 +74,22 @@ def test_fused_repeated_launches_reuse_tickets():
     assert step.errors() == 0
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+def test_step_form_chosen_by_the_plan():
+    """q_len 1 steps that fill the GPU with short chunks run as one kernel; very
+    small batches, long chunks and verify blocks as three; the flags override."""
+    import fp8_kv_paged_gb300 as okc
+    sliding = W.config("sliding_decode")
+    seq = W.generate(sliding)["seq_lens"]
+    assert okc.okc_attn_plan_sizes(sliding, seq)["step_kernels"] == 1
+    assert okc.okc_attn_plan_sizes(sliding, seq, {"flags": okc.PLAN_STEP_THREE_LAUNCHES})["step_kernels"] == 3
+    tiny = W.config("tiny_sliding_decode")
+    tseq = W.generate(tiny)["seq_lens"]
+    assert okc.okc_attn_plan_sizes(tiny, tseq)["step_kernels"] == 3
+    assert okc.okc_attn_plan_sizes(tiny, tseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 1
+    full = dict(W.config("full_decode_32k"), max_pages=32769, num_pages=64 * 32769)
+    assert okc.okc_attn_plan_sizes(full, np.full(64, 32768, np.int32))["step_kernels"] == 3
+    verify = W.config("verify_block")
+    vseq = W.generate(verify)["seq_lens"]
+    assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
