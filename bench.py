@@ -41,6 +41,13 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per step"
+# DRAM bytes (read + write) per launch of a step's dominant kernel, from one ncu
+# capture of that kernel on that workload (dram__bytes_read.sum +
+# dram__bytes_write.sum); a kernel changed since its capture has no entry.
+NCU_TRAFFIC = {
+    ("sliding_decode", "decode_kernel<fused step>"): 33.081088e6 + 11.008e3,
+    ("verify_block", "decode_tc_kernel"): 17.211648e6 + 0.0,
+}
 WORKLOAD = "sliding_decode"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -123,6 +130,28 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+# ---- replicas (N > 1): each rank runs its own independent batch; no data-path collective
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s batch: independent requests per replica."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the slowest replica's time); x itself at world 1."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every replica's tokens over the slowest replica's step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
 
 
 def cpu_oracle_run(cfg, inp, budget_s: float, max_steps: int | None = None):
@@ -234,7 +263,7 @@ def main():
     okc.build()
 
     cfg = W.config(args.workload)
-    inp = W.generate(cfg, seed=cfg["seed"] + 7919 * rank)
+    inp = W.generate(cfg, seed=rank_seed(cfg["seed"], rank))
     T = cfg["batch"] * cfg["q_len"]
     kvb = kv_bytes(cfg, inp["seq_lens"])
 
@@ -296,11 +325,7 @@ def main():
             ev1.record(stream)
         barrier()
         w1 = time.time()
-        ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t_ = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t_, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t_.item())
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
         return ms / steps_total, w0, w1
 
     def barrier():
@@ -334,7 +359,7 @@ def main():
             okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
                                 s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
                                 s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
-        kname = "decode_kernel"
+        kname = "decode_tc_kernel" if 2 <= cfg["q_len"] <= 8 else "decode_kernel"
     kernel_ms, _, _ = timed(one_kernel, max(R, min(args.steps, 20 * R)), 3)
     kernel_us = 1000.0 * kernel_ms
     clk = clocks.stop(t_wall0, t_wall1)
@@ -350,14 +375,14 @@ def main():
                 step.run(sets[i % n_sets], eps=inp["eps"], stream=stream)
         oms, _, _ = timed(run_other, max(R, min(args.steps, 20 * R)), 3)
         other = {"path": "fused" if other_fused else "three_call", "ms_per_step": oms,
-                 "value": T * world / (oms * 1e-3)}
+                 "value": job_throughput(T, world, oms)}
 
     # end to end through the public API with host buffers
     e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(args.steps, 200), fused=fused)
 
     peak, peak_kind = measured_peak_hbm()
     achieved = kvb / (kernel_us * 1e-6) / 1e9
-    value = T * world / (ms_step * 1e-3)
+    value = job_throughput(T, world, ms_step)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -373,7 +398,8 @@ def main():
         "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
         "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": NCU_TRAFFIC.get((args.workload, kname)), "algorithmic_bytes": kvb,
                      "peak_source": peak_kind, "avg_launch_us": kernel_us},
         "clocks": clk,
         "e2e": e2e,
