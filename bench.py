@@ -47,6 +47,8 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 NCU_TRAFFIC = {
     ("sliding_decode", "decode_kernel<fused step>"): 33.081088e6 + 11.008e3,
     ("verify_block", "decode_tc_kernel"): 17.211648e6 + 0.0,
+    ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
+    ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
 }
 WORKLOAD = "sliding_decode"
 FALLBACK_HBM_GBS = 6800.0
