@@ -46,7 +46,6 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
     ("sliding_decode", "decode_kernel<fused step>"): 33.081088e6 + 11.008e3,
-    ("verify_block", "decode_tc_kernel"): 17.211648e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
     ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
 }
@@ -346,7 +345,8 @@ def main():
     for s_ in sets:
         step_np.run(s_, eps=inp["eps"], stream=stream)
     stream.synchronize()
-    one_launch = fused and step.sizes["step_kernels"] == 1  # the form okc_attn_step takes for this plan
+    step_kernels = step.sizes["step_kernels"]  # the form okc_attn_step takes for this plan
+    one_launch = fused and step_kernels == 1
     if one_launch:
         def one_kernel(i):
             s_ = sets[i % n_sets]
@@ -393,7 +393,7 @@ def main():
         "config": {"workload": args.workload, "batch": cfg["batch"], "q_len": cfg["q_len"],
                    "page_size": cfg["page_size"], "window": cfg["window"],
                    "rope_theta": cfg["rope_theta"], "kv_bytes_per_step": kvb,
-                   "path": ("okc_attn_step (one launch)" if one_launch else "okc_attn_step (three kernels)")
+                   "path": "okc_attn_step (%d kernel%s)" % (step_kernels, "" if step_kernels == 1 else "s")
                    if fused else "three calls",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
@@ -405,7 +405,7 @@ def main():
                      "peak_source": peak_kind, "avg_launch_us": kernel_us},
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": (1 if one_launch else 3) * args.steps,
+        "gpu_launches": (step_kernels if fused else 3) * args.steps,
     }
     if other:
         line["compare"] = other

@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
     {
       const int wg = warp & 3;
       const uint32_t vs = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
-#pragma unroll
+#pragma unroll 1
       for (int it = 0; it < 4; it++) {
         const int a8 = 2 * wg + (it >> 1);   // key group
         const int cbase = (it & 1) * 4;      // first 16-dim group of this x4
