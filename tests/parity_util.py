@@ -29,12 +29,14 @@ def to_device(cfg: dict, inp: dict, device="cuda", rope_positions: int | None = 
 
 
 def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None = None,
-            fused: bool = False, plan_seq=None) -> dict:
-    """One step through the three calls (fused=False) or okc_attn_step (fused=True).
-    plan_seq: host lengths the plan is made with (default: the inputs' own)."""
+            fused: bool = False, plan_seq=None, plan_form: bool = False) -> dict:
+    """One step through the three calls (fused=False) or okc_attn_step (fused=True:
+    in its one-kernel form wherever that exists, or in the form the plan chooses
+    with plan_form=True). plan_seq: host lengths the plan is made with (default:
+    the inputs' own)."""
     import fp8_kv_paged_gb300 as okc
     d = dev_inp if dev_inp is not None else to_device(cfg, inp)
-    if fused:  # the one-kernel form wherever it exists (q_len 1), whatever the plan would choose
+    if fused and not plan_form:
         opts = dict(opts or {}, flags=(opts or {}).get("flags", 0) | okc.PLAN_STEP_ONE_LAUNCH)
     step = okc.AttnStep(cfg, inp["seq_lens"] if plan_seq is None else plan_seq, opts=opts)
     out = step.run_fused(d, eps=inp["eps"]) if fused else step.run(d, eps=inp["eps"])
@@ -96,8 +98,8 @@ def check_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, rows_mask: np.ndarray 
 
 
 def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, expect_errors: int = 0,
-               fused: bool = False, plan_seq=None):
-    gpu = run_gpu(cfg, inp, opts, fused=fused, plan_seq=plan_seq)
+               fused: bool = False, plan_seq=None, plan_form: bool = False):
+    gpu = run_gpu(cfg, inp, opts, fused=fused, plan_seq=plan_seq, plan_form=plan_form)
     k = inp["k_cache"].copy()
     v = inp["v_cache"].copy()
     q8, _ = oracle.prepare(cfg, inp, k, v)
@@ -108,4 +110,5 @@ def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, e
     rep["out"] = check_out(gpu["out"], ref, rows_mask)
     assert gpu["errors"] == expect_errors, f"device error word {gpu['errors']:#x}"
     rep["num_work"] = gpu["sizes"]["num_work"]
+    rep["step_kernels"] = gpu["sizes"]["step_kernels"]
     return rep

@@ -1,7 +1,9 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
-benchmark times (default plan): every written cache row and every q byte is
-compared; the bf16 output is compared on sampled query rows that the oracle
-computes one by one (all rows where that is cheap)."""
+benchmark times (okc_attn_step with the default plan, in the form the plan
+chooses) and through the three calls: every written cache row is compared
+(and every q byte on the three-call path); the bf16 output is compared on
+sampled query rows that the oracle computes one by one (all rows where that is
+cheap)."""
 import numpy as np
 import pytest
 
@@ -39,5 +41,7 @@ def test_full_size(name, n_req):
     cfg = W.config(name)
     inp = W.generate(cfg)
     mask = None if n_req is None else _rows_mask(cfg, inp, n_req, seed=cfg["seed"])
+    rep = full_check(cfg, inp, rows_mask=mask, fused=True, plan_form=True)  # as the benchmark runs it
+    print(name, "step", rep)
     rep = full_check(cfg, inp, rows_mask=mask)
-    print(name, rep)
+    print(name, "three calls", rep)

@@ -52,6 +52,8 @@ def test_forced_split_sizes(name, chunk):
     ([300, 17, 1000], 4, 256, 16),
     ([900, 33], 16, 512, 256),
     ([63, 64, 65, 127, 128, 129], 1, 64, 64),
+    ([0, 5, 3000], 1, 1, 1),                 # window 1: each query sees only its own key
+    ([0, 5, 3000], 8, 1, 16),
 ])
 def test_edge_shapes(seq, L, window, P):
     cfg = W.config("tiny_sliding_decode", batch=len(seq), q_len=L, window=window, page_size=P,
@@ -140,3 +142,36 @@ def test_verify_block_both_decode_kernels(seq, L, P, kv_scale):
     for flags in (0, okc.PLAN_NO_TCGEN05):
         full_check(cfg, inp, opts={"flags": flags} if flags else None)
         full_check(cfg, inp, opts={"flags": flags, "chunk_keys": 100})
+
+
+def test_empty_batch_is_a_no_op():
+    """B = 0: the plan is valid and every call returns OK without launching."""
+    import fp8_kv_paged_gb300 as okc
+    cfg = dict(W.config("sliding_decode"), batch=0, max_pages=1, num_pages=1)
+    seq = np.zeros(0, np.int32)
+    sizes = okc.okc_attn_plan_sizes(cfg, seq)
+    assert sizes["num_work"] == 0 and sizes["num_tokens"] == 0
+    step = okc.AttnStep(cfg, seq)
+    z8 = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    zf = torch.zeros(16, dtype=torch.float32, device="cuda")
+    zi = torch.zeros(16, dtype=torch.int32, device="cuda")
+    zl = torch.zeros(16, dtype=torch.int64, device="cuda")
+    zb = torch.zeros((1, 2304), dtype=torch.bfloat16, device="cuda")
+    d = {"qkv": zb, "positions": zl, "cache_loc": zl, "k_cache": z8, "v_cache": z8, "k_scale": zf,
+         "v_scale": zf, "page_table": zi, "cache_seqlens": zi, "cu_seqlens_q": zi, "seq_lens": zi,
+         "norm_weight": None, "rope_table": torch.zeros((4, 64), dtype=torch.float32, device="cuda")}
+    step.run(d)
+    step.run_fused(d)
+    torch.cuda.synchronize()
+    assert step.errors() == 0
+
+
+@pytest.mark.parametrize("L", [1, 4])
+def test_many_requests(L):
+    """1500 short requests: many more work items than resident CTA slots."""
+    cfg = W.config("sliding_decode", batch=1500, q_len=L, seq=("uniform", 0, 400))
+    inp = W.generate(cfg)
+    rep = full_check(cfg, inp)
+    assert rep["num_work"] >= 1500
+    full_check(cfg, inp, fused=True, plan_form=True)
+    full_check(cfg, inp, fused=True)
