@@ -4,9 +4,12 @@ One step = the whole block over one batch of the sliding-window decode
 workload: B=64, L=1, Hq=16, Hkv=2, d=64, seq_lens uniform in [1024, 8192],
 page_size 1, window 2048, RoPE theta 5e5, kv_scale 1 (synthetic, seeded).
 
-The timed step is okc_attn_step (the whole block in one launch; --path
-three_call times okc_prepare_qkv -> okc_attn_decode -> okc_attn_combine_normgate
-instead, and the line's "compare" entry times the other path the same way).
+The timed step is okc_attn_step in the form its plan chooses (one fused kernel
+for this workload; prepare, decode and combine for others: the line's
+config.path says which). --path three_call times okc_prepare_qkv ->
+okc_attn_decode -> okc_attn_combine_normgate instead, and the line's "compare"
+entry times the other path the same way. --workload picks another of the five
+workloads.
 
 Timing: W warm-up steps, then exactly K steps, replayed from CUDA graphs of
 the step's launches; consecutive steps rotate over independent copies of the

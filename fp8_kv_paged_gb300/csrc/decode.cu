@@ -7,10 +7,12 @@
 // all L query tokens, so that at page_size 1 every key is one contiguous 128-byte
 // cache row per tensor (K and V).
 //
-// Warp-specialised pipeline. One producer warp turns page-table entries into
-// cache rows and gathers them with 16-byte cp.async (eight lanes per 128-byte
-// row, so one warp instruction fetches four rows) into a ring of kStages tiles
-// of 64 keys; each tile's K and V rows land at a 144-byte pitch so that the
+// Warp-specialised pipeline. Four producer warps (16 keys of every tile each)
+// turn page-table entries into cache rows and gather them with 16-byte
+// cp.async (eight lanes per 128-byte row, so one warp instruction fetches four
+// rows) into a ring of kStages tiles of 64 keys (the first page ids are loaded
+// from the plan's key range while the device lengths load, and reloaded only
+// if they differ); each tile's K and V rows land at a 144-byte pitch so that the
 // consumers' ldmatrix reads are bank-conflict free. Each producer lane signals
 // a stage's "full" mbarrier when its copies have landed
 // (cp.async.mbarrier.arrive); consumer warps release a stage through its
@@ -42,6 +44,11 @@
 //        movmatrix transpose per 8x8 block.
 // Epilogue: warps that split the keys of a tile merge (m, l, O) through shared
 // memory; the item writes O/l (times v_scale) and its base-2 log-sum-exp.
+//
+// The FUSED variant (q_len 1, okc_attn_step in its one-kernel form) also runs
+// steps 1-3 (q from qkv in the consumers' fragment layout; the new token's K/V
+// row computed by the warp that owns its tile row and written to the cache)
+// and step 5 (the last CTA of each request merges the splits).
 #include "normgate.cuh"
 #include "okc_common.cuh"
 #include "okc_internal.h"
