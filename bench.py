@@ -443,28 +443,32 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
     op = torch.empty(sizes["o_partial_bytes"] // 4, dtype=torch.float32, device=dev)
     lp = torch.empty(sizes["lse_partial_bytes"] // 4, dtype=torch.float32, device=dev)
     out = torch.empty_like(out_host, device=dev)
+    # the step's inputs, and the plan's upload (the workspace up to its q scratch)
     h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names) + \
-        sizes["workspace_bytes"] - 256
+        sizes["workspace_bytes"] - sizes["q_fp8_bytes"]
     d2h = out_host.numel() * 2
+
+    host_io = dict(pinned, out=out_host)
+    dev_io = dict({k: dev_in[k] for k in names}, out=out)
 
     def one():
         plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
+        if fused:  # one C call: host->device copies, the step, device->host copy, synchronize
+            okc.okc_attn_step_host(plan, host_io, dev_io, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
+                                   dev_in["v_scale"], dev_in["rope_table"], dev_in["norm_weight"], inp["eps"],
+                                   op, lp, stream)
+            plan.close()
+            return
         for k in names:
             dev_in[k].copy_(pinned[k], non_blocking=True)
-        if fused:
-            okc.okc_attn_step(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
-                              dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
-                              dev_in["page_table"], dev_in["cache_seqlens"], dev_in["cu_seqlens_q"],
-                              dev_in["seq_lens"], dev_in["norm_weight"], inp["eps"], op, lp, out, stream)
-        else:
-            okc.okc_prepare_qkv(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
-                                dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
-                                q8, stream)
-            okc.okc_attn_decode(plan, q8, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
-                                dev_in["v_scale"], dev_in["page_table"], dev_in["cache_seqlens"],
-                                dev_in["cu_seqlens_q"], dev_in["seq_lens"], op, lp, stream)
-            okc.okc_attn_combine_normgate(plan, op, lp, dev_in["qkv"], dev_in["norm_weight"], inp["eps"], out,
-                                          stream)
+        okc.okc_prepare_qkv(plan, dev_in["qkv"], dev_in["positions"], dev_in["cache_loc"], dev_in["k_cache"],
+                            dev_in["v_cache"], dev_in["k_scale"], dev_in["v_scale"], dev_in["rope_table"],
+                            q8, stream)
+        okc.okc_attn_decode(plan, q8, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
+                            dev_in["v_scale"], dev_in["page_table"], dev_in["cache_seqlens"],
+                            dev_in["cu_seqlens_q"], dev_in["seq_lens"], op, lp, stream)
+        okc.okc_attn_combine_normgate(plan, op, lp, dev_in["qkv"], dev_in["norm_weight"], inp["eps"], out,
+                                      stream)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
         plan.close()
@@ -479,7 +483,7 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
         el = time.perf_counter() - t0
     return {"value": T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / steps, "steps": steps,
-            "api": "okc_attn_plan + okc_attn_step" if fused else "okc_attn_plan + three calls"}
+            "api": "okc_attn_plan + okc_attn_step_host" if fused else "okc_attn_plan + three calls"}
 
 
 if __name__ == "__main__":

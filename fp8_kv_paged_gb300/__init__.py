@@ -18,7 +18,7 @@ from . import build as _build_mod
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
-           "okc_attn_decode_combine_noalloc", "okc_attn_step",
+           "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
            "EXPORTED_SYMBOLS"]
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
-    "okc_attn_step",
+    "okc_attn_step", "okc_attn_step_host",
 ]
 
 
@@ -55,6 +55,13 @@ class _Config(ctypes.Structure):
 class _Options(ctypes.Structure):
     _fields_ = [("chunk_keys", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class _HostStep(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("qkv_host", "positions_host", "cache_loc_host", "cache_seqlens_host", "cu_seqlens_q_host",
+                 "seq_lens_host", "page_table_host", "out_host", "qkv", "positions", "cache_loc",
+                 "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table", "out")]
 
 
 class _Sizes(ctypes.Structure):
@@ -108,6 +115,8 @@ def load(path: str | None = None):
     lib.okc_attn_combine_normgate.argtypes = [P, P, P, P, P, f32, P, P]
     lib.okc_attn_step.restype = st
     lib.okc_attn_step.argtypes = [P] * 9 + [i32] + [P] * 5 + [f32, P, P, P, P]
+    lib.okc_attn_step_host.restype = st
+    lib.okc_attn_step_host.argtypes = [P, ctypes.POINTER(_HostStep)] + [P] * 5 + [i32, P, f32, P, P, P]
     lib.okc_attn_decode_combine_noalloc.restype = st
     lib.okc_attn_decode_combine_noalloc.argtypes = [ctypes.POINTER(_Config), P] + [P] * 11 + [f32, P, P]
     _lib = lib
@@ -243,6 +252,23 @@ def okc_attn_step(plan: Plan, qkv, positions, cache_loc, k_cache, v_cache, k_sca
                                 _ptr(norm_weight), eps, _ptr(o_partial), _ptr(lse_partial), _ptr(out),
                                 _stream(stream)),
            "okc_attn_step")
+
+
+STEP_IO = ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table", "out")
+
+
+def okc_attn_step_host(plan: Plan, host: dict, dev: dict, k_cache, v_cache, k_scale, v_scale, rope_table,
+                       norm_weight, eps, o_partial, lse_partial, stream=None):
+    """One step from host buffers (see the header): host / dev map each name of
+    STEP_IO to a host tensor (pinned for asynchronous copies) and the device
+    buffer it is copied to; returns once host["out"] holds the output."""
+    io = _HostStep(**{k + "_host": (None if host.get(k) is None else host[k].data_ptr()) for k in STEP_IO},
+                   **{k: (None if dev.get(k) is None else dev[k].data_ptr()) for k in STEP_IO})
+    npos = 0 if rope_table is None else rope_table.shape[0]
+    _check(load().okc_attn_step_host(plan.handle, ctypes.byref(io), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(rope_table), npos, _ptr(norm_weight), eps,
+                                     _ptr(o_partial), _ptr(lse_partial), _stream(stream)),
+           "okc_attn_step_host")
 
 
 def okc_attn_decode_combine_noalloc(cfg: dict, seq_lens_host, q_fp8, k_cache, v_cache, k_scale,

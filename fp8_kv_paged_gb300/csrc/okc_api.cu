@@ -3,7 +3,10 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <tuple>
 #include <vector>
 
 #include "okc_common.cuh"
@@ -189,12 +192,25 @@ bool use_tc(const okc_attn_config* c, const okc_plan_options* o) {
   return c->q_len >= 2 && c->q_len <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
 }
 
+// Resident decode CTAs per SM for (device, q_len, kernel family), queried once
+// per key: the query also raises the kernels' shared-memory limit on the device.
+int cached_ctas_per_sm(int dev, int L, bool tc) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, bool>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(dev, L, tc);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const int occ = okc::decode_ctas_per_sm(L, tc);
+  if (occ > 0) cache[key] = occ;
+  return occ;
+}
+
 int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count_out) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  // the occupancy query also raises the kernels' shared-memory limit: always run it
-  const int occ = okc::decode_ctas_per_sm(c->q_len, use_tc(c, o));
+  const int occ = cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
   if (occ <= 0) return -1;
   const int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : occ;
   if (sm_count_out) *sm_count_out = sms;
@@ -274,13 +290,18 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   const float scale = (float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
   p->scale_log2 = (float)((double)scale * 1.4426950408889634);
 
+  // One upload of the workspace's head: the zeroed error word, the work list,
+  // the request table and the zeroed arrival counters, as laid out on the device.
+  const size_t up_bytes = static_cast<size_t>(p->d_q8 - ws);
+  p->upload.assign(up_bytes, 0);
+  if (!p->work.empty())
+    std::memcpy(p->upload.data() + (reinterpret_cast<uint8_t*>(p->d_work) - ws), p->work.data(),
+                p->work.size() * sizeof(WorkItem));
+  if (!p->req.empty())
+    std::memcpy(p->upload.data() + (reinterpret_cast<uint8_t*>(p->d_req) - ws), p->req.data(),
+                p->req.size() * sizeof(ReqInfo));
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, okc::kWsHeader, str);
-  if (e == cudaSuccess && cfg->batch > 0) e = cudaMemsetAsync(p->d_tickets, 0, cfg->batch * sizeof(int32_t), str);
-  if (e == cudaSuccess && !p->work.empty())
-    e = cudaMemcpyAsync(p->d_work, p->work.data(), p->work.size() * sizeof(WorkItem), cudaMemcpyHostToDevice, str);
-  if (e == cudaSuccess && !p->req.empty())
-    e = cudaMemcpyAsync(p->d_req, p->req.data(), p->req.size() * sizeof(ReqInfo), cudaMemcpyHostToDevice, str);
+  cudaError_t e = cudaMemcpyAsync(ws, p->upload.data(), up_bytes, cudaMemcpyHostToDevice, str);
   if (e != cudaSuccess) {
     delete p;
     return OKC_ERR_CUDA;
@@ -507,6 +528,50 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
                        cu_seqlens_q, seq_lens, o_partial, lse_partial, stream);
   if (st != OKC_OK) return st;
   return okc_attn_combine_normgate(plan, o_partial, lse_partial, qkv, norm_weight, eps, out, stream);
+}
+
+okc_status okc_attn_step_host(okc_attn_plan_t plan, const okc_host_step* io, uint8_t* k_cache, uint8_t* v_cache,
+                              const float* k_scale, const float* v_scale, const float* rope_table,
+                              int32_t rope_positions, const void* norm_weight, float eps, float* o_partial,
+                              float* lse_partial, okc_stream stream) {
+  if (!plan || !io) return OKC_ERR_INVALID;
+  const okc_attn_config& c = plan->cfg;
+  const size_t T = (size_t)plan->sizes.num_tokens, B = (size_t)c.batch;
+  if (B > 0 && (!io->qkv_host || !io->cache_loc_host || !io->cache_seqlens_host || !io->cu_seqlens_q_host ||
+                !io->page_table_host || !io->out_host || !io->qkv || !io->cache_loc || !io->cache_seqlens ||
+                !io->cu_seqlens_q || !io->page_table || !io->out))
+    return OKC_ERR_INVALID;
+  if ((io->positions_host == nullptr) != (io->positions == nullptr) ||
+      (io->seq_lens_host == nullptr) != (io->seq_lens == nullptr))
+    return OKC_ERR_INVALID;
+  cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  const size_t width = (size_t)(2 * c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim;
+  struct Copy {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } in[] = {
+      {io->qkv, io->qkv_host, T * width * 2},
+      {io->positions, io->positions_host, T * sizeof(int64_t)},
+      {io->cache_loc, io->cache_loc_host, T * sizeof(int64_t)},
+      {io->cache_seqlens, io->cache_seqlens_host, B * sizeof(int32_t)},
+      {io->cu_seqlens_q, io->cu_seqlens_q_host, (B + 1) * sizeof(int32_t)},
+      {io->seq_lens, io->seq_lens_host, B * sizeof(int32_t)},
+      {io->page_table, io->page_table_host, B * (size_t)c.max_pages * sizeof(int32_t)},
+  };
+  if (B > 0) {
+    for (const Copy& cp : in)
+      if (cp.src && cp.bytes && cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, str) != cudaSuccess)
+        return OKC_ERR_CUDA;
+  }
+  okc_status st = okc_attn_step(plan, io->qkv, io->positions, io->cache_loc, k_cache, v_cache, k_scale, v_scale,
+                                rope_table, rope_positions, io->page_table, io->cache_seqlens, io->cu_seqlens_q,
+                                io->seq_lens, norm_weight, eps, o_partial, lse_partial, io->out, stream);
+  if (st != OKC_OK) return st;
+  const size_t out_bytes = T * (size_t)c.num_q_heads * c.head_dim * 2;
+  if (out_bytes && cudaMemcpyAsync(io->out_host, io->out, out_bytes, cudaMemcpyDeviceToHost, str) != cudaSuccess)
+    return OKC_ERR_CUDA;
+  return cudaStreamSynchronize(str) == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }
 
 }  // extern "C"

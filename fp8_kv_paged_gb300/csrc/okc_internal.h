@@ -100,6 +100,7 @@ struct okc_attn_plan_s {
   okc_attn_sizes sizes;
   std::vector<okc::WorkItem> work;
   std::vector<okc::ReqInfo> req;
+  std::vector<uint8_t> upload;  // the workspace head as uploaded (one host-to-device copy)
   void* workspace;
   unsigned* d_err;
   okc::WorkItem* d_work;

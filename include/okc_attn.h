@@ -237,6 +237,42 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
                          const int32_t* seq_lens, const void* norm_weight, float eps, float* o_partial,
                          float* lse_partial, void* out, okc_stream stream);
 
+/*
+ * One step from host buffers: the per-step inputs live in host memory (pinned
+ * memory keeps the copies asynchronous), the caches, scales, RoPE table, norm
+ * weight and scratch stay resident on the device. The call copies each host
+ * input to its device buffer, runs okc_attn_step on them, copies the output
+ * back to out_host and synchronizes `stream`: on OKC_OK the output is on the
+ * host. Device buffers are caller-owned and sized as the host ones: qkv bf16
+ * [T, (2Hq+2Hkv)*64]; positions / cache_loc int64 [T]; cache_seqlens,
+ * seq_lens int32 [B]; cu_seqlens_q int32 [B+1]; page_table int32
+ * [B, max_pages]; out bf16 [T, Hq*64]. positions (and its host copy) may be
+ * NULL when rope_theta == 0, seq_lens when unchecked; each pair is NULL
+ * together or not at all.
+ */
+typedef struct okc_host_step {
+  const void* qkv_host;
+  const int64_t* positions_host;
+  const int64_t* cache_loc_host;
+  const int32_t* cache_seqlens_host;
+  const int32_t* cu_seqlens_q_host;
+  const int32_t* seq_lens_host;
+  const int32_t* page_table_host;
+  void* out_host;
+  void* qkv;
+  int64_t* positions;
+  int64_t* cache_loc;
+  int32_t* cache_seqlens;
+  int32_t* cu_seqlens_q;
+  int32_t* seq_lens;
+  int32_t* page_table;
+  void* out;
+} okc_host_step;
+okc_status okc_attn_step_host(okc_attn_plan_t plan, const okc_host_step* io, uint8_t* k_cache, uint8_t* v_cache,
+                              const float* k_scale, const float* v_scale, const float* rope_table,
+                              int32_t rope_positions, const void* norm_weight, float eps, float* o_partial,
+                              float* lse_partial, okc_stream stream);
+
 const char* okc_status_string(okc_status status);
 
 /*

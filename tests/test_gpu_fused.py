@@ -93,3 +93,27 @@ def test_step_form_chosen_by_the_plan():
     verify = W.config("verify_block")
     vseq = W.generate(verify)["seq_lens"]
     assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
+
+
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block", "full_decode_32k"])
+def test_step_from_host_buffers(name):
+    """okc_attn_step_host: host inputs copied in, the step, the output copied
+    back: equal to okc_attn_step on device buffers, bit for bit."""
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    d = to_device(cfg, inp)
+    ref = run_gpu(cfg, inp, fused=True, plan_form=True)
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+            for k in ("positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table")}
+    host["qkv"] = torch.from_numpy(np.ascontiguousarray(inp["qkv"]).view(np.int16)).pin_memory()
+    host["out"] = torch.empty((inp["qkv"].shape[0], 1024), dtype=torch.int16).pin_memory()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    okc.okc_attn_step_host(step.plan, host, dev, d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                           d.get("rope_table"), d["norm_weight"], inp["eps"], step.o_partial, step.lse_partial)
+    assert step.errors() == 0
+    assert np.array_equal(host["out"].numpy().view(np.uint16), ref["out"])
+    assert np.array_equal(d["k_cache"].cpu().numpy(), ref["k_cache"])
