@@ -173,16 +173,25 @@ def cpu_oracle_run(cfg, inp, budget_s: float, max_steps: int | None = None):
                  seq_lens=inp["seq_lens"][bs], page_table=inp["page_table"][bs],
                  cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
         return c, d
+    oracle.step(*sub([0]))  # load and warm the library
+    # a pass over all requests sizes the sample: whole passes while they fit
+    # the budget, else the requests that fit it (estimated from one request
+    # when a whole pass would be far over the budget)
     t0 = time.perf_counter()
-    c1, d1 = sub([0])
-    oracle.step(c1, d1)
-    per_req = max(time.perf_counter() - t0, 1e-4)
-    nreq = int(max(1, min(B, budget_s / per_req)))
-    reps = 1
-    if nreq == B:
-        reps = int(max(1, budget_s / (per_req * B)))
-        if max_steps is not None:
-            reps = max(1, min(reps, max_steps))
+    oracle.step(*sub([B - 1]))
+    est = max(time.perf_counter() - t0, 1e-5) * B
+    if est > 2 * budget_s:
+        pass_s = est
+    else:
+        c, d = sub(list(range(B)))
+        t0 = time.perf_counter()
+        oracle.step(c, d)
+        pass_s = max(time.perf_counter() - t0, 1e-4)
+    nreq, reps = B, int(max(1, budget_s / pass_s))
+    if max_steps is not None:
+        reps = max(1, min(reps, max_steps))
+    if pass_s > budget_s:
+        nreq = int(max(1, B * budget_s / pass_s))
     c, d = sub(list(range(nreq)))
     t0 = time.perf_counter()
     for _ in range(reps):
@@ -247,7 +256,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", default="okc", choices=["okc", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(W.WORKLOADS))
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work in cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="fused", choices=["fused", "three_call"],
                     help="okc_attn_step (one launch) or okc_prepare_qkv + okc_attn_decode + okc_attn_combine_normgate")
