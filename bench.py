@@ -52,6 +52,7 @@ NCU_TRAFFIC = {
     ("verify_block", "decode_tc_kernel"): 17.210112e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
     ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 802.778112e6 + 7.543808e6,
 }
 WORKLOAD = "sliding_decode"
 FALLBACK_HBM_GBS = 6800.0

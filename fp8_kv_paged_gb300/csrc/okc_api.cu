@@ -155,10 +155,12 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
 
 // Kernels okc_attn_step launches: 1 (the fused step kernel, q_len 1) when the
 // work list fills at least half of the resident CTA slots with chunks of at
-// most 2048 keys (measured faster there: the merge tail is short against the
-// step), else 3 (prepare, decode, combine: faster for very small batches,
-// where the kernels' latencies overlap under programmatic launch, and for long
-// chunks, where the separate merge overlaps the decode's tail).
+// most 2048 keys, or takes more than one wave (measured faster there: the
+// merge tail is short against the step, or the first wave's merges overlap
+// the second wave), else 3 (prepare, decode, combine: faster for very small
+// batches, where the kernels' latencies overlap under programmatic launch, and
+// for one wave of long chunks, where the separate merge overlaps the decode's
+// tail).
 int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_options* o, int slots) {
   if (c->q_len != 1) return 3;
   const int flags = o ? o->flags : 0;
@@ -166,7 +168,8 @@ int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_
   if (flags & OKC_PLAN_STEP_ONE_LAUNCH) return 1;
   int64_t max_chunk = 0;
   for (const ReqInfo& q : s.req) max_chunk = std::max<int64_t>(max_chunk, q.chunk_keys);
-  return (2 * (int64_t)s.work.size() >= slots && max_chunk <= 2048) ? 1 : 3;
+  const int64_t W = (int64_t)s.work.size();
+  return (2 * W >= slots && (max_chunk <= 2048 || W > slots)) ? 1 : 3;
 }
 
 okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {

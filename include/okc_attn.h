@@ -222,7 +222,8 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
  * in the plan workspace, reset after use; no CTA waits on another) merges the
  * request's splits and writes `out`. The plan chooses this one-kernel form for
  * q_len 1 when its work list fills at least half of the GPU's resident CTA
- * slots with chunks of at most 2048 keys (sizes.step_kernels == 1, or forced by
+ * slots with chunks of at most 2048 keys or takes more than one wave of them
+ * (sizes.step_kernels == 1, or forced by
  * OKC_PLAN_STEP_ONE_LAUNCH); otherwise, and always for q_len > 1, the call runs
  * the three kernels, keeping q in the plan workspace. Either way the results
  * equal the three calls' bit for bit.

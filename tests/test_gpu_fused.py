@@ -89,7 +89,11 @@ def test_step_form_chosen_by_the_plan():
     assert okc.okc_attn_plan_sizes(tiny, tseq)["step_kernels"] == 3
     assert okc.okc_attn_plan_sizes(tiny, tseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 1
     full = dict(W.config("full_decode_32k"), max_pages=32769, num_pages=64 * 32769)
-    assert okc.okc_attn_plan_sizes(full, np.full(64, 32768, np.int32))["step_kernels"] == 3
+    assert okc.okc_attn_plan_sizes(full, np.full(64, 32768, np.int32))["step_kernels"] == 3  # one wave, long chunks
+    mixed = W.config("mixed_full_decode")
+    mseq = W.generate(mixed)["seq_lens"]
+    msz = okc.okc_attn_plan_sizes(mixed, mseq)
+    assert msz["step_kernels"] == 1 and msz["num_work"] > 456  # more than one wave
     verify = W.config("verify_block")
     vseq = W.generate(verify)["seq_lens"]
     assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
