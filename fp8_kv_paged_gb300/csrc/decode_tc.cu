@@ -379,13 +379,13 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
     const float m_new = (m == -INFINITY || mx > m + kTcRescale) ? fmaxf(m, mx) : m;
     const float alpha = m_new == m ? 1.f : (m == -INFINITY ? 0.f : fast_exp2(m - m_new));
     if (k >= kTcGroups && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
-      float ov[32];
+      float ov[16];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; h2++) {
-        tmem_ld32(tO + 32 * h2, ov);
+      for (int h4 = 0; h4 < 4; h4++) {
+        tmem_ld16(tO + 16 * h4, ov);
 #pragma unroll
-        for (int d = 0; d < 32; d++) ov[d] *= alpha;
-        tmem_st32(tO + 32 * h2, ov);
+        for (int d = 0; d < 16; d++) ov[d] *= alpha;
+        tmem_st16(tO + 16 * h4, ov);
       }
       tmem_st1(tL, tmem_ld1(tL) * alpha);
     }
