@@ -18,8 +18,9 @@ every step streams its KV rows from HBM. CUDA events on the launching stream,
 a device synchronize and a barrier on both sides, max over ranks. The step's
 dominant kernel is then timed alone (launches without programmatic overlap)
 for the roofline. `e2e` repeats the step through the public API from pinned host
-buffers: per step the plan, the host-to-device copies of the step's inputs,
-the step's calls and the device-to-host copy of the output.
+buffers: per step the plan, the step's inputs moved from host memory to the GPU
+(read in place by the kernels over the host link: the buffers are page-locked
+and mapped), the step's calls and the output written back to host memory.
 
 --impl reference times the CPU oracle (the only other implementation of the
 block here) on the host cores, on a bounded sample of the same workload.
@@ -434,9 +435,11 @@ def main():
 
 
 def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
-    """Per step: plan from host seq_lens, pinned host->device copies of the step's
-    inputs, the step (okc_attn_step, or the three calls), device->host copy of the
-    output; K steps timed on the host clock."""
+    """Per step: plan from host seq_lens, the step's inputs from pinned host
+    memory (okc_attn_step_host: read in place by the kernels; the three calls:
+    copied to device buffers first), the step, the output back in host memory;
+    K steps timed on the host clock. h2d counts the host input bytes the step
+    consumes (the kernels read only the page-table entries they need)."""
     names = ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table")
     host = W.to_torch({**inp, "k_cache": inp["k_cache"][:1], "v_cache": inp["v_cache"][:1]}, "cpu")
     pinned = {k: host[k].pin_memory() for k in names}

@@ -84,25 +84,36 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   const int64_t min_chunk = 128, kItemCost = 128;
   int64_t nmax = 1;
   for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
+  // (key counts and budgets are below 2^31: 32-bit divisions)
+  auto cdiv = [](int64_t a, int64_t b) { return (int64_t)(((uint32_t)a + (uint32_t)b - 1u) / (uint32_t)b); };
   auto items = [&](int64_t C) {
     int64_t w = 0;
-    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, (nvis[b] + C - 1) / C);
+    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, cdiv(nvis[b], C));
     return w;
   };
   int64_t Cbud = std::max<int64_t>(min_chunk, nmax);
   if (slots > 0 && B > 0) {
     double best = -1.0;
+    const int64_t cmax = std::max<int64_t>(min_chunk, nmax);  // items(cmax) = B
     for (int m = 1; m <= 4; m++) {
-      int64_t lo_c = min_chunk, hi_c = std::max<int64_t>(min_chunk, nmax);
-      while (lo_c < hi_c) {  // smallest C with items(C) <= m * slots (items(nmax) = B)
+      // smallest C in [min_chunk, cmax] with items(C) <= cap (cmax when none).
+      // Since total / C <= items(C) <= total / C + B, that C is at least
+      // ceil(total / cap) and at most ceil(total / (cap - B)) when cap > B.
+      const int64_t cap = (int64_t)m * slots;
+      int64_t lo_c = cmax, hi_c = cmax;
+      if (cap > B) {
+        lo_c = std::min(cmax, std::max(min_chunk, (total + cap - 1) / cap));
+        hi_c = std::min(cmax, std::max(lo_c, (total + cap - B - 1) / (cap - B)));
+      }
+      while (lo_c < hi_c) {
         const int64_t mid = (lo_c + hi_c) / 2;
-        if (items(mid) <= (int64_t)m * slots) hi_c = mid; else lo_c = mid + 1;
+        if (items(mid) <= cap) hi_c = mid; else lo_c = mid + 1;
       }
       const int64_t C = lo_c, W = items(C);
       int64_t biggest = 0;
       for (int b = 0; b < B; b++) {
-        const int64_t k = std::max<int64_t>(1, (nvis[b] + C - 1) / C);
-        biggest = std::max(biggest, (nvis[b] + k - 1) / k);
+        const int64_t k = std::max<int64_t>(1, cdiv(nvis[b], C));
+        biggest = std::max(biggest, cdiv(nvis[b], k));
       }
       const double mean = (double)(total + W * kItemCost) / (double)W;
       const double waves = (double)((W + slots - 1) / slots);
@@ -132,24 +143,51 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
     r->max_chunks = std::max<int>(r->max_chunks, (int)nch);
     wbase += nch;
   }
-  r->work.clear();
-  r->work.reserve((size_t)wbase);
+  // Launch order: the largest items first (the last chunk of a request may be
+  // short), ties in slot order. A request's items before its last all hold
+  // chunk_keys keys, so the order is a merge of two sorted runs: those items,
+  // request by request in (chunk_keys desc, request) order, and the last
+  // items in (keys desc, request) order. Sort words pack (2^31-1 - keys, b).
+  auto last_keys = [&](int b) {
+    const ReqInfo& q = r->req[b];
+    return nvis[b] - (int64_t)(q.nchunks - 1) * q.chunk_keys;
+  };
+  auto pack = [](int64_t keys, int b) { return ((uint64_t)(0x7FFFFFFF - keys) << 32) | (uint32_t)b; };
+  std::vector<uint64_t> run_full, run_last((size_t)B);
+  run_full.reserve((size_t)B);
   for (int b = 0; b < B; b++) {
+    if (r->req[b].nchunks > 1) run_full.push_back(pack(r->req[b].chunk_keys, b));
+    run_last[(size_t)b] = pack(last_keys(b), b);
+  }
+  std::sort(run_full.begin(), run_full.end());
+  std::sort(run_last.begin(), run_last.end());
+  r->work.resize((size_t)wbase);
+  size_t out = 0, il = 0;
+  auto emit = [&](int b, int k) {
     const ReqInfo& q = r->req[b];
     const int64_t n = (int64_t)seq[b] + L, lo = n - nvis[b];
-    for (int k = 0; k < q.nchunks; k++) {
-      const int64_t j0 = lo + (int64_t)k * q.chunk_keys, j1 = std::min<int64_t>(n, j0 + q.chunk_keys);
-      r->work.push_back(WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)j1, q.chunk_keys, q.nchunks, q.wbase});
+    const int64_t j0 = lo + (int64_t)k * q.chunk_keys, j1 = std::min<int64_t>(n, j0 + q.chunk_keys);
+    r->work[out++] = WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)j1, q.chunk_keys, q.nchunks, q.wbase};
+  };
+  auto emit_last_before = [&](uint64_t key_word, int32_t slot) {  // last items ahead of (key, slot)
+    while (il < run_last.size()) {
+      const uint64_t w = run_last[il];
+      const int b = (int)(w & 0xFFFFFFFFu);
+      const int32_t ls = r->req[b].wbase + r->req[b].nchunks - 1;
+      if ((w >> 32) > (key_word >> 32) || ((w >> 32) == (key_word >> 32) && ls > slot)) break;
+      emit(b, r->req[b].nchunks - 1);
+      il++;
+    }
+  };
+  for (const uint64_t w : run_full) {
+    const int b = (int)(w & 0xFFFFFFFFu);
+    for (int k = 0; k + 1 < r->req[b].nchunks; k++) {
+      emit_last_before(w, r->req[b].wbase + k);
+      emit(b, k);
     }
   }
-  // launch the largest items first (the last chunk of a request may be short)
-  auto keys = [&](const WorkItem& w) {
-    const ReqInfo& q = r->req[w.b];
-    const int64_t start = (int64_t)w.chunk * q.chunk_keys;
-    return std::min<int64_t>(q.chunk_keys, nvis[w.b] - start);
-  };
-  std::stable_sort(r->work.begin(), r->work.end(),
-                   [&](const WorkItem& x, const WorkItem& y) { return keys(x) > keys(y); });
+  emit_last_before(~0ull, 0);
+  (void)out;
   return OKC_OK;
 }
 
@@ -221,6 +259,17 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// The device address of a page-locked, device-mapped host buffer, else NULL
+// (pageable or unknown memory).
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
 
 }  // namespace
 
@@ -548,31 +597,41 @@ okc_status okc_attn_step_host(okc_attn_plan_t plan, const okc_host_step* io, uin
       (io->seq_lens_host == nullptr) != (io->seq_lens == nullptr))
     return OKC_ERR_INVALID;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) return cudaStreamSynchronize(str) == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
   const size_t width = (size_t)(2 * c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim;
-  struct Copy {
-    void* dst;
-    const void* src;
-    size_t bytes;
-  } in[] = {
-      {io->qkv, io->qkv_host, T * width * 2},
-      {io->positions, io->positions_host, T * sizeof(int64_t)},
-      {io->cache_loc, io->cache_loc_host, T * sizeof(int64_t)},
-      {io->cache_seqlens, io->cache_seqlens_host, B * sizeof(int32_t)},
-      {io->cu_seqlens_q, io->cu_seqlens_q_host, (B + 1) * sizeof(int32_t)},
-      {io->seq_lens, io->seq_lens_host, B * sizeof(int32_t)},
-      {io->page_table, io->page_table_host, B * (size_t)c.max_pages * sizeof(int32_t)},
+  // Each input is read where the device can read it: straight from the host
+  // buffer when that is page-locked and mapped and aligned as the kernels load
+  // it (16-byte vectors of qkv, naturally aligned indices), else from its
+  // device buffer after a copy.
+  bool fail = false;
+  auto source = [&](const void* host, void* dev, size_t bytes, uintptr_t align) -> const void* {
+    if (!host) return nullptr;
+    const void* mapped = mapped_host(host);
+    if (mapped && (reinterpret_cast<uintptr_t>(mapped) & (align - 1)) == 0) return mapped;
+    if (bytes && cudaMemcpyAsync(dev, host, bytes, cudaMemcpyHostToDevice, str) != cudaSuccess) fail = true;
+    return dev;
   };
-  if (B > 0) {
-    for (const Copy& cp : in)
-      if (cp.src && cp.bytes && cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, str) != cudaSuccess)
-        return OKC_ERR_CUDA;
-  }
-  okc_status st = okc_attn_step(plan, io->qkv, io->positions, io->cache_loc, k_cache, v_cache, k_scale, v_scale,
-                                rope_table, rope_positions, io->page_table, io->cache_seqlens, io->cu_seqlens_q,
-                                io->seq_lens, norm_weight, eps, o_partial, lse_partial, io->out, stream);
+  const void* qkv = source(io->qkv_host, io->qkv, T * width * 2, 16);
+  const void* positions = source(io->positions_host, io->positions, T * sizeof(int64_t), 8);
+  const void* cache_loc = source(io->cache_loc_host, io->cache_loc, T * sizeof(int64_t), 8);
+  const void* cache_seqlens = source(io->cache_seqlens_host, io->cache_seqlens, B * sizeof(int32_t), 4);
+  const void* cu_seqlens_q = source(io->cu_seqlens_q_host, io->cu_seqlens_q, (B + 1) * sizeof(int32_t), 4);
+  const void* seq_lens = source(io->seq_lens_host, io->seq_lens, B * sizeof(int32_t), 4);
+  const void* page_table = source(io->page_table_host, io->page_table, B * (size_t)c.max_pages * sizeof(int32_t), 4);
+  if (fail) return OKC_ERR_CUDA;
+  // the output: written straight into the host buffer when mapped and aligned
+  const void* out_mapped = mapped_host(io->out_host);
+  void* out = (out_mapped && aligned16(out_mapped)) ? const_cast<void*>(out_mapped) : io->out;
+  okc_status st = okc_attn_step(plan, qkv, static_cast<const int64_t*>(positions),
+                                static_cast<const int64_t*>(cache_loc), k_cache, v_cache, k_scale, v_scale, rope_table,
+                                rope_positions, static_cast<const int32_t*>(page_table),
+                                static_cast<const int32_t*>(cache_seqlens), static_cast<const int32_t*>(cu_seqlens_q),
+                                static_cast<const int32_t*>(seq_lens), norm_weight, eps, o_partial, lse_partial, out,
+                                stream);
   if (st != OKC_OK) return st;
   const size_t out_bytes = T * (size_t)c.num_q_heads * c.head_dim * 2;
-  if (out_bytes && cudaMemcpyAsync(io->out_host, io->out, out_bytes, cudaMemcpyDeviceToHost, str) != cudaSuccess)
+  if (out == io->out && out_bytes &&
+      cudaMemcpyAsync(io->out_host, io->out, out_bytes, cudaMemcpyDeviceToHost, str) != cudaSuccess)
     return OKC_ERR_CUDA;
   return cudaStreamSynchronize(str) == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }

@@ -239,17 +239,23 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
                          float* lse_partial, void* out, okc_stream stream);
 
 /*
- * One step from host buffers: the per-step inputs live in host memory (pinned
- * memory keeps the copies asynchronous), the caches, scales, RoPE table, norm
- * weight and scratch stay resident on the device. The call copies each host
- * input to its device buffer, runs okc_attn_step on them, copies the output
- * back to out_host and synchronizes `stream`: on OKC_OK the output is on the
- * host. Device buffers are caller-owned and sized as the host ones: qkv bf16
- * [T, (2Hq+2Hkv)*64]; positions / cache_loc int64 [T]; cache_seqlens,
- * seq_lens int32 [B]; cu_seqlens_q int32 [B+1]; page_table int32
- * [B, max_pages]; out bf16 [T, Hq*64]. positions (and its host copy) may be
- * NULL when rope_theta == 0, seq_lens when unchecked; each pair is NULL
- * together or not at all.
+ * One step from host buffers: the per-step inputs live in host memory, the
+ * caches, scales, RoPE table, norm weight and scratch stay resident on the
+ * device. The call runs okc_attn_step on the inputs and synchronizes `stream`:
+ * on OKC_OK the output is in out_host. A host buffer in page-locked memory
+ * that the device can address (cudaHostAlloc / cudaMallocHost, or
+ * cudaHostRegister'ed with mapping; unified addressing maps them by default)
+ * is read by the kernels in place, over the host link, and out_host is then
+ * written in place: no copy. Any other host buffer (pageable memory, or qkv /
+ * out_host not 16-byte aligned) is copied with cudaMemcpyAsync to its device
+ * buffer first (out: from its device buffer afterwards); device buffers of
+ * mapped host buffers are left untouched. Device buffers are caller-owned and
+ * sized as the host ones: qkv bf16 [T, (2Hq+2Hkv)*64]; positions / cache_loc
+ * int64 [T]; cache_seqlens, seq_lens int32 [B]; cu_seqlens_q int32 [B+1];
+ * page_table int32 [B, max_pages]; out bf16 [T, Hq*64]. positions (and its
+ * host copy) may be NULL when rope_theta == 0, seq_lens when unchecked; each
+ * pair is NULL together or not at all. The host buffers must not change until
+ * the call returns.
  */
 typedef struct okc_host_step {
   const void* qkv_host;

@@ -99,10 +99,28 @@ def test_step_form_chosen_by_the_plan():
     assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
 
 
+def _host_tensor(a, memory):
+    """A host tensor holding `a`: pinned, pageable, or pinned at an address one
+    element past an aligned allocation (misaligned for 16-byte vectors)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if memory == "pageable":
+        return t.clone()
+    if memory == "pinned":
+        return t.pin_memory()
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype).pin_memory()
+    view = flat[1:].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned_offset"])
 @pytest.mark.parametrize("name", ["sliding_decode", "verify_block", "full_decode_32k"])
-def test_step_from_host_buffers(name):
-    """okc_attn_step_host: host inputs copied in, the step, the output copied
-    back: equal to okc_attn_step on device buffers, bit for bit."""
+def test_step_from_host_buffers(name, memory):
+    """okc_attn_step_host: host inputs copied in (one gather kernel for
+    device-mapped pinned buffers, at any alignment; the copy engine for
+    pageable ones), the step, the output copied back: equal to okc_attn_step on
+    device buffers, bit for bit."""
     import fp8_kv_paged_gb300 as okc
     import torch
     from test_gpu_parity import SMALL
@@ -111,10 +129,10 @@ def test_step_from_host_buffers(name):
     d = to_device(cfg, inp)
     ref = run_gpu(cfg, inp, fused=True, plan_form=True)
     step = okc.AttnStep(cfg, inp["seq_lens"])
-    host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+    host = {k: _host_tensor(inp[k], memory)
             for k in ("positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table")}
-    host["qkv"] = torch.from_numpy(np.ascontiguousarray(inp["qkv"]).view(np.int16)).pin_memory()
-    host["out"] = torch.empty((inp["qkv"].shape[0], 1024), dtype=torch.int16).pin_memory()
+    host["qkv"] = _host_tensor(np.ascontiguousarray(inp["qkv"]).view(np.int16), memory)
+    host["out"] = _host_tensor(np.zeros((inp["qkv"].shape[0], 1024), np.int16), memory)
     dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
     okc.okc_attn_step_host(step.plan, host, dev, d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
                            d.get("rope_table"), d["norm_weight"], inp["eps"], step.o_partial, step.lse_partial)
