@@ -50,7 +50,7 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
     ("sliding_decode", "decode_kernel<fused step>"): 33.081088e6 + 11.008e3,
-    ("verify_block", "decode_tc_kernel"): 17.209344e6 + 0.0,
+    ("verify_block", "decode_tc_kernel"): 17.207040e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
     ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
     ("mixed_full_decode", "decode_kernel<fused step>"): 802.778112e6 + 7.543808e6,

@@ -19,27 +19,37 @@
 //
 // Warps: 0-3 and 4-7 are two softmax warpgroups that take alternate tiles
 // (thread r of a group owns q row r), 8 issues the MMAs (one thread) and owns
-// the TMEM allocation, 9-10 gather (the cp.async producer of decode.cu; K rows
-// land in the MMA's canonical layout, V rows in a staging tile). Each group j
-// has its own S and O in TMEM and its own P and V^T tiles in shared memory, so
-// one group's softmax overlaps the other group's MMAs. Per tile k of group j:
+// the TMEM allocation, 9-10 gather: on pages of 8 or more rows warp 9 issues
+// TMA tile loads (8-row boxes, 128-byte swizzle, read by the MMA through a
+// swizzled descriptor), else both warps run the cp.async producer of
+// decode.cu (K rows in the MMA's no-swizzle canonical layout, V rows in a
+// staging tile). Each group j has its own S and O in TMEM and its own P and
+// V^T tiles in shared memory, so one group's softmax overlaps the other
+// group's MMAs. Per tile k of group j:
 //   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
 //   group j: wait s_ready_j -> S row from TMEM -> arrive(s_free_j) -> mask; row
 //            max; P = 2^(s - m) (f16) into shared memory; V tile E4M3 -> f16
 //            transposed (ldmatrix, exact conversion, stmatrix.trans)
 //            -> arrive(p_ready_j)
 //   MMA:     wait p_ready_j -> free the stage -> O_j += P V -> commit(pv_done_j)
-// O accumulates in TMEM against a reference max m per row that moves only when
-// the row's max grows past m + 8 (in log2 units; P stays <= 2^8): then the
-// row's O is rescaled in TMEM (tcgen05.ld / st) before the next PV. At the end
-// group 0 merges both groups' (m, l, O) and writes O/l (times v_scale) and the
-// base-2 LSE per row, as decode.cu does; the combine kernel merges the splits.
+// O accumulates in TMEM against a reference max m per row that moves when the
+// row's max grows past m + kTcRescale (log2 units; 0 by default: the exact
+// running max, P <= 1): then the row's O is rescaled in TMEM (tcgen05.ld / st)
+// before the next PV. At the end group 0 merges both groups' (m, l, O) and
+// writes O/l (times v_scale) and the base-2 LSE per row, as decode.cu does;
+// the combine kernel merges the splits.
 //
-// Shared-memory operands use the no-swizzle K-major layout (8-row x 16-byte
-// core matrices; core matrices 128 bytes apart along K, 8-row groups 1024
-// bytes apart for 128-byte rows). Every wait is bounded (mbar_wait); on a
-// timeout the kernel flags OKC_DEVERR_TIMEOUT, waits for the MMAs it issued
-// and frees its TMEM before it returns.
+// Shared-memory operands Q, P, V^T (and K on the cp.async path) use the
+// no-swizzle K-major layout (8-row x 16-byte core matrices; core matrices 128
+// bytes apart along K, 8-row groups 1024 bytes apart for 128-byte rows); K on
+// the TMA path the 128-byte-swizzle K-major layout. Every wait is bounded
+// (mbar_wait); on a timeout the kernel flags OKC_DEVERR_TIMEOUT, waits for the
+// copies and MMAs it issued and frees its TMEM before it returns.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
 #include "okc_common.cuh"
 #include "okc_internal.h"
 
@@ -85,7 +95,24 @@ __device__ __forceinline__ uint32_t canon(int r, int kb) {
   return (uint32_t)((r >> 3) * kTcSbo + (kb >> 4) * kTcLbo + (r & 7) * 16 + (kb & 15));
 }
 
-__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
+// The K and V caches as 2-D byte tensors [num_rows, 128] for TMA tile loads of
+// 8 rows (one swizzle atom), used when a page holds a multiple of 8 rows.
+struct TcMaps {
+  CUtensorMap k, v;
+};
+
+// kTma: K and V tiles arrive by TMA, eight 8-row boxes per tile (one page id
+// each), into the 128-byte-swizzle layout; tiles start at the chunk's first key
+// rounded down to a multiple of 8 (those rows share the page of the first key
+// and hold earlier keys of the request; they are masked). The 8-row group that
+// holds the chunk's last key comes by cp.async, up to that key only: past the
+// request's last key a page may hold any bytes, and a NaN there would reach
+// the PV product through P = 0. Rows never loaded keep what the stage held
+// before (zeros at the start, else keys of earlier tiles). Otherwise tiles
+// arrive by 16-byte cp.async per row chunk (any page size).
+template <bool kTma>
+__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_constant__ DecodeArgs a,
+                                                               const __grid_constant__ TcMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sb = smem_u32(smem);
@@ -100,7 +127,9 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
   const WorkItem wk = a.work[blockIdx.x];  // plan data
   if (tid == 0) {
     for (int s = 0; s < kTcStages; s++) {
-      mbar_init(full_bar(s), 32 * kTcProducers);  // one cp.async-tracked arrival per producer lane
+      // TMA: one arrival with the tile's box bytes and one cp.async-tracked
+      // arrival per lane of the issuing warp; cp.async: one per producer lane
+      mbar_init(full_bar(s), kTma ? 1 + 32 : 32 * kTcProducers);
       mbar_init(empty_bar(s), 1);                  // the MMA thread frees a stage
     }
     for (int j = 0; j < kTcGroups; j++) {
@@ -123,9 +152,16 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
   static_assert(kKeysPW == 16 || kKeysPW == 32, "at most one page id per producer lane per tile");
   const int pw = warp - (kTcMmaWarp + 1), kbase = pw * kKeysPW;
   const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
+  // (TMA: producer warp 0 alone; its lane l < 8 loads the id of the tile's
+  // 8-row group l, tiles starting at the key range's start rounded down to 8)
   auto load_ids = [&](int& dst, int tile, int jb, int je) {
-    const int j = jb + tile * kTcTileKeys + kbase + lane;
-    dst = (lane < kKeysPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+    if constexpr (kTma) {
+      const int j = (jb & ~7) + tile * kTcTileKeys + 8 * lane;
+      dst = (pw == 0 && lane < 8 && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+    } else {
+      const int j = jb + tile * kTcTileKeys + kbase + lane;
+      dst = (lane < kKeysPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+    }
   };
   int ids[kTcStages];
   if (warp > kTcMmaWarp) {
@@ -150,7 +186,14 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
   const int j1 = min(n, j0 + wk.chunk_keys);
   if (wk.chunk == wk.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
-  const int ntiles = j1 > j0 ? (j1 - j0 + kTcTileKeys - 1) / kTcTileKeys : 0;
+  const int jt = kTma ? (j0 & ~7) : j0;  // first key of tile 0 (keys below j0 are masked)
+  const int ntiles = j1 > j0 ? (j1 - jt + kTcTileKeys - 1) / kTcTileKeys : 0;
+  if constexpr (kTma) {
+    // V rows a tile leaves unloaded must hold finite values: zero the stages
+    for (int i = tid; i < kTcStages * kTcTileKeys * kTcVPitch / 16; i += kTcThreads)
+      *reinterpret_cast<uint4*>(smem + kTcV + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();  // before the TMA loads write the same bytes
+  }
   tc_fence_before();
   __syncthreads();  // barriers initialised, TMEM address in shared memory
   tc_fence_after();
@@ -166,34 +209,77 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
     const int newk = n - ql;  // keys >= newk are written by the prepare kernel
     const int rr = lane >> 3, ch = lane & 7;
     bool dep = false, bad_page = false;
+    // (TMA: the first producer warp alone issues the loads; the block keeps the
+    // second, idle: without it the compiler takes 140 registers per thread
+    // instead of 112, and the step was slower)
+    if (kTma && pw != 0) return;
     auto issue = [&](int k, int id) {
       const int s = k % kTcStages;
       const uint32_t sK = sb + kTcK + s * (kTcTileKeys * 128), sV = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
-      const int tj = j0 + k * kTcTileKeys;
+      const int tj = jt + k * kTcTileKeys;
       if (!dep && min(j1, tj + kTcTileKeys) > newk) {  // this tile holds a key prepare writes
         pdl_wait();
         dep = true;
       }
-#pragma unroll
-      for (int i = 0; i < kKeysPW / 4; i++) {
-        const int rl = rr + 4 * i;
-        const int r = kbase + rl;
-        const int pg = __shfl_sync(0xffffffffu, id, rl);
-        const int j = tj + r;
-        int64_t row = 0;
-        int bytes = 0;
-        if (j < j1) {
-          if (pg >= 0 && pg < a.num_pages) {
-            row = ((int64_t)pg << a.page_shift) | (j & pmask);
-            bytes = 16;
+      if constexpr (kTma) {
+        // lane l < 8: the 8 rows of keys tj + 8l .. +7 lie in one page
+        const int key = tj + 8 * lane;
+        int nrows = 0;  // rows of group l to load: 8, or up to the chunk's last key
+        int row = 0;
+        if (lane < 8 && key < j1) {
+          if (id >= 0 && id < a.num_pages) {
+            row = (id << a.page_shift) | (key & pmask);
+            nrows = min(8, j1 - key);
           } else {
             bad_page = true;
           }
         }
-        cp_async_16(sK + canon(r, ch * 16), a.kc + row * kRowBytes + ch * 16, bytes);
-        cp_async_16(sV + r * kTcVPitch + ch * 16, a.vc + row * kRowBytes + ch * 16, bytes);
+        const unsigned whole = __ballot_sync(0xffffffffu, nrows == 8);
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(whole) * 2u * 1024u);
+        __syncwarp();
+        if (nrows == 8) {
+          tma_load_2d(sK + lane * 1024, &maps.k, 0, row, full_bar(s));
+          tma_load_2d(sV + lane * 1024, &maps.v, 0, row, full_bar(s));
+        }
+        // the group cut by the chunk's end (at most one): its rows by 16-byte
+        // cp.async chunks into the same swizzled positions, all lanes
+        const unsigned cut = __ballot_sync(0xffffffffu, nrows > 0 && nrows < 8);
+        if (cut) {
+          const int gc = __ffs(cut) - 1;
+          const int crow = __shfl_sync(0xffffffffu, row, gc), cn = __shfl_sync(0xffffffffu, nrows, gc);
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int cid = lane + 32 * h, r = cid >> 3, c = cid & 7;  // row r, chunk c of the group
+            if (r < cn) {
+              const uint32_t off = gc * 1024 + r * 128 + ((c ^ r) * 16);
+              cp_async_16(sK + off, a.kc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
+              cp_async_16(sV + off, a.vc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
+            }
+          }
+        }
+        cp_async_mbar_arrive(full_bar(s));
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKeysPW / 4; i++) {
+          const int rl = rr + 4 * i;
+          const int r = kbase + rl;
+          const int pg = __shfl_sync(0xffffffffu, id, rl);
+          const int j = tj + r;
+          int64_t row = 0;
+          int bytes = 0;
+          if (j < j1) {
+            if (pg >= 0 && pg < a.num_pages) {
+              row = ((int64_t)pg << a.page_shift) | (j & pmask);
+              bytes = 16;
+            } else {
+              bad_page = true;
+            }
+          }
+          cp_async_16(sK + canon(r, ch * 16), a.kc + row * kRowBytes + ch * 16, bytes);
+          cp_async_16(sV + r * kTcVPitch + ch * 16, a.vc + row * kRowBytes + ch * 16, bytes);
+        }
+        cp_async_mbar_arrive(full_bar(s));
       }
-      cp_async_mbar_arrive(full_bar(s));
     };
 #pragma unroll
     for (int t = 0; t < kTcStages; t++) {
@@ -201,6 +287,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
       load_ids(ids[t], t + kTcStages, j0, j1);
     }
     bool ok = true;
+    int issued = min(ntiles, kTcStages);  // tiles whose copies were issued
     for (int k0 = kTcStages; k0 < ntiles && ok; k0 += kTcStages) {
 #pragma unroll
       for (int u = 0; u < kTcStages; u++) {
@@ -208,10 +295,17 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
         if (k >= ntiles) break;
         if (!mbar_wait(empty_bar(u), ((k / kTcStages) & 1) ^ 1)) { ok = false; break; }
         issue(k, ids[u]);
+        issued = k + 1;
         load_ids(ids[u], k + kTcStages, j0, j1);
       }
     }
-    if (bad_page && ch == 0) set_error(a.err, OKC_DEVERR_PAGE);
+    if (bad_page && (kTma || ch == 0)) set_error(a.err, OKC_DEVERR_PAGE);
+    if constexpr (kTma) {
+      // the CTA's shared memory must outlive the copies in flight: wait (bounded,
+      // also after a timeout) until the last issued tile of every stage landed
+      for (int k = max(0, issued - kTcStages); k < issued; k++)
+        if (!mbar_wait(full_bar(k % kTcStages), (k / kTcStages) & 1)) ok = false;
+    }
     if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
     cp_async_wait<0>();
     return;
@@ -233,7 +327,8 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)  // 128 bytes of K: 32 per instruction (two core matrices)
           umma_f8(tmem + tc_col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
-                  umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_qk, kk > 0);
+                  kTma ? umma_desc_sw128(kt + kk * 32, kTcSbo) : umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
+                  id_qk, kk > 0);
         umma_commit(s_ready(j));
         return true;
       };
@@ -341,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
     const bool w = mbar_wait(s_ready(jw), (k >> 1) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
     tc_fence_after();
-    const int tile_j = j0 + k * kTcTileKeys;
+    const int tile_j = jt + k * kTcTileKeys;
     float s0[32], s1[32];
     tmem_ld32(tS, s0);
     tmem_ld32(tS + 32, s1);
@@ -351,7 +446,8 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
     // causal, chunk end; none for a dead row); row max on the raw scores
     int klo = 0, khi = 0;
     if (live) {
-      klo = a.window > 0 ? max(0, pos - a.window + 1 - tile_j) : 0;
+      klo = max(j0 - tile_j, a.window > 0 ? pos - a.window + 1 - tile_j : 0);
+      klo = max(0, klo);
       khi = min(kTcTileKeys, min(j1, pos + 1) - tile_j);
     }
     const uint32_t kn = khi > klo ? (uint32_t)(khi - klo) : 0u;
@@ -416,7 +512,11 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
         const int cbase = (it & 1) * 4;      // first 16-dim group of this x4
         uint32_t rg[4];
         // matrix mi = lane >> 3: keys a8*8 + (lane & 7), bytes 16 (cbase + mi) .. +15
-        ldsm_x4(rg, vs + (a8 * 8 + (lane & 7)) * kTcVPitch + (cbase + (lane >> 3)) * 16);
+        // (TMA: 8-row groups 1024 bytes apart, chunks XORed with the row mod 8)
+        if constexpr (kTma)
+          ldsm_x4(rg, vs + a8 * 1024 + (lane & 7) * 128 + (((cbase + (lane >> 3)) ^ (lane & 7)) * 16));
+        else
+          ldsm_x4(rg, vs + (a8 * 8 + (lane & 7)) * kTcVPitch + (cbase + (lane >> 3)) * 16);
         // rg[mi]: key a8*8 + lane/4, dims 16 (cbase+mi) + 4 (lane%4) + {0,1,2,3}
         uint32_t lo4[4], hi4[4];
 #pragma unroll
@@ -492,6 +592,39 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(DecodeArgs a) {
 
 }  // namespace
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null when unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<EncodeTiledFn>(nullptr);
+    }
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A cache viewed as [rows, 128] bytes, loaded as boxes of 8 rows with 128-byte
+// swizzle.
+bool encode_cache_map(CUtensorMap* m, const uint8_t* base, int64_t rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn || rows < 8) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+  const cuuint32_t box[2] = {(cuuint32_t)kRowBytes, 8};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
   if (a.L < 2 || a.L > 8) return cudaErrorInvalidValue;
@@ -505,16 +638,26 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, a);
+  // pages of 8 or more rows: TMA boxes of 8 rows never cross a page
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const int64_t rows = (int64_t)a.num_pages << a.page_shift;
+  if (a.page_shift >= 3 && encode_cache_map(&maps.k, a.kc, rows) && encode_cache_map(&maps.v, a.vc, rows))
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true>, a, maps);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false>, a, maps);
 }
 
 int decode_tc_ctas_per_sm() {
-  int nb = 0;
-  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
-    return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_tc_kernel, kTcThreads, kTcSmem) != cudaSuccess)
-    return 0;
-  return nb;
+  int lowest = 0;
+  for (int v = 0; v < 2; v++) {
+    auto kern = v ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+    int nb = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kTcThreads, kTcSmem) != cudaSuccess)
+      return 0;
+    lowest = v ? std::min(lowest, nb) : nb;
+  }
+  return lowest;
 }
 
 }  // namespace okc

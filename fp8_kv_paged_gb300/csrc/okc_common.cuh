@@ -109,6 +109,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (i >= kWaitMinPolls && global_ns() - t0 > kWaitNs) return false;
   }
 }
+// Arrive on mbarrier `bar` and add `bytes` to the transaction count its
+// current phase waits for (the bytes of the bulk copies that complete on it).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+// TMA: the box at (x, y) of the 2-D tensor map `tmap` (a kernel parameter)
+// into shared memory at `dst`; completes `bytes` of transactions on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 // Arrive on mbarrier `bar` once every cp.async this thread has issued so far has
 // completed (the arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
@@ -157,6 +171,16 @@ __device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);  // descriptor version 1, no swizzle
+}
+// The same for the 128-byte-swizzle K-major layout that a TMA tile load with
+// 128-byte swizzling writes: rows of 128 bytes whose 16-byte chunks are XORed
+// with the row index mod 8, 8-row groups `sbo` bytes apart, the tile
+// 1024-byte aligned; the leading offset is unused. A step along K inside the
+// 128-byte row adds its byte offset to saddr (the swizzle applies to the
+// resulting address).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+         (1ull << 46) | (2ull << 61);  // descriptor version 1, layout 2 = 128-byte swizzle
 }
 // Instruction descriptor: f32 accumulator, A/B format code `ab` (kind::f16: 0 =
 // f16; kind::f8f6f4: 0 = E4M3), both K-major, M x N.

@@ -107,6 +107,14 @@ def test_bad_inputs_flag_errors_without_faulting():
     d = to_device(cfg, dict(inp, seq_lens=inp["seq_lens"] + 1))
     gpu = run_gpu(cfg, inp, dev_inp=d)
     assert gpu["errors"] & okc.DEVERR_LENGTHS
+    # 5) a page id past the pool in a verify block on 64-row pages (the TMA
+    # loads of the tcgen05 decode skip it)
+    vcfg = W.config("verify_block", batch=3, seq=("list", [300, 1000, 2500]))
+    vinp = W.generate(vcfg)
+    vbad = dict(vinp, page_table=vinp["page_table"].copy())
+    vbad["page_table"][1, 5] = vcfg["num_pages"] + 7
+    gpu = run_gpu(vcfg, vbad)
+    assert gpu["errors"] & okc.DEVERR_PAGE
 
 
 @pytest.mark.parametrize("fused", [False, True])
@@ -131,6 +139,8 @@ def test_plan_lengths_longer_than_device_lengths(fused):
     ([50, 900, 2047, 2048, 2049], 2, 1, 1.0),
     ([0, 1, 63, 64, 65], 4, 16, 1.0),
     ([5000, 3], 6, 64, 0.5),
+    ([31, 500, 1999, 7], 3, 8, 1.0),         # pages of one 8-row TMA box
+    ([1000, 4100, 2053], 8, 32, 0.5),
 ])
 def test_verify_block_both_decode_kernels(seq, L, P, kv_scale):
     """Blocks of 2..8 tokens decode on the tcgen05 kernel by default and on the
