@@ -49,11 +49,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("sliding_decode", "decode_kernel<fused step>"): 33.081088e6 + 11.008e3,
+    ("sliding_decode", "decode_kernel<fused step>"): 33.082624e6 + 9.728e3,
     ("verify_block", "decode_tc_kernel"): 17.207040e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
     ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
-    ("mixed_full_decode", "decode_kernel<fused step>"): 802.778112e6 + 7.543808e6,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 803.087872e6 + 7.382016e6,
 }
 WORKLOAD = "sliding_decode"
 FALLBACK_HBM_GBS = 6800.0
@@ -263,6 +263,8 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "three_call"],
                     help="okc_attn_step (one launch) or okc_prepare_qkv + okc_attn_decode + okc_attn_combine_normgate")
     ap.add_argument("--no-compare", action="store_true", help="skip timing the other path")
+    ap.add_argument("--chunk-keys", type=int, default=0,
+                    help="keys per split work item (plan option; 0 = the plan's heuristic)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -296,7 +298,8 @@ def main():
     sets = [base] + [{k: (None if t is None else (t if k in ("rope_table", "k_scale", "v_scale", "norm_weight")
                                                    else t.clone())) for k, t in base.items()}
                      for _ in range(n_sets - 1)]
-    step = okc.AttnStep(cfg, inp["seq_lens"])
+    plan_opts = {"chunk_keys": args.chunk_keys} if args.chunk_keys else None
+    step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts)
     stream = torch.cuda.Stream(device=dev)
     fused = args.path == "fused"
 
@@ -356,7 +359,7 @@ def main():
 
     # the step's dominant kernel alone, K launches, no programmatic overlap: the
     # fused step kernel, or the decode kernel of the three-call path
-    step_np = okc.AttnStep(cfg, inp["seq_lens"], opts={"flags": okc.PLAN_NO_PDL})
+    step_np = okc.AttnStep(cfg, inp["seq_lens"], opts=dict(plan_opts or {}, flags=okc.PLAN_NO_PDL))
     for s_ in sets:
         step_np.run(s_, eps=inp["eps"], stream=stream)
     stream.synchronize()

@@ -144,7 +144,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   int64_t W = 0;
   for (int b = 0; b < B; b++) {
     const int64_t k = std::max<int64_t>(1, (nvis[b] + budget - 1) / budget);
-    const int64_t chunk = std::max<int64_t>(16, ((nvis[b] + k - 1) / k + 15) / 16 * 16);
+    const int64_t chunk = split_chunk_keys(nvis[b], k, use_tc && cfg->page_size >= 8 ? 7 : 0);
     const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (W + nch > kMaxWork) return OKC_ERR_WORKSPACE;
     req[b] = ReqInfo{(int32_t)W, (int32_t)nch, (int32_t)chunk, 0};

@@ -126,6 +126,9 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
     }
   }
   (void)total;
+  // q_len 2..8 decodes on the tcgen05 kernel, fed by TMA on pages of 8+ rows
+  const bool tc_tma = L >= 2 && L <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05)) && c->page_size >= 8;
+  const int64_t tma_pad = tc_tma ? 7 : 0;
   r->req.assign(B, ReqInfo{0, 0, 0, 0});
   int64_t wbase = 0;
   for (int b = 0; b < B; b++) {
@@ -134,8 +137,7 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
       chunk = o->chunk_keys;
     } else {
       const int64_t k = std::max<int64_t>(1, (nvis[b] + Cbud - 1) / Cbud);
-      chunk = (nvis[b] + k - 1) / k;
-      chunk = std::max<int64_t>(16, (chunk + 15) / 16 * 16);
+      chunk = okc::split_chunk_keys(nvis[b], k, tma_pad);
     }
     const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (nch > (1 << 20) || wbase + nch > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;

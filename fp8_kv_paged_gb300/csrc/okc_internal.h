@@ -116,6 +116,18 @@ struct okc_attn_plan_s {
 
 namespace okc {
 
+// Keys per split work item for a request of `nvis` visible keys split `k`
+// ways: nvis / k rounded up so that the item's 64-key tiles are whole ones,
+// counting the up to `pad` keys before the item that a tile start rounded
+// down to a multiple of 8 adds (7 for the TMA-fed tcgen05 decode, else 0).
+// No item gets more tiles than unrounded, and the last item of a request is
+// shorter, so a request takes no more tiles in all.
+inline int64_t split_chunk_keys(int64_t nvis, int64_t k, int64_t pad) {
+  const int64_t x = (nvis + k - 1) / k;
+  const int64_t r = (x + pad + 63) / 64 * 64 - pad;
+  return r > 64 - pad ? r : 64 - pad;
+}
+
 // Kernel launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_prepare(const PrepareArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
