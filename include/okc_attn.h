@@ -185,8 +185,11 @@ okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t*
  * of the plan covers a key range of one request for all its query rows and both
  * KV heads, and writes a normalized f32 partial output (already times v_scale)
  * and its base-2 log-sum-exp. q_len 2..8 runs on the tcgen05 kernel (M = 128
- * query rows per request, accumulators in tensor memory) unless the plan was
- * made with OKC_PLAN_NO_TCGEN05; q_len 1 and 9..16 on the warp-level MMA kernel.
+ * query rows per request, accumulators in tensor memory; on pages of 8 or more
+ * rows its K/V tiles arrive by TMA through tensor maps the call encodes for
+ * k_cache and v_cache, so page_size * num_pages rows must be addressable from
+ * both base pointers) unless the plan was made with OKC_PLAN_NO_TCGEN05; q_len
+ * 1 and 9..16 on the warp-level MMA kernel.
  *  q_fp8          from okc_prepare_qkv
  *  page_table     int32 [B, max_pages]
  *  cache_seqlens  int32 [B] = seq_lens + L; cu_seqlens_q int32 [B+1] = 0, L, 2L, ...
