@@ -464,13 +464,12 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
         sizes["workspace_bytes"] - sizes["q_fp8_bytes"]
     d2h = out_host.numel() * 2
 
-    host_io = dict(pinned, out=out_host)
-    dev_io = dict({k: dev_in[k] for k in names}, out=out)
+    io = okc.HostStepIO(dict(pinned, out=out_host), dict({k: dev_in[k] for k in names}, out=out))
 
     def one():
         plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
         if fused:  # one C call: host->device copies, the step, device->host copy, synchronize
-            okc.okc_attn_step_host(plan, host_io, dev_io, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
+            okc.okc_attn_step_host(plan, io, None, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
                                    dev_in["v_scale"], dev_in["rope_table"], dev_in["norm_weight"], inp["eps"],
                                    op, lp, stream)
             plan.close()

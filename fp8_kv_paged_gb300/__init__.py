@@ -18,7 +18,7 @@ from . import build as _build_mod
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
-           "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "STEP_IO",
+           "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
            "EXPORTED_SYMBOLS"]
@@ -257,15 +257,28 @@ def okc_attn_step(plan: Plan, qkv, positions, cache_loc, k_cache, v_cache, k_sca
 STEP_IO = ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table", "out")
 
 
-def okc_attn_step_host(plan: Plan, host: dict, dev: dict, k_cache, v_cache, k_scale, v_scale, rope_table,
+class HostStepIO:
+    """The buffers of okc_attn_step_host marshalled once: host / dev map each
+    name of STEP_IO to a host tensor (pinned and mapped: read in place) and
+    the device buffer used when it is not. Reuse it for every step that uses
+    the same buffers (it keeps the tensors alive)."""
+
+    def __init__(self, host: dict, dev: dict):
+        self.host, self.dev = dict(host), dict(dev)
+        self.struct = _HostStep(
+            **{k + "_host": (None if host.get(k) is None else host[k].data_ptr()) for k in STEP_IO},
+            **{k: (None if dev.get(k) is None else dev[k].data_ptr()) for k in STEP_IO})
+        self.ref = ctypes.byref(self.struct)
+
+
+def okc_attn_step_host(plan: Plan, host, dev, k_cache, v_cache, k_scale, v_scale, rope_table,
                        norm_weight, eps, o_partial, lse_partial, stream=None):
-    """One step from host buffers (see the header): host / dev map each name of
-    STEP_IO to a host tensor (pinned for asynchronous copies) and the device
-    buffer it is copied to; returns once host["out"] holds the output."""
-    io = _HostStep(**{k + "_host": (None if host.get(k) is None else host[k].data_ptr()) for k in STEP_IO},
-                   **{k: (None if dev.get(k) is None else dev[k].data_ptr()) for k in STEP_IO})
+    """One step from host buffers (see the header); returns once the output is
+    in host["out"]. `host` is a HostStepIO (then `dev` is None) or the host
+    dict of one, with `dev` its device dict."""
+    io = host if isinstance(host, HostStepIO) else HostStepIO(host, dev)
     npos = 0 if rope_table is None else rope_table.shape[0]
-    _check(load().okc_attn_step_host(plan.handle, ctypes.byref(io), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+    _check(load().okc_attn_step_host(plan.handle, io.ref, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                      _ptr(v_scale), _ptr(rope_table), npos, _ptr(norm_weight), eps,
                                      _ptr(o_partial), _ptr(lse_partial), _stream(stream)),
            "okc_attn_step_host")
