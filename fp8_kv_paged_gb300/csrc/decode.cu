@@ -597,18 +597,21 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 
   if constexpr (FUSED) {
     // Last CTA of the request merges every split and applies the norm-gate: once
-    // the CTA's partials are written (barrier), one thread publishes them (fence)
-    // and takes a ticket; the CTA that draws the last ticket fences again, then
-    // reads all partials (L2 loads) and resets the counter for the next launch.
-    // Nothing waits on another CTA.
+    // the CTA's partials are written (barrier), one thread takes a ticket with
+    // an acquire-release atomic (publishing them; measured 0.5 us faster on the
+    // sliding step than a fence on each side of a relaxed atomic); the CTA that
+    // draws the last ticket reads all partials (L2 loads) and resets the counter
+    // for the next launch. Nothing waits on another CTA.
     volatile int& s_last = *reinterpret_cast<int*>(smem + kFlagOffset);
     if (pos_err && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
     named_bar_sync(1, NCW * 32);
     if (tid == 0) {
-      __threadfence();
-      const bool last = atomicAdd(a.tickets + b, 1) == wk.nchunks - 1;
-      if (last) __threadfence();
-      s_last = last;
+      // the release publishes the partials the CTA wrote (they precede it
+      // through the barrier); for the last CTA the acquire orders the other
+      // splits' partials before the merge's reads (the barrier below)
+      int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + b) : "memory");
+      s_last = prev == wk.nchunks - 1;
     }
     named_bar_sync(1, NCW * 32);
     if (s_last) {
