@@ -265,6 +265,8 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip timing the other path")
     ap.add_argument("--chunk-keys", type=int, default=0,
                     help="keys per split work item (plan option; 0 = the plan's heuristic)")
+    ap.add_argument("--step-form", default="plan", choices=["plan", "one", "three"],
+                    help="okc_attn_step as one kernel or three (plan option; default: the plan's choice)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -298,7 +300,12 @@ def main():
     sets = [base] + [{k: (None if t is None else (t if k in ("rope_table", "k_scale", "v_scale", "norm_weight")
                                                    else t.clone())) for k, t in base.items()}
                      for _ in range(n_sets - 1)]
-    plan_opts = {"chunk_keys": args.chunk_keys} if args.chunk_keys else None
+    plan_opts = {}
+    if args.chunk_keys:
+        plan_opts["chunk_keys"] = args.chunk_keys
+    if args.step_form != "plan":
+        plan_opts["flags"] = okc.PLAN_STEP_ONE_LAUNCH if args.step_form == "one" else okc.PLAN_STEP_THREE_LAUNCHES
+    plan_opts = plan_opts or None
     step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts)
     stream = torch.cuda.Stream(device=dev)
     fused = args.path == "fused"
@@ -359,7 +366,8 @@ def main():
 
     # the step's dominant kernel alone, K launches, no programmatic overlap: the
     # fused step kernel, or the decode kernel of the three-call path
-    step_np = okc.AttnStep(cfg, inp["seq_lens"], opts=dict(plan_opts or {}, flags=okc.PLAN_NO_PDL))
+    step_np = okc.AttnStep(cfg, inp["seq_lens"],
+                           opts=dict(plan_opts or {}, flags=(plan_opts or {}).get("flags", 0) | okc.PLAN_NO_PDL))
     for s_ in sets:
         step_np.run(s_, eps=inp["eps"], stream=stream)
     stream.synchronize()
