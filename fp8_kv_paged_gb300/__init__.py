@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build_mod
 
-__all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes",
+__all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes", "okc_attn_plan_items",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
-    "okc_attn_step", "okc_attn_step_host",
+    "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items",
 ]
 
 
@@ -54,7 +54,7 @@ class _Config(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("chunk_keys", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("sm_count", ctypes.c_int32)]
 
 
 class _HostStep(ctypes.Structure):
@@ -96,6 +96,9 @@ def load(path: str | None = None):
     lib.okc_attn_plan_sizes.restype = st
     lib.okc_attn_plan_sizes.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options),
                                         ctypes.POINTER(_Sizes)]
+    lib.okc_attn_plan_items.restype = st
+    lib.okc_attn_plan_items.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options), P, i32,
+                                        ctypes.POINTER(ctypes.c_int32)]
     lib.okc_attn_plan.restype = st
     lib.okc_attn_plan.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options), P,
                                   ctypes.c_size_t, P, ctypes.POINTER(ctypes.c_void_p)]
@@ -150,7 +153,7 @@ def _options(opts: dict | None):
     if not opts:
         return None
     return ctypes.byref(_Options(opts.get("chunk_keys", 0), opts.get("flags", 0),
-                                 opts.get("ctas_per_sm", 0), 0))
+                                 opts.get("ctas_per_sm", 0), opts.get("sm_count", 0)))
 
 
 def _sizes_dict(z: _Sizes) -> dict:
@@ -164,6 +167,22 @@ def okc_attn_plan_sizes(cfg: dict, seq_lens_host, opts: dict | None = None) -> d
     _check(lib.okc_attn_plan_sizes(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p),
                                    _options(opts), ctypes.byref(z)), "okc_attn_plan_sizes")
     return _sizes_dict(z)
+
+
+def okc_attn_plan_items(cfg: dict, seq_lens_host, opts: dict | None = None) -> np.ndarray:
+    """The plan's split work list in launch order: int32 [items, 3] rows of
+    (request, first key, end key) (see the header). Host only when opts give
+    both ctas_per_sm and sm_count."""
+    lib = load()
+    seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _options(opts),
+                                   None, 0, ctypes.byref(n)), "okc_attn_plan_items")
+    out = np.zeros((n.value, 3), dtype=np.int32)
+    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _options(opts),
+                                   out.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n)),
+           "okc_attn_plan_items")
+    return out
 
 
 class Plan:

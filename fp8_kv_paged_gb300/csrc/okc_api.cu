@@ -250,12 +250,15 @@ int cached_ctas_per_sm(int dev, int L, bool tc) {
 }
 
 int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count_out) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  const int occ = cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
-  if (occ <= 0) return -1;
-  const int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : occ;
+  int sms = (o && o->sm_count > 0) ? o->sm_count : 0;
+  int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : 0;
+  if (sms == 0 || per_sm == 0) {  // read from the current device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (per_sm == 0) per_sm = cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
+    if (per_sm <= 0) return -1;
+  }
   if (sm_count_out) *sm_count_out = sms;
   return sms * per_sm;
 }
@@ -301,6 +304,28 @@ okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_le
   st = compute_sizes(cfg, s, sizes);
   sizes->step_kernels = step_kernels(cfg, s, opts, slots);
   return st;
+}
+
+okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                               const okc_plan_options* opts, int32_t* items, int32_t capacity,
+                               int32_t* count) {
+  okc_status st = check_config(cfg);
+  if (st != OKC_OK) return st;
+  if (!count || capacity < 0 || (capacity > 0 && !items) || (cfg->batch > 0 && !seq_lens_host))
+    return OKC_ERR_INVALID;
+  const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
+  if (slots < 0) return OKC_ERR_CUDA;
+  SplitResult s;
+  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  if (st != OKC_OK) return st;
+  *count = (int32_t)s.work.size();
+  if ((int64_t)s.work.size() > capacity) return capacity == 0 && !items ? OKC_OK : OKC_ERR_WORKSPACE;
+  for (size_t i = 0; i < s.work.size(); i++) {
+    items[3 * i] = s.work[i].b;
+    items[3 * i + 1] = s.work[i].j0;
+    items[3 * i + 2] = s.work[i].j1;
+  }
+  return OKC_OK;
 }
 
 okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,

@@ -92,7 +92,9 @@ typedef struct okc_plan_options {
                               OKC_PLAN_STEP_ONE_LAUNCH / OKC_PLAN_STEP_THREE_LAUNCHES: force the form
                               of okc_attn_step at q_len 1 (default: chosen by the plan) */
   int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
-  int32_t reserved;
+  int32_t sm_count;        /* SMs the split heuristic assumes; 0 = the current device's. With
+                              ctas_per_sm also set, planning (okc_attn_plan_sizes,
+                              okc_attn_plan_items) makes no CUDA call */
 } okc_plan_options;
 #define OKC_PLAN_NO_PDL 0x1
 #define OKC_PLAN_NO_TCGEN05 0x2
@@ -120,6 +122,20 @@ typedef struct okc_attn_plan_s* okc_attn_plan_t;
  */
 okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                                const okc_plan_options* opts, okc_attn_sizes* sizes);
+
+/*
+ * The split work list a plan made with the same arguments would launch, for
+ * inspection (load balance, tests): item i covers keys [first, end) of request
+ * `request`, items in launch order, written as items[3*i + 0..2] = request,
+ * first key, end key. Keys are counted from the request's first cached token;
+ * the ranges assume the device lengths equal seq_lens_host + q_len.
+ * `capacity` is the number of items `items` can hold; *count receives the
+ * number of items (with items == NULL and capacity 0, only the count).
+ * Returns OKC_ERR_WORKSPACE, with *count set, when capacity is too small.
+ */
+okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                               const okc_plan_options* opts, int32_t* items, int32_t capacity,
+                               int32_t* count);
 
 /*
  * okc_attn_plan — the per-step plan ("Differs from SGLang" note of the problem

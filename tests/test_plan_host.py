@@ -1,0 +1,126 @@
+"""The split planner on the host (no GPU: okc_plan_options gives the SM count
+and the CTAs per SM, so planning makes no CUDA call): every request's visible
+keys are covered once, in order, by its work items; item sizes are whole
+64-key tiles (counting the TMA-fed tile start of the tcgen05 path); items
+launch largest first; the item count respects the waves the heuristic allows;
+the plan's sizes agree with its item list; and the step form follows the
+documented rule on the workloads' shapes."""
+import numpy as np
+import pytest
+
+import fp8_kv_paged_gb300 as okc
+import workloads as W
+
+SMS, CTAS = 152, 3  # a GB300 at the q_len-1 decode's occupancy
+HOST = {"sm_count": SMS, "ctas_per_sm": CTAS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    okc.build()
+    return okc.load()
+
+
+def _visible(cfg, seq):
+    """[lo, hi) of each request's visible keys: the union of its q_len queries'
+    windows (all keys up to the block's last on full-attention layers)."""
+    L, w = cfg["q_len"], cfg["window"]
+    hi = seq.astype(np.int64) + L
+    lo = np.maximum(0, seq.astype(np.int64) - w + 1) if w > 0 else np.zeros_like(hi)
+    return lo, hi
+
+
+def _check_cover(cfg, seq, items):
+    lo, hi = _visible(cfg, seq)
+    B = len(seq)
+    by_req = [[] for _ in range(B)]
+    for b, j0, j1 in items:
+        assert 0 <= b < B and j0 < j1
+        by_req[b].append((int(j0), int(j1)))
+    for b in range(B):
+        r = sorted(by_req[b])
+        assert r, f"request {b} has no work item"
+        assert r[0][0] == lo[b] and r[-1][1] == hi[b]
+        for (a0, a1), (b0, b1) in zip(r, r[1:]):
+            assert a1 == b0, f"request {b}: gap or overlap at {a1}/{b0}"
+    return by_req
+
+
+def _pad(cfg, opts=None):
+    tc = 2 <= cfg["q_len"] <= 8 and not ((opts or {}).get("flags", 0) & okc.PLAN_NO_TCGEN05)
+    return 7 if tc and cfg["page_size"] >= 8 else 0
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_workload_plans_cover_every_key_once(name):
+    cfg = W.config(name)
+    seq = W.lengths(cfg)
+    items = okc.okc_attn_plan_items(cfg, seq, HOST)
+    by_req = _check_cover(cfg, seq, items)
+    sizes = okc.okc_attn_plan_sizes(cfg, seq, HOST)
+    assert sizes["num_work"] == len(items)
+    assert sizes["max_chunks"] == max(len(r) for r in by_req)
+    # launch order: the largest items first
+    lens = items[:, 2] - items[:, 1]
+    assert np.all(np.diff(lens) <= 0)
+    # every item but a request's last has the same size, whole 64-key tiles
+    pad = _pad(cfg)
+    for r in by_req:
+        full = {j1 - j0 for j0, j1 in r[:-1]}
+        assert len(full) <= 1
+        if full:
+            c = full.pop()
+            assert (c + pad) % 64 == 0, c
+            assert r[-1][1] - r[-1][0] <= c
+    # at most four waves of the resident slots (or one item per request)
+    assert len(items) <= max(len(seq), 4 * SMS * CTAS)
+
+
+def test_step_form_rule_on_the_workloads():
+    """One kernel for q_len 1 when the items fill at least half the slots with
+    chunks of <= 2048 keys or take more than one wave; else three."""
+    want = {"tiny_sliding_decode": 3, "sliding_decode": 1, "full_decode_32k": 3, "verify_block": 3,
+            "mixed_full_decode": 1}
+    for name, k in want.items():
+        cfg = W.config(name)
+        seq = W.lengths(cfg)
+        assert okc.okc_attn_plan_sizes(cfg, seq, HOST)["step_kernels"] == k, name
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_batches(seed):
+    rng = np.random.default_rng(7000 + seed)
+    L = int(rng.choice([1, 2, 4, 8, 12]))
+    P = int(rng.choice([1, 8, 16, 64]))
+    window = int(rng.choice([0, 1, 64, 2048]))
+    B = int(rng.integers(1, 300))
+    seq = rng.integers(0, 40000, size=B).astype(np.int32)
+    max_pages = (int(seq.max()) + L + P - 1) // P + 1
+    cfg = dict(W.config("tiny_sliding_decode"), batch=B, q_len=L, page_size=P, window=window,
+               max_pages=max_pages, num_pages=B * max_pages)
+    opts = dict(HOST, ctas_per_sm=int(rng.integers(1, 5)))
+    items = okc.okc_attn_plan_items(cfg, seq, opts)
+    by_req = _check_cover(cfg, seq, items)
+    pad = _pad(cfg)
+    for r in by_req:
+        if len(r) > 1:
+            assert (r[0][1] - r[0][0] + pad) % 64 == 0
+    assert len(items) <= max(B, 4 * SMS * opts["ctas_per_sm"])
+    # a forced split size is used as given
+    forced = okc.okc_attn_plan_items(cfg, seq, dict(opts, chunk_keys=100))
+    for r in _check_cover(cfg, seq, forced):
+        assert all(j1 - j0 == 100 for j0, j1 in r[:-1])
+
+
+def test_edge_cases():
+    cfg = dict(W.config("tiny_sliding_decode"), batch=3, q_len=8, window=2048, page_size=16,
+               max_pages=4, num_pages=12)
+    seq = np.array([0, 1, 40], np.int32)
+    items = okc.okc_attn_plan_items(cfg, seq, HOST)
+    _check_cover(cfg, seq, items)
+    assert len(items) == 3  # short requests: one item each
+    empty = dict(cfg, batch=0)
+    assert len(okc.okc_attn_plan_items(empty, np.zeros(0, np.int32), HOST)) == 0
+    # a context past the page table is rejected on the host
+    with pytest.raises(okc.OkcError):
+        okc.okc_attn_plan_items(cfg, np.array([0, 1, 4 * 16], np.int32), HOST)

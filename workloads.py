@@ -80,6 +80,18 @@ def _e4m3_normal_fill(rng: np.random.Generator, n: int, chunk: int = 1 << 24) ->
     return out
 
 
+def lengths(cfg: dict, seed: int | None = None) -> np.ndarray:
+    """The seq_lens generate() draws for cfg (the same first draw of the same
+    seed), without building the caches; also fills cfg's max_pages / num_pages."""
+    rng = np.random.default_rng(cfg["seed"] if seed is None else seed)
+    B, L, P = cfg["batch"], cfg["q_len"], cfg["page_size"]
+    seq = _seq_lens(rng, cfg["seq"], B)
+    n_pages = (seq.astype(np.int64) + L + P - 1) // P
+    cfg["max_pages"] = max(1, int(n_pages.max())) if B else 1
+    cfg["num_pages"] = max(1, int(n_pages.sum()))
+    return seq
+
+
 def generate(cfg: dict, seed: int | None = None) -> dict:
     """Build one step's inputs as numpy arrays; also fills cfg's max_pages / num_pages."""
     rng = np.random.default_rng(cfg["seed"] if seed is None else seed)
