@@ -314,7 +314,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     }
     if (bad_page && ch == 0) set_error(a.err, OKC_DEVERR_PAGE);
     if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
-    cp_async_wait<0>();  // this warp's copies have landed before it leaves
+    cp_async_wait_all();  // this warp's copies have landed before it leaves
     return;
   }
 

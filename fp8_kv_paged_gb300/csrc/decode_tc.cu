@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
         if (!mbar_wait(full_bar(k % kTcStages), (k / kTcStages) & 1)) ok = false;
     }
     if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
-    cp_async_wait<0>();
+    cp_async_wait_all();
     return;
   }
 
