@@ -49,11 +49,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("sliding_decode", "decode_kernel<fused step>"): 33.079552e6 + 13.824e3,
-    ("verify_block", "decode_tc_kernel"): 17.207040e6 + 0.0,
-    ("full_decode_32k", "decode_kernel"): 545.488128e6 + 3.42912e6,
+    ("sliding_decode", "decode_kernel<fused step>"): 33.0816e6 + 8.96e3,
+    ("verify_block", "decode_tc_kernel"): 17.207552e6 + 0.0,
+    ("full_decode_32k", "decode_kernel"): 545.487872e6 + 3.411968e6,
     ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
-    ("mixed_full_decode", "decode_kernel<fused step>"): 803.080448e6 + 7.500032e6,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 803.03872e6 + 7.589632e6,
 }
 WORKLOAD = "sliding_decode"
 FALLBACK_HBM_GBS = 6800.0
