@@ -86,9 +86,19 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
   // (key counts and budgets are below 2^31: 32-bit divisions)
   auto cdiv = [](int64_t a, int64_t b) { return (int64_t)(((uint32_t)a + (uint32_t)b - 1u) / (uint32_t)b); };
+  // On window layers every request whose context fills the window sees the
+  // same window + L - 1 keys: the search counts those once (times their number).
+  const int64_t nsat = c->window > 0 ? (int64_t)c->window + L - 1 : -1;
+  int64_t n_at_sat = 0;
+  std::vector<int64_t> rest;
+  rest.reserve((size_t)B);
+  for (int b = 0; b < B; b++) {
+    if (nvis[b] == nsat) n_at_sat++;
+    else rest.push_back(nvis[b]);
+  }
   auto items = [&](int64_t C) {
-    int64_t w = 0;
-    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, cdiv(nvis[b], C));
+    int64_t w = n_at_sat ? n_at_sat * std::max<int64_t>(1, cdiv(nsat, C)) : 0;
+    for (const int64_t v : rest) w += std::max<int64_t>(1, cdiv(v, C));
     return w;
   };
   int64_t Cbud = std::max<int64_t>(min_chunk, nmax);
@@ -111,10 +121,9 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
       }
       const int64_t C = lo_c, W = items(C);
       int64_t biggest = 0;
-      for (int b = 0; b < B; b++) {
-        const int64_t k = std::max<int64_t>(1, cdiv(nvis[b], C));
-        biggest = std::max(biggest, cdiv(nvis[b], k));
-      }
+      auto item_keys = [&](int64_t v) { return cdiv(v, std::max<int64_t>(1, cdiv(v, C))); };
+      if (n_at_sat) biggest = item_keys(nsat);
+      for (const int64_t v : rest) biggest = std::max(biggest, item_keys(v));
       const double mean = (double)(total + W * kItemCost) / (double)W;
       const double waves = (double)((W + slots - 1) / slots);
       const double score = std::max((double)(biggest + kItemCost), waves * mean);
