@@ -190,7 +190,7 @@ class Plan:
 
     def __init__(self, handle, cfg, workspace):
         self.handle = handle
-        self.cfg = dict(cfg)
+        self.cfg = cfg  # the caller's config (not copied: plans are made every step)
         self.workspace = workspace  # keep the device buffer alive with the plan
 
     @property
