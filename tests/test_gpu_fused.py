@@ -139,3 +139,42 @@ def test_step_from_host_buffers(name, memory):
     assert step.errors() == 0
     assert np.array_equal(host["out"].numpy().view(np.uint16), ref["out"])
     assert np.array_equal(d["k_cache"].cpu().numpy(), ref["k_cache"])
+
+
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block", "tiny_sliding_decode"])
+def test_step_replays_from_a_cuda_graph(name):
+    """okc_attn_step captured in a CUDA graph and replayed after the caller
+    rewrote its input buffers (new qkv, new cache contents, same lengths) gives
+    the eager result for the new contents, bit for bit: the kernels read every
+    input and length from device memory when they run."""
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    other = W.generate(dict(cfg), seed=cfg["seed"] + 101)
+    inp2 = dict(inp, qkv=other["qkv"], k_cache=np.roll(inp["k_cache"], 3), v_cache=np.roll(inp["v_cache"], 5))
+    d = to_device(cfg, inp)
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step.run_fused(d, eps=inp["eps"], stream=s)  # warm the launch path
+    s.synchronize()
+    d = to_device(cfg, inp)  # fresh caches: the warm-up wrote the new rows
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run_fused(d, eps=inp["eps"], stream=s)
+    for case in (inp, inp2):
+        fresh = to_device(cfg, case)
+        for k in ("qkv", "k_cache", "v_cache"):
+            d[k].copy_(fresh[k])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        got_out = step.out.view(torch.int16).cpu().numpy().view(np.uint16)
+        got_k = d["k_cache"].cpu().numpy()
+        ref = run_gpu(cfg, case, plan_form=True, fused=True)
+        assert step.errors() == 0
+        assert np.array_equal(got_out, ref["out"])
+        assert np.array_equal(got_k, ref["k_cache"])
