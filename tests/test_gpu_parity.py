@@ -133,6 +133,19 @@ def test_plan_lengths_longer_than_device_lengths(fused):
     full_check(cfg, inp, opts={"chunk_keys": 96}, plan_seq=plan_seq, fused=fused)
 
 
+def test_plan_lengths_longer_than_device_lengths_verify_block():
+    """The same for a verify block on 64-row pages: the tcgen05 decode's TMA
+    tiles start from the device lengths' key ranges (rounded down to 8)."""
+    cfg = W.config("verify_block", batch=5, seq=("uniform", 300, 3000))
+    inp = W.generate(cfg)
+    pad = np.full((cfg["batch"], 2), -1, np.int32)  # room in the page table for the plan's lengths
+    inp["page_table"] = np.concatenate([inp["page_table"], pad], axis=1)
+    cfg["max_pages"] += 2
+    plan_seq = inp["seq_lens"] + 45
+    full_check(cfg, inp, plan_seq=plan_seq)
+    full_check(cfg, inp, opts={"chunk_keys": 200}, plan_seq=plan_seq)
+
+
 @pytest.mark.parametrize("seq,L,P,kv_scale", [
     ([100, 300], 8, 64, 0.5),
     ([2100, 2600, 4000, 70], 8, 64, 0.5),
