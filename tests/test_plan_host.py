@@ -124,3 +124,31 @@ def test_edge_cases():
     # a context past the page table is rejected on the host
     with pytest.raises(okc.OkcError):
         okc.okc_attn_plan_items(cfg, np.array([0, 1, 4 * 16], np.int32), HOST)
+
+
+def test_items_capacity_and_count_only():
+    """count-only query (items NULL, capacity 0), a too-small buffer
+    (OKC_ERR_WORKSPACE with the count set), and the exact buffer."""
+    import ctypes
+    lib = okc.load()
+    cfg = W.config("sliding_decode")
+    seq = np.ascontiguousarray(W.lengths(cfg), dtype=np.int32)
+    c = okc._config(cfg)
+    o = okc._options(HOST)
+    n = ctypes.c_int32(-1)
+    sp = seq.ctypes.data_as(ctypes.c_void_p)
+    assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, None, 0, ctypes.byref(n)) == okc.OK
+    total = n.value
+    assert total == okc.okc_attn_plan_sizes(cfg, seq, HOST)["num_work"]
+    small = np.zeros((total - 1, 3), np.int32)
+    n.value = -1
+    st = lib.okc_attn_plan_items(ctypes.byref(c), sp, o, small.ctypes.data_as(ctypes.c_void_p), total - 1,
+                                 ctypes.byref(n))
+    assert st == okc.ERR_WORKSPACE and n.value == total
+    full = np.zeros((total, 3), np.int32)
+    assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, full.ctypes.data_as(ctypes.c_void_p), total,
+                                   ctypes.byref(n)) == okc.OK
+    assert np.array_equal(full, okc.okc_attn_plan_items(cfg, seq, HOST))
+    # a null count or a negative capacity is an argument error
+    assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, None, 0, None) == okc.ERR_INVALID
+    assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, None, -1, ctypes.byref(n)) == okc.ERR_INVALID
