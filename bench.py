@@ -52,7 +52,6 @@ NCU_TRAFFIC = {
     ("sliding_decode", "decode_kernel<fused step>"): 33.0816e6 + 8.96e3,
     ("verify_block", "decode_tc_kernel"): 17.207552e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.487872e6 + 3.411968e6,
-    ("mixed_full_decode", "decode_kernel"): 799.795456e6 + 5.9712e6,
     ("mixed_full_decode", "decode_kernel<fused step>"): 803.03872e6 + 7.589632e6,
 }
 WORKLOAD = "sliding_decode"
