@@ -50,7 +50,7 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
     ("sliding_decode", "decode_kernel<fused step>"): 33.0816e6 + 8.96e3,
-    ("verify_block", "decode_tc_kernel"): 17.207552e6 + 0.0,
+    ("verify_block", "decode_tc_kernel"): 17.207808e6 + 0.0,
     ("full_decode_32k", "decode_kernel"): 545.487872e6 + 3.411968e6,
     ("mixed_full_decode", "decode_kernel<fused step>"): 803.03872e6 + 7.589632e6,
 }

@@ -8,7 +8,8 @@
 // rows g*64 + i*8 + hh for KV head g, token i, head g*8 + hh; rows of tokens
 // past q_len are zero and ignored) as ONE M = 128 operand:
 //   S [128 x 64 keys]  = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
-//   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16)
+//   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16,
+//                         P read from tensor memory)
 // where column 128 of the B operand is all ones, so O's column 128 is the row
 // sum of P as the tensor core saw it (f16 P, f32 sums): the softmax
 // denominator, consistent with the numerator and kept by the same rescales.
@@ -23,12 +24,12 @@
 // TMA tile loads (8-row boxes, 128-byte swizzle, read by the MMA through a
 // swizzled descriptor), else both warps run the cp.async producer of
 // decode.cu (K rows in the MMA's no-swizzle canonical layout, V rows in a
-// staging tile). Each group j has its own S and O in TMEM and its own P and
-// V^T tiles in shared memory, so one group's softmax overlaps the other
-// group's MMAs. Per tile k of group j:
+// staging tile). Each group j has its own S, P and O in TMEM and its own V^T
+// tile in shared memory, so one group's softmax overlaps the other group's
+// MMAs. Per tile k of group j:
 //   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
 //   group j: wait s_ready_j -> S row from TMEM -> arrive(s_free_j) -> mask; row
-//            max; P = 2^(s - m) (f16) into shared memory; V tile E4M3 -> f16
+//            max; P = 2^(s - m) (f16 pairs) into TMEM (tcgen05.st); V tile E4M3 -> f16
 //            transposed (ldmatrix, exact conversion, stmatrix.trans)
 //            -> arrive(p_ready_j)
 //   MMA:     wait p_ready_j -> free the stage -> O_j += P V -> commit(pv_done_j)
@@ -39,7 +40,7 @@
 // writes O/l (times v_scale) and the base-2 LSE per row, as decode.cu does;
 // the combine kernel merges the splits.
 //
-// Shared-memory operands Q, P, V^T (and K on the cp.async path) use the
+// Shared-memory operands Q, V^T (and K on the cp.async path) use the
 // no-swizzle K-major layout (8-row x 16-byte core matrices; core matrices 128
 // bytes apart along K, 8-row groups 1024 bytes apart for 128-byte rows); K on
 // the TMA path the 128-byte-swizzle K-major layout. Every wait is bounded
@@ -75,10 +76,9 @@ constexpr float kTcRescale = OKC_TC_RESCALE;  // log2 headroom of the reference 
 constexpr int kTcQ = 0;                                              // Q E4M3 [128 x 128 B]
 constexpr int kTcK = kTcQ + kTcRows * 128;                           // K E4M3 [stage][64 x 128 B]
 constexpr int kTcV = kTcK + kTcStages * kTcTileKeys * 128;           // V E4M3 [stage][64 x 144 B]
-constexpr int kTcP = kTcV + kTcStages * kTcTileKeys * kTcVPitch;     // P f16 [group][128 x 64]
 constexpr int kTcPvN = 144;                                          // PV's N: 128 dims + the ones column
 constexpr int kTcVTBytes = kTcPvN * 128;
-constexpr int kTcVT = kTcP + kTcGroups * kTcRows * 128;              // [V | 1]^T f16 [group][144 x 64 keys]
+constexpr int kTcVT = kTcV + kTcStages * kTcTileKeys * kTcVPitch;    // [V | 1]^T f16 [group][144 x 64 keys]
 constexpr int kTcX = kTcVT + kTcGroups * kTcVTBytes;                 // group 1's reference max per row
 constexpr int kTcBar = kTcX + kTcRows * 8;
 // barriers: full[S], empty[S], s_ready[2], p_ready[2], pv_done[2], s_free[2], mma_done
@@ -87,8 +87,10 @@ constexpr int kTcSmem = kTcTmemSlot + 16 + 2048;  // + slack past the last opera
 constexpr uint32_t kTcCols = 512;  // TMEM columns: S_j at 64 j (64), O_j at 128 + 160 j (144)
 __host__ __device__ constexpr uint32_t tc_col_s(int j) { return 64u * j; }
 __host__ __device__ constexpr uint32_t tc_col_o(int j) { return 128u + 160u * j; }
-static_assert(tc_col_o(1) + kTcPvN <= kTcCols, "TMEM columns");
-static_assert(kTcQ % 1024 == 0 && kTcK % 1024 == 0 && kTcP % 1024 == 0 && kTcVT % 1024 == 0, "operand alignment");
+// P_j (f16, two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j
+__host__ __device__ constexpr uint32_t tc_col_p(int j) { return 432u + 32u * j; }
+static_assert(tc_col_o(1) + kTcPvN <= tc_col_p(0) && tc_col_p(1) + 32 <= kTcCols, "TMEM columns");
+static_assert(kTcQ % 1024 == 0 && kTcK % 1024 == 0 && kTcVT % 1024 == 0, "operand alignment");
 
 // Byte offset of (row r, byte kb) in a canonical tile of 128-byte rows.
 __device__ __forceinline__ uint32_t canon(int r, int kb) {
@@ -339,11 +341,11 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
         fence_proxy_async();
         tc_fence_after();
         mbar_arrive(empty_bar(k % kTcStages));  // K read (S_k consumed), V converted: the stage is free
-        const uint32_t pa = sb + kTcP + j * (kTcRows * 128), va = sb + kTcVT + j * kTcVTBytes;
+        const uint32_t va = sb + kTcVT + j * kTcVTBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)  // 64 keys: 16 per instruction
-          umma_f16(tmem + tc_col_o(j), umma_desc(pa + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
-                   umma_desc(va + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_pv, (k >= kTcGroups || kk > 0) ? 1u : 0u);
+          umma_f16_ta(tmem + tc_col_o(j), tmem + tc_col_p(j) + kk * 8,
+                      umma_desc(va + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_pv, (k >= kTcGroups || kk > 0) ? 1u : 0u);
         umma_commit(pv_done(j));
         return true;
       };
@@ -427,7 +429,8 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   const uint32_t tS = t_lane + tc_col_s(jw);              // this row's S
   const uint32_t tO = t_lane + tc_col_o(jw) + 64 * g;      // this row's O half
   const uint32_t tL = t_lane + tc_col_o(jw) + 128;         // this row's P sum
-  const uint32_t sP = kTcP + jw * (kTcRows * 128), sVT = kTcVT + jw * kTcVTBytes;
+  const uint32_t tP = t_lane + tc_col_p(jw);               // this row's P (f16 pairs)
+  const uint32_t sVT = kTcVT + jw * kTcVTBytes;
   float m = -INFINITY;  // reference max (log2 units)
   bool ok = true;
   int last = -1;  // this group's last tile
@@ -487,18 +490,16 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     }
     m = m_new;
     const float m_use = m == -INFINITY ? 0.f : m;
-    // ---- P row (f16) into this group's canonical A tile, 8 keys per 16-byte
-    // chunk: p = 2^(s * scale - m) in f32, rounded to f16
+    // ---- P row (f16) into this group's TMEM P columns (the PV's A operand),
+    // two keys per column: p = 2^(s * scale - m) in f32, rounded to f16
+    {
+      uint32_t pw[32];
 #pragma unroll
-    for (int c8 = 0; c8 < 8; c8++) {
-      uint32_t pw4[4];
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const int c = c8 * 8 + 2 * e;
-        const float x0 = c < 32 ? s0[c] : s1[c - 32], x1 = c + 1 < 32 ? s0[c + 1] : s1[c - 31];
-        pw4[e] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
+      for (int c = 0; c < 32; c++) {
+        const float x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32], x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+        pw[c] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
       }
-      *reinterpret_cast<uint4*>(smem + sP + canon(r, c8 * 16)) = make_uint4(pw4[0], pw4[1], pw4[2], pw4[3]);
+      tmem_st32u(tP, pw);
     }
     // ---- V tile E4M3 -> f16, transposed into this group's canonical B tile
     // (dims x keys). Warp w of the group converts key groups 2w, 2w+1 (8 keys
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
         }
       }
     }
-    fence_proxy_async();  // P and V^T, written through the generic proxy, for the MMA
+    fence_proxy_async();  // V^T, written through the generic proxy, for the MMA
     tc_fence_before();
     mbar_arrive(p_ready(jw));
     last = k;
