@@ -185,15 +185,9 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t sbo
 __host__ __device__ constexpr uint32_t umma_idesc(uint32_t ab, int M, int N) {
   return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// The same with A read from tensor memory (lane = row, 32-bit columns holding
-// two f16 values each, lower K index in the low half).
+// kind::f16 MMA (f16 x f16 -> f32 in TMEM) with A read from tensor memory (lane
+// = row, 32-bit columns holding two f16 values each, lower K index in the low
+// half) and B from shared memory.
 __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                             uint32_t acc) {
   asm volatile(
