@@ -445,7 +445,7 @@ def main():
 
 
 def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
-    """Per step: plan from host seq_lens, the step's inputs from pinned host
+    """Per step: the plan re-made in place from the host seq_lens, the step's inputs from pinned host
     memory (okc_attn_step_host: read in place by the kernels; the three calls:
     copied to device buffers first), the step, the output back in host memory;
     K steps timed on the host clock. h2d counts the host input bytes the step
@@ -473,13 +473,14 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
 
     io = okc.HostStepIO(dict(pinned, out=out_host), dict({k: dev_in[k] for k in names}, out=out))
 
+    plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
+
     def one():
-        plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
-        if fused:  # one C call: host->device copies, the step, device->host copy, synchronize
+        plan.update(inp["seq_lens"], stream)  # the step's plan, re-made in place from the host lengths
+        if fused:  # one C call: the step from host buffers, output in host memory, synchronize
             okc.okc_attn_step_host(plan, io, None, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
                                    dev_in["v_scale"], dev_in["rope_table"], dev_in["norm_weight"], inp["eps"],
                                    op, lp, stream)
-            plan.close()
             return
         for k in names:
             dev_in[k].copy_(pinned[k], non_blocking=True)
@@ -493,7 +494,6 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
                                       stream)
         out_host.copy_(out, non_blocking=True)
         stream.synchronize()
-        plan.close()
 
     with torch.cuda.stream(stream):
         for _ in range(5):
@@ -503,9 +503,10 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
         for _ in range(steps):
             one()
         el = time.perf_counter() - t0
+    plan.close()
     return {"value": T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": 1000.0 * el / steps, "steps": steps,
-            "api": "okc_attn_plan + okc_attn_step_host" if fused else "okc_attn_plan + three calls"}
+            "api": "okc_attn_plan_update + okc_attn_step_host" if fused else "okc_attn_plan_update + three calls"}
 
 
 if __name__ == "__main__":

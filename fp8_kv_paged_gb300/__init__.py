@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
-    "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items",
+    "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items", "okc_attn_plan_update",
 ]
 
 
@@ -102,6 +102,8 @@ def load(path: str | None = None):
     lib.okc_attn_plan.restype = st
     lib.okc_attn_plan.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options), P,
                                   ctypes.c_size_t, P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.okc_attn_plan_update.restype = st
+    lib.okc_attn_plan_update.argtypes = [P, P, P]
     lib.okc_attn_plan_destroy.restype = st
     lib.okc_attn_plan_destroy.argtypes = [P]
     lib.okc_attn_plan_get_sizes.restype = st
@@ -192,6 +194,13 @@ class Plan:
         self.handle = handle
         self.cfg = cfg  # the caller's config (not copied: plans are made every step)
         self.workspace = workspace  # keep the device buffer alive with the plan
+
+    def update(self, seq_lens_host, stream=None):
+        """Re-plan in place for the next step's host lengths (see the header)."""
+        seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+        _check(load().okc_attn_plan_update(self.handle, seq.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+               "okc_attn_plan_update")
+        return self
 
     @property
     def sizes(self) -> dict:

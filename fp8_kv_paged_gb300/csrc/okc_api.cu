@@ -274,6 +274,38 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The plan takes a split result: sizes, work list, request table, and the
+// workspace layout (error word | work list | request table | arrival counters | q).
+void set_splits(okc_attn_plan_s* p, SplitResult& s, const okc_attn_sizes& z) {
+  p->sizes = z;
+  p->work.swap(s.work);
+  p->req.swap(s.req);
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  p->d_err = reinterpret_cast<unsigned*>(ws);
+  p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
+  p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
+  p->d_tickets =
+      reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
+  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(p->cfg.batch * sizeof(int32_t));
+}
+
+// Bytes of the workspace head the plan uploads (everything before q).
+size_t upload_bytes(const okc_attn_plan_s* p) {
+  return static_cast<size_t>(p->d_q8 - static_cast<uint8_t*>(p->workspace));
+}
+
+// The work list and request table at their workspace offsets in a zeroed
+// host image of the head (the error word and arrival counters stay zero).
+void write_head(const okc_attn_plan_s* p, uint8_t* head) {
+  const uint8_t* ws = static_cast<const uint8_t*>(p->workspace);
+  if (!p->work.empty())
+    std::memcpy(head + (reinterpret_cast<const uint8_t*>(p->d_work) - ws), p->work.data(),
+                p->work.size() * sizeof(WorkItem));
+  if (!p->req.empty())
+    std::memcpy(head + (reinterpret_cast<const uint8_t*>(p->d_req) - ws), p->req.data(),
+                p->req.size() * sizeof(ReqInfo));
+}
+
 // The device address of a page-locked, device-mapped host buffer, else NULL
 // (pageable or unknown memory).
 const void* mapped_host(const void* p) {
@@ -360,16 +392,9 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   if (!p) return OKC_ERR_INVALID;
   p->cfg = *cfg;
   if (opts) p->opts = *opts; else std::memset(&p->opts, 0, sizeof p->opts);
-  p->sizes = z;
-  p->work = std::move(s.work);
-  p->req = std::move(s.req);
   p->workspace = workspace;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p->d_err = reinterpret_cast<unsigned*>(ws);
-  p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
-  p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
-  p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
-  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(cfg->batch * sizeof(int32_t));
+  p->workspace_bytes = workspace_bytes;
+  p->slots = slots;
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
@@ -377,19 +402,14 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   // softmax scale: the float32 value of sm_scale * qk_scale_factor, in base 2
   const float scale = (float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
   p->scale_log2 = (float)((double)scale * 1.4426950408889634);
-
+  set_splits(p, s, z);
   // One upload of the workspace's head: the zeroed error word, the work list,
   // the request table and the zeroed arrival counters, as laid out on the device.
-  const size_t up_bytes = static_cast<size_t>(p->d_q8 - ws);
+  const size_t up_bytes = upload_bytes(p);
   p->upload.assign(up_bytes, 0);
-  if (!p->work.empty())
-    std::memcpy(p->upload.data() + (reinterpret_cast<uint8_t*>(p->d_work) - ws), p->work.data(),
-                p->work.size() * sizeof(WorkItem));
-  if (!p->req.empty())
-    std::memcpy(p->upload.data() + (reinterpret_cast<uint8_t*>(p->d_req) - ws), p->req.data(),
-                p->req.size() * sizeof(ReqInfo));
+  write_head(p, p->upload.data());
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(ws, p->upload.data(), up_bytes, cudaMemcpyHostToDevice, str);
+  cudaError_t e = cudaMemcpyAsync(workspace, p->upload.data(), up_bytes, cudaMemcpyHostToDevice, str);
   if (e != cudaSuccess) {
     delete p;
     return OKC_ERR_CUDA;
@@ -398,7 +418,61 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   return OKC_OK;
 }
 
+okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream) {
+  if (!plan || (plan->cfg.batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
+  SplitResult s;
+  s.work.swap(plan->work);  // reuse the vectors' capacity
+  s.req.swap(plan->req);
+  okc_status st = make_splits(&plan->cfg, seq_lens_host, &plan->opts, plan->slots, &s);
+  if (st != OKC_OK) {
+    s.work.swap(plan->work);
+    s.req.swap(plan->req);
+    return st;
+  }
+  okc_attn_sizes z;
+  compute_sizes(&plan->cfg, s, &z);
+  z.step_kernels = step_kernels(&plan->cfg, s, &plan->opts, plan->slots);
+  if (plan->workspace_bytes < z.workspace_bytes) {
+    s.work.swap(plan->work);
+    s.req.swap(plan->req);
+    return OKC_ERR_WORKSPACE;
+  }
+  set_splits(plan, s, z);
+  const size_t up_bytes = upload_bytes(plan);
+  // the staging buffer may still feed the previous update's copy
+  if (plan->pinned_done && cudaEventSynchronize(plan->pinned_done) != cudaSuccess) return OKC_ERR_CUDA;
+  if (plan->pinned_bytes < up_bytes) {
+    if (plan->pinned) cudaFreeHost(plan->pinned);
+    plan->pinned = nullptr;
+    plan->pinned_bytes = 0;
+    const size_t want = std::max<size_t>(up_bytes, 64 * 1024);
+    if (cudaMallocHost(&plan->pinned, want) != cudaSuccess) {
+      plan->pinned = nullptr;
+      return OKC_ERR_CUDA;
+    }
+    plan->pinned_bytes = want;
+  }
+  if (!plan->pinned_done && cudaEventCreateWithFlags(&plan->pinned_done, cudaEventDisableTiming) != cudaSuccess) {
+    plan->pinned_done = nullptr;
+    return OKC_ERR_CUDA;
+  }
+  uint8_t* head = static_cast<uint8_t*>(plan->pinned);
+  std::memset(head, 0, up_bytes);
+  write_head(plan, head);
+  cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(plan->workspace, head, up_bytes, cudaMemcpyHostToDevice, str) != cudaSuccess ||
+      cudaEventRecord(plan->pinned_done, str) != cudaSuccess)
+    return OKC_ERR_CUDA;
+  return OKC_OK;
+}
+
 okc_status okc_attn_plan_destroy(okc_attn_plan_t plan) {
+  if (!plan) return OKC_OK;
+  if (plan->pinned_done) {
+    cudaEventSynchronize(plan->pinned_done);  // the staging buffer's last copy
+    cudaEventDestroy(plan->pinned_done);
+  }
+  if (plan->pinned) cudaFreeHost(plan->pinned);
   delete plan;
   return OKC_OK;
 }

@@ -102,6 +102,13 @@ struct okc_attn_plan_s {
   std::vector<okc::ReqInfo> req;
   std::vector<uint8_t> upload;  // the workspace head as uploaded (one host-to-device copy)
   void* workspace;
+  size_t workspace_bytes;
+  int slots;                    // resident CTA slots the splits were made for
+  // okc_attn_plan_update: a page-locked staging buffer for the upload (grown on
+  // demand) and the event of its last copy (the buffer is reused after it)
+  void* pinned = nullptr;
+  size_t pinned_bytes = 0;
+  cudaEvent_t pinned_done = nullptr;
   unsigned* d_err;
   okc::WorkItem* d_work;
   okc::ReqInfo* d_req;

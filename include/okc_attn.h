@@ -155,6 +155,21 @@ okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_le
 okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                          const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
                          okc_stream stream, okc_attn_plan_t* plan_out);
+/*
+ * Re-plans an existing plan in place for the next step's host lengths (same
+ * config, options and workspace): the split list is recomputed and uploaded
+ * asynchronously on `stream`, like okc_attn_plan, without creating a plan. The
+ * first call allocates a page-locked staging buffer for the upload (freed by
+ * okc_attn_plan_destroy); later calls allocate nothing while the head fits it,
+ * and wait for the staging buffer's previous copy before reusing it. The
+ * scratch sizes may change with the lengths: read them with
+ * okc_attn_plan_get_sizes. Returns OKC_ERR_WORKSPACE, leaving the plan as it
+ * was, when the new plan needs a larger workspace than the plan was made with.
+ * The workspace is overwritten in stream order: kernels of the previous step
+ * issued on other streams must be ordered before the call.
+ */
+okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream);
+
 okc_status okc_attn_plan_destroy(okc_attn_plan_t plan);
 okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
 /* Synchronizes `stream`, then reads and returns the OKC_DEVERR_* bits seen so far. */

@@ -178,3 +178,54 @@ def test_step_replays_from_a_cuda_graph(name):
         assert step.errors() == 0
         assert np.array_equal(got_out, ref["out"])
         assert np.array_equal(got_k, ref["k_cache"])
+
+
+def _shorter(cfg, inp, d):
+    """The same batch d tokens earlier: every context d keys shorter (same
+    caches and page table, positions and cache rows moved back)."""
+    out = dict(inp)
+    out["seq_lens"] = inp["seq_lens"] - d
+    out["cache_seqlens"] = inp["cache_seqlens"] - d
+    out["positions"] = inp["positions"] - d
+    P, L = cfg["page_size"], cfg["q_len"]
+    req = np.repeat(np.arange(cfg["batch"]), L)
+    pos = out["positions"]
+    out["cache_loc"] = inp["page_table"][req, pos // P].astype(np.int64) * P + pos % P
+    return out
+
+
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block"])
+def test_plan_update_in_place_matches_a_fresh_plan(name):
+    """okc_attn_plan_update re-plans an existing plan for the next lengths: the
+    step then equals one made with a fresh plan bit for bit; a workspace too
+    small for the new plan is refused and the plan keeps its previous split."""
+    import fp8_kv_paged_gb300 as okc
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    shorter = _shorter(cfg, inp, 150)
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    for case in (shorter, inp, shorter):
+        step.plan.update(case["seq_lens"])
+        z = step.plan.sizes
+        assert z == okc.okc_attn_plan_sizes(cfg, case["seq_lens"])
+        assert z["o_partial_bytes"] <= step.o_partial.numel() * 4
+        d = to_device(cfg, case)
+        out = step.run_fused(d, eps=case["eps"])
+        import torch
+        torch.cuda.synchronize()
+        ref = run_gpu(cfg, case, plan_form=True, fused=True)
+        assert step.errors() == 0
+        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+    # a plan whose workspace fits only short contexts refuses longer ones
+    tiny = {k: (np.minimum(v, 40) if k == "seq_lens" else v) for k, v in inp.items()}
+    import torch
+    sz = okc.okc_attn_plan_sizes(cfg, tiny["seq_lens"])
+    big = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"])
+    if big["workspace_bytes"] > sz["workspace_bytes"]:
+        ws = torch.empty(sz["workspace_bytes"], dtype=torch.uint8, device="cuda")
+        plan = okc.okc_attn_plan(cfg, tiny["seq_lens"], ws)
+        with pytest.raises(okc.OkcError):
+            plan.update(inp["seq_lens"])
+        assert plan.sizes == sz
+        plan.close()
