@@ -15,7 +15,8 @@ import numpy as np
 
 from . import build as _build_mod
 
-__all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_sizes", "okc_attn_plan_items",
+__all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_create", "okc_attn_plan_sizes",
+           "okc_attn_plan_items", "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
@@ -35,6 +36,8 @@ EXPORTED_SYMBOLS = [
     "okc_attn_plan_read_errors", "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
     "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items", "okc_attn_plan_update",
+    "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size", "okc_attn_plan_create",
+    "okc_attn_plan_scratch_sizes",
 ]
 
 
@@ -102,6 +105,16 @@ def load(path: str | None = None):
     lib.okc_attn_plan.restype = st
     lib.okc_attn_plan.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options), P,
                                   ctypes.c_size_t, P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.okc_attn_plan_max_sizes.restype = st
+    lib.okc_attn_plan_max_sizes.argtypes = [ctypes.POINTER(_Config), i32, ctypes.POINTER(_Options),
+                                            ctypes.POINTER(_Sizes)]
+    lib.okc_attn_plan_workspace_size.restype = st
+    lib.okc_attn_plan_workspace_size.argtypes = [ctypes.POINTER(_Config), i32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.okc_attn_plan_create.restype = st
+    lib.okc_attn_plan_create.argtypes = [ctypes.POINTER(_Config), P, P, ctypes.c_size_t, P,
+                                         ctypes.POINTER(ctypes.c_void_p)]
+    lib.okc_attn_plan_scratch_sizes.restype = st
+    lib.okc_attn_plan_scratch_sizes.argtypes = [P, ctypes.POINTER(_Sizes)]
     lib.okc_attn_plan_update.restype = st
     lib.okc_attn_plan_update.argtypes = [P, P, P]
     lib.okc_attn_plan_destroy.restype = st
@@ -134,14 +147,14 @@ def _check(status: int, where: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
         import torch
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+    return stream if isinstance(stream, int) else stream.cuda_stream
 
 
 def _config(cfg: dict) -> _Config:
@@ -166,9 +179,25 @@ def okc_attn_plan_sizes(cfg: dict, seq_lens_host, opts: dict | None = None) -> d
     lib = load()
     seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
     z = _Sizes()
-    _check(lib.okc_attn_plan_sizes(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p),
+    _check(lib.okc_attn_plan_sizes(ctypes.byref(_config(cfg)), seq.ctypes.data,
                                    _options(opts), ctypes.byref(z)), "okc_attn_plan_sizes")
     return _sizes_dict(z)
+
+
+def okc_attn_plan_max_sizes(cfg: dict, max_context: int, opts: dict | None = None) -> dict:
+    """Bounds of okc_attn_plan_sizes over every step whose requests hold at
+    most max_context tokens after it (see the header)."""
+    z = _Sizes()
+    _check(load().okc_attn_plan_max_sizes(ctypes.byref(_config(cfg)), max_context, _options(opts), ctypes.byref(z)),
+           "okc_attn_plan_max_sizes")
+    return _sizes_dict(z)
+
+
+def okc_attn_plan_workspace_size(cfg: dict, max_total_ctx: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().okc_attn_plan_workspace_size(ctypes.byref(_config(cfg)), max_total_ctx, ctypes.byref(n)),
+           "okc_attn_plan_workspace_size")
+    return n.value
 
 
 def okc_attn_plan_items(cfg: dict, seq_lens_host, opts: dict | None = None) -> np.ndarray:
@@ -178,11 +207,11 @@ def okc_attn_plan_items(cfg: dict, seq_lens_host, opts: dict | None = None) -> n
     lib = load()
     seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
     n = ctypes.c_int32(0)
-    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _options(opts),
+    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data, _options(opts),
                                    None, 0, ctypes.byref(n)), "okc_attn_plan_items")
     out = np.zeros((n.value, 3), dtype=np.int32)
-    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _options(opts),
-                                   out.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n)),
+    _check(lib.okc_attn_plan_items(ctypes.byref(_config(cfg)), seq.ctypes.data, _options(opts),
+                                   out.ctypes.data, n.value, ctypes.byref(n)),
            "okc_attn_plan_items")
     return out
 
@@ -198,7 +227,7 @@ class Plan:
     def update(self, seq_lens_host, stream=None):
         """Re-plan in place for the next step's host lengths (see the header)."""
         seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
-        _check(load().okc_attn_plan_update(self.handle, seq.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+        _check(load().okc_attn_plan_update(self.handle, seq.ctypes.data, _stream(stream)),
                "okc_attn_plan_update")
         return self
 
@@ -206,6 +235,11 @@ class Plan:
     def sizes(self) -> dict:
         z = _Sizes()
         _check(load().okc_attn_plan_get_sizes(self.handle, ctypes.byref(z)), "okc_attn_plan_get_sizes")
+        return _sizes_dict(z)
+
+    def scratch_sizes(self) -> dict:
+        z = _Sizes()
+        _check(load().okc_attn_plan_scratch_sizes(self.handle, ctypes.byref(z)), "okc_attn_plan_scratch_sizes")
         return _sizes_dict(z)
 
     def close(self):
@@ -225,9 +259,20 @@ def okc_attn_plan(cfg: dict, seq_lens_host, workspace, opts: dict | None = None,
     seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
     h = ctypes.c_void_p()
     nbytes = workspace.numel() * workspace.element_size()
-    _check(lib.okc_attn_plan(ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p),
+    _check(lib.okc_attn_plan(ctypes.byref(_config(cfg)), seq.ctypes.data,
                              _options(opts), _ptr(workspace), nbytes, _stream(stream), ctypes.byref(h)),
            "okc_attn_plan")
+    return Plan(h, cfg, workspace)
+
+
+def okc_attn_plan_create(cfg: dict, seq_lens_host, workspace, stream=None) -> Plan:
+    """okc_attn_plan with the default options."""
+    seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    h = ctypes.c_void_p()
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().okc_attn_plan_create(ctypes.byref(_config(cfg)), seq.ctypes.data,
+                                       _ptr(workspace), nbytes, _stream(stream), ctypes.byref(h)),
+           "okc_attn_plan_create")
     return Plan(h, cfg, workspace)
 
 
@@ -319,7 +364,7 @@ def okc_attn_decode_combine_noalloc(cfg: dict, seq_lens_host, q_fp8, k_cache, v_
     callers that cannot allocate device memory (see the header)."""
     seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
     _check(load().okc_attn_decode_combine_noalloc(
-        ctypes.byref(_config(cfg)), seq.ctypes.data_as(ctypes.c_void_p), _ptr(q_fp8), _ptr(k_cache),
+        ctypes.byref(_config(cfg)), seq.ctypes.data, _ptr(q_fp8), _ptr(k_cache),
         _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(cache_seqlens),
         _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(qkv), _ptr(norm_weight), eps, _ptr(out),
         _stream(stream)), "okc_attn_decode_combine_noalloc")

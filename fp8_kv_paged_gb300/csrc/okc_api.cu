@@ -64,6 +64,7 @@ struct SplitResult {
 okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
                        int slots, SplitResult* r) {
   const int B = c->batch, L = c->q_len;
+  if (o && o->chunk_keys != 0 && o->chunk_keys < 16) return OKC_ERR_INVALID;
   std::vector<int64_t> nvis(B);
   int64_t total = 0;
   for (int b = 0; b < B; b++) {
@@ -86,24 +87,46 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
   // (key counts and budgets are below 2^31: 32-bit divisions)
   auto cdiv = [](int64_t a, int64_t b) { return (int64_t)(((uint32_t)a + (uint32_t)b - 1u) / (uint32_t)b); };
-  // On window layers every request whose context fills the window sees the
-  // same window + L - 1 keys: the search counts those once (times their number).
-  const int64_t nsat = c->window > 0 ? (int64_t)c->window + L - 1 : -1;
-  int64_t n_at_sat = 0;
+  // The search evaluates items(C) only at budgets C >= c_floor (the least any
+  // wave count below can pick), where a request of at most c_floor keys is one
+  // item: those are counted once. Requests of the largest size (on window
+  // layers every request whose context fills the window, on full layers a
+  // batch of equal contexts) are counted once times their number.
+  const int64_t c_floor =
+      slots > 0 ? std::max<int64_t>(min_chunk, (total + 4 * (int64_t)slots - 1) / (4 * (int64_t)slots)) : min_chunk;
+  int64_t n_top = 0, n_small = 0, max_small = 0;
   std::vector<int64_t> rest;
   rest.reserve((size_t)B);
   for (int b = 0; b < B; b++) {
-    if (nvis[b] == nsat) n_at_sat++;
-    else rest.push_back(nvis[b]);
+    const int64_t v = nvis[b];
+    if (v == nmax) {
+      n_top++;
+    } else if (v <= c_floor) {
+      n_small++;
+      max_small = std::max(max_small, v);
+    } else {
+      rest.push_back(v);
+    }
   }
+  // items(C) = sum over requests of ceil(n_b / C) (every n_b >= 1): the
+  // quotient from one reciprocal per C, corrected to the exact integer (the
+  // double estimate of a quotient below 2^31 is off by at most one), instead
+  // of a division per request
   auto items = [&](int64_t C) {
-    int64_t w = n_at_sat ? n_at_sat * std::max<int64_t>(1, cdiv(nsat, C)) : 0;
-    for (const int64_t v : rest) w += std::max<int64_t>(1, cdiv(v, C));
+    const double rc = 1.0 / (double)C;
+    auto nch = [&](int64_t v) {
+      int64_t q = (int64_t)((double)(v - 1) * rc);  // floor((v - 1) / C), +-1
+      q -= (int64_t)(q * C > v - 1);
+      q += (int64_t)((q + 1) * C <= v - 1);
+      return q + 1;
+    };
+    int64_t w = n_small + (n_top ? n_top * nch(nmax) : 0);
+    for (const int64_t v : rest) w += nch(v);
     return w;
   };
   int64_t Cbud = std::max<int64_t>(min_chunk, nmax);
   if (slots > 0 && B > 0) {
-    double best = -1.0;
+    double best = -1.0, excess = 0.5 * B;
     const int64_t cmax = std::max<int64_t>(min_chunk, nmax);  // items(cmax) = B
     for (int m = 1; m <= 4; m++) {
       // smallest C in [min_chunk, cmax] with items(C) <= cap (cmax when none).
@@ -115,14 +138,34 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
         lo_c = std::min(cmax, std::max(min_chunk, (total + cap - 1) / cap));
         hi_c = std::min(cmax, std::max(lo_c, (total + cap - B - 1) / (cap - B)));
       }
+      // Safeguarded search: probe where the model items(C) = total / C + e
+      // puts items at cap (e: the excess over total / C seen at the last
+      // probe, between 0 and B), clamped into the bracket, and bisect after a
+      // probe that did not halve it. Every probe keeps the answer inside
+      // [lo_c, hi_c] with items(hi_c) <= cap, so the result is the bisection's,
+      // in a few probes instead of log2 of the bracket.
+      int64_t w_hi = -1;  // items(hi_c), once probed
+      bool model = true;
       while (lo_c < hi_c) {
-        const int64_t mid = (lo_c + hi_c) / 2;
-        if (items(mid) <= cap) hi_c = mid; else lo_c = mid + 1;
+        const int64_t width = hi_c - lo_c;
+        int64_t probe = (lo_c + hi_c) / 2;
+        if (model && (double)cap > excess) {
+          const double g = std::ceil((double)total / ((double)cap - excess));
+          probe = g <= (double)lo_c ? lo_c : g >= (double)(hi_c - 1) ? hi_c - 1 : (int64_t)g;
+        }
+        const int64_t w = items(probe);
+        excess = (double)w - (double)total / (double)probe;
+        if (w <= cap) {
+          hi_c = probe;
+          w_hi = w;
+        } else {
+          lo_c = probe + 1;
+        }
+        model = 2 * (hi_c - lo_c) <= width;
       }
-      const int64_t C = lo_c, W = items(C);
-      int64_t biggest = 0;
+      const int64_t C = lo_c, W = w_hi >= 0 && hi_c == C ? w_hi : items(C);
       auto item_keys = [&](int64_t v) { return cdiv(v, std::max<int64_t>(1, cdiv(v, C))); };
-      if (n_at_sat) biggest = item_keys(nsat);
+      int64_t biggest = std::max(max_small, n_top ? item_keys(nmax) : 0);  // a request of v <= C keys: v
       for (const int64_t v : rest) biggest = std::max(biggest, item_keys(v));
       const double mean = (double)(total + W * kItemCost) / (double)W;
       const double waves = (double)((W + slots - 1) / slots);
@@ -221,9 +264,9 @@ int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_
   return (2 * W >= slots && (max_chunk <= 2048 || W > slots)) ? 1 : 3;
 }
 
-okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {
+// Buffer sizes for W work items (the workspace, q and the split partials).
+void sizes_for(const okc_attn_config* c, int64_t W, int max_chunks, okc_attn_sizes* z) {
   const int64_t T = (int64_t)c->batch * c->q_len;
-  const int64_t W = (int64_t)s.work.size();
   const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
   z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo)) +
@@ -234,9 +277,31 @@ okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_att
   z->lse_partial_bytes = round_up(W * rows * sizeof(float));
   z->num_work = (int32_t)W;
   z->num_tokens = (int32_t)T;
-  z->max_chunks = s.max_chunks;
+  z->max_chunks = max_chunks;
   z->step_kernels = 3;
+}
+
+okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {
+  sizes_for(c, (int64_t)s.work.size(), s.max_chunks, z);
   return OKC_OK;
+}
+
+// Upper bounds of the split counts over every step whose requests each hold at
+// most max_context keys after the step. A request of n visible keys gets
+// ceil(n / chunk_keys) items under a forced chunk size; under the heuristic
+// k = ceil(n / C) items for the budget C >= 128 (its chunk holds at least
+// ceil(n / k) keys), and the budget's work list either fits the m waves it was
+// chosen for (m <= 4: at most 4 x slots items) or is one item per request.
+void split_bounds(const okc_attn_config* c, int64_t max_context, const okc_plan_options* o, int slots,
+                  int64_t* max_work, int64_t* max_chunks) {
+  const int64_t B = c->batch;
+  const int64_t nvis = c->window > 0 ? std::min<int64_t>(max_context, (int64_t)c->window + c->q_len - 1)
+                                     : max_context;
+  const int64_t per = (o && o->chunk_keys > 0) ? o->chunk_keys : 128;
+  const int64_t k = std::max<int64_t>(1, (nvis + per - 1) / per);
+  *max_chunks = k;
+  *max_work = B * k;
+  if (!(o && o->chunk_keys > 0)) *max_work = std::min(*max_work, std::max<int64_t>(B, 4 * (int64_t)slots));
 }
 
 // Step 4 of a 2..8-token block runs on the tcgen05 kernel unless the plan says not to.
@@ -347,6 +412,32 @@ okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_le
   return st;
 }
 
+okc_status okc_attn_plan_max_sizes(const okc_attn_config* cfg, int32_t max_context, const okc_plan_options* opts,
+                                   okc_attn_sizes* sizes) {
+  okc_status st = check_config(cfg);
+  if (st != OKC_OK) return st;
+  if (!sizes || max_context < cfg->q_len || (int64_t)max_context > (int64_t)cfg->max_pages * cfg->page_size)
+    return OKC_ERR_INVALID;
+  if (opts && opts->chunk_keys != 0 && opts->chunk_keys < 16) return OKC_ERR_INVALID;
+  const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
+  if (slots < 0) return OKC_ERR_CUDA;
+  int64_t W = 0, kmax = 0;
+  split_bounds(cfg, max_context, opts, slots, &W, &kmax);
+  if (cfg->batch == 0) W = kmax = 0;
+  if (kmax > (1 << 20) || W > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
+  sizes_for(cfg, W, (int)kmax, sizes);
+  sizes->step_kernels = 0;  // depends on the lengths
+  return OKC_OK;
+}
+
+okc_status okc_attn_plan_workspace_size(const okc_attn_config* cfg, int32_t max_total_ctx, size_t* bytes) {
+  if (!bytes) return OKC_ERR_INVALID;
+  okc_attn_sizes z;
+  const okc_status st = okc_attn_plan_max_sizes(cfg, max_total_ctx, nullptr, &z);
+  if (st == OKC_OK) *bytes = z.workspace_bytes;
+  return st;
+}
+
 okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                                const okc_plan_options* opts, int32_t* items, int32_t capacity,
                                int32_t* count) {
@@ -418,6 +509,11 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   return OKC_OK;
 }
 
+okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_lens_host, void* workspace,
+                                size_t workspace_bytes, okc_stream stream, okc_attn_plan_t* plan_out) {
+  return okc_attn_plan(cfg, seq_lens_host, nullptr, workspace, workspace_bytes, stream, plan_out);
+}
+
 okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream) {
   if (!plan || (plan->cfg.batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
   SplitResult s;
@@ -481,6 +577,10 @@ okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes) 
   if (!plan || !sizes) return OKC_ERR_INVALID;
   *sizes = plan->sizes;
   return OKC_OK;
+}
+
+okc_status okc_attn_plan_scratch_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes) {
+  return okc_attn_plan_get_sizes(plan, sizes);
 }
 
 okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, uint32_t* flags_host) {

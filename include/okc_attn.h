@@ -7,6 +7,7 @@
  * q.to(float8_e4m3fn), flash_attn_with_kvcache, rms_norm_gate). One step of it:
  *
  *   okc_attn_plan              host, once per decode step, shared by all layers
+ *                              (okc_attn_plan_create: the same with default options)
  *   okc_prepare_qkv            steps 1-3: q/k RMSNorm (+RoPE), K/V E4M3 scatter, q E4M3
  *   okc_attn_decode            step 4: split-KV paged causal GQA attention
  *   okc_attn_combine_normgate  split merge fused with step 5, RMSNorm x sigmoid(gate)
@@ -138,6 +139,24 @@ okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_le
                                int32_t* count);
 
 /*
+ * Upper bounds of okc_attn_plan_sizes over every step of this config whose
+ * requests each hold at most max_context tokens after the step
+ * (seq_lens_host[b] + q_len <= max_context), under the same options and on
+ * the same device: buffers of these sizes serve all such steps, so a plan
+ * made in a workspace of workspace_bytes never fails okc_attn_plan_update
+ * with OKC_ERR_WORKSPACE on them, and scratch of these sizes never needs to
+ * grow. num_work and max_chunks are bounds as well; num_tokens is exact;
+ * step_kernels is 0 (it depends on the lengths). Host only (no GPU work; the
+ * device is queried for its SM count and occupancy unless opts give both).
+ * Returns OKC_ERR_INVALID when max_context < q_len or max_context exceeds
+ * max_pages * page_size.
+ */
+okc_status okc_attn_plan_max_sizes(const okc_attn_config* cfg, int32_t max_context, const okc_plan_options* opts,
+                                   okc_attn_sizes* sizes);
+/* The workspace bound of okc_attn_plan_max_sizes with the default options. */
+okc_status okc_attn_plan_workspace_size(const okc_attn_config* cfg, int32_t max_total_ctx, size_t* bytes);
+
+/*
  * okc_attn_plan — the per-step plan ("Differs from SGLang" note of the problem
  * file: positions, cache rows, lengths and the attention schedule are built once
  * per step for all layers). Validates cfg, splits every request's visible keys
@@ -155,6 +174,9 @@ okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_le
 okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                          const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
                          okc_stream stream, okc_attn_plan_t* plan_out);
+/* okc_attn_plan with the default options. */
+okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_lens_host, void* workspace,
+                                size_t workspace_bytes, okc_stream stream, okc_attn_plan_t* plan_out);
 /*
  * Re-plans an existing plan in place for the next step's host lengths (same
  * config, options and workspace): the split list is recomputed and uploaded
@@ -171,7 +193,10 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
 okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream);
 
 okc_status okc_attn_plan_destroy(okc_attn_plan_t plan);
+/* The plan's sizes: the workspace it needs and the caller's scratch (q_fp8 and
+   the split partials) for its step. okc_attn_plan_scratch_sizes is the same call. */
 okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
+okc_status okc_attn_plan_scratch_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
 /* Synchronizes `stream`, then reads and returns the OKC_DEVERR_* bits seen so far. */
 okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, uint32_t* flags_host);
 

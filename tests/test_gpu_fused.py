@@ -229,3 +229,33 @@ def test_plan_update_in_place_matches_a_fresh_plan(name):
             plan.update(inp["seq_lens"])
         assert plan.sizes == sz
         plan.close()
+
+
+def test_workspace_sized_for_the_longest_context_serves_every_update():
+    """A workspace of okc_attn_plan_workspace_size(max context) holds the plan
+    of every step up to that context: okc_attn_plan_create on short contexts,
+    then okc_attn_plan_update to longer ones never runs out of room, and each
+    step's sizes stay within okc_attn_plan_max_sizes (the device's own SM
+    count and occupancy); okc_attn_plan_scratch_sizes equals the plan's sizes."""
+    import torch
+    import fp8_kv_paged_gb300 as okc
+    for name in ("sliding_decode", "verify_block", "mixed_full_decode"):
+        cfg = W.config(name)
+        seq = W.lengths(cfg)
+        max_context = int(seq.max()) + cfg["q_len"]
+        nbytes = okc.okc_attn_plan_workspace_size(cfg, max_context)
+        bound = okc.okc_attn_plan_max_sizes(cfg, max_context)
+        assert nbytes == bound["workspace_bytes"]
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        plan = okc.okc_attn_plan_create(cfg, np.minimum(seq, 5), ws)
+        rng = np.random.default_rng(5)
+        for frac in (0.01, 0.3, 1.0):
+            s = np.minimum(seq, (rng.random(len(seq)) * frac * max_context).astype(np.int32))
+            for case in (s, seq):
+                plan.update(case)
+                z = plan.scratch_sizes()
+                assert z == plan.sizes == okc.okc_attn_plan_sizes(cfg, case)
+                for f in ("workspace_bytes", "q_fp8_bytes", "o_partial_bytes", "lse_partial_bytes", "num_work"):
+                    assert z[f] <= bound[f], (name, f)
+        torch.cuda.synchronize()
+        plan.close()

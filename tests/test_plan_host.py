@@ -152,3 +152,59 @@ def test_items_capacity_and_count_only():
     # a null count or a negative capacity is an argument error
     assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, None, 0, None) == okc.ERR_INVALID
     assert lib.okc_attn_plan_items(ctypes.byref(c), sp, o, None, -1, ctypes.byref(n)) == okc.ERR_INVALID
+
+
+_SIZE_FIELDS = ("workspace_bytes", "q_fp8_bytes", "o_partial_bytes", "lse_partial_bytes", "num_work", "max_chunks")
+
+
+def _within_bounds(cfg, seq, opts, max_context):
+    bound = okc.okc_attn_plan_max_sizes(cfg, max_context, opts)
+    got = okc.okc_attn_plan_sizes(cfg, seq, opts)
+    for f in _SIZE_FIELDS:
+        assert got[f] <= bound[f], (f, got[f], bound[f])
+    assert got["num_tokens"] == bound["num_tokens"]
+    return got, bound
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_max_sizes_bound_every_step(seed):
+    """okc_attn_plan_max_sizes bounds okc_attn_plan_sizes for every batch whose
+    contexts stay within max_context: random lengths, every request at the
+    bound, every request short, forced split sizes, all occupancies."""
+    rng = np.random.default_rng(9100 + seed)
+    L = int(rng.choice([1, 2, 8, 16]))
+    P = int(rng.choice([1, 8, 64]))
+    window = int(rng.choice([0, 64, 2048]))
+    B = int(rng.choice([1, 7, 64, 300, 1500]))
+    max_context = int(rng.integers(L, 140000))
+    max_pages = (max_context + P - 1) // P
+    cfg = dict(W.config("tiny_sliding_decode"), batch=B, q_len=L, page_size=P, window=window,
+               max_pages=max_pages, num_pages=B * max_pages)
+    for opts in (dict(HOST, ctas_per_sm=int(rng.integers(1, 5))), dict(HOST, chunk_keys=int(rng.integers(16, 3000)))):
+        for seq in (rng.integers(0, max_context - L + 1, size=B),
+                    np.full(B, max_context - L),
+                    np.minimum(rng.integers(0, 200, size=B), max_context - L)):
+            _within_bounds(cfg, seq.astype(np.int32), opts, max_context)
+
+
+def test_max_sizes_on_the_workloads_and_errors():
+    """On each workload's shape the bound holds and is at most four waves of
+    items (one per request when requests outnumber them); max_context below
+    q_len or past the page table is an argument error."""
+    for name in W.WORKLOADS:
+        cfg = W.config(name)
+        seq = W.lengths(cfg)
+        max_context = int(seq.max()) + cfg["q_len"]
+        _, bound = _within_bounds(cfg, seq, HOST, max_context)
+        assert bound["num_work"] <= max(cfg["batch"], 4 * SMS * CTAS)
+    cfg = W.config("sliding_decode")
+    seq = W.lengths(cfg)  # (sets the page-table shape in cfg)
+    for bad in (0, cfg["max_pages"] * cfg["page_size"] + 1):
+        with pytest.raises(okc.OkcError) as e:
+            okc.okc_attn_plan_max_sizes(cfg, bad, HOST)
+        assert e.value.status == okc.ERR_INVALID
+    with pytest.raises(okc.OkcError) as e:
+        okc.okc_attn_plan_sizes(cfg, seq, dict(HOST, chunk_keys=15))
+    assert e.value.status == okc.ERR_INVALID
+    empty = dict(cfg, batch=0)
+    assert okc.okc_attn_plan_max_sizes(empty, 10, HOST)["num_work"] == 0
