@@ -19,7 +19,7 @@ __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_
            "okc_attn_plan_items", "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
-           "okc_attn_decode_combine_noalloc", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
+           "okc_attn_decode_combine_noalloc", "okc_selftest_bounded_wait", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
            "EXPORTED_SYMBOLS"]
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
     "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items", "okc_attn_plan_update",
     "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size", "okc_attn_plan_create",
-    "okc_attn_plan_scratch_sizes",
+    "okc_attn_plan_scratch_sizes", "okc_selftest_bounded_wait",
 ]
 
 
@@ -115,6 +115,8 @@ def load(path: str | None = None):
                                          ctypes.POINTER(ctypes.c_void_p)]
     lib.okc_attn_plan_scratch_sizes.restype = st
     lib.okc_attn_plan_scratch_sizes.argtypes = [P, ctypes.POINTER(_Sizes)]
+    lib.okc_selftest_bounded_wait.restype = st
+    lib.okc_selftest_bounded_wait.argtypes = [P, i32, P]
     lib.okc_attn_plan_update.restype = st
     lib.okc_attn_plan_update.argtypes = [P, P, P]
     lib.okc_attn_plan_destroy.restype = st
@@ -281,6 +283,12 @@ def okc_attn_plan_read_errors(plan: Plan, stream=None) -> int:
     _check(load().okc_attn_plan_read_errors(plan.handle, _stream(stream), ctypes.byref(v)),
            "okc_attn_plan_read_errors")
     return v.value
+
+
+def okc_selftest_bounded_wait(err, limit_us: int, stream=None):
+    """Launch the bounded-wait diagnostic (see the header); `err` is a device
+    uint32 tensor that receives OKC_DEVERR_TIMEOUT when the wait gives up."""
+    _check(load().okc_selftest_bounded_wait(_ptr(err), limit_us, _stream(stream)), "okc_selftest_bounded_wait")
 
 
 def okc_rope_table_init(rope_theta: float, num_positions: int, table, stream=None):

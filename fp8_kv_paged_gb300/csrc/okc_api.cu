@@ -382,6 +382,21 @@ const void* mapped_host(const void* p) {
   return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
+// One warp waits on a shared-memory mbarrier that nothing arrives on, with the
+// bounded wait every kernel uses (here limited to limit_ns), and flags the
+// timeout the way the kernels do; the kernel then returns.
+__global__ void bounded_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = okc::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    okc::mbar_init(b, 1);
+    okc::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = okc::mbar_wait(b, 0, limit_ns);
+  if (!__any_sync(0xffffffffu, ok) && threadIdx.x == 0) okc::set_error(err, OKC_DEVERR_TIMEOUT);
+}
+
 }  // namespace
 
 extern "C" {
@@ -591,6 +606,13 @@ okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, ui
   if (cudaStreamSynchronize(s) != cudaSuccess) return OKC_ERR_CUDA;
   *flags_host = v;
   return OKC_OK;
+}
+
+okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream stream) {
+  if (!err || limit_us < 1 || limit_us > 1000000) return OKC_ERR_INVALID;
+  bounded_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<unsigned*>(err), (uint64_t)limit_us * 1000u);
+  return cudaGetLastError() == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }
 
 okc_status okc_rope_table_init(float rope_theta, int32_t num_positions, float* table, okc_stream stream) {

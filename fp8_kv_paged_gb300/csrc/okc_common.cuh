@@ -99,12 +99,12 @@ __device__ __forceinline__ uint64_t global_ns() {
 // poll count keeps a kernel that was preempted mid-wait from giving up early).
 constexpr uint32_t kWaitMinPolls = 1u << 12;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s; a tile lands within microseconds
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; i++) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i >= kWaitMinPolls && global_ns() - t0 > kWaitNs) return false;
+    if (i >= kWaitMinPolls && global_ns() - t0 > limit_ns) return false;
   }
 }
 // Arrive on mbarrier `bar` and add `bytes` to the transaction count its

@@ -342,6 +342,18 @@ okc_status okc_attn_step_host(okc_attn_plan_t plan, const okc_host_step* io, uin
 const char* okc_status_string(okc_status status);
 
 /*
+ * Diagnostic of the kernels' bounded waits on the current device: one warp
+ * waits on a shared-memory mbarrier that nothing arrives on, with the same
+ * bounded wait every kernel uses but a limit of limit_us microseconds (at
+ * least 4096 polls), ORs OKC_DEVERR_TIMEOUT into *err when the wait gives up,
+ * and returns: the launch completes and the context stays usable. Nothing
+ * faults and nothing hangs. err: device, one uint32, not cleared by the call.
+ * Asynchronous on `stream`. Returns OKC_ERR_INVALID for a null err or a limit
+ * outside [1, 1000000] us (checked before any GPU work).
+ */
+okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream stream);
+
+/*
  * okc_attn_decode_combine_noalloc — okc_attn_decode followed by
  * okc_attn_combine_normgate, for callers that cannot allocate device memory.
  * The paper has no counterpart of this entry point.

@@ -79,3 +79,8 @@ def test_null_arguments_rejected(lib):
     assert lib.okc_rope_table_init(5e5, 0, None, None) == okc.ERR_INVALID
     v = ctypes.c_uint32()
     assert lib.okc_attn_plan_read_errors(None, None, ctypes.byref(v)) == okc.ERR_INVALID
+    # the bounded-wait diagnostic checks its arguments before any GPU work
+    assert lib.okc_selftest_bounded_wait(None, 1000, None) == okc.ERR_INVALID
+    dummy = ctypes.c_uint32()
+    assert lib.okc_selftest_bounded_wait(ctypes.byref(dummy), 0, None) == okc.ERR_INVALID
+    assert lib.okc_selftest_bounded_wait(ctypes.byref(dummy), 1000001, None) == okc.ERR_INVALID
