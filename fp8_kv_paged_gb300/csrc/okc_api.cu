@@ -543,15 +543,19 @@ okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_ho
   okc_attn_sizes z;
   compute_sizes(&plan->cfg, s, &z);
   z.step_kernels = step_kernels(&plan->cfg, s, &plan->opts, plan->slots);
-  if (plan->workspace_bytes < z.workspace_bytes) {
+  // the staging buffer (the head up to q: error word, work list, request
+  // table, arrival counters) is made ready before the plan changes, so that a
+  // failure here leaves the plan as it was
+  auto restore = [&](okc_status e) {
     s.work.swap(plan->work);
     s.req.swap(plan->req);
-    return OKC_ERR_WORKSPACE;
-  }
-  set_splits(plan, s, z);
-  const size_t up_bytes = upload_bytes(plan);
+    return e;
+  };
+  if (plan->workspace_bytes < z.workspace_bytes) return restore(OKC_ERR_WORKSPACE);
+  const size_t up_bytes = okc::kWsHeader + round_up(s.work.size() * sizeof(WorkItem)) +
+                          round_up(s.req.size() * sizeof(ReqInfo)) + round_up(plan->cfg.batch * sizeof(int32_t));
   // the staging buffer may still feed the previous update's copy
-  if (plan->pinned_done && cudaEventSynchronize(plan->pinned_done) != cudaSuccess) return OKC_ERR_CUDA;
+  if (plan->pinned_done && cudaEventSynchronize(plan->pinned_done) != cudaSuccess) return restore(OKC_ERR_CUDA);
   if (plan->pinned_bytes < up_bytes) {
     if (plan->pinned) cudaFreeHost(plan->pinned);
     plan->pinned = nullptr;
@@ -559,14 +563,16 @@ okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_ho
     const size_t want = std::max<size_t>(up_bytes, 64 * 1024);
     if (cudaMallocHost(&plan->pinned, want) != cudaSuccess) {
       plan->pinned = nullptr;
-      return OKC_ERR_CUDA;
+      return restore(OKC_ERR_CUDA);
     }
     plan->pinned_bytes = want;
   }
   if (!plan->pinned_done && cudaEventCreateWithFlags(&plan->pinned_done, cudaEventDisableTiming) != cudaSuccess) {
     plan->pinned_done = nullptr;
-    return OKC_ERR_CUDA;
+    return restore(OKC_ERR_CUDA);
   }
+  set_splits(plan, s, z);
+  if (upload_bytes(plan) != up_bytes) return OKC_ERR_INVALID;  // (layout invariant)
   uint8_t* head = static_cast<uint8_t*>(plan->pinned);
   std::memset(head, 0, up_bytes);
   write_head(plan, head);

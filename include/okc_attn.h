@@ -186,7 +186,9 @@ okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_l
  * and wait for the staging buffer's previous copy before reusing it. The
  * scratch sizes may change with the lengths: read them with
  * okc_attn_plan_get_sizes. Returns OKC_ERR_WORKSPACE, leaving the plan as it
- * was, when the new plan needs a larger workspace than the plan was made with.
+ * was, when the new plan needs a larger workspace than the plan was made with
+ * (okc_attn_plan_max_sizes gives a workspace that never does). After
+ * OKC_ERR_CUDA the plan may no longer match its workspace: destroy it.
  * The workspace is overwritten in stream order: kernels of the previous step
  * issued on other streams must be ordered before the call.
  */
