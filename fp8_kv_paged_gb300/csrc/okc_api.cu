@@ -531,26 +531,24 @@ okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_l
 
 okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream) {
   if (!plan || (plan->cfg.batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
+  // The new split is built in the spare lists (the ones the previous update
+  // replaced: their capacity is reused); the plan's current lists, sizes and
+  // workspace stay as they are until every step that can fail has passed.
   SplitResult s;
-  s.work.swap(plan->work);  // reuse the vectors' capacity
-  s.req.swap(plan->req);
+  s.work.swap(plan->spare_work);
+  s.req.swap(plan->spare_req);
+  auto restore = [&](okc_status e) {
+    s.work.swap(plan->spare_work);
+    s.req.swap(plan->spare_req);
+    return e;
+  };
   okc_status st = make_splits(&plan->cfg, seq_lens_host, &plan->opts, plan->slots, &s);
-  if (st != OKC_OK) {
-    s.work.swap(plan->work);
-    s.req.swap(plan->req);
-    return st;
-  }
+  if (st != OKC_OK) return restore(st);
   okc_attn_sizes z;
   compute_sizes(&plan->cfg, s, &z);
   z.step_kernels = step_kernels(&plan->cfg, s, &plan->opts, plan->slots);
-  // the staging buffer (the head up to q: error word, work list, request
-  // table, arrival counters) is made ready before the plan changes, so that a
-  // failure here leaves the plan as it was
-  auto restore = [&](okc_status e) {
-    s.work.swap(plan->work);
-    s.req.swap(plan->req);
-    return e;
-  };
+  // the staging buffer for the head (up to q: error word, work list, request
+  // table, arrival counters) is made ready before the plan changes
   if (plan->workspace_bytes < z.workspace_bytes) return restore(OKC_ERR_WORKSPACE);
   const size_t up_bytes = okc::kWsHeader + round_up(s.work.size() * sizeof(WorkItem)) +
                           round_up(s.req.size() * sizeof(ReqInfo)) + round_up(plan->cfg.batch * sizeof(int32_t));
@@ -571,8 +569,9 @@ okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_ho
     plan->pinned_done = nullptr;
     return restore(OKC_ERR_CUDA);
   }
-  set_splits(plan, s, z);
-  if (upload_bytes(plan) != up_bytes) return OKC_ERR_INVALID;  // (layout invariant)
+  set_splits(plan, s, z);  // s now holds the replaced lists: they become the spares
+  s.work.swap(plan->spare_work);
+  s.req.swap(plan->spare_req);
   uint8_t* head = static_cast<uint8_t*>(plan->pinned);
   std::memset(head, 0, up_bytes);
   write_head(plan, head);

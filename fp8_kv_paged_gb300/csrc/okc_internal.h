@@ -100,6 +100,8 @@ struct okc_attn_plan_s {
   okc_attn_sizes sizes;
   std::vector<okc::WorkItem> work;
   std::vector<okc::ReqInfo> req;
+  std::vector<okc::WorkItem> spare_work;  // okc_attn_plan_update: the lists replaced by the
+  std::vector<okc::ReqInfo> spare_req;    // last update, reused for the next one's capacity
   std::vector<uint8_t> upload;  // the workspace head as uploaded (one host-to-device copy)
   void* workspace;
   size_t workspace_bytes;
