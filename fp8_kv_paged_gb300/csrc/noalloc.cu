@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "okc_common.cuh"
 #include "okc_internal.h"
@@ -25,7 +26,7 @@ namespace okc {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
-constexpr int kMaxWork = 4096;     // work items per call (host stack arrays below)
+constexpr int kMaxWork = 4096;     // work items per call
 constexpr int kMaxBatch = 2048;    // requests per call
 constexpr int kMaxDevices = 64;
 
@@ -84,7 +85,8 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     return OKC_ERR_INVALID;
   if (c.batch > kMaxBatch) return OKC_ERR_WORKSPACE;
 
-  // Work list on the stack (no heap): the same split rule as okc_attn_plan.
+  // The work list of okc_attn_plan with the default options (the same split
+  // rule, launch order and kernel choice), for this device's resident CTA slots.
   const int B = c.batch, L = c.q_len;
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -93,69 +95,11 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   const bool use_tc = L >= 2 && L <= 8;  // the default plan's kernel choice
   const int per_sm = decode_ctas_per_sm(L, use_tc);
   if (per_sm <= 0) return OKC_ERR_CUDA;
-  int64_t nvis[kMaxBatch];
-  int64_t total = 0;
-  for (int b = 0; b < B; b++) {
-    if (seq_lens_host[b] < 0) return OKC_ERR_INVALID;
-    const int64_t hi = (int64_t)seq_lens_host[b] + L;
-    if (hi > (int64_t)c.max_pages * c.page_size) return OKC_ERR_INVALID;
-    const int64_t lo = c.window > 0 ? std::max<int64_t>(0, (int64_t)seq_lens_host[b] - c.window + 1) : 0;
-    nvis[b] = hi - lo;
-    total += nvis[b];
-  }
-  // The key budget of okc_attn_plan: for m = 1..4 waves of the resident CTA slots,
-  // the smallest C whose items fit m waves, scored as max(largest item,
-  // ceil(items / slots) * mean item) with kItemCost keys added per item.
-  const int64_t slots = (int64_t)sms * per_sm;
-  const int64_t kItemCost = 128;
-  int64_t nmax = 1;
-  for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
-  auto items = [&](int64_t C) {
-    int64_t w = 0;
-    for (int b = 0; b < B; b++) w += std::max<int64_t>(1, (nvis[b] + C - 1) / C);
-    return w;
-  };
-  int64_t budget = std::max<int64_t>(128, nmax);
-  double best = -1.0;
-  for (int m = 1; m <= 4; m++) {
-    int64_t lo_c = 128, hi_c = std::max<int64_t>(128, nmax);
-    while (lo_c < hi_c) {
-      const int64_t mid = (lo_c + hi_c) / 2;
-      if (items(mid) <= (int64_t)m * slots) hi_c = mid; else lo_c = mid + 1;
-    }
-    const int64_t C = lo_c, Wc = items(C);
-    int64_t biggest = 0;
-    for (int b = 0; b < B; b++) {
-      const int64_t k = std::max<int64_t>(1, (nvis[b] + C - 1) / C);
-      biggest = std::max(biggest, (nvis[b] + k - 1) / k);
-    }
-    const double mean = (double)(total + Wc * kItemCost) / (double)Wc;
-    const double waves = (double)((Wc + slots - 1) / slots);
-    const double score = std::max((double)(biggest + kItemCost), waves * mean);
-    if (best < 0.0 || score < best) {
-      best = score;
-      budget = C;
-    }
-    if (C == 128) break;
-  }
-  (void)total;
-  WorkItem work[kMaxWork];  // ~180 KB of stack in all, no heap
-  ReqInfo req[kMaxBatch];
-  int64_t W = 0;
-  for (int b = 0; b < B; b++) {
-    const int64_t k = std::max<int64_t>(1, (nvis[b] + budget - 1) / budget);
-    const int64_t chunk = split_chunk_keys(nvis[b], k, use_tc && cfg->page_size >= 8 ? 7 : 0);
-    const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
-    if (W + nch > kMaxWork) return OKC_ERR_WORKSPACE;
-    req[b] = ReqInfo{(int32_t)W, (int32_t)nch, (int32_t)chunk, 0};
-    const int64_t n = (int64_t)seq_lens_host[b] + L, lo = n - nvis[b];
-    for (int64_t i = 0; i < nch; i++) {
-      const int64_t j0 = lo + i * chunk, j1 = std::min<int64_t>(n, j0 + chunk);
-      work[W + i] = WorkItem{b, (int32_t)i, (int32_t)(W + i), (int32_t)j0,
-                             (int32_t)j1, (int32_t)chunk, (int32_t)nch, (int32_t)W};
-    }
-    W += nch;
-  }
+  SplitResult split;
+  const okc_status st = make_splits(cfg, seq_lens_host, nullptr, sms * per_sm, &split);
+  if (st != OKC_OK) return st;
+  const int64_t W = (int64_t)split.work.size();
+  if (W > kMaxWork) return OKC_ERR_WORKSPACE;
   // Scratch layout in the static array: work list | request table | LSE | partial outputs.
   const int64_t rows = (int64_t)L * kNumQHeads;
   const size_t off_req = up256((size_t)W * sizeof(WorkItem));
@@ -169,8 +113,10 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   uint8_t* s8 = static_cast<uint8_t*>(base);
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   // pageable sources are staged before cudaMemcpyAsync returns
-  if (cudaMemcpyAsync(s8, work, (size_t)W * sizeof(WorkItem), cudaMemcpyHostToDevice, str) != cudaSuccess ||
-      cudaMemcpyAsync(s8 + off_req, req, (size_t)B * sizeof(ReqInfo), cudaMemcpyHostToDevice, str) != cudaSuccess)
+  if (cudaMemcpyAsync(s8, split.work.data(), (size_t)W * sizeof(WorkItem), cudaMemcpyHostToDevice, str) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(s8 + off_req, split.req.data(), (size_t)B * sizeof(ReqInfo), cudaMemcpyHostToDevice, str) !=
+          cudaSuccess)
     return OKC_ERR_CUDA;
 
   int shift = 0;

@@ -12,7 +12,9 @@
 #include "okc_common.cuh"
 #include "okc_internal.h"
 
+using okc::make_splits;
 using okc::ReqInfo;
+using okc::SplitResult;
 using okc::WorkItem;
 
 namespace {
@@ -47,11 +49,7 @@ int page_shift(int P) {
   return s;
 }
 
-struct SplitResult {
-  std::vector<WorkItem> work;
-  std::vector<ReqInfo> req;
-  int max_chunks = 0;
-};
+}  // namespace
 
 // Split every request's visible keys into work items. Visible keys of request b:
 // [lo, seq+L) with lo = max(0, seq - window + 1) on window layers (the union of
@@ -61,7 +59,7 @@ struct SplitResult {
 // is shorter, so short or windowed requests get few splits and long ones many
 // (the H200 bound cdiv(132, B*Hkv) of "012-attention-local-splits.py" plays the
 // same role with a fixed SM count).
-okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
+okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
                        int slots, SplitResult* r) {
   const int B = c->batch, L = c->q_len;
   if (o && o->chunk_keys != 0 && o->chunk_keys < 16) return OKC_ERR_INVALID;
@@ -244,6 +242,8 @@ okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_p
   (void)out;
   return OKC_OK;
 }
+
+namespace {
 
 // Kernels okc_attn_step launches: 1 (the fused step kernel, q_len 1) when the
 // work list fills at least half of the resident CTA slots with chunks of at

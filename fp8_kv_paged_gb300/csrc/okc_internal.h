@@ -137,6 +137,18 @@ inline int64_t split_chunk_keys(int64_t nvis, int64_t k, int64_t pad) {
   return r > 64 - pad ? r : 64 - pad;
 }
 
+// A step's split: the work items in launch order, the per-request table, and
+// the largest number of items of one request.
+struct SplitResult {
+  std::vector<WorkItem> work;
+  std::vector<ReqInfo> req;
+  int max_chunks = 0;
+};
+// The plan's split rule (okc_api.cu): every request's visible keys into work
+// items for `slots` resident CTA slots, under the plan options (may be null).
+okc_status make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o, int slots,
+                       SplitResult* r);
+
 // Kernel launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_prepare(const PrepareArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
