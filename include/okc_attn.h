@@ -358,7 +358,7 @@ okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream
 /*
  * okc_attn_decode_combine_noalloc — okc_attn_decode followed by
  * okc_attn_combine_normgate, for callers that cannot allocate device memory.
- * The paper has no counterpart of this entry point.
+ * "012-attention-local-splits.py" has no counterpart of this entry point.
  *
  * Who needs it: an op hosted inside a framework that owns every device
  * allocation and hands the op only its input and output buffers (a plugin or
@@ -367,7 +367,8 @@ okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream
  * takes no plan, workspace or scratch buffer: the work list, the per-request
  * table and the split partials live in one static device array of 8 MiB inside
  * the library, which every GPU that loads the library holds until the process
- * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ * exits. It makes no device allocation (no cudaMalloc, cudaFree or other CUDA
+ * allocating routine); its host-side work list is ordinary heap memory.
  *
  * Arguments are those of okc_attn_plan (cfg, seq_lens_host), okc_attn_decode and
  * okc_attn_combine_normgate; q_fp8 must already hold okc_prepare_qkv's output.
