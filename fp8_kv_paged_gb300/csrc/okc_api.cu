@@ -40,6 +40,8 @@ okc_status check_config(const okc_attn_config* c) {
   if (!is_pow2(c->page_size) || c->page_size > 256) return OKC_ERR_UNSUPPORTED;
   // every flat cache row and page-table index must fit the kernels' int32 key math
   if ((int64_t)c->max_pages * c->page_size > (int64_t)1 << 30) return OKC_ERR_UNSUPPORTED;
+  // token counts (grids of one CTA per token, int32 sizes) stay far below 2^31
+  if ((int64_t)c->batch * c->q_len > (int64_t)1 << 26) return OKC_ERR_UNSUPPORTED;
   return OKC_OK;
 }
 

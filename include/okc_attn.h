@@ -66,7 +66,8 @@ typedef enum okc_status {
  * Mirrors the problem file's `class Config`. The library runs the per-GPU shape
  * of Muse Spark under TP8: num_q_heads = 16, num_kv_heads = 2, head_dim = 64
  * (anything else returns OKC_ERR_UNSUPPORTED), q_len in [1, 16], page_size a
- * power of two in [1, 256].
+ * power of two in [1, 256], max_pages * page_size <= 2^30 and batch * q_len <=
+ * 2^26 (larger: OKC_ERR_UNSUPPORTED).
  */
 typedef struct okc_attn_config {
   int32_t batch;           /* B: requests in the step */

@@ -61,6 +61,8 @@ def _cfg(**kw):
     (dict(kv_scale=-1.0), okc.ERR_INVALID),
     (dict(rope_theta=float("nan")), okc.ERR_INVALID),
     (dict(num_q_heads=15), okc.ERR_INVALID),
+    (dict(batch=(1 << 22) + 1, q_len=16), okc.ERR_UNSUPPORTED),  # 2^26 tokens + 16
+    (dict(max_pages=(1 << 30) + 1), okc.ERR_UNSUPPORTED),
 ])
 def test_bad_config_rejected_before_gpu_work(lib, bad, status):
     """Config validation runs first, so these need no GPU."""
