@@ -4,7 +4,9 @@ tests/plan_update_host.cu: okc_attn_plan_update's in-place updates equal fresh
 plans byte for byte, and refused or failed updates leave the plan unchanged.
 tests/noalloc_host.cu: okc_attn_decode_combine_noalloc uploads the plan's split
 and launches over it inside its static array, and refuses exactly the calls
-past its documented limits."""
+past its documented limits. tests/c_abi_host.c: the header compiles as strict
+C99 without CUDA headers, and a C program linked against libokc_attn.so runs the
+host-only entry points."""
 import os
 import shutil
 import subprocess
@@ -34,3 +36,17 @@ def test_plan_update_equals_fresh_plans_and_failures_leave_it_unchanged(tmp_path
 
 def test_noalloc_uploads_the_plans_split_within_its_array(tmp_path):
     _run_harness(tmp_path, "noalloc_host", 2000)
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    import fp8_kv_paged_gb300 as okc
+    lib = okc.build()
+    exe = str(tmp_path / "c_abi_host")
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           "-o", exe, os.path.join(ROOT, "tests", "c_abi_host.c"), lib, "-Wl,-rpath," + os.path.dirname(lib)]
+    subprocess.run(cmd, check=True, capture_output=True, text=True, timeout=300)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
