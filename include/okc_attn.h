@@ -192,6 +192,11 @@ okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_l
  * OKC_ERR_CUDA the plan may no longer match its workspace: destroy it.
  * The workspace is overwritten in stream order: kernels of the previous step
  * issued on other streams must be ordered before the call.
+ * CUDA graphs: a launch captured in a graph keeps the grid size and the
+ * workspace offsets of the plan as it was at capture. Replaying it after an
+ * update is valid only while num_work is unchanged (the work list and request
+ * table then keep their offsets); after an update that changed num_work,
+ * capture again before replaying.
  */
 okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream);
 
