@@ -183,15 +183,18 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
   const int64_t tma_pad = tc_tma ? 7 : 0;
   r->req.assign(B, ReqInfo{0, 0, 0, 0});
   int64_t wbase = 0;
+  int64_t prev_n = -1, chunk = 0, nch = 0;  // requests of equal size share their split
   for (int b = 0; b < B; b++) {
-    int64_t chunk;
-    if (o && o->chunk_keys > 0) {
-      chunk = o->chunk_keys;
-    } else {
-      const int64_t k = std::max<int64_t>(1, (nvis[b] + Cbud - 1) / Cbud);
-      chunk = okc::split_chunk_keys(nvis[b], k, tma_pad);
+    if (nvis[b] != prev_n) {
+      prev_n = nvis[b];
+      if (o && o->chunk_keys > 0) {
+        chunk = o->chunk_keys;
+      } else {
+        const int64_t k = std::max<int64_t>(1, cdiv(nvis[b], Cbud));
+        chunk = okc::split_chunk_keys(nvis[b], k, tma_pad);
+      }
+      nch = std::max<int64_t>(1, cdiv(nvis[b], chunk));
     }
-    const int64_t nch = std::max<int64_t>(1, (nvis[b] + chunk - 1) / chunk);
     if (nch > (1 << 20) || wbase + nch > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
     r->req[b] = ReqInfo{(int32_t)wbase, (int32_t)nch, (int32_t)chunk, 0};
     r->max_chunks = std::max<int>(r->max_chunks, (int)nch);
@@ -216,32 +219,33 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
   std::sort(run_full.begin(), run_full.end());
   std::sort(run_last.begin(), run_last.end());
   r->work.resize((size_t)wbase);
-  size_t out = 0, il = 0;
-  auto emit = [&](int b, int k) {
-    const ReqInfo& q = r->req[b];
-    const int64_t n = (int64_t)seq[b] + L, lo = n - nvis[b];
-    const int64_t j0 = lo + (int64_t)k * q.chunk_keys, j1 = std::min<int64_t>(n, j0 + q.chunk_keys);
-    r->work[out++] = WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)j1, q.chunk_keys, q.nchunks, q.wbase};
-  };
+  WorkItem* out = r->work.data();
+  size_t il = 0;
   auto emit_last_before = [&](uint64_t key_word, int32_t slot) {  // last items ahead of (key, slot)
     while (il < run_last.size()) {
       const uint64_t w = run_last[il];
       const int b = (int)(w & 0xFFFFFFFFu);
-      const int32_t ls = r->req[b].wbase + r->req[b].nchunks - 1;
+      const ReqInfo& q = r->req[b];
+      const int32_t ls = q.wbase + q.nchunks - 1;
       if ((w >> 32) > (key_word >> 32) || ((w >> 32) == (key_word >> 32) && ls > slot)) break;
-      emit(b, r->req[b].nchunks - 1);
+      const int64_t n = (int64_t)seq[b] + L, j0 = n - nvis[b] + (int64_t)(q.nchunks - 1) * q.chunk_keys;
+      *out++ = WorkItem{b, q.nchunks - 1, ls, (int32_t)j0, (int32_t)n, q.chunk_keys, q.nchunks, q.wbase};
       il++;
     }
   };
+  // A request's items before its last take slots wbase .. wbase + nchunks - 2,
+  // a range no other request's slot falls into, so the last items that go
+  // before any of them go before the first: one merge step per request.
   for (const uint64_t w : run_full) {
     const int b = (int)(w & 0xFFFFFFFFu);
-    for (int k = 0; k + 1 < r->req[b].nchunks; k++) {
-      emit_last_before(w, r->req[b].wbase + k);
-      emit(b, k);
-    }
+    const ReqInfo& q = r->req[b];
+    emit_last_before(w, q.wbase);
+    int64_t j0 = (int64_t)seq[b] + L - nvis[b];  // these items hold chunk_keys keys each
+    for (int k = 0; k + 1 < q.nchunks; k++, j0 += q.chunk_keys)
+      *out++ = WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)(j0 + q.chunk_keys), q.chunk_keys, q.nchunks,
+                        q.wbase};
   }
   emit_last_before(~0ull, 0);
-  (void)out;
   return OKC_OK;
 }
 
