@@ -9,7 +9,9 @@
 // arrival counters) and reports the same sizes as a fresh plan of the same
 // lengths, within okc_attn_plan_max_sizes; a failed staging allocation, a
 // length past the page table and a too-small workspace each leave the plan's
-// sizes and workspace head unchanged, and the plan keeps working afterwards.
+// sizes and workspace head unchanged, and the plan keeps working afterwards;
+// the default-option entry points (okc_attn_plan_create, _scratch_sizes,
+// _workspace_size) agree with the general ones.
 #include <cuda_runtime.h>
 #include <cstdio>
 #include <cstdlib>
@@ -30,6 +32,7 @@ static cudaError_t fake_event_create(cudaEvent_t* e, unsigned) { *e = (cudaEvent
 static cudaError_t fake_event_record(cudaEvent_t, cudaStream_t) { return cudaSuccess; }
 static cudaError_t fake_event_destroy(cudaEvent_t) { return cudaSuccess; }
 static cudaError_t fake_get_device(int* d) { *d = 0; return cudaSuccess; }
+static cudaError_t fake_attr(int* v, cudaDeviceAttr, int) { *v = 152; return cudaSuccess; }
 #define cudaMemcpyAsync fake_memcpy_async
 #define cudaMallocHost fake_malloc_host
 #define cudaFreeHost fake_free_host
@@ -38,6 +41,7 @@ static cudaError_t fake_get_device(int* d) { *d = 0; return cudaSuccess; }
 #define cudaEventRecord fake_event_record
 #define cudaEventDestroy fake_event_destroy
 #define cudaGetDevice fake_get_device
+#define cudaDeviceGetAttribute fake_attr
 #include "okc_api.cu"
 namespace okc {
 cudaError_t launch_prepare(const PrepareArgs&, bool, cudaStream_t) { return cudaSuccess; }
@@ -148,5 +152,31 @@ int main(int argc, char** argv) {
     okc_attn_plan_destroy(p);
   }
   CHECK(g_alloc_failures > 0);
+  // the default-option forms: okc_attn_plan_create is okc_attn_plan with no
+  // options, okc_attn_plan_scratch_sizes its sizes, okc_attn_plan_workspace_size
+  // the workspace bound of okc_attn_plan_max_sizes (152 SMs, the stubs' occupancy)
+  for (int it = 0; it < 200; it++) {
+    const int L = std::vector<int>{1, 8}[g() % 2];
+    const int B = 1 + g() % 300, maxctx = 1 + g() % 40000, max_pages = maxctx + L + 1;
+    okc_attn_config c = {B, L, 16, 2, 64, 1, (g() % 2) ? 2048 : 0, max_pages, B * max_pages, 5e5f, 5.473f, 0.125f,
+                         1.f};
+    std::vector<int32_t> s(B);
+    for (auto& x : s) x = g() % (maxctx + 1);
+    size_t wsb = 0;
+    okc_attn_sizes bound, z1, z2;
+    CHECK(okc_attn_plan_workspace_size(&c, maxctx + L, &wsb) == OKC_OK);
+    CHECK(okc_attn_plan_max_sizes(&c, maxctx + L, nullptr, &bound) == OKC_OK && bound.workspace_bytes == wsb);
+    std::vector<uint8_t> a(wsb + 256), b2(wsb + 256);
+    uint8_t* wa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(a.data()) + 255) / 256 * 256);
+    uint8_t* wb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(b2.data()) + 255) / 256 * 256);
+    okc_attn_plan_t p1 = nullptr, p2 = nullptr;
+    CHECK(okc_attn_plan_create(&c, s.data(), wa, wsb, nullptr, &p1) == OKC_OK);
+    CHECK(okc_attn_plan(&c, s.data(), nullptr, wb, wsb, nullptr, &p2) == OKC_OK);
+    CHECK(okc_attn_plan_scratch_sizes(p1, &z1) == OKC_OK && okc_attn_plan_get_sizes(p2, &z2) == OKC_OK);
+    CHECK(memcmp(&z1, &z2, sizeof z1) == 0 && z1.workspace_bytes <= wsb && z1.num_work <= bound.num_work);
+    CHECK(memcmp(wa, wb, head_bytes(p1)) == 0);
+    okc_attn_plan_destroy(p1);
+    okc_attn_plan_destroy(p2);
+  }
   printf("ok: %d updates compared with fresh plans, %d failed staging allocations\n", cases, g_alloc_failures);
 }
