@@ -4,7 +4,9 @@ tests/plan_update_host.cu: okc_attn_plan_update's in-place updates equal fresh
 plans byte for byte, and refused or failed updates leave the plan unchanged.
 tests/noalloc_host.cu: okc_attn_decode_combine_noalloc uploads the plan's split
 and launches over it inside its static array, and refuses exactly the calls
-past its documented limits. tests/c_abi_host.c: the header compiles as strict
+past its documented limits. tests/step_host_routing.cu: okc_attn_step_host
+reads each mapped, aligned host buffer in place and copies every other one
+with its exact byte count, for every combination. tests/c_abi_host.c: the header compiles as strict
 C99 without CUDA headers, and a C program linked against libokc_attn.so runs the
 host-only entry points."""
 import os
@@ -36,6 +38,10 @@ def test_plan_update_equals_fresh_plans_and_failures_leave_it_unchanged(tmp_path
 
 def test_noalloc_uploads_the_plans_split_within_its_array(tmp_path):
     _run_harness(tmp_path, "noalloc_host", 2000)
+
+
+def test_step_host_routes_every_buffer_as_documented(tmp_path):
+    _run_harness(tmp_path, "step_host_routing", 0)
 
 
 def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
