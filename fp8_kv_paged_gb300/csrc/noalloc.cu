@@ -79,9 +79,10 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     return OKC_ERR_INVALID;
   const bool scaled = c.kv_scale != 1.f;
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
-  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  if (!al16(q_fp8) || !al16(k_cache) || !al16(v_cache) || !al16(qkv) || !al16(out) ||
-      (norm_weight && !al16(norm_weight)))
+  auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+  if (!al(q_fp8, 16) || !al(k_cache, 16) || !al(v_cache, 16) || !al(qkv, 16) || !al(out, 16) ||
+      (norm_weight && !al(norm_weight, 16)) || !al(page_table, 4) || !al(cache_seqlens, 4) ||
+      !al(cu_seqlens_q, 4) || !al(seq_lens, 4) || !al(k_scale, 4) || !al(v_scale, 4))
     return OKC_ERR_INVALID;
   if (c.batch > kMaxBatch) return OKC_ERR_WORKSPACE;
 

@@ -344,6 +344,9 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// Natural alignment of the element type the kernels load through p (null passes:
+// the null checks are separate).
+bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0; }
 
 // The plan takes a split result: sizes, work list, request table, and the
 // workspace layout (error word | work list | request table | arrival counters | q).
@@ -653,7 +656,9 @@ okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t*
   const int T = plan->sizes.num_tokens;
   if (T == 0) return OKC_OK;
   if (!qkv || !cache_loc || !k_cache || !v_cache || !q_fp8) return OKC_ERR_INVALID;
-  if (!aligned16(qkv) || !aligned16(q_fp8)) return OKC_ERR_INVALID;
+  if (!aligned16(qkv) || !aligned16(q_fp8) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned(positions, 8) || !aligned(cache_loc, 8) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return OKC_ERR_INVALID;
   const bool rope = c.rope_theta != 0.f;
   const bool scaled = c.kv_scale != 1.f;
   if (rope && (!positions || !rope_table || !aligned16(rope_table) || rope_positions < 1 ||
@@ -691,7 +696,9 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
   if (!q_fp8 || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q ||
       !o_partial || !lse_partial)
     return OKC_ERR_INVALID;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_partial) || !aligned16(q_fp8))
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_partial) || !aligned16(q_fp8) ||
+      !aligned(lse_partial, 4) || !aligned(page_table, 4) || !aligned(cache_seqlens, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
     return OKC_ERR_INVALID;
   const bool scaled = c.kv_scale != 1.f;
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
@@ -732,7 +739,7 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
   const int T = plan->sizes.num_tokens;
   if (T == 0) return OKC_OK;
   if (!o_partial || !lse_partial || !qkv || !out) return OKC_ERR_INVALID;
-  if (!aligned16(qkv) || !aligned16(out) || !aligned16(o_partial) ||
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(o_partial) || !aligned(lse_partial, 4) ||
       (norm_weight && !aligned16(norm_weight)))
     return OKC_ERR_INVALID;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return OKC_ERR_INVALID;
@@ -764,7 +771,10 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
       !o_partial || !lse_partial || !out)
     return OKC_ERR_INVALID;
   if (!aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_partial) ||
-      !aligned16(out) || (norm_weight && !aligned16(norm_weight)))
+      !aligned16(out) || (norm_weight && !aligned16(norm_weight)) || !aligned(lse_partial, 4) ||
+      !aligned(positions, 8) || !aligned(cache_loc, 8) || !aligned(page_table, 4) ||
+      !aligned(cache_seqlens, 4) || !aligned(cu_seqlens_q, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) ||
+      !aligned(v_scale, 4))
     return OKC_ERR_INVALID;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return OKC_ERR_INVALID;
   const bool rope = c.rope_theta != 0.f;

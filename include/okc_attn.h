@@ -21,6 +21,10 @@
  *  - Argument errors are detected on the host before any launch and return
  *    OKC_ERR_INVALID / OKC_ERR_UNSUPPORTED without touching the GPU. A failed
  *    launch returns OKC_ERR_CUDA. Nothing throws and nothing exits.
+ *  - Alignment: qkv, out, q_fp8, the caches, o_partial and the norm weight
+ *    16 bytes (vector loads and stores); positions and cache_loc 8 bytes; the
+ *    int32 arrays, lse_partial and the scale scalars 4 bytes. A pointer that is
+ *    not is an argument error (OKC_ERR_INVALID), never a misaligned access.
  *  - Errors that only the device can see (a cache row, page id or position out
  *    of range) never fault: the kernel skips the access, reads zeros where a
  *    key was expected, and ORs an OKC_DEVERR_* bit into the plan's device error

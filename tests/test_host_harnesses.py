@@ -6,7 +6,9 @@ tests/noalloc_host.cu: okc_attn_decode_combine_noalloc uploads the plan's split
 and launches over it inside its static array, and refuses exactly the calls
 past its documented limits. tests/step_host_routing.cu: okc_attn_step_host
 reads each mapped, aligned host buffer in place and copies every other one
-with its exact byte count, for every combination. tests/c_abi_host.c: the header compiles as strict
+with its exact byte count, for every combination. tests/arg_validation_host.cu:
+the launching calls refuse missing or misaligned buffers, unusable RoPE
+tables, missing scales and bad eps before any launch. tests/c_abi_host.c: the header compiles as strict
 C99 without CUDA headers, and a C program linked against libokc_attn.so runs the
 host-only entry points."""
 import os
@@ -42,6 +44,10 @@ def test_noalloc_uploads_the_plans_split_within_its_array(tmp_path):
 
 def test_step_host_routes_every_buffer_as_documented(tmp_path):
     _run_harness(tmp_path, "step_host_routing", 0)
+
+
+def test_launching_calls_refuse_bad_arguments_before_any_launch(tmp_path):
+    _run_harness(tmp_path, "arg_validation_host", 0)
 
 
 def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
