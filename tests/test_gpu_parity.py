@@ -71,6 +71,19 @@ def test_norm_weight_none_and_no_rope_scaled():
     full_check(cfg, inp)
 
 
+@pytest.mark.parametrize("name", ["verify_block", "sliding_decode"])
+def test_distinct_k_and_v_scales(name):
+    """The scaled cache path with k_scale != v_scale, both non-dyadic (0.7 and
+    0.6: the bf16 cast after the division changes E4M3 codes), through the three
+    calls and through okc_attn_step in both of its forms."""
+    cfg = W.config(name, **SMALL[name], kv_scale=0.7, k_scale=0.7, v_scale=0.6)
+    inp = W.generate(cfg)
+    assert inp["k_scale"] != inp["v_scale"]
+    full_check(cfg, inp)
+    full_check(cfg, inp, fused=True)
+    full_check(cfg, inp, fused=True, plan_form=True)
+
+
 def test_rope_table_matches_oracle_rows():
     import fp8_kv_paged_gb300 as okc
     n = 140000

@@ -48,6 +48,15 @@ MUTANTS = [
      [lambda: TA.test_matches_dense_brute_force(1, 4, 3, (6, 16), 0.5)]),
     ("sigmoid_sign", "1.0 / (1.0 + exp(-g))", "1.0 / (1.0 + exp(g))",
      [TA.test_normgate_saturated_gate_is_plain_rmsnorm]),
+    # the scaled cache path ("012-attention-local-splits.py", `_prepare_qkv`, `if SCALED:`)
+    ("k_divided_by_v_scale", "(key / k_scale)", "(key / v_scale)",
+     [TP.test_scaled_cache_codes_from_the_definition]),
+    ("v_divided_by_k_scale", "(value / v_scale)", "(value / k_scale)",
+     [TP.test_scaled_cache_codes_from_the_definition]),
+    ("no_bf16_after_k_scale", "key = (float)orc_bf16_round((double)(key / k_scale));", "key = key / k_scale;",
+     [TP.test_scaled_cache_codes_from_the_definition]),
+    ("no_bf16_after_v_scale", "value = (float)orc_bf16_round((double)(value / v_scale));",
+     "value = value / v_scale;", [TP.test_scaled_cache_codes_from_the_definition]),
 ]
 
 

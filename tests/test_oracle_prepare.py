@@ -179,3 +179,107 @@ def test_scaled_path_halving_scale_doubles_values():
         normal = (e >= 1) & (e <= 13)
         assert normal.sum() > 100
         assert np.array_equal(cb[normal], ca[normal] + 8)
+
+
+# ---- the scaled cache path, from its definition ------------------------------
+# "012-attention-local-splits.py", `_prepare_qkv`, `if SCALED:`: the normalised
+# (and rotated) key is divided by k_scale and cast to bf16, the raw value by
+# v_scale and cast to bf16, then both are stored as E4M3. The pin computes the
+# stored codes independently: float32 IEEE division (numpy), bf16 by torch's
+# cast, E4M3 by brute-force nearest-code search. Non-power-of-two scales, k_scale
+# != v_scale, and values chosen so that the bf16 cast before E4M3 changes the
+# code (double rounding), so that a swapped divisor or a dropped bf16 cast fails.
+# (A scale of 0.75 cannot show the double rounding: 4v/3 of a bf16 v never lies
+# within half a bf16 step of an E4M3 rounding midpoint without being one, so
+# that divisor could not tell a dropped bf16 cast apart.)
+
+K_SCALE, V_SCALE = np.float32(0.7), np.float32(0.6)
+
+
+def _e4m3_brute(vals):
+    from test_oracle_formats import _brute_force_code, _e4m3_table
+    codes, table = _e4m3_table()
+    return np.array([_brute_force_code(float(v), codes, table) for v in np.ravel(vals)], np.uint8)
+
+
+def _bf16(x):
+    """float32 -> bf16 (torch's round-to-nearest-even cast) -> float64."""
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def _stored(x, scale):
+    """The definition: E4M3(bf16(float32(x / scale)))."""
+    q = np.asarray(x, np.float32) / np.float32(scale)  # one IEEE float32 division
+    return _e4m3_brute(_bf16(q))
+
+
+def _double_rounding_values(lo, hi, scale):
+    """bf16 values in [lo, hi) whose E4M3 code changes when the float32 quotient
+    is cast to bf16 first (and the rest, for filler)."""
+    bits = np.arange(0x3C00, 0x4100, dtype=np.uint16)  # bf16 patterns of [2^-7, 8)
+    v = oracle.bf16_value(bits)
+    v = v[(v >= lo) & (v < hi)]
+    q = (v.astype(np.float32) / np.float32(scale)).astype(np.float32)
+    sens = _e4m3_brute(_bf16(q)) != _e4m3_brute(q)
+    return v[sens], v[~sens]
+
+
+def _unit_rms_head(payload, rng):
+    """A bf16 head of 64 values: `payload` (62 values) and two values that bring
+    the mean square within 1e-4 of 1, so that the normalised head equals the head
+    itself (x * rsqrt(ms + 1e-5) differs from x by < 1.1e-4 relative, far inside
+    half a bf16 step: the bf16 rounding returns x)."""
+    assert len(payload) == 62
+    r = 64.0 - float(np.sum(np.asarray(payload) ** 2))
+    assert r > 1.0
+    cand = oracle.bf16_value(np.arange(0x3C00, 0x4100, dtype=np.uint16))
+    cand = cand[cand * cand < r]
+    best = None
+    for a in cand:
+        b = float(_bf16(np.array([np.sqrt(r - a * a)], np.float32))[0])
+        err = abs(a * a + b * b - r)
+        if best is None or err < best[0]:
+            best = (err, a, b)
+    _, a, b = best
+    head = np.concatenate([payload, [a, -b]])
+    rng.shuffle(head)
+    ms = float(np.mean(head ** 2))
+    assert abs(ms - 1.0) <= 1e-4, ms
+    return head
+
+
+def test_scaled_cache_codes_from_the_definition():
+    rng = np.random.default_rng(11)
+    cfg = W.config("tiny_sliding_decode", batch=1, seq=("list", [37]), rope_theta=0.0, kv_scale=0.7,
+                   k_scale=float(K_SCALE), v_scale=float(V_SCALE))
+    inp = W.generate(cfg)
+    assert inp["k_scale"] == K_SCALE and inp["v_scale"] == V_SCALE
+    ks_sens, ks_rest = _double_rounding_values(0.25, 0.95, K_SCALE)
+    vs_sens, vs_rest = _double_rounding_values(0.05, 6.0, V_SCALE)
+    assert len(ks_sens) >= 4 and len(vs_sens) >= 8, (len(ks_sens), len(vs_sens))
+    qkv = inp["qkv"].copy()
+    k_heads, v_heads = [], []
+    for g in range(HKV):
+        pick = np.concatenate([ks_sens[g::2], rng.choice(ks_rest, 62 - len(ks_sens[g::2]), replace=False)])
+        pick = pick * rng.choice([-1.0, 1.0], size=62)
+        k_heads.append(_unit_rms_head(pick, rng))
+        vv = np.concatenate([vs_sens[g::2][:40], rng.choice(vs_rest, 64 - len(vs_sens[g::2][:40]), replace=False)])
+        v_heads.append(vv * rng.choice([-1.0, 1.0], size=64))
+    for g in range(HKV):
+        qkv[0, KCOL + g * D:KCOL + (g + 1) * D] = oracle.bf16_bits(k_heads[g])
+        qkv[0, VCOL + g * D:VCOL + (g + 1) * D] = oracle.bf16_bits(v_heads[g])
+    inp = dict(inp, qkv=qkv)
+    _, k, v, skipped = _run(cfg, inp)
+    assert skipped == 0
+    row = int(inp["cache_loc"][0])
+    got_k = k.reshape(-1, HKV * D)[row].reshape(HKV, D)
+    got_v = v.reshape(-1, HKV * D)[row].reshape(HKV, D)
+    for g in range(HKV):
+        assert np.array_equal(got_k[g], _stored(k_heads[g], K_SCALE)), f"k head {g}"
+        assert np.array_equal(got_v[g], _stored(v_heads[g], V_SCALE)), f"v head {g}"
+    # the unscaled path stores E4M3(x) for the same heads (the normalised k head is x)
+    _, k1, v1, _ = _run(dict(cfg, kv_scale=1.0), dict(inp, k_scale=np.float32(1), v_scale=np.float32(1)))
+    for g in range(HKV):
+        assert np.array_equal(k1.reshape(-1, HKV * D)[row].reshape(HKV, D)[g], _e4m3_brute(k_heads[g]))
+        assert np.array_equal(v1.reshape(-1, HKV * D)[row].reshape(HKV, D)[g], _e4m3_brute(v_heads[g]))

@@ -12,6 +12,8 @@ Every input is synthetic: qkv ~ N(0,1) in bf16, cache rows = E4M3 of N(0,1),
 physical pages a random permutation of a pool sized to the total, page_table
 -1 beyond each request's pages, positions = seq_len + i, cache_loc from the
 page table, cache_seqlens = seq_lens + L, cu_seqlens_q = 0, L, 2L, ...
+On the scaled path (kv_scale != 1) the device scales are k_scale = v_scale =
+kv_scale unless the config names its own "k_scale" / "v_scale".
 """
 from __future__ import annotations
 
@@ -126,7 +128,8 @@ def generate(cfg: dict, seed: int | None = None) -> dict:
         cache_seqlens=(seq + L).astype(np.int32),
         cu_seqlens_q=(np.arange(B + 1) * L).astype(np.int32), seq_lens=seq,
         page_table=page_table, k_cache=k_cache, v_cache=v_cache,
-        k_scale=np.float32(cfg["kv_scale"]), v_scale=np.float32(cfg["kv_scale"]),
+        k_scale=np.float32(cfg.get("k_scale", cfg["kv_scale"])),
+        v_scale=np.float32(cfg.get("v_scale", cfg["kv_scale"])),
         norm_weight=weight, eps=float(cfg["eps"]),
     )
 
