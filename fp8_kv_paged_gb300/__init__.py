@@ -18,7 +18,7 @@ from . import build as _build_mod
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_create", "okc_attn_plan_sizes",
            "okc_attn_plan_items", "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
-           "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "AttnStep",
+           "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "okc_attn_plan_clear_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_selftest_bounded_wait", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = [
     "okc_attn_combine_normgate", "okc_status_string", "okc_attn_decode_combine_noalloc",
     "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items", "okc_attn_plan_update",
     "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size", "okc_attn_plan_create",
-    "okc_attn_plan_scratch_sizes", "okc_selftest_bounded_wait",
+    "okc_attn_plan_scratch_sizes", "okc_selftest_bounded_wait", "okc_attn_plan_clear_errors",
 ]
 
 
@@ -123,6 +123,8 @@ def load(path: str | None = None):
     lib.okc_attn_plan_destroy.argtypes = [P]
     lib.okc_attn_plan_get_sizes.restype = st
     lib.okc_attn_plan_get_sizes.argtypes = [P, ctypes.POINTER(_Sizes)]
+    lib.okc_attn_plan_clear_errors.restype = st
+    lib.okc_attn_plan_clear_errors.argtypes = [P, P]
     lib.okc_attn_plan_read_errors.restype = st
     lib.okc_attn_plan_read_errors.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.okc_rope_table_init.restype = st
@@ -283,6 +285,10 @@ def okc_attn_plan_read_errors(plan: Plan, stream=None) -> int:
     _check(load().okc_attn_plan_read_errors(plan.handle, _stream(stream), ctypes.byref(v)),
            "okc_attn_plan_read_errors")
     return v.value
+
+
+def okc_attn_plan_clear_errors(plan: Plan, stream=None):
+    _check(load().okc_attn_plan_clear_errors(plan.handle, _stream(stream)), "okc_attn_plan_clear_errors")
 
 
 def okc_selftest_bounded_wait(err, limit_us: int, stream=None):

@@ -94,7 +94,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return OKC_ERR_CUDA;
   const bool use_tc = L >= 2 && L <= 8;  // the default plan's kernel choice
-  const int per_sm = decode_ctas_per_sm(L, use_tc);
+  const int per_sm = cached_ctas_per_sm(dev, L, use_tc);
   if (per_sm <= 0) return OKC_ERR_CUDA;
   SplitResult split;
   const okc_status st = make_splits(cfg, seq_lens_host, nullptr, sms * per_sm, &split);

@@ -315,9 +315,11 @@ bool use_tc(const okc_attn_config* c, const okc_plan_options* o) {
   return c->q_len >= 2 && c->q_len <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
 }
 
+}  // namespace
+
 // Resident decode CTAs per SM for (device, q_len, kernel family), queried once
 // per key: the query also raises the kernels' shared-memory limit on the device.
-int cached_ctas_per_sm(int dev, int L, bool tc) {
+int okc::cached_ctas_per_sm(int dev, int L, bool tc) {
   static std::mutex mu;
   static std::map<std::tuple<int, int, bool>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
@@ -329,6 +331,8 @@ int cached_ctas_per_sm(int dev, int L, bool tc) {
   return occ;
 }
 
+namespace {
+
 int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count_out) {
   int sms = (o && o->sm_count > 0) ? o->sm_count : 0;
   int per_sm = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : 0;
@@ -336,7 +340,7 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    if (per_sm == 0) per_sm = cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
+    if (per_sm == 0) per_sm = okc::cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
     if (per_sm <= 0) return -1;
   }
   if (sm_count_out) *sm_count_out = sms;
@@ -584,8 +588,11 @@ okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_ho
   uint8_t* head = static_cast<uint8_t*>(plan->pinned);
   std::memset(head, 0, up_bytes);
   write_head(plan, head);
+  // The upload starts past the header: the device error word keeps the bits
+  // earlier steps set until the caller reads or clears them.
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(plan->workspace, head, up_bytes, cudaMemcpyHostToDevice, str) != cudaSuccess ||
+  if (cudaMemcpyAsync(static_cast<uint8_t*>(plan->workspace) + okc::kWsHeader, head + okc::kWsHeader,
+                      up_bytes - okc::kWsHeader, cudaMemcpyHostToDevice, str) != cudaSuccess ||
       cudaEventRecord(plan->pinned_done, str) != cudaSuccess)
     return OKC_ERR_CUDA;
   return OKC_OK;
@@ -620,6 +627,13 @@ okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, ui
   if (cudaStreamSynchronize(s) != cudaSuccess) return OKC_ERR_CUDA;
   *flags_host = v;
   return OKC_OK;
+}
+
+okc_status okc_attn_plan_clear_errors(okc_attn_plan_t plan, okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  return cudaMemsetAsync(plan->d_err, 0, sizeof(unsigned), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OKC_OK
+             : OKC_ERR_CUDA;
 }
 
 okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream stream) {

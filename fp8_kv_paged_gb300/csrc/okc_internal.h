@@ -162,6 +162,9 @@ cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, flo
 // tcgen05 kernel for q_len 2..8), the lower of the three-call and the fused
 // variant (0 on error).
 int decode_ctas_per_sm(int L, bool tc);
+// decode_ctas_per_sm for device `dev`, queried once per (device, L, tc) and
+// cached (the query also raises the kernels' shared-memory limit on the device).
+int cached_ctas_per_sm(int dev, int L, bool tc);
 // The tcgen05 decode kernel for q_len 2..8 (decode_tc.cu).
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
 int decode_tc_ctas_per_sm();

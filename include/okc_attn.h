@@ -195,7 +195,9 @@ okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_l
  * (okc_attn_plan_max_sizes gives a workspace that never does). After
  * OKC_ERR_CUDA the plan may no longer match its workspace: destroy it.
  * The workspace is overwritten in stream order: kernels of the previous step
- * issued on other streams must be ordered before the call.
+ * issued on other streams must be ordered before the call. The device error
+ * word is not part of the upload: bits set by earlier steps stay until
+ * okc_attn_plan_clear_errors (or a new okc_attn_plan) clears them.
  * CUDA graphs: a launch captured in a graph keeps the grid size and the
  * workspace offsets of the plan as it was at capture. Replaying it after an
  * update is valid only while num_work is unchanged (the work list and request
@@ -209,8 +211,13 @@ okc_status okc_attn_plan_destroy(okc_attn_plan_t plan);
    the split partials) for its step. okc_attn_plan_scratch_sizes is the same call. */
 okc_status okc_attn_plan_get_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
 okc_status okc_attn_plan_scratch_sizes(okc_attn_plan_t plan, okc_attn_sizes* sizes);
-/* Synchronizes `stream`, then reads and returns the OKC_DEVERR_* bits seen so far. */
+/* Synchronizes `stream`, then reads and returns the OKC_DEVERR_* bits seen so
+   far: every bit the plan's kernels set since okc_attn_plan made the plan or
+   okc_attn_plan_clear_errors last cleared them (okc_attn_plan_update keeps them). */
 okc_status okc_attn_plan_read_errors(okc_attn_plan_t plan, okc_stream stream, uint32_t* flags_host);
+/* Zeroes the plan's device error word, asynchronously on `stream` (ordered after
+   the kernels issued before it on that stream). */
+okc_status okc_attn_plan_clear_errors(okc_attn_plan_t plan, okc_stream stream);
 
 /*
  * RoPE cos|sin table, built once per theta like the problem file's `_cos_sin`:

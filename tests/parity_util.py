@@ -97,6 +97,22 @@ def check_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, rows_mask: np.ndarray 
     return {"max_abs": mx, "mean_abs": mean, "exact": float(np.mean(g == r))}
 
 
+def oracle_ref(cfg: dict, inp: dict, rows_mask=None) -> dict:
+    """The oracle's step on copies of the caches: q8, caches, bf16 out bits."""
+    return oracle.step(cfg, inp, rows_mask)
+
+
+def check_against_oracle(cfg: dict, inp: dict, out_bits: np.ndarray, k_cache=None, v_cache=None,
+                         ref: dict | None = None) -> dict:
+    """A step's output (bf16 bits [T, Hq*64]) and, when given, its caches after
+    the step, against the oracle on the same inputs under the acceptance bounds."""
+    ref = ref if ref is not None else oracle_ref(cfg, inp)
+    rep = {"out": check_out(np.asarray(out_bits).reshape(ref["out"].shape), ref["out"])}
+    if k_cache is not None:
+        rep.update(check_caches(inp, {"k_cache": k_cache, "v_cache": v_cache}, ref["k_cache"], ref["v_cache"]))
+    return rep
+
+
 def full_check(cfg: dict, inp: dict, opts: dict | None = None, rows_mask=None, expect_errors: int = 0,
                fused: bool = False, plan_seq=None, plan_form: bool = False):
     gpu = run_gpu(cfg, inp, opts, fused=fused, plan_seq=plan_seq, plan_form=plan_form)

@@ -5,11 +5,13 @@
 // source is compiled in, so the real planner code runs on the host.
 //
 // Checks, over random configs, options and lengths: every in-place update
-// uploads the same workspace head (error word, work list, request table,
-// arrival counters) and reports the same sizes as a fresh plan of the same
-// lengths, within okc_attn_plan_max_sizes; a failed staging allocation, a
-// length past the page table and a too-small workspace each leave the plan's
-// sizes and workspace head unchanged, and the plan keeps working afterwards;
+// uploads the same workspace head (work list, request table, arrival
+// counters) and reports the same sizes as a fresh plan of the same lengths,
+// within okc_attn_plan_max_sizes, and leaves the device error word (the
+// header) as the kernels left it; a failed staging allocation, a length past
+// the page table and a too-small workspace each leave the plan's sizes and
+// workspace head unchanged, and the plan keeps working afterwards; a failed
+// upload returns OKC_ERR_CUDA, and a later update makes the plan whole again;
 // the default-option entry points (okc_attn_plan_create, _scratch_sizes,
 // _workspace_size) agree with the general ones.
 #include <cuda_runtime.h>
@@ -18,8 +20,9 @@
 #include <cstring>
 #include <random>
 #include <vector>
-static int g_fail_mallochost = 0, g_copies = 0, g_alloc_failures = 0;
+static int g_fail_mallochost = 0, g_copies = 0, g_alloc_failures = 0, g_fail_memcpy = 0, g_upload_failures = 0;
 static cudaError_t fake_memcpy_async(void* d, const void* s, size_t n, cudaMemcpyKind, cudaStream_t) {
+  if (g_fail_memcpy) { g_fail_memcpy--; return cudaErrorLaunchFailure; }
   memcpy(d, s, n); g_copies++; return cudaSuccess;
 }
 static cudaError_t fake_malloc_host(void** p, size_t n) {
@@ -100,6 +103,11 @@ int main(int argc, char** argv) {
           CHECK(head_bytes(p) == head_before.size());
         }
         g_fail_mallochost = 0;
+      } else if (mode == 2) {  // the upload itself fails: reported, and the next update repairs the plan
+        g_fail_memcpy = 1;
+        CHECK(okc_attn_plan_update(p, s1.data(), nullptr) == OKC_ERR_CUDA);
+        g_fail_memcpy = 0;
+        g_upload_failures++;
       } else if (mode == 1) {  // a length past the page table: refused, plan unchanged
         auto bad = s1;
         bad[g() % B] = max_pages * P;  // + L > max_pages * P
@@ -109,7 +117,11 @@ int main(int argc, char** argv) {
         CHECK(memcmp(&before, &after, sizeof before) == 0);
         CHECK(memcmp(head_before.data(), w, head_before.size()) == 0);
       }
+      // bits the kernels set in the error word survive the update
+      const uint32_t err_word = (uint32_t)g() | 1u;
+      memcpy(w, &err_word, sizeof err_word);
       CHECK(okc_attn_plan_update(p, s1.data(), nullptr) == OKC_OK);
+      CHECK(memcmp(w, &err_word, sizeof err_word) == 0);
       okc_attn_plan_t q = nullptr;
       CHECK(okc_attn_plan(&c, s1.data(), &o, w2, bound.workspace_bytes, nullptr, &q) == OKC_OK);
       okc_attn_sizes zp, zq;
@@ -117,7 +129,9 @@ int main(int argc, char** argv) {
       okc_attn_plan_get_sizes(q, &zq);
       CHECK(memcmp(&zp, &zq, sizeof zp) == 0);
       CHECK(head_bytes(p) == head_bytes(q));
-      CHECK(memcmp(w, w2, head_bytes(p)) == 0);  // the uploaded heads are identical
+      // the uploaded heads are identical past the header (the fresh plan zeroed its error word)
+      CHECK(memcmp(w + okc::kWsHeader, w2 + okc::kWsHeader, head_bytes(p) - okc::kWsHeader) == 0);
+      memset(w, 0, sizeof err_word);
       CHECK(zp.workspace_bytes <= bound.workspace_bytes && zp.o_partial_bytes <= bound.o_partial_bytes &&
             zp.num_work <= bound.num_work);
       okc_attn_plan_destroy(q);
@@ -151,7 +165,7 @@ int main(int argc, char** argv) {
     }
     okc_attn_plan_destroy(p);
   }
-  CHECK(g_alloc_failures > 0);
+  CHECK(g_alloc_failures > 0 && g_upload_failures > 0);
   // the default-option forms: okc_attn_plan_create is okc_attn_plan with no
   // options, okc_attn_plan_scratch_sizes its sizes, okc_attn_plan_workspace_size
   // the workspace bound of okc_attn_plan_max_sizes (152 SMs, the stubs' occupancy)
@@ -178,5 +192,6 @@ int main(int argc, char** argv) {
     okc_attn_plan_destroy(p1);
     okc_attn_plan_destroy(p2);
   }
-  printf("ok: %d updates compared with fresh plans, %d failed staging allocations\n", cases, g_alloc_failures);
+  printf("ok: %d updates compared with fresh plans, %d failed staging allocations, %d failed uploads\n", cases,
+         g_alloc_failures, g_upload_failures);
 }

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from parity_util import full_check, run_gpu, to_device
+from parity_util import check_against_oracle, full_check, run_gpu, to_device
 from test_gpu_parity import SMALL
 
 pytestmark = pytest.mark.gpu
@@ -139,6 +139,8 @@ def test_step_from_host_buffers(name, memory):
     assert step.errors() == 0
     assert np.array_equal(host["out"].numpy().view(np.uint16), ref["out"])
     assert np.array_equal(d["k_cache"].cpu().numpy(), ref["k_cache"])
+    check_against_oracle(cfg, inp, host["out"].numpy().view(np.uint16), d["k_cache"].cpu().numpy(),
+                         d["v_cache"].cpu().numpy())
 
 
 @pytest.mark.parametrize("name", ["sliding_decode", "verify_block", "tiny_sliding_decode"])
@@ -178,6 +180,7 @@ def test_step_replays_from_a_cuda_graph(name):
         assert step.errors() == 0
         assert np.array_equal(got_out, ref["out"])
         assert np.array_equal(got_k, ref["k_cache"])
+        check_against_oracle(cfg, case, got_out, got_k, d["v_cache"].cpu().numpy())
 
 
 def _shorter(cfg, inp, d):
@@ -216,7 +219,9 @@ def test_plan_update_in_place_matches_a_fresh_plan(name):
         torch.cuda.synchronize()
         ref = run_gpu(cfg, case, plan_form=True, fused=True)
         assert step.errors() == 0
-        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, ref["out"])
+        check_against_oracle(cfg, case, got, d["k_cache"].cpu().numpy(), d["v_cache"].cpu().numpy())
     # a plan whose workspace fits only short contexts refuses longer ones
     tiny = {k: (np.minimum(v, 40) if k == "seq_lens" else v) for k, v in inp.items()}
     import torch
@@ -259,3 +264,27 @@ def test_workspace_sized_for_the_longest_context_serves_every_update():
                     assert z[f] <= bound[f], (name, f)
         torch.cuda.synchronize()
         plan.close()
+
+
+def test_plan_update_keeps_the_device_error_word():
+    """Bits the kernels set in the plan's error word survive okc_attn_plan_update
+    (the update uploads the work list past the word) until
+    okc_attn_plan_clear_errors zeroes it; a clean step then reports nothing."""
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    cfg = W.config("sliding_decode", batch=4, seq=("uniform", 500, 900))
+    inp = W.generate(cfg)
+    bad = dict(inp, page_table=inp["page_table"].copy())
+    bad["page_table"][2, 10] = cfg["num_pages"] + 5  # a visible key's page past the pool
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    step.run_fused(to_device(cfg, bad), eps=inp["eps"])
+    assert step.errors() == okc.DEVERR_PAGE
+    step.plan.update(inp["seq_lens"] - 7)
+    assert step.errors() == okc.DEVERR_PAGE
+    okc.okc_attn_plan_clear_errors(step.plan)
+    assert step.errors() == 0
+    step.plan.update(inp["seq_lens"])
+    out = step.run_fused(to_device(cfg, inp), eps=inp["eps"])
+    torch.cuda.synchronize()
+    assert step.errors() == 0
+    check_against_oracle(cfg, inp, out.view(torch.int16).cpu().numpy().view(np.uint16))

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import workloads as W
-from parity_util import OUT_MAX_ABS, OUT_MEAN_ABS, to_device
+from parity_util import OUT_MAX_ABS, OUT_MEAN_ABS, check_against_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +27,9 @@ def _three_call(okc, cfg, inp, d):
     return step, out
 
 
-def _noalloc(okc, cfg, inp, d, q_fp8):
-    out = torch.full((inp["qkv"].shape[0], 16 * 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+def _noalloc(okc, cfg, inp, d, q_fp8, out=None):
+    if out is None:
+        out = torch.full((inp["qkv"].shape[0], 16 * 64), float("nan"), dtype=torch.bfloat16, device="cuda")
     okc.okc_attn_decode_combine_noalloc(
         cfg, inp["seq_lens"], q_fp8, d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
         d["page_table"], d["cache_seqlens"], d["cu_seqlens_q"], d["seq_lens"], d["qkv"],
@@ -64,6 +65,30 @@ def test_noalloc_matches_three_call_path(cuda_lib):
         out = _noalloc(okc, cfg, inp, d, step.q_fp8)
         exact = _compare(out, ref)
         assert exact == 1.0  # same kernels, same merge order: bit-identical
+        # and against the oracle on the same inputs, under the acceptance bounds
+        check_against_oracle(cfg, inp, out.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def test_noalloc_call_takes_no_device_memory(cuda_lib):
+    """After the first call on the device (which loads the library's module and,
+    with it, the static array), further calls leave the device's free memory
+    unchanged: they allocate nothing."""
+    okc = cuda_lib
+    cfg = W.config("sliding_decode", batch=8, seq=("uniform", 1024, 3000))
+    inp = W.generate(cfg)
+    d = to_device(cfg, inp)
+    step, ref = _three_call(okc, cfg, inp, d)
+    outs = [torch.empty_like(ref) for _ in range(3)]  # every tensor allocated up front
+    _noalloc(okc, cfg, inp, d, step.q_fp8, outs[0])
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for o in outs[1:]:
+        _noalloc(okc, cfg, inp, d, step.q_fp8, o)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    for o in outs:
+        assert torch.equal(o, ref)
 
 
 def test_noalloc_rejects_steps_beyond_its_scratch(cuda_lib):
