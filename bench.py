@@ -1,15 +1,19 @@
 """Benchmark of the paged-FP8 gated attention block on GB300.
 
-One step = the whole block over one batch of the sliding-window decode
-workload: B=64, L=1, Hq=16, Hkv=2, d=64, seq_lens uniform in [1024, 8192],
-page_size 1, window 2048, RoPE theta 5e5, kv_scale 1 (synthetic, seeded).
+One step = the whole block over one batch of a workload. The headline line is
+the largest workload that fits one GPU, the mixed full-attention decode batch:
+B=256, L=1, Hq=16, Hkv=2, d=64, seq_lens log-uniform in [1, 131072], page_size
+1, window 0 (no RoPE), kv_scale 1 (synthetic, seeded; about 0.73 GB of KV rows
+per step). The same line carries, under "workloads", the same measurements for
+the other four workloads (tiny sliding decode, sliding decode, full decode at
+32k, verify block); --workload picks another headline and --no-others drops
+the rest.
 
 The timed step is okc_attn_step in the form its plan chooses (one fused kernel
-for this workload; prepare, decode and combine for others: the line's
-config.path says which). --path three_call times okc_prepare_qkv ->
-okc_attn_decode -> okc_attn_combine_normgate instead, and the line's "compare"
-entry times the other path the same way. --workload picks another of the five
-workloads.
+or prepare, decode and combine: the entry's config.path says which). --path
+three_call times okc_prepare_qkv -> okc_attn_decode ->
+okc_attn_combine_normgate instead, and the headline's "compare" entry times
+the other path the same way.
 
 Timing: W warm-up steps, then exactly K steps, replayed from CUDA graphs of
 the step's launches; consecutive steps rotate over independent copies of the
@@ -17,14 +21,18 @@ inputs (cache pools, page tables, qkv) whose total exceeds 3x the L2 cache, so
 every step streams its KV rows from HBM. CUDA events on the launching stream,
 a device synchronize and a barrier on both sides, max over ranks. The step's
 dominant kernel is then timed alone (launches without programmatic overlap)
-for the roofline. `e2e` repeats the step through the public API from pinned host
-buffers: per step the plan, the step's inputs moved from host memory to the GPU
-(read in place by the kernels over the host link: the buffers are page-locked
-and mapped), the step's calls and the output written back to host memory.
+for the roofline. `e2e` repeats the step through the public API from pinned
+host buffers: per step the plan, the step's inputs moved from host memory to
+the GPU (read in place by the kernels over the host link: the buffers are
+page-locked and mapped), the step's calls and the output written back to host
+memory.
 
---impl reference times the CPU oracle (the only other implementation of the
-block here) on the host cores, on a bounded sample of the same workload.
-Multi-GPU: replicas only (each rank runs its own independent batch).
+cpu_baseline: the CPU oracle as it stands on a bounded sample of each workload
+(whole requests), single-threaded and on all host cores (one thread per core,
+each running the oracle's attention on its own share of the requests; ctypes
+calls release the interpreter lock), with the core count and CPU model.
+--impl reference times that oracle alone, on all host cores, as the reference
+arm. Multi-GPU: replicas only (each rank runs its own independent batch).
 """
 from __future__ import annotations
 
@@ -36,6 +44,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -54,7 +63,7 @@ NCU_TRAFFIC = {
     ("full_decode_32k", "decode_kernel"): 545.487872e6 + 3.411968e6,
     ("mixed_full_decode", "decode_kernel<fused step>"): 803.03872e6 + 7.589632e6,
 }
-WORKLOAD = "sliding_decode"
+WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -76,6 +85,32 @@ def measured_peak_hbm():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 class ClockSampler:
@@ -160,83 +195,135 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
     return tokens_per_rank * world / (ms_per_step * 1e-3)
 
 
-def cpu_oracle_run(cfg, inp, budget_s: float, max_steps: int | None = None):
-    """Time the oracle (as it stands) on a bounded sample: whole requests of the
-    workload, as many as fit the budget. Returns (tokens/s, sample text, tokens)."""
-    import oracle
+# ------------------------------------------------------------ CPU oracle timing
+
+def _requests(cfg, inp, bs):
+    """The step restricted to requests `bs` (uniform q_len), sharing the caches."""
+    L = cfg["q_len"]
+    bs = np.asarray(bs, np.int64)
+    rows = (bs[:, None] * L + np.arange(L)[None, :]).reshape(-1)
+    c = dict(cfg, batch=len(bs))
+    d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows], cache_loc=inp["cache_loc"][rows],
+             cache_seqlens=inp["cache_seqlens"][bs], seq_lens=inp["seq_lens"][bs],
+             page_table=np.ascontiguousarray(inp["page_table"][bs]),
+             cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
+    return c, d, rows
+
+
+def visible_keys(cfg, seq_lens) -> np.ndarray:
+    """Keys each request's queries see in all (the union over its q_len queries)."""
+    L, w = cfg["q_len"], cfg["window"]
+    n = np.asarray(seq_lens, np.int64) + L
+    return np.minimum(n, w + L - 1) if w > 0 else n
+
+
+def oracle_seconds_per_request(cfg, inp) -> float:
+    """The oracle's time for a request of the workload's mean size, from one
+    timed pass over its first few requests (after a warm pass)."""
+    probe = OracleRunner(cfg, inp, min(cfg["batch"], 4))
+    probe.run()  # load and warm the library
+    t0 = time.perf_counter()
+    probe.run()
+    per_key = max(time.perf_counter() - t0, 1e-5) / float(probe.cost.sum())
+    return per_key * float(visible_keys(cfg, inp["seq_lens"]).mean())
+
+
+class OracleRunner:
+    """The oracle's step (prepare, attention, norm-gate: the functions as they
+    stand) over the first `nreq` requests of a workload, with the attention of
+    the requests spread over `threads` host threads (longest first, each thread
+    a share of similar cost). Caches are copied once, outside every timing:
+    the prepare step rewrites the same rows with the same codes each pass."""
+
+    def __init__(self, cfg, inp, nreq):
+        import oracle
+        self.o = oracle
+        self.cfg, self.inp = cfg, inp
+        self.c, self.d, _ = _requests(cfg, inp, np.arange(nreq))
+        self.k = inp["k_cache"].copy()
+        self.v = inp["v_cache"].copy()
+        self.cost = visible_keys(cfg, self.d["seq_lens"])
+
+    def groups(self, threads):
+        order = np.argsort(-self.cost, kind="stable")
+        load = np.zeros(threads)
+        groups = [[] for _ in range(threads)]
+        for b in order:
+            i = int(np.argmin(load))
+            groups[i].append(int(b))
+            load[i] += self.cost[b]
+        return [sorted(g) for g in groups if g]
+
+    def run(self, threads=1, pool=None):
+        o, c, d = self.o, self.c, self.d
+        q8, _ = o.prepare(c, d, self.k, self.v)
+        if threads == 1 or pool is None:
+            out, _ = o.attention(c, d, q8, self.k, self.v)
+        else:
+            out = np.zeros((q8.shape[0], c["num_q_heads"], 64), np.float64)
+
+            def part(g):
+                cg, dg, rows = _requests(c, d, g)
+                og, _ = o.attention(cg, dg, np.ascontiguousarray(q8[rows]), self.k, self.v)
+                out[rows] = og
+            list(pool.map(part, self.groups(threads)))
+        return o.normgate(c, out, d["qkv"], d.get("norm_weight"), d["eps"])
+
+
+def cpu_oracle_baseline(cfg, inp, budget_s: float) -> dict:
+    """The oracle as it stands on a bounded sample (whole requests) of the
+    workload: tokens/s single-threaded and on all host cores."""
     B, L = cfg["batch"], cfg["q_len"]
-    # one request first to size the sample
-    def sub(bs):
-        c = dict(cfg, batch=len(bs))
-        rows = np.concatenate([np.arange(b * L, (b + 1) * L) for b in bs])
-        d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows],
-                 cache_loc=inp["cache_loc"][rows], cache_seqlens=inp["cache_seqlens"][bs],
-                 seq_lens=inp["seq_lens"][bs], page_table=inp["page_table"][bs],
-                 cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
-        return c, d
-    oracle.step(*sub([0]))  # load and warm the library
-    # a pass over all requests sizes the sample: whole passes while they fit
-    # the budget, else the requests that fit it (estimated from one request
-    # when a whole pass would be far over the budget)
+    cores = host_cores()
+    per_req = oracle_seconds_per_request(cfg, inp)
+    nreq = int(max(1, min(B, 0.5 * budget_s / per_req)))
+    r = OracleRunner(cfg, inp, nreq)
     t0 = time.perf_counter()
-    oracle.step(*sub([B - 1]))
-    est = max(time.perf_counter() - t0, 1e-5) * B
-    if est > 2 * budget_s:
-        pass_s = est
-    else:
-        c, d = sub(list(range(B)))
-        t0 = time.perf_counter()
-        oracle.step(c, d)
-        pass_s = max(time.perf_counter() - t0, 1e-4)
-    nreq, reps = B, int(max(1, budget_s / pass_s))
-    if max_steps is not None:
-        reps = max(1, min(reps, max_steps))
-    if pass_s > budget_s:
-        nreq = int(max(1, B * budget_s / pass_s))
-    c, d = sub(list(range(nreq)))
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.step(c, d)
-    el = time.perf_counter() - t0
-    toks = nreq * L * reps
-    sample = f"{nreq} of {B} requests x {reps} pass(es) of {cfg['name']}, single-threaded C oracle"
-    return toks / el, sample, toks, el
+    r.run()
+    single_s = time.perf_counter() - t0
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        r.run(cores, pool)  # warm the threads
+        reps, el = 0, 0.0
+        while reps < 1 or (el < 0.25 * budget_s and reps < 1000):
+            t0 = time.perf_counter()
+            r.run(cores, pool)
+            el += time.perf_counter() - t0
+            reps += 1
+    toks = nreq * L
+    model = cpu_model()
+    return {"value": toks / single_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nreq} of {B} requests of {cfg['name']} (one pass), single-threaded C oracle",
+            "seconds": single_s,
+            "all_cores": {"value": toks * reps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                          "sample": f"{nreq} of {B} requests x {reps} pass(es), attention spread over {cores} "
+                                    "host threads", "seconds": el},
+            "nproc": cores, "cpu_model": model}
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle as it stands, on the host cores, each of
+    """The reference arm: the CPU oracle as it stands, on all host cores, each of
     the K steps one bounded sample (whole requests) of the same workload."""
     if rank != 0:
         return
-    import oracle
     cfg = W.config(args.workload)
     inp = W.generate(cfg)
     B, L = cfg["batch"], cfg["q_len"]
-
-    def sub(bs):
-        c = dict(cfg, batch=len(bs))
-        rows = np.concatenate([np.arange(b * L, (b + 1) * L) for b in bs])
-        d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows],
-                 cache_loc=inp["cache_loc"][rows], cache_seqlens=inp["cache_seqlens"][bs],
-                 seq_lens=inp["seq_lens"][bs], page_table=inp["page_table"][bs],
-                 cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
-        return c, d
-
-    t0 = time.perf_counter()
-    oracle.step(*sub([0]))
-    per_req = max(time.perf_counter() - t0, 1e-4)
-    total_budget = 90.0  # seconds of oracle work for the whole run
-    nreq = int(max(1, min(B, total_budget / (per_req * max(1, args.steps + args.warmup)))))
-    c, d = sub(list(range(nreq)))
-    for _ in range(args.warmup):
-        oracle.step(c, d)
+    cores = host_cores()
+    per_req = oracle_seconds_per_request(cfg, inp)
+    total_budget = 60.0  # seconds of oracle work (all cores) for the whole run
+    nreq = int(max(1, min(B, total_budget * cores / (per_req * max(1, args.steps + args.warmup)))))
+    r = OracleRunner(cfg, inp, nreq)
     el = 0.0
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle.step(c, d)
-        el += time.perf_counter() - t0
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(args.warmup):
+            r.run(cores, pool)
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            r.run(cores, pool)
+            el += time.perf_counter() - t0
     value = nreq * L * args.steps / el
-    sample = f"{nreq} of {B} requests of {args.workload} per step, single-threaded C oracle"
+    sample = (f"{nreq} of {B} requests of {args.workload} per step, C oracle with its attention spread over "
+              f"{cores} host threads ({cpu_model()})")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps * B / nreq,
@@ -244,23 +331,192 @@ def run_reference(args, world, rank):
         "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "batch": B, "q_len": L, "page_size": cfg["page_size"],
                    "window": cfg["window"], "rope_theta": cfg["rope_theta"]},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- GPU measurement
+
+class Bench:
+    """Shared state of one bench run on one GPU."""
+
+    def __init__(self, args, world, rank, local):
+        import torch
+        import fp8_kv_paged_gb300 as okc
+        self.torch, self.okc = torch, okc
+        self.args, self.world, self.rank = args, world, rank
+        self.dev = torch.device("cuda", local)
+        self.stream = torch.cuda.Stream(device=self.dev)
+        self.l2 = torch.cuda.get_device_properties(self.dev).L2_cache_size
+
+    def barrier(self):
+        self.torch.cuda.synchronize(self.dev)
+        if self.world > 1:
+            self.torch.distributed.barrier()
+
+    def capture(self, fn, nsteps):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            fn(0)  # warm the launch path
+        self.stream.synchronize()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(nsteps):
+                fn(i)
+        return g
+
+    def timed(self, fn, steps_total, warm, R):
+        """ms per step of `steps_total` steps replayed from graphs (exact count)."""
+        torch = self.torch
+        r_, m_ = divmod(steps_total, R)
+        g_main = self.capture(fn, R) if r_ else None
+        g_rem = self.capture(fn, m_) if m_ else None
+        nw = max(3, min(warm, R))
+        g_warm = self.capture(fn, nw)
+        left = warm
+        while left > 0:
+            g_warm.replay()
+            left -= nw
+        self.barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.time()
+        with torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            for _ in range(r_):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(self.stream)
+        self.barrier()
+        w1 = time.time()
+        ms = max_over_ranks(ev0.elapsed_time(ev1), self.world, self.dev)
+        return ms / steps_total, w0, w1
+
+    def measure(self, name, steps, warmup, clocks=None, compare=False, cpu=True):
+        """Every figure of one workload: the step, its dominant kernel alone, e2e, CPU baseline."""
+        torch, okc, args, dev, stream = self.torch, self.okc, self.args, self.dev, self.stream
+        cfg = W.config(name)
+        inp = W.generate(cfg, seed=rank_seed(cfg["seed"], self.rank))
+        T = cfg["batch"] * cfg["q_len"]
+        kvb = kv_bytes(cfg, inp["seq_lens"])
+
+        # independent input sets so that consecutive steps miss in L2
+        base = W.to_torch(inp, dev)
+        if cfg["rope_theta"] != 0.0:
+            npos = int(inp["positions"].max()) + 1
+            base["rope_table"] = torch.empty((npos, 64), dtype=torch.float32, device=dev)
+            okc.okc_rope_table_init(cfg["rope_theta"], npos, base["rope_table"])
+        set_bytes = sum(t.numel() * t.element_size() for k, t in base.items()
+                        if t is not None and k not in ("rope_table",))
+        n_sets = max(2, math.ceil(3 * self.l2 / set_bytes))
+        shared = ("rope_table", "k_scale", "v_scale", "norm_weight")
+        sets = [base] + [{k: (None if t is None else (t if k in shared else t.clone())) for k, t in base.items()}
+                         for _ in range(n_sets - 1)]
+        plan_opts = {}
+        if args.chunk_keys:
+            plan_opts["chunk_keys"] = args.chunk_keys
+        if args.step_form != "plan":
+            plan_opts["flags"] = okc.PLAN_STEP_ONE_LAUNCH if args.step_form == "one" else \
+                okc.PLAN_STEP_THREE_LAUNCHES
+        plan_opts = plan_opts or None
+        step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts)
+        fused = args.path == "fused"
+
+        def run_step(st, s_, use_fused):
+            if use_fused:
+                st.run_fused(s_, eps=inp["eps"], stream=stream)
+            else:
+                st.run(s_, eps=inp["eps"], stream=stream)
+
+        R = n_sets * max(1, 48 // n_sets)  # steps per graph replay
+        if clocks is not None:
+            clocks.start()
+            time.sleep(0.3)
+        ms_step, t_wall0, t_wall1 = self.timed(lambda i: run_step(step, sets[i % n_sets], fused), steps, warmup, R)
+
+        # the step's dominant kernel alone, no programmatic overlap: the fused
+        # step kernel, or the decode kernel of the three-call path
+        step_np = okc.AttnStep(cfg, inp["seq_lens"],
+                               opts=dict(plan_opts or {}, flags=(plan_opts or {}).get("flags", 0) | okc.PLAN_NO_PDL))
+        for s_ in sets:
+            step_np.run(s_, eps=inp["eps"], stream=stream)
+        stream.synchronize()
+        step_kernels = step.sizes["step_kernels"]
+        if fused and step_kernels == 1:
+            def one_kernel(i):
+                s_ = sets[i % n_sets]
+                okc.okc_attn_step(step_np.plan, s_["qkv"], s_["positions"], s_["cache_loc"], s_["k_cache"],
+                                  s_["v_cache"], s_["k_scale"], s_["v_scale"], s_["rope_table"], s_["page_table"],
+                                  s_["cache_seqlens"], s_["cu_seqlens_q"], s_["seq_lens"], s_["norm_weight"],
+                                  inp["eps"], step_np.o_partial, step_np.lse_partial, step_np.out, stream)
+            kname = "decode_kernel<fused step>"
+        else:
+            def one_kernel(i):
+                s_ = sets[i % n_sets]
+                okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
+                                    s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
+                                    s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
+            kname = "decode_tc_kernel" if 2 <= cfg["q_len"] <= 8 else "decode_kernel"
+        kernel_ms, _, _ = self.timed(one_kernel, max(R, min(steps, 20 * R)), 3, R)
+        kernel_us = 1000.0 * kernel_ms
+        clk = clocks.stop(t_wall0, t_wall1) if clocks is not None else None
+
+        other = {}
+        if compare:
+            def run_other(i):
+                run_step(step, sets[i % n_sets], not fused)
+            oms, _, _ = self.timed(run_other, max(R, min(steps, 20 * R)), 3, R)
+            other = {"path": "three_call" if fused else "fused", "ms_per_step": oms,
+                     "value": job_throughput(T, self.world, oms)}
+
+        e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(max(steps, 20), 200), fused=fused)
+        peak, peak_kind = measured_peak_hbm()
+        achieved = kvb / (kernel_us * 1e-6) / 1e9
+        res = {
+            "value": job_throughput(T, self.world, ms_step), "unit": "tokens/s", "ms_per_step": ms_step,
+            "config": {"workload": name, "batch": cfg["batch"], "q_len": cfg["q_len"],
+                       "page_size": cfg["page_size"], "window": cfg["window"], "rope_theta": cfg["rope_theta"],
+                       "kv_scale": cfg["kv_scale"], "kv_bytes_per_step": kvb,
+                       "path": "okc_attn_step (%d kernel%s)" % (step_kernels, "" if step_kernels == 1 else "s")
+                       if fused else "three calls",
+                       "num_work": step.sizes["num_work"],
+                       "parallelism": "replicas" if self.world > 1 else "single-gpu",
+                       "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
+            "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
+            "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
+            "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": NCU_TRAFFIC.get((name, kname)), "algorithmic_bytes": kvb,
+                         "peak_source": peak_kind, "avg_launch_us": kernel_us},
+            "e2e": e2e,
+            "gpu_launches": (step_kernels if fused else 3) * steps,
+        }
+        if clk is not None:
+            res["clocks"] = clk
+        if other:
+            res["compare"] = other
+        if cpu and self.rank == 0 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_oracle_baseline(cfg, inp, budget_s=args.cpu_budget)
+        del sets, base, step, step_np
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50000)
-    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="okc", choices=["okc", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=list(W.WORKLOADS))
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work in cpu_baseline")
+    ap.add_argument("--no-others", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="fused", choices=["fused", "three_call"],
-                    help="okc_attn_step (one launch) or okc_prepare_qkv + okc_attn_decode + okc_attn_combine_normgate")
+                    help="okc_attn_step or okc_prepare_qkv + okc_attn_decode + okc_attn_combine_normgate")
     ap.add_argument("--no-compare", action="store_true", help="skip timing the other path")
     ap.add_argument("--chunk-keys", type=int, default=0,
                     help="keys per split work item (plan option; 0 = the plan's heuristic)")
@@ -278,166 +534,26 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     okc.build()
-
-    cfg = W.config(args.workload)
-    inp = W.generate(cfg, seed=rank_seed(cfg["seed"], rank))
-    T = cfg["batch"] * cfg["q_len"]
-    kvb = kv_bytes(cfg, inp["seq_lens"])
-
-    # independent input sets so that consecutive steps miss in L2
-    base = W.to_torch(inp, dev)
-    if cfg["rope_theta"] != 0.0:
-        npos = int(inp["positions"].max()) + 1
-        base["rope_table"] = torch.empty((npos, 64), dtype=torch.float32, device=dev)
-        okc.okc_rope_table_init(cfg["rope_theta"], npos, base["rope_table"])
-    set_bytes = sum(t.numel() * t.element_size() for k, t in base.items()
-                    if t is not None and k not in ("rope_table",))
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_sets = max(2, math.ceil(3 * l2 / set_bytes))
-    sets = [base] + [{k: (None if t is None else (t if k in ("rope_table", "k_scale", "v_scale", "norm_weight")
-                                                   else t.clone())) for k, t in base.items()}
-                     for _ in range(n_sets - 1)]
-    plan_opts = {}
-    if args.chunk_keys:
-        plan_opts["chunk_keys"] = args.chunk_keys
-    if args.step_form != "plan":
-        plan_opts["flags"] = okc.PLAN_STEP_ONE_LAUNCH if args.step_form == "one" else okc.PLAN_STEP_THREE_LAUNCHES
-    plan_opts = plan_opts or None
-    step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts)
-    stream = torch.cuda.Stream(device=dev)
-    fused = args.path == "fused"
-
-    def run_step(st, s_):
-        if fused:
-            st.run_fused(s_, eps=inp["eps"], stream=stream)
-        else:
-            st.run(s_, eps=inp["eps"], stream=stream)
-
-    def capture(fn, nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            fn(0)  # warm the launch path
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(nsteps):
-                fn(i)
-        return g
-
-    R = n_sets * max(1, 48 // n_sets)  # steps per graph replay
-    reps, rem = divmod(args.steps, R)
-
-    def timed(fn, steps_total, warm):
-        """ms per step of `steps_total` steps replayed from graphs (exact count)."""
-        r_, m_ = divmod(steps_total, R)
-        g_main = capture(fn, R)
-        g_rem = capture(fn, m_) if m_ else None
-        g_warm = capture(fn, max(3, min(warm, R)))
-        left = warm
-        while left > 0:
-            g_warm.replay()
-            left -= max(3, min(warm, R))
-        barrier()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0 = time.time()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(r_):
-                g_main.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            ev1.record(stream)
-        barrier()
-        w1 = time.time()
-        ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-        return ms / steps_total, w0, w1
-
-    def barrier():
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
+    b = Bench(args, world, rank, local)
 
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    ms_step, t_wall0, t_wall1 = timed(lambda i: run_step(step, sets[i % n_sets]), args.steps, args.warmup)
-
-    # the step's dominant kernel alone, K launches, no programmatic overlap: the
-    # fused step kernel, or the decode kernel of the three-call path
-    step_np = okc.AttnStep(cfg, inp["seq_lens"],
-                           opts=dict(plan_opts or {}, flags=(plan_opts or {}).get("flags", 0) | okc.PLAN_NO_PDL))
-    for s_ in sets:
-        step_np.run(s_, eps=inp["eps"], stream=stream)
-    stream.synchronize()
-    step_kernels = step.sizes["step_kernels"]  # the form okc_attn_step takes for this plan
-    one_launch = fused and step_kernels == 1
-    if one_launch:
-        def one_kernel(i):
-            s_ = sets[i % n_sets]
-            okc.okc_attn_step(step_np.plan, s_["qkv"], s_["positions"], s_["cache_loc"], s_["k_cache"],
-                              s_["v_cache"], s_["k_scale"], s_["v_scale"], s_["rope_table"], s_["page_table"],
-                              s_["cache_seqlens"], s_["cu_seqlens_q"], s_["seq_lens"], s_["norm_weight"],
-                              inp["eps"], step_np.o_partial, step_np.lse_partial, step_np.out, stream)
-        kname = "decode_kernel<fused step>"
-    else:
-        def one_kernel(i):
-            s_ = sets[i % n_sets]
-            okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
-                                s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
-                                s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
-        kname = "decode_tc_kernel" if 2 <= cfg["q_len"] <= 8 else "decode_kernel"
-    kernel_ms, _, _ = timed(one_kernel, max(R, min(args.steps, 20 * R)), 3)
-    kernel_us = 1000.0 * kernel_ms
-    clk = clocks.stop(t_wall0, t_wall1)
-
-    # the other path, for comparison (same timing method)
-    other = {}
-    if not args.no_compare:
-        other_fused = not fused
-        def run_other(i):
-            if other_fused:
-                step.run_fused(sets[i % n_sets], eps=inp["eps"], stream=stream)
-            else:
-                step.run(sets[i % n_sets], eps=inp["eps"], stream=stream)
-        oms, _, _ = timed(run_other, max(R, min(args.steps, 20 * R)), 3)
-        other = {"path": "fused" if other_fused else "three_call", "ms_per_step": oms,
-                 "value": job_throughput(T, world, oms)}
-
-    # end to end through the public API with host buffers
-    e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(args.steps, 200), fused=fused)
-
-    peak, peak_kind = measured_peak_hbm()
-    achieved = kvb / (kernel_us * 1e-6) / 1e9
-    value = job_throughput(T, world, ms_step)
+    head = b.measure(args.workload, args.steps, args.warmup, clocks=clocks, compare=not args.no_compare)
+    others = {}
+    if not args.no_others:
+        for name in W.WORKLOADS:
+            if name != args.workload:
+                others[name] = b.measure(name, args.steps, args.warmup)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3/f16->f32",
-        "data": "synthetic (seeded), L2 defeated by rotating %d input sets > 3x L2" % n_sets,
-        "config": {"workload": args.workload, "batch": cfg["batch"], "q_len": cfg["q_len"],
-                   "page_size": cfg["page_size"], "window": cfg["window"],
-                   "rope_theta": cfg["rope_theta"], "kv_bytes_per_step": kvb,
-                   "path": "okc_attn_step (%d kernel%s)" % (step_kernels, "" if step_kernels == 1 else "s")
-                   if fused else "three calls",
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
-        "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
-        "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
-        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": NCU_TRAFFIC.get((args.workload, kname)), "algorithmic_bytes": kvb,
-                     "peak_source": peak_kind, "avg_launch_us": kernel_us},
-        "clocks": clk,
-        "e2e": e2e,
-        "gpu_launches": (step_kernels if fused else 3) * args.steps,
+        "data": "synthetic (seeded); L2 defeated by rotating independent input sets > 3x L2",
     }
-    if other:
-        line["compare"] = other
-    if rank == 0 and not args.no_cpu_baseline:
-        v, sample, toks, el = cpu_oracle_run(cfg, inp, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": sample, "seconds": el}
+    line.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step")})
+    line["gpu_launches"] = head["gpu_launches"] + sum(o["gpu_launches"] for o in others.values())
+    if others:
+        line["workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -463,8 +579,8 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
     sizes = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"])
     ws = torch.empty(sizes["workspace_bytes"], dtype=torch.uint8, device=dev)
     q8 = torch.empty(sizes["q_fp8_bytes"], dtype=torch.uint8, device=dev)
-    op = torch.empty(sizes["o_partial_bytes"] // 4, dtype=torch.float32, device=dev)
-    lp = torch.empty(sizes["lse_partial_bytes"] // 4, dtype=torch.float32, device=dev)
+    op = torch.empty(max(16, sizes["o_partial_bytes"]) // 4, dtype=torch.float32, device=dev)
+    lp = torch.empty(max(16, sizes["lse_partial_bytes"]) // 4, dtype=torch.float32, device=dev)
     out = torch.empty_like(out_host, device=dev)
     # the step's inputs, and the plan's upload (the workspace up to its q scratch)
     h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names) + \
