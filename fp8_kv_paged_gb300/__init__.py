@@ -22,6 +22,7 @@ __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_
            "okc_attn_decode_combine_noalloc", "okc_selftest_bounded_wait", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
+           "QNORM_BF16", "QNORM_FOLDED_SCALE",
            "EXPORTED_SYMBOLS"]
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
@@ -30,6 +31,7 @@ PLAN_NO_PDL = 0x1
 PLAN_NO_TCGEN05 = 0x2
 PLAN_STEP_ONE_LAUNCH = 0x4
 PLAN_STEP_THREE_LAUNCHES = 0x8
+QNORM_BF16, QNORM_FOLDED_SCALE = 0, 1
 
 EXPORTED_SYMBOLS = [
     "okc_attn_plan_sizes", "okc_attn_plan", "okc_attn_plan_destroy", "okc_attn_plan_get_sizes",
@@ -52,7 +54,8 @@ class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("batch", "q_len", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "window",
                  "max_pages", "num_pages")] + \
-               [(n, ctypes.c_float) for n in ("rope_theta", "qk_scale_factor", "sm_scale", "kv_scale")]
+               [(n, ctypes.c_float) for n in ("rope_theta", "qk_scale_factor", "sm_scale", "kv_scale")] + \
+               [("q_norm", ctypes.c_int32)]
 
 
 class _Options(ctypes.Structure):
@@ -165,7 +168,7 @@ def _config(cfg: dict) -> _Config:
     return _Config(cfg["batch"], cfg["q_len"], cfg["num_q_heads"], cfg["num_kv_heads"],
                    cfg["head_dim"], cfg["page_size"], cfg["window"], cfg["max_pages"],
                    cfg["num_pages"], cfg["rope_theta"], cfg["qk_scale_factor"], cfg["sm_scale"],
-                   cfg["kv_scale"])
+                   cfg["kv_scale"], int(cfg.get("q_norm", 0)))
 
 
 def _options(opts: dict | None):

@@ -105,7 +105,8 @@ __device__ __forceinline__ void fused_q_frag(const DecodeArgs& a, int64_t t, int
   const float inv = rms_inverse<4, 16>(x, kRmsEps);
   float y[16];
 #pragma unroll
-  for (int i = 0; i < 16; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
+  for (int i = 0; i < 16; i++)  // OKC_QNORM_FOLDED_SCALE: the factor before the one bf16 rounding
+    y[i] = bf16_round(a.q_fold ? __fmul_rn(__fmul_rn(x[i], inv), a.q_scale) : __fmul_rn(x[i], inv));
   if (a.rope && live) {
     const int64_t pos = a.positions[t];
     if (pos >= 0 && pos < a.rope_positions) {

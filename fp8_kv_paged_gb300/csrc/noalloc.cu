@@ -69,7 +69,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   if (c.batch < 1 || c.q_len < 1 || c.q_len > 16 || c.window < 0 || c.max_pages < 1 ||
       c.num_pages < 1 || !(c.sm_scale > 0.f) || !(c.qk_scale_factor > 0.f) || !(c.kv_scale > 0.f) ||
       !std::isfinite(c.sm_scale) || !std::isfinite(c.qk_scale_factor) || !std::isfinite(c.kv_scale) ||
-      !(eps >= 0.f) || !std::isfinite(eps))
+      !(eps >= 0.f) || !std::isfinite(eps) || (c.q_norm != OKC_QNORM_BF16 && c.q_norm != OKC_QNORM_FOLDED_SCALE))
     return OKC_ERR_INVALID;
   if (c.head_dim != kHeadDim || c.num_q_heads != kNumQHeads || c.num_kv_heads != kNumKvHeads ||
       c.page_size < 1 || c.page_size > 256 || (c.page_size & (c.page_size - 1)) ||
@@ -146,8 +146,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   d.page_shift = shift;
   d.scaled = scaled;
   d.T = B * L;
-  const float scale = (float)((double)c.sm_scale * (double)c.qk_scale_factor);
-  d.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  d.scale_log2 = softmax_scale_log2(c);
   if (launch_decode(d, (int)W, false, str) != cudaSuccess) return OKC_ERR_CUDA;
 
   CombineArgs m;

@@ -34,6 +34,7 @@ okc_status check_config(const okc_attn_config* c) {
   if (!(c->sm_scale > 0.f) || !(c->qk_scale_factor > 0.f) || !(c->kv_scale > 0.f)) return OKC_ERR_INVALID;
   if (!std::isfinite(c->sm_scale) || !std::isfinite(c->qk_scale_factor) || !std::isfinite(c->kv_scale))
     return OKC_ERR_INVALID;
+  if (c->q_norm != OKC_QNORM_BF16 && c->q_norm != OKC_QNORM_FOLDED_SCALE) return OKC_ERR_INVALID;
   if (c->head_dim != okc::kHeadDim || c->num_q_heads != okc::kNumQHeads ||
       c->num_kv_heads != okc::kNumKvHeads)
     return OKC_ERR_UNSUPPORTED;
@@ -518,9 +519,7 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
   p->tc = use_tc(cfg, opts);
-  // softmax scale: the float32 value of sm_scale * qk_scale_factor, in base 2
-  const float scale = (float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
-  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p->scale_log2 = okc::softmax_scale_log2(*cfg);
   set_splits(p, s, z);
   // One upload of the workspace's head: the zeroed error word, the work list,
   // the request table and the zeroed arrival counters, as laid out on the device.
@@ -695,6 +694,8 @@ okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t*
   a.rope_positions = rope ? rope_positions : 0;
   a.rope = rope;
   a.scaled = scaled;
+  a.q_fold = c.q_norm == OKC_QNORM_FOLDED_SCALE;
+  a.q_scale = c.qk_scale_factor;
   cudaError_t e = okc::launch_prepare(a, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }
@@ -834,6 +835,8 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.weight = static_cast<const uint16_t*>(norm_weight);
   a.out = static_cast<uint16_t*>(out);
   a.eps = eps;
+  a.q_fold = c.q_norm == OKC_QNORM_FOLDED_SCALE;
+  a.q_scale = c.qk_scale_factor;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   if (plan->sizes.step_kernels == 1) {
     cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, str);

@@ -44,6 +44,8 @@ struct PrepareArgs {
   int32_t rope_positions;
   int32_t rope;
   int32_t scaled;
+  int32_t q_fold;  // OKC_QNORM_FOLDED_SCALE: q heads are x * rstd * q_scale in float32, then bf16
+  float q_scale;   // qk_scale_factor under q_fold
 };
 
 struct DecodeArgs {
@@ -78,6 +80,8 @@ struct DecodeArgs {
   uint16_t* out;            // bf16 [T, Hq*64]
   float eps;
   int32_t tc;               // 1: q_len 2..8 runs on the tcgen05 kernel (decode_tc.cu)
+  int32_t q_fold;           // as PrepareArgs (the fused step derives q itself)
+  float q_scale;
 };
 
 struct CombineArgs {
@@ -124,6 +128,15 @@ struct okc_attn_plan_s {
 };
 
 namespace okc {
+
+// The softmax scale in base 2: f32(sm_scale * qk_scale_factor) * log2(e) under
+// OKC_QNORM_BF16 (the factor folded into the scale, as the problem file does),
+// f32(sm_scale) * log2(e) under OKC_QNORM_FOLDED_SCALE (the factor is inside q).
+inline float softmax_scale_log2(const okc_attn_config& c) {
+  const float scale = c.q_norm == OKC_QNORM_FOLDED_SCALE ? c.sm_scale
+                                                          : (float)((double)c.sm_scale * (double)c.qk_scale_factor);
+  return (float)((double)scale * 1.4426950408889634);
+}
 
 // Keys per split work item for a request of `nvis` visible keys split `k`
 // ways: nvis / k rounded up so that the item's 64-key tiles are whole ones,

@@ -10,6 +10,10 @@
 // register swap. Each lane stores its 8 E4M3 bytes with one 8-byte store; the
 // 8 lanes of a head cover the head's 64-byte segment of the row.
 //
+// Under OKC_QNORM_FOLDED_SCALE (the vLLM CuTeDSL qk_norm with an output scale)
+// a q head is bf16(f32(f32(x * rstd) * qk_scale_factor)): both products in
+// float32, the bf16 store its only rounding to bf16.
+//
 // Numerics (the reading the oracle also takes): the RMS inverse is the float32
 // rounding of 1/sqrt(sum(x^2)/64 + eps) (rms_inverse: float32 arithmetic with a
 // double-precision fallback near rounding boundaries, so the rounding does not
@@ -64,8 +68,13 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_kernel(PrepareArgs a) {
 
   if (h < kNumQHeads + kNumKvHeads) {
     float y[8];
+    if (a.q_fold && h < kNumQHeads) {  // q under OKC_QNORM_FOLDED_SCALE: the factor before the one bf16 rounding
 #pragma unroll
-    for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
+      for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(__fmul_rn(x[i], inv), a.q_scale));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; i++) y[i] = bf16_round(__fmul_rn(x[i], inv));
+    }
     if (a.rope) {
       const int64_t pos = a.positions[t];
       if (pos >= 0 && pos < a.rope_positions) {

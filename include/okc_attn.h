@@ -87,7 +87,24 @@ typedef struct okc_attn_config {
   float qk_scale_factor;   /* folded into the softmax scale */
   float sm_scale;          /* softmax scale before the factor, 1/8 */
   float kv_scale;          /* != 1 selects the scaled cache path (K/V divided by k/v_scale on write) */
+  int32_t q_norm;          /* OKC_QNORM_BF16 (0) or OKC_QNORM_FOLDED_SCALE (1), below */
 } okc_attn_config;
+/*
+ * q_norm selects the arithmetic of the q heads' RMSNorm (step 1):
+ *  OKC_QNORM_BF16         the problem file's `_prepare_qkv`: q = bf16(x * rstd),
+ *                         and qk_scale_factor is folded into the softmax scale
+ *                         (softmax_scale = f32(sm_scale * qk_scale_factor));
+ *  OKC_QNORM_FOLDED_SCALE the vLLM CuTeDSL `qk_norm` with an output scale
+ *                         (`QKNormDirectKernel.kernel`, `qk_norm(x, head_dim,
+ *                         eps, scale)`): q = bf16(f32(f32(x * rstd) * qk_scale_factor)),
+ *                         the float32 products rounded as float32 and the bf16
+ *                         store the only rounding to bf16; the factor is then
+ *                         inside q and softmax_scale = sm_scale.
+ * k heads are normed with scale 1 in both (the same arithmetic); RoPE, the E4M3
+ * casts and the cache layout do not change.
+ */
+#define OKC_QNORM_BF16 0
+#define OKC_QNORM_FOLDED_SCALE 1
 
 /* Optional plan knobs. Pass NULL for the defaults (all zero). */
 typedef struct okc_plan_options {

@@ -46,7 +46,8 @@ def build(force: bool = False) -> str:
 class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("batch", "q_len", "hq", "hkv", "page_size", "window", "max_pages", "num_pages")] + \
-               [(n, ctypes.c_float) for n in ("rope_theta", "qk_scale_factor", "sm_scale", "kv_scale")]
+               [(n, ctypes.c_float) for n in ("rope_theta", "qk_scale_factor", "sm_scale", "kv_scale")] + \
+               [("q_norm", ctypes.c_int32)]
 
 
 def _bind(lib):
@@ -122,7 +123,8 @@ def _ptr(a: np.ndarray | None):
 def _cfg(cfg: dict) -> _Cfg:
     return _Cfg(cfg["batch"], cfg["q_len"], cfg["num_q_heads"], cfg["num_kv_heads"],
                 cfg["page_size"], cfg["window"], cfg["max_pages"], cfg["num_pages"],
-                cfg["rope_theta"], cfg["qk_scale_factor"], cfg["sm_scale"], cfg["kv_scale"])
+                cfg["rope_theta"], cfg["qk_scale_factor"], cfg["sm_scale"], cfg["kv_scale"],
+                int(cfg.get("q_norm", 0)))
 
 
 # ------------------------------------------------------------------ formats

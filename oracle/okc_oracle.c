@@ -22,6 +22,12 @@
  *    exact values (libm in double, rounded once).
  *  - The attention output is rounded to bf16 once (FA3 returns bf16) before the
  *    norm-gate; the norm-gate is evaluated in double and rounded once to bf16.
+ *  - q_norm 1 (the vLLM CuTeDSL `qk_norm` page, `QKNormDirectKernel.kernel` and
+ *    the `qk_norm(x, head_dim, eps, scale)` wrapper): a q head is x * rstd times
+ *    the output scale, both products float32 operations, and the store to bf16
+ *    is its only rounding to bf16; the output scale is the query factor
+ *    (qk_scale_factor), so it leaves the softmax scale, which is then sm_scale
+ *    alone. k heads are normed with scale 1, which is the q_norm 0 arithmetic.
  *
  * Every function works on plain arrays; bf16 values travel as uint16 bit patterns,
  * E4M3 values as uint8 codes.
@@ -143,6 +149,7 @@ void orc_rope_row(float theta, int64_t pos, float* cos_out /* [32] */, float* si
 typedef struct orc_cfg {
   int32_t batch, q_len, hq, hkv, page_size, window, max_pages, num_pages;
   float rope_theta, qk_scale_factor, sm_scale, kv_scale;
+  int32_t q_norm; /* 0: the problem file's norm; 1: the vLLM qk_norm with the query factor folded in */
 } orc_cfg;
 
 /*
@@ -176,7 +183,16 @@ int64_t orc_prepare(const orc_cfg* cfg, int64_t T, const uint16_t* qkv, const in
         double sumsq = 0.0;
         for (int c = 0; c < ORC_D; c++) sumsq += (double)x[c] * (double)x[c];
         float inv = (float)(1.0 / sqrt(sumsq / ORC_D + (double)eps));
-        for (int c = 0; c < ORC_D; c++) y[c] = (float)orc_bf16_round((double)(x[c] * inv));
+        if (h < hq && cfg->q_norm == 1) {
+          /* float32 x * rstd, float32 times the output scale, one bf16 rounding */
+          for (int c = 0; c < ORC_D; c++) {
+            const float normed = x[c] * inv;
+            const float scaled_q = normed * cfg->qk_scale_factor;
+            y[c] = (float)orc_bf16_round((double)scaled_q);
+          }
+        } else {
+          for (int c = 0; c < ORC_D; c++) y[c] = (float)orc_bf16_round((double)(x[c] * inv));
+        }
         if (rope) {
           /* Interleaved pairs (2i, 2i+1) share angle i; the partner of column c
            * is column c^1, normalised and rounded like y. */
@@ -220,7 +236,8 @@ int64_t orc_prepare(const orc_cfg* cfg, int64_t T, const uint16_t* qkv, const in
  * request b is the cache row page_table[b][j / P] * P + j % P; the logit is
  * (q . K_j) * softmax_scale with K_j = E4M3 value * k_scale (scaled path) and
  * o = sum_j softmax_j V_j, V_j = E4M3 value * v_scale (scaled path).
- * The softmax scale is the float32 value of sm_scale * qk_scale_factor.
+ * The softmax scale is the float32 value of sm_scale * qk_scale_factor, or of
+ * sm_scale alone under q_norm 1 (the factor is then inside q).
  *
  * Only rows with mask[t*Hq + h] != 0 are computed (mask NULL = all rows).
  * o: double [T, Hq, 64]; lse (may be NULL): natural log-sum-exp of the logits.
@@ -233,7 +250,8 @@ int64_t orc_attention(const orc_cfg* cfg, const uint8_t* q8, const uint8_t* k_ca
   const int hq = cfg->hq, hkv = cfg->hkv, group = hq / hkv, P = cfg->page_size;
   const int scaled = cfg->kv_scale != 1.0f;
   const double ks = scaled ? (double)k_scale : 1.0, vs = scaled ? (double)v_scale : 1.0;
-  const double scale = (double)(float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
+  const double scale = cfg->q_norm == 1 ? (double)cfg->sm_scale
+                                         : (double)(float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor);
   int64_t bad = 0;
   double val[256]; /* decoded E4M3 codes, so the loops below are plain multiply-adds */
   for (int c = 0; c < 256; c++) val[c] = orc_e4m3_value((uint8_t)c);

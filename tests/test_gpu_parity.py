@@ -84,6 +84,20 @@ def test_distinct_k_and_v_scales(name):
     full_check(cfg, inp, fused=True, plan_form=True)
 
 
+@pytest.mark.parametrize("name", ["sliding_decode", "verify_block", "full_decode_32k", "tiny_sliding_decode"])
+def test_folded_q_norm(name):
+    """q_norm = OKC_QNORM_FOLDED_SCALE (the vLLM qk_norm with the query factor as
+    its output scale): q bytes bit-identical to the oracle's mode, the softmax
+    scale sm_scale alone; through the three calls and okc_attn_step."""
+    import fp8_kv_paged_gb300 as okc
+    cfg = W.config(name, **SMALL[name], q_norm=okc.QNORM_FOLDED_SCALE)
+    inp = W.generate(cfg)
+    rep = full_check(cfg, inp)
+    assert rep["q8"]["match"] == 1.0
+    full_check(cfg, inp, fused=True)
+    full_check(cfg, inp, fused=True, plan_form=True)
+
+
 def test_rope_table_matches_oracle_rows():
     import fp8_kv_paged_gb300 as okc
     n = 140000

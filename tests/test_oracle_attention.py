@@ -26,7 +26,10 @@ def _dense_reference(cfg, inp, q8, k_cache, v_cache):
     L, P, w = cfg["q_len"], cfg["page_size"], cfg["window"]
     ks = float(inp["k_scale"]) if cfg["kv_scale"] != 1.0 else 1.0
     vs = float(inp["v_scale"]) if cfg["kv_scale"] != 1.0 else 1.0
-    scale = float(np.float32(cfg["sm_scale"] * cfg["qk_scale_factor"]))
+    if cfg.get("q_norm", 0) == 1:  # the factor is inside q (the vLLM qk_norm with an output scale)
+        scale = float(np.float32(cfg["sm_scale"]))
+    else:
+        scale = float(np.float32(cfg["sm_scale"] * cfg["qk_scale_factor"]))
     kc = k_cache.reshape(-1, HKV, D)
     vc = v_cache.reshape(-1, HKV, D)
     out = np.zeros((q8.shape[0], HQ, D))
@@ -62,8 +65,9 @@ def _dense_reference(cfg, inp, q8, k_cache, v_cache):
     (8, 4, 5, (0, 13), 0.5),
     (1, 4, 3, (6, 16), 0.5),
 ])
-def test_matches_dense_brute_force(L, P, window, seq, kv_scale):
+def test_matches_dense_brute_force(L, P, window, seq, kv_scale, q_norm=0):
     cfg, inp = _tiny(L=L, P=P, window=window, seq=seq, kv_scale=kv_scale)
+    cfg["q_norm"] = q_norm
     if kv_scale != 1.0:
         inp["k_scale"] = np.float32(kv_scale)
         inp["v_scale"] = np.float32(kv_scale * 1.5)
@@ -74,6 +78,33 @@ def test_matches_dense_brute_force(L, P, window, seq, kv_scale):
     assert bad == 0
     assert np.max(np.abs(o - ref)) < 1e-12
     assert np.max(np.abs(lse - ref_lse)) < 1e-10
+
+
+def test_folded_q_norm_matches_dense_brute_force():
+    """q_norm 1: the softmax scale is sm_scale alone (the factor is inside q)."""
+    test_matches_dense_brute_force(8, 4, 5, (0, 13), 0.5, q_norm=1)
+    test_matches_dense_brute_force(1, 1, 0, (5, 11), 1.0, q_norm=1)
+
+
+def test_folded_q_norm_computes_the_same_block():
+    """Both q norms compute the same attention up to the E4M3 rounding of q: the
+    logits q.k * scale agree within the quantisation of q (the factor moved from
+    the scale into q), and the block's outputs agree to within that noise."""
+    for seq, L, w in (((300, 2100, 40), 1, 2048), ((500, 900), 8, 0)):
+        cfg = W.config("tiny_sliding_decode", batch=len(seq), q_len=L, window=w, seq=("list", list(seq)))
+        inp = W.generate(cfg)
+        a = oracle.step(dict(cfg, q_norm=0), inp)
+        b = oracle.step(dict(cfg, q_norm=1), inp)
+        qa = oracle.e4m3_value(a["q8"]) * cfg["qk_scale_factor"]
+        qb = oracle.e4m3_value(b["q8"])
+        # each E4M3 value is within 1/16 relative of what it rounds, so |qa - qb| <=
+        # (1/8) / (15/16) of the larger, plus the absolute error of the rotation
+        # (its bf16 roundings are relative to the pair's norm, ~3 * 2^-9 * 5.473)
+        assert np.all(np.abs(qa - qb) <= (2.0 / 15.0) * np.maximum(np.abs(qa), np.abs(qb)) + 0.05)
+        oa = oracle.bf16_value(a["out"])
+        ob = oracle.bf16_value(b["out"])
+        err = np.abs(oa - ob)
+        assert err.mean() < 0.05 and np.corrcoef(oa.ravel(), ob.ravel())[0, 1] > 0.985, (err.mean(), err.max())
 
 
 def _attend(cfg, inp, k, v, q8):
@@ -166,7 +197,10 @@ def test_lse_merge_of_key_splits():
     # use the dense reference on masked chunks instead
     ref, _ = _dense_reference(cfg, inp, q8, k, v)
     kc = oracle.e4m3_value(k.reshape(-1, HKV, D)); vc = oracle.e4m3_value(v.reshape(-1, HKV, D))
-    scale = float(np.float32(cfg["sm_scale"] * cfg["qk_scale_factor"]))
+    if cfg.get("q_norm", 0) == 1:  # the factor is inside q (the vLLM qk_norm with an output scale)
+        scale = float(np.float32(cfg["sm_scale"]))
+    else:
+        scale = float(np.float32(cfg["sm_scale"] * cfg["qk_scale_factor"]))
     b, t = 1, 1
     n = int(inp["cache_seqlens"][b])
     rows = inp["page_table"][b, :n]

@@ -55,6 +55,17 @@ MUTANTS = [
      [TP.test_scaled_cache_codes_from_the_definition]),
     ("no_bf16_after_k_scale", "key = (float)orc_bf16_round((double)(key / k_scale));", "key = key / k_scale;",
      [TP.test_scaled_cache_codes_from_the_definition]),
+    # q_norm 1 (the vLLM CuTeDSL qk_norm page, QKNormDirectKernel.kernel: float32
+    # through the scale, the store the only rounding)
+    ("q_norm_bf16_before_scale", "const float scaled_q = normed * cfg->qk_scale_factor;",
+     "const float scaled_q = (float)orc_bf16_round((double)normed) * cfg->qk_scale_factor;",
+     [TP.test_folded_q_norm_is_one_bf16_rounding_of_the_float32_chain]),
+    ("q_norm_scale_dropped", "const float scaled_q = normed * cfg->qk_scale_factor;",
+     "const float scaled_q = normed;",
+     [TP.test_folded_q_norm_is_one_bf16_rounding_of_the_float32_chain]),
+    ("q_norm_factor_kept_in_softmax", "cfg->q_norm == 1 ? (double)cfg->sm_scale",
+     "cfg->q_norm == 1 ? (double)(float)((double)cfg->sm_scale * (double)cfg->qk_scale_factor)",
+     [TA.test_folded_q_norm_matches_dense_brute_force]),
     ("no_bf16_after_v_scale", "value = (float)orc_bf16_round((double)(value / v_scale));",
      "value = value / v_scale;", [TP.test_scaled_cache_codes_from_the_definition]),
 ]

@@ -283,3 +283,60 @@ def test_scaled_cache_codes_from_the_definition():
     for g in range(HKV):
         assert np.array_equal(k1.reshape(-1, HKV * D)[row].reshape(HKV, D)[g], _e4m3_brute(k_heads[g]))
         assert np.array_equal(v1.reshape(-1, HKV * D)[row].reshape(HKV, D)[g], _e4m3_brute(v_heads[g]))
+
+
+# ---- q_norm 1: the vLLM qk_norm with the query factor folded into q ----------
+# The vLLM CuTeDSL `qk_norm` page (`QKNormDirectKernel.kernel`: y = x * rstd in
+# float32, y = y * scale in float32, then the store to the output dtype is the
+# only rounding). The pin evaluates that chain in exact rational arithmetic:
+# rstd = the float32 nearest to 1/sqrt(mean(x^2) + eps) (80-digit decimal),
+# each product the float32 nearest to the exact product, then bf16 nearest
+# even, then E4M3 by brute-force nearest code; no bf16 value in between.
+
+def _rne_f32(fr):
+    """The float32 nearest to the rational `fr` (ties to the even significand)."""
+    from fractions import Fraction
+    f = np.float32(float(fr))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    return min(cands, key=lambda c: (abs(Fraction(float(c)) - fr), int(np.array(c, np.float32).view(np.uint32)) & 1))
+
+
+def _rstd_f32(x):
+    """float32 nearest to 1/sqrt(mean(x^2) + eps32), from 80-digit decimals."""
+    import decimal
+    from fractions import Fraction
+    ms = sum(Fraction(float(v)) ** 2 for v in x) / len(x) + Fraction(float(np.float32(1e-5)))
+    with decimal.localcontext() as ctx:
+        ctx.prec = 80
+        r = decimal.Decimal(1) / (decimal.Decimal(ms.numerator) / decimal.Decimal(ms.denominator)).sqrt()
+    return _rne_f32(Fraction(r))
+
+
+def _folded_q_codes(x, s, bf16_between=False):
+    from fractions import Fraction
+    inv = Fraction(float(_rstd_f32(x)))
+    s = Fraction(float(np.float32(s)))
+    y2 = []
+    for v in x:
+        y1 = _rne_f32(Fraction(float(v)) * inv)
+        if bf16_between:  # the mistake the pin must catch: a bf16 value before the scale
+            y1 = np.float32(_bf16(np.array([y1], np.float32))[0])
+        y2.append(_rne_f32(Fraction(float(y1)) * s))
+    return _e4m3_brute(_bf16(np.array(y2, np.float32)))
+
+
+def test_folded_q_norm_is_one_bf16_rounding_of_the_float32_chain():
+    cfg = W.config("tiny_sliding_decode", rope_theta=0.0, q_norm=1)
+    inp = W.generate(cfg)
+    q8, k8, _, _ = _run(cfg, inp)
+    sensitive = 0
+    for t in range(q8.shape[0]):
+        for h in range(0, HQ, 3):
+            x = oracle.bf16_value(inp["qkv"][t, QCOL + h * D:QCOL + (h + 1) * D])
+            want = _folded_q_codes(x, cfg["qk_scale_factor"])
+            assert np.array_equal(q8[t, h], want), (t, h)
+            sensitive += int(np.sum(_folded_q_codes(x, cfg["qk_scale_factor"], bf16_between=True) != want))
+    assert sensitive >= 4  # the inputs tell a bf16 value before the scale apart
+    # k heads are normed with scale 1: the cache rows equal q_norm 0's
+    _, k0, _, _ = _run(dict(cfg, q_norm=0), inp)
+    assert np.array_equal(k8, k0)
