@@ -65,16 +65,41 @@ NCU_TRAFFIC = {
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
-def kv_bytes(cfg, seq_lens) -> int:
+def _q_lens(cfg, seq_lens, q_lens):
+    return np.full(len(seq_lens), cfg["q_len"], np.int64) if q_lens is None else np.asarray(q_lens, np.int64)
+
+
+def kv_bytes(cfg, seq_lens, q_lens=None) -> int:
     """Algorithmic KV-stream bytes of one step: each request's visible keys (the
-    union over its L queries) read once, K and V rows of Hkv x 64 E4M3 bytes."""
-    L, w = cfg["q_len"], cfg["window"]
-    n = seq_lens.astype(np.int64) + L
+    union over its new tokens' windows) read once, K and V rows of Hkv x 64 E4M3
+    bytes. q_lens: new tokens per request (default q_len each)."""
+    ql = _q_lens(cfg, seq_lens, q_lens)
+    w = cfg["window"]
+    n = np.asarray(seq_lens, np.int64) + ql
     if w > 0:
-        n = np.minimum(n, w + L - 1)
+        n = np.minimum(n, w + ql - 1)
+    n = np.where(ql > 0, n, 0)
     return int(n.sum()) * cfg["num_kv_heads"] * cfg["head_dim"] * 2
+
+
+def token_keys(cfg, seq_lens, q_lens=None) -> np.ndarray:
+    """Per request: the sum over its new tokens of the keys each token sees."""
+    ql = _q_lens(cfg, seq_lens, q_lens)
+    w = cfg["window"]
+    out = np.zeros(len(ql), np.int64)
+    for b, (s0, q) in enumerate(zip(np.asarray(seq_lens, np.int64), ql)):
+        k = s0 + np.arange(1, q + 1, dtype=np.int64)  # token i sees keys 0 .. s0 + i
+        out[b] = int(np.minimum(k, w).sum()) if w > 0 else int(k.sum())
+    return out
+
+
+def attention_flops(cfg, seq_lens, q_lens=None) -> int:
+    """Algorithmic flops of step 4: every query row (token x q head) takes a
+    64-wide dot product (QK) and a 64-wide multiply-add (PV) per visible key."""
+    return int(token_keys(cfg, seq_lens, q_lens).sum()) * 4 * cfg["head_dim"] * cfg["num_q_heads"]
 
 
 def measured_peak_hbm():
@@ -85,6 +110,20 @@ def measured_peak_hbm():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_peak_tensor():
+    """Dense tensor peak of step 4's contractions, TFLOP/s: QK in E4M3 (twice the
+    bf16 rate, the nominal fp8 : bf16 ratio) and PV in f16 (the bf16 rate), equal
+    flops each, so time at peak is F/2 / (2P) + F/2 / P and the combined peak
+    4P/3, P the measured dense bf16 rate (burst: the kernel is timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v * 4.0 / 3.0, "measured bf16 x 4/3"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS * 4.0 / 3.0, "fallback bf16 x 4/3"
 
 
 def host_cores() -> int:
@@ -198,51 +237,39 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 # ------------------------------------------------------------ CPU oracle timing
 
 def _requests(cfg, inp, bs):
-    """The step restricted to requests `bs` (uniform q_len), sharing the caches."""
-    L = cfg["q_len"]
+    """The step restricted to requests `bs`, sharing the caches (any q lengths)."""
     bs = np.asarray(bs, np.int64)
-    rows = (bs[:, None] * L + np.arange(L)[None, :]).reshape(-1)
+    cu = inp["cu_seqlens_q"].astype(np.int64)
+    ql = cu[bs + 1] - cu[bs]
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in bs]) if len(bs) else np.zeros(0, np.int64)
     c = dict(cfg, batch=len(bs))
     d = dict(inp, qkv=inp["qkv"][rows], positions=inp["positions"][rows], cache_loc=inp["cache_loc"][rows],
              cache_seqlens=inp["cache_seqlens"][bs], seq_lens=inp["seq_lens"][bs],
              page_table=np.ascontiguousarray(inp["page_table"][bs]),
-             cu_seqlens_q=(np.arange(len(bs) + 1) * L).astype(np.int32))
+             cu_seqlens_q=np.concatenate([[0], np.cumsum(ql)]).astype(np.int32))
     return c, d, rows
-
-
-def visible_keys(cfg, seq_lens) -> np.ndarray:
-    """Keys each request's queries see in all (the union over its q_len queries)."""
-    L, w = cfg["q_len"], cfg["window"]
-    n = np.asarray(seq_lens, np.int64) + L
-    return np.minimum(n, w + L - 1) if w > 0 else n
-
-
-def oracle_seconds_per_request(cfg, inp) -> float:
-    """The oracle's time for a request of the workload's mean size, from one
-    timed pass over its first few requests (after a warm pass)."""
-    probe = OracleRunner(cfg, inp, min(cfg["batch"], 4))
-    probe.run()  # load and warm the library
-    t0 = time.perf_counter()
-    probe.run()
-    per_key = max(time.perf_counter() - t0, 1e-5) / float(probe.cost.sum())
-    return per_key * float(visible_keys(cfg, inp["seq_lens"]).mean())
 
 
 class OracleRunner:
     """The oracle's step (prepare, attention, norm-gate: the functions as they
-    stand) over the first `nreq` requests of a workload, with the attention of
-    the requests spread over `threads` host threads (longest first, each thread
-    a share of similar cost). Caches are copied once, outside every timing:
-    the prepare step rewrites the same rows with the same codes each pass."""
+    stand) on the whole workload, its attention and norm-gate on a uniform
+    sample of `frac` of the query rows (token x head; all rows at 1), spread
+    over `threads` host threads (requests grouped by cost, each thread a share
+    of similar cost). Caches are copied once, outside every timing: the prepare
+    step rewrites the same rows with the same codes each pass."""
 
-    def __init__(self, cfg, inp, nreq):
+    def __init__(self, cfg, inp, frac=1.0, seed=0):
         import oracle
         self.o = oracle
-        self.cfg, self.inp = cfg, inp
-        self.c, self.d, _ = _requests(cfg, inp, np.arange(nreq))
+        self.c, self.d = cfg, inp
         self.k = inp["k_cache"].copy()
         self.v = inp["v_cache"].copy()
-        self.cost = visible_keys(cfg, self.d["seq_lens"])
+        T, hq = inp["qkv"].shape[0], cfg["num_q_heads"]
+        self.mask = None
+        if frac < 1.0:
+            self.mask = (np.random.default_rng(seed).random((T, hq)) < frac).astype(np.uint8)
+        self.rows = T * hq if self.mask is None else int(self.mask.sum())
+        self.cost = token_keys(cfg, inp["seq_lens"], inp["q_lens"]) * frac
 
     def groups(self, threads):
         order = np.argsort(-self.cost, kind="stable")
@@ -258,26 +285,41 @@ class OracleRunner:
         o, c, d = self.o, self.c, self.d
         q8, _ = o.prepare(c, d, self.k, self.v)
         if threads == 1 or pool is None:
-            out, _ = o.attention(c, d, q8, self.k, self.v)
+            out, _ = o.attention(c, d, q8, self.k, self.v, self.mask)
         else:
             out = np.zeros((q8.shape[0], c["num_q_heads"], 64), np.float64)
 
             def part(g):
                 cg, dg, rows = _requests(c, d, g)
-                og, _ = o.attention(cg, dg, np.ascontiguousarray(q8[rows]), self.k, self.v)
+                m = None if self.mask is None else np.ascontiguousarray(self.mask[rows])
+                og, _ = o.attention(cg, dg, np.ascontiguousarray(q8[rows]), self.k, self.v, m)
                 out[rows] = og
             list(pool.map(part, self.groups(threads)))
-        return o.normgate(c, out, d["qkv"], d.get("norm_weight"), d["eps"])
+        return o.normgate(c, out, d["qkv"], d.get("norm_weight"), d["eps"], self.mask)
+
+
+def oracle_sample_fraction(cfg, inp, seconds: float) -> float:
+    """The fraction of query rows the single-threaded oracle computes in about
+    `seconds`, from a timed probe (after a warm pass) on a small uniform sample."""
+    rows_all = inp["qkv"].shape[0] * cfg["num_q_heads"]
+    key_rows = float(token_keys(cfg, inp["seq_lens"], inp["q_lens"]).sum()) * cfg["num_q_heads"]
+    frac = min(1.0, 2.0e6 / max(key_rows, 1.0))
+    probe = OracleRunner(cfg, inp, frac, seed=1)
+    probe.run()  # load and warm the library
+    t0 = time.perf_counter()
+    probe.run()
+    el = max(time.perf_counter() - t0, 1e-6)
+    rows_per_s = probe.rows / el  # query rows of the workload's mix per second
+    return float(min(1.0, seconds * rows_per_s / rows_all))
 
 
 def cpu_oracle_baseline(cfg, inp, budget_s: float) -> dict:
-    """The oracle as it stands on a bounded sample (whole requests) of the
-    workload: tokens/s single-threaded and on all host cores."""
-    B, L = cfg["batch"], cfg["q_len"]
+    """The oracle as it stands on a bounded sample of the workload (a uniform
+    sample of its query rows): tokens/s single-threaded and on all host cores."""
+    B = cfg["batch"]
     cores = host_cores()
-    per_req = oracle_seconds_per_request(cfg, inp)
-    nreq = int(max(1, min(B, 0.5 * budget_s / per_req)))
-    r = OracleRunner(cfg, inp, nreq)
+    frac = oracle_sample_fraction(cfg, inp, 0.5 * budget_s)
+    r = OracleRunner(cfg, inp, frac)
     t0 = time.perf_counter()
     r.run()
     single_s = time.perf_counter() - t0
@@ -289,30 +331,30 @@ def cpu_oracle_baseline(cfg, inp, budget_s: float) -> dict:
             r.run(cores, pool)
             el += time.perf_counter() - t0
             reps += 1
-    toks = nreq * L
-    model = cpu_model()
+    toks = r.rows / cfg["num_q_heads"]  # query rows counted as tokens
+    what = "all" if frac >= 1.0 else f"{100.0 * frac:.3g}% (uniform sample)"
     return {"value": toks / single_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{nreq} of {B} requests of {cfg['name']} (one pass), single-threaded C oracle",
+            "sample": f"{what} of the query rows of {B} requests of {cfg['name']} (one pass), single-threaded C oracle",
             "seconds": single_s,
             "all_cores": {"value": toks * reps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                          "sample": f"{nreq} of {B} requests x {reps} pass(es), attention spread over {cores} "
-                                    "host threads", "seconds": el},
-            "nproc": cores, "cpu_model": model}
+                          "sample": f"the same rows x {reps} pass(es), attention spread over {cores} host threads",
+                          "seconds": el},
+            "nproc": cores, "cpu_model": cpu_model()}
 
 
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle as it stands, on all host cores, each of
-    the K steps one bounded sample (whole requests) of the same workload."""
+    the K steps one bounded sample (a uniform sample of the query rows) of the
+    same workload."""
     if rank != 0:
         return
     cfg = W.config(args.workload)
     inp = W.generate(cfg)
     B, L = cfg["batch"], cfg["q_len"]
     cores = host_cores()
-    per_req = oracle_seconds_per_request(cfg, inp)
     total_budget = 60.0  # seconds of oracle work (all cores) for the whole run
-    nreq = int(max(1, min(B, total_budget * cores / (per_req * max(1, args.steps + args.warmup)))))
-    r = OracleRunner(cfg, inp, nreq)
+    frac = oracle_sample_fraction(cfg, inp, total_budget * cores / max(1, args.steps + args.warmup))
+    r = OracleRunner(cfg, inp, frac)
     el = 0.0
     with ThreadPoolExecutor(max_workers=cores) as pool:
         for _ in range(args.warmup):
@@ -321,12 +363,15 @@ def run_reference(args, world, rank):
             t0 = time.perf_counter()
             r.run(cores, pool)
             el += time.perf_counter() - t0
-    value = nreq * L * args.steps / el
-    sample = (f"{nreq} of {B} requests of {args.workload} per step, C oracle with its attention spread over "
+    toks = r.rows / cfg["num_q_heads"]
+    value = toks * args.steps / el
+    T = inp["qkv"].shape[0]
+    what = "all" if frac >= 1.0 else f"{100.0 * frac:.3g}% (uniform sample)"
+    sample = (f"{what} of the query rows of {args.workload} per step, C oracle with its attention spread over "
               f"{cores} host threads ({cpu_model()})")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps * B / nreq,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * T / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "batch": B, "q_len": L, "page_size": cfg["page_size"],
@@ -399,8 +444,10 @@ class Bench:
         torch, okc, args, dev, stream = self.torch, self.okc, self.args, self.dev, self.stream
         cfg = W.config(name)
         inp = W.generate(cfg, seed=rank_seed(cfg["seed"], self.rank))
-        T = cfg["batch"] * cfg["q_len"]
-        kvb = kv_bytes(cfg, inp["seq_lens"])
+        T = inp["qkv"].shape[0]
+        ql = inp["q_lens"] if "q_lens" in cfg else None  # per-request q lengths (prefill/extend)
+        kvb = kv_bytes(cfg, inp["seq_lens"], ql)
+        flops = attention_flops(cfg, inp["seq_lens"], ql)
 
         # independent input sets so that consecutive steps miss in L2
         base = W.to_torch(inp, dev)
@@ -421,7 +468,7 @@ class Bench:
             plan_opts["flags"] = okc.PLAN_STEP_ONE_LAUNCH if args.step_form == "one" else \
                 okc.PLAN_STEP_THREE_LAUNCHES
         plan_opts = plan_opts or None
-        step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts)
+        step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts, q_lens=ql)
         fused = args.path == "fused"
 
         def run_step(st, s_, use_fused):
@@ -439,7 +486,8 @@ class Bench:
         # the step's dominant kernel alone, no programmatic overlap: the fused
         # step kernel, or the decode kernel of the three-call path
         step_np = okc.AttnStep(cfg, inp["seq_lens"],
-                               opts=dict(plan_opts or {}, flags=(plan_opts or {}).get("flags", 0) | okc.PLAN_NO_PDL))
+                               opts=dict(plan_opts or {}, flags=(plan_opts or {}).get("flags", 0) | okc.PLAN_NO_PDL),
+                               q_lens=ql)
         for s_ in sets:
             step_np.run(s_, eps=inp["eps"], stream=stream)
         stream.synchronize()
@@ -458,7 +506,7 @@ class Bench:
                 okc.okc_attn_decode(step_np.plan, step_np.q_fp8, s_["k_cache"], s_["v_cache"], s_["k_scale"],
                                     s_["v_scale"], s_["page_table"], s_["cache_seqlens"], s_["cu_seqlens_q"],
                                     s_["seq_lens"], step_np.o_partial, step_np.lse_partial, stream)
-            kname = "decode_tc_kernel" if 2 <= cfg["q_len"] <= 8 else "decode_kernel"
+            kname = "decode_tc_kernel" if cfg["q_len"] >= 2 else "decode_kernel"
         kernel_ms, _, _ = self.timed(one_kernel, max(R, min(steps, 20 * R)), 3, R)
         kernel_us = 1000.0 * kernel_ms
         clk = clocks.stop(t_wall0, t_wall1) if clocks is not None else None
@@ -473,10 +521,24 @@ class Bench:
 
         e2e = run_e2e(cfg, inp, okc, torch, dev, stream, steps=min(max(steps, 20), 200), fused=fused)
         peak, peak_kind = measured_peak_hbm()
+        tpeak, tpeak_kind = measured_peak_tensor()
         achieved = kvb / (kernel_us * 1e-6) / 1e9
+        tflops = flops / (kernel_us * 1e-6) / 1e12
+        # the bound: HBM while the step's flops per algorithmic KV byte stay below
+        # the ratio of the two peaks (decode: 16 flop/B, verify: 128), else the
+        # tensor cores (prefill/extend: thousands of flops per KV byte)
+        if flops / max(kvb, 1) < tpeak * 1e12 / (peak * 1e9):
+            roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": NCU_TRAFFIC.get((name, kname)), "algorithmic_bytes": kvb,
+                    "peak_source": peak_kind, "avg_launch_us": kernel_us, "tflops": tflops}
+        else:
+            roof = {"kernel": kname, "bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": tflops / tpeak, "traffic": NCU_TRAFFIC.get((name, kname)), "algorithmic_flops": flops,
+                    "algorithmic_bytes": kvb, "kv_gbs": achieved, "peak_source": tpeak_kind,
+                    "avg_launch_us": kernel_us}
         res = {
             "value": job_throughput(T, self.world, ms_step), "unit": "tokens/s", "ms_per_step": ms_step,
-            "config": {"workload": name, "batch": cfg["batch"], "q_len": cfg["q_len"],
+            "config": {"workload": name, "batch": cfg["batch"], "q_len": cfg["q_len"], "tokens": T,
                        "page_size": cfg["page_size"], "window": cfg["window"], "rope_theta": cfg["rope_theta"],
                        "kv_scale": cfg["kv_scale"], "kv_bytes_per_step": kvb,
                        "path": "okc_attn_step (%d kernel%s)" % (step_kernels, "" if step_kernels == 1 else "s")
@@ -486,10 +548,7 @@ class Bench:
                        "l2": "inputs rotate over %d sets (%.0f MB total > 3x L2)" % (n_sets, n_sets * set_bytes / 1e6)},
             "kv_stream_gbs_step": kvb / (ms_step * 1e-3) / 1e9,
             "kv_stream_frac_step": kvb / (ms_step * 1e-3) / 1e9 / peak,
-            "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak,
-                         "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": NCU_TRAFFIC.get((name, kname)), "algorithmic_bytes": kvb,
-                         "peak_source": peak_kind, "avg_launch_us": kernel_us},
+            "roofline": roof,
             "e2e": e2e,
             "gpu_launches": (step_kernels if fused else 3) * steps,
         }
@@ -574,9 +633,10 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
         npos = int(inp["positions"].max()) + 1
         dev_in["rope_table"] = torch.empty((npos, 64), dtype=torch.float32, device=dev)
         okc.okc_rope_table_init(cfg["rope_theta"], npos, dev_in["rope_table"], stream)
-    T = cfg["batch"] * cfg["q_len"]
+    T = inp["qkv"].shape[0]
+    ql = inp["q_lens"] if "q_lens" in cfg else None
     out_host = torch.empty((T, cfg["num_q_heads"] * cfg["head_dim"]), dtype=torch.bfloat16).pin_memory()
-    sizes = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"])
+    sizes = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"], q_lens=ql)
     ws = torch.empty(sizes["workspace_bytes"], dtype=torch.uint8, device=dev)
     q8 = torch.empty(sizes["q_fp8_bytes"], dtype=torch.uint8, device=dev)
     op = torch.empty(max(16, sizes["o_partial_bytes"]) // 4, dtype=torch.float32, device=dev)
@@ -589,10 +649,10 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
 
     io = okc.HostStepIO(dict(pinned, out=out_host), dict({k: dev_in[k] for k in names}, out=out))
 
-    plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream)
+    plan = okc.okc_attn_plan(cfg, inp["seq_lens"], ws, stream=stream, q_lens=ql)
 
     def one():
-        plan.update(inp["seq_lens"], stream)  # the step's plan, re-made in place from the host lengths
+        plan.update(inp["seq_lens"], stream, q_lens=ql)  # the step's plan, re-made in place from the host lengths
         if fused:  # one C call: the step from host buffers, output in host memory, synchronize
             okc.okc_attn_step_host(plan, io, None, dev_in["k_cache"], dev_in["v_cache"], dev_in["k_scale"],
                                    dev_in["v_scale"], dev_in["rope_table"], dev_in["norm_weight"], inp["eps"],

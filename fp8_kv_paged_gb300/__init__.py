@@ -16,7 +16,8 @@ import numpy as np
 from . import build as _build_mod
 
 __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_create", "okc_attn_plan_sizes",
-           "okc_attn_plan_items", "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size",
+           "okc_attn_plan_items", "okc_attn_plan_items_varlen", "okc_attn_plan_max_sizes",
+           "okc_attn_plan_workspace_size",
            "okc_rope_table_init", "okc_prepare_qkv", "okc_attn_decode",
            "okc_attn_combine_normgate", "okc_attn_plan_read_errors", "okc_attn_plan_clear_errors", "AttnStep",
            "okc_attn_decode_combine_noalloc", "okc_selftest_bounded_wait", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
@@ -40,6 +41,8 @@ EXPORTED_SYMBOLS = [
     "okc_attn_step", "okc_attn_step_host", "okc_attn_plan_items", "okc_attn_plan_update",
     "okc_attn_plan_max_sizes", "okc_attn_plan_workspace_size", "okc_attn_plan_create",
     "okc_attn_plan_scratch_sizes", "okc_selftest_bounded_wait", "okc_attn_plan_clear_errors",
+    "okc_attn_plan_varlen", "okc_attn_plan_sizes_varlen", "okc_attn_plan_items_varlen",
+    "okc_attn_plan_update_varlen",
 ]
 
 
@@ -60,7 +63,7 @@ class _Config(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("chunk_keys", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("sm_count", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("sm_count", ctypes.c_int32), ("max_context", ctypes.c_int32)]
 
 
 class _HostStep(ctypes.Structure):
@@ -102,6 +105,17 @@ def load(path: str | None = None):
     lib.okc_attn_plan_sizes.restype = st
     lib.okc_attn_plan_sizes.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options),
                                         ctypes.POINTER(_Sizes)]
+    lib.okc_attn_plan_sizes_varlen.restype = st
+    lib.okc_attn_plan_sizes_varlen.argtypes = [ctypes.POINTER(_Config), P, P, ctypes.POINTER(_Options),
+                                               ctypes.POINTER(_Sizes)]
+    lib.okc_attn_plan_items_varlen.restype = st
+    lib.okc_attn_plan_items_varlen.argtypes = [ctypes.POINTER(_Config), P, P, ctypes.POINTER(_Options), P, i32,
+                                               ctypes.POINTER(ctypes.c_int32)]
+    lib.okc_attn_plan_varlen.restype = st
+    lib.okc_attn_plan_varlen.argtypes = [ctypes.POINTER(_Config), P, P, ctypes.POINTER(_Options), P,
+                                         ctypes.c_size_t, P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.okc_attn_plan_update_varlen.restype = st
+    lib.okc_attn_plan_update_varlen.argtypes = [P, P, P, P]
     lib.okc_attn_plan_items.restype = st
     lib.okc_attn_plan_items.argtypes = [ctypes.POINTER(_Config), P, ctypes.POINTER(_Options), P, i32,
                                         ctypes.POINTER(ctypes.c_int32)]
@@ -175,19 +189,33 @@ def _options(opts: dict | None):
     if not opts:
         return None
     return ctypes.byref(_Options(opts.get("chunk_keys", 0), opts.get("flags", 0),
-                                 opts.get("ctas_per_sm", 0), opts.get("sm_count", 0)))
+                                 opts.get("ctas_per_sm", 0), opts.get("sm_count", 0),
+                                 opts.get("max_context", 0)))
 
 
 def _sizes_dict(z: _Sizes) -> dict:
     return {f: getattr(z, f) for f, _ in _Sizes._fields_}
 
 
-def okc_attn_plan_sizes(cfg: dict, seq_lens_host, opts: dict | None = None) -> dict:
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _data(a):
+    return None if a is None else a.ctypes.data
+
+
+def okc_attn_plan_sizes(cfg: dict, seq_lens_host, opts: dict | None = None, q_lens=None) -> dict:
+    """Sizes of a step; q_lens (int32 [B]) gives per-request q lengths (varlen)."""
     lib = load()
-    seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    seq, ql = _i32(seq_lens_host), _i32(q_lens)
     z = _Sizes()
-    _check(lib.okc_attn_plan_sizes(ctypes.byref(_config(cfg)), seq.ctypes.data,
-                                   _options(opts), ctypes.byref(z)), "okc_attn_plan_sizes")
+    if ql is None:
+        _check(lib.okc_attn_plan_sizes(ctypes.byref(_config(cfg)), seq.ctypes.data,
+                                       _options(opts), ctypes.byref(z)), "okc_attn_plan_sizes")
+    else:
+        _check(lib.okc_attn_plan_sizes_varlen(ctypes.byref(_config(cfg)), seq.ctypes.data, ql.ctypes.data,
+                                              _options(opts), ctypes.byref(z)), "okc_attn_plan_sizes_varlen")
     return _sizes_dict(z)
 
 
@@ -223,6 +251,20 @@ def okc_attn_plan_items(cfg: dict, seq_lens_host, opts: dict | None = None) -> n
     return out
 
 
+def okc_attn_plan_items_varlen(cfg: dict, seq_lens_host, q_lens, opts: dict | None = None) -> np.ndarray:
+    """The split work list of a varlen step: int32 [items, 4] rows of (request,
+    first token of the item's query block, first key, end key)."""
+    lib = load()
+    seq, ql = _i32(seq_lens_host), _i32(q_lens)
+    n = ctypes.c_int32(0)
+    args = (ctypes.byref(_config(cfg)), seq.ctypes.data, _data(ql), _options(opts))
+    _check(lib.okc_attn_plan_items_varlen(*args, None, 0, ctypes.byref(n)), "okc_attn_plan_items_varlen")
+    out = np.zeros((n.value, 4), dtype=np.int32)
+    _check(lib.okc_attn_plan_items_varlen(*args, out.ctypes.data, n.value, ctypes.byref(n)),
+           "okc_attn_plan_items_varlen")
+    return out
+
+
 class Plan:
     """Owns an okc_attn_plan_t handle (destroyed with the object)."""
 
@@ -231,11 +273,16 @@ class Plan:
         self.cfg = cfg  # the caller's config (not copied: plans are made every step)
         self.workspace = workspace  # keep the device buffer alive with the plan
 
-    def update(self, seq_lens_host, stream=None):
-        """Re-plan in place for the next step's host lengths (see the header)."""
-        seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
-        _check(load().okc_attn_plan_update(self.handle, seq.ctypes.data, _stream(stream)),
-               "okc_attn_plan_update")
+    def update(self, seq_lens_host, stream=None, q_lens=None):
+        """Re-plan in place for the next step's host lengths (see the header);
+        q_lens: new per-request q lengths (varlen), else the plan keeps its own."""
+        seq, ql = _i32(seq_lens_host), _i32(q_lens)
+        if ql is None:
+            _check(load().okc_attn_plan_update(self.handle, seq.ctypes.data, _stream(stream)),
+                   "okc_attn_plan_update")
+        else:
+            _check(load().okc_attn_plan_update_varlen(self.handle, seq.ctypes.data, ql.ctypes.data, _stream(stream)),
+                   "okc_attn_plan_update_varlen")
         return self
 
     @property
@@ -261,14 +308,21 @@ class Plan:
             pass
 
 
-def okc_attn_plan(cfg: dict, seq_lens_host, workspace, opts: dict | None = None, stream=None) -> Plan:
+def okc_attn_plan(cfg: dict, seq_lens_host, workspace, opts: dict | None = None, stream=None,
+                  q_lens=None) -> Plan:
+    """The step's plan in `workspace`; q_lens (int32 [B]) makes it a varlen plan."""
     lib = load()
-    seq = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    seq, ql = _i32(seq_lens_host), _i32(q_lens)
     h = ctypes.c_void_p()
     nbytes = workspace.numel() * workspace.element_size()
-    _check(lib.okc_attn_plan(ctypes.byref(_config(cfg)), seq.ctypes.data,
-                             _options(opts), _ptr(workspace), nbytes, _stream(stream), ctypes.byref(h)),
-           "okc_attn_plan")
+    if ql is None:
+        _check(lib.okc_attn_plan(ctypes.byref(_config(cfg)), seq.ctypes.data,
+                                 _options(opts), _ptr(workspace), nbytes, _stream(stream), ctypes.byref(h)),
+               "okc_attn_plan")
+    else:
+        _check(lib.okc_attn_plan_varlen(ctypes.byref(_config(cfg)), seq.ctypes.data, ql.ctypes.data,
+                                        _options(opts), _ptr(workspace), nbytes, _stream(stream), ctypes.byref(h)),
+               "okc_attn_plan_varlen")
     return Plan(h, cfg, workspace)
 
 
@@ -398,18 +452,22 @@ class AttnStep:
     norm_weight (bf16 [64] or None) and rope_table (float32 or None).
     """
 
-    def __init__(self, cfg: dict, seq_lens_host, device=None, opts: dict | None = None, stream=None):
+    def __init__(self, cfg: dict, seq_lens_host, device=None, opts: dict | None = None, stream=None,
+                 q_lens=None):
         import torch
         self.cfg = dict(cfg)
         self.device = device or torch.device("cuda")
-        sizes = okc_attn_plan_sizes(cfg, seq_lens_host, opts)
+        sizes = okc_attn_plan_sizes(cfg, seq_lens_host, opts, q_lens)
         self.workspace = torch.empty(sizes["workspace_bytes"], dtype=torch.uint8, device=self.device)
-        self.plan = okc_attn_plan(cfg, seq_lens_host, self.workspace, opts, stream)
+        self.plan = okc_attn_plan(cfg, seq_lens_host, self.workspace, opts, stream, q_lens)
         sizes = self.plan.sizes
         self.sizes = sizes
+        # a fixed-capacity plan's scratch serves every step within its max_context
+        scratch = okc_attn_plan_max_sizes(cfg, opts["max_context"], opts) if (opts or {}).get("max_context") else sizes
         self.q_fp8 = torch.empty(sizes["q_fp8_bytes"], dtype=torch.uint8, device=self.device)
-        self.o_partial = torch.empty(max(16, sizes["o_partial_bytes"]) // 4, dtype=torch.float32, device=self.device)
-        self.lse_partial = torch.empty(max(16, sizes["lse_partial_bytes"]) // 4, dtype=torch.float32, device=self.device)
+        self.o_partial = torch.empty(max(16, scratch["o_partial_bytes"]) // 4, dtype=torch.float32, device=self.device)
+        self.lse_partial = torch.empty(max(16, scratch["lse_partial_bytes"]) // 4, dtype=torch.float32,
+                                       device=self.device)
         T = sizes["num_tokens"]
         self.out = torch.empty((T, cfg["num_q_heads"] * cfg["head_dim"]), dtype=torch.bfloat16, device=self.device)
 

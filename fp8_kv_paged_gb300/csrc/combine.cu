@@ -2,9 +2,9 @@
 // (the rms_norm_gate call of "012-attention-local-splits.py"). The arithmetic
 // is normgate.cuh's, shared with the fused step kernel's last-CTA epilogue.
 //
-// One CTA per token, 8 lanes per q head (16 heads -> 128 threads); a lane owns
-// 8 consecutive columns (two float4 loads per split, one 16-byte gate load,
-// one 16-byte output store).
+// One CTA per token: blockIdx.x the query block, blockIdx.y its token; 8 lanes
+// per q head (16 heads -> 128 threads); a lane owns 8 consecutive columns (two
+// float4 loads per split, one 16-byte gate load, one 16-byte output store).
 #include "normgate.cuh"
 #include "okc_internal.h"
 
@@ -15,10 +15,12 @@ namespace {
 constexpr int kCombThreads = 8 * kNumQHeads;  // 128
 
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
-  const int t = blockIdx.x;
+  const int i = blockIdx.y;  // token of the block
   const int h = threadIdx.x >> 3;
   const int c0 = (threadIdx.x & 7) * 8;
-  const int b = t / a.L, i = t - b * a.L;
+  const BlockInfo bl = a.blk[blockIdx.x];  // plan data
+  if (i >= bl.ntok) return;
+  const int t = bl.t0 + i;
 
   // caller inputs first (overlaps the decode kernel's tail)
   float g[8], w[8];
@@ -26,20 +28,20 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   pdl_wait();
   pdl_launch_dependents();
 
-  const ReqInfo rq = a.req[b];
-  const int rows = a.L * kNumQHeads;
+  const int rows = a.S * kNumQHeads;
   const int row = i * kNumQHeads + h;
-  merge_normgate(a.lse_part + (int64_t)rq.wbase * rows + row, rows,
-                 a.o_part + ((int64_t)rq.wbase * rows + row) * kHeadDim + c0, (int64_t)rows * kHeadDim,
-                 rq.nchunks, g, w, a.eps, a.out + (size_t)t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
+  merge_normgate(a.lse_part + (int64_t)bl.wbase * rows + row, rows,
+                 a.o_part + ((int64_t)bl.wbase * rows + row) * kHeadDim + c0, (int64_t)rows * kHeadDim,
+                 bl.nchunks, g, w, a.eps, a.out + (size_t)t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s) {
-  if (a.T == 0) return cudaSuccess;
+  if (a.T == 0 || a.nblocks == 0) return cudaSuccess;
+  if (a.S < 1 || a.S > 16) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.T);
+  cfg.gridDim = dim3(a.nblocks, a.S);
   cfg.blockDim = dim3(kCombThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -3,9 +3,10 @@
 // paged, causal, window_size (window-1, 0), softmax_scale sm_scale*qk_scale_factor,
 // k/v descale on the scaled path).
 //
-// Work item = (request b, chunk of its visible keys), covering BOTH KV heads and
-// all L query tokens, so that at page_size 1 every key is one contiguous 128-byte
-// cache row per tensor (K and V).
+// Work item = (query block of a request, chunk of its visible keys), covering
+// BOTH KV heads and all the block's query tokens (the whole request for q_len 1
+// and 2..16; blocks of 16 consecutive tokens for longer ones), so that at
+// page_size 1 every key is one contiguous 128-byte cache row per tensor (K and V).
 //
 // Warp-specialised pipeline. Four producer warps (16 keys of every tile each)
 // turn page-table entries into cache rows and gather them with 16-byte
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 
   // The work item is plan data (written when the plan was made): it is read
   // before the programmatic-dependency wait, overlapping the previous kernel.
+  // A fixed-capacity plan launches its capacity: CTAs past the live count return.
+  if (a.live_work && (int)blockIdx.x >= *a.live_work) return;
   const WorkItem wk = a.work[blockIdx.x];
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
@@ -202,8 +205,8 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     pdl_wait();
     pdl_launch_dependents();
     // the gate logits and norm weight the merge reads at the end: into L2 now
-    // (token b*L is the request's first token for the usual cu_seqlens_q)
-    if (tid < 16) prefetch_l2(a.qkv + (int64_t)b * a.L * kQkvWidth + kGateCol + tid * 64);
+    // (the block's first token under the plan's q lengths)
+    if (tid < 16) prefetch_l2(a.qkv + (int64_t)wk.t0 * kQkvWidth + kGateCol + tid * 64);
     if (tid == 16 && a.weight) prefetch_l2(a.weight);
   }
 
@@ -248,10 +251,15 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     if (qb < 0 || qb + ql > a.T) ql = 0;
     n = max(ql, min(n, a.max_pages * P));
   }
-  const int lo = a.window > 0 ? max(0, n - ql - a.window + 1) : 0;  // first key any query sees
+  // this block's tokens i0 .. i0 + nt - 1 of the request, at positions pbase + tok
+  const int ntk = max(0, min(a.S, ql - wk.i0));
+  if (ntk != wk.ntok || (wk.last && wk.i0 + ntk < ql)) bad_len = true;  // q lengths differ from the plan's
+  const int pbase = n - ql + wk.i0;
+  const int hi = pbase + ntk;                                           // keys < hi
+  const int lo = a.window > 0 ? max(0, pbase - a.window + 1) : 0;     // first key any query sees
   const int j0 = lo + wk.chunk * wk.chunk_keys;
-  const int j1 = min(n, j0 + wk.chunk_keys);
-  if (wk.chunk == wk.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
+  const int j1 = min(hi, j0 + wk.chunk_keys);
+  if (wk.chunk == wk.nchunks - 1 && j1 < hi) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
   const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;
   __syncthreads();  // barriers initialised
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
     for (int nt = 0; nt < NTW; nt++) {
       const int tok = tok0 + nt;
-      fused_q_frag(a, (int64_t)qb + (tok < ql ? tok : 0), g * kGroup + gq, tq, tok < ql, qf[nt], pos_err);
+      fused_q_frag(a, (int64_t)qb + wk.i0 + (tok < ntk ? tok : 0), g * kGroup + gq, tq, tok < ntk, qf[nt], pos_err);
     }
   } else {
     pdl_wait();  // q_fp8 is the prepare kernel's output
@@ -342,11 +350,11 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
     for (int nt = 0; nt < NTW; nt++) {
       const int tok = tok0 + nt;
-      const uint8_t* qrow = a.q8 + ((int64_t)(qb + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
+      const uint8_t* qrow = a.q8 + ((int64_t)(qb + wk.i0 + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
 #pragma unroll
       for (int kk = 0; kk < 2; kk++) {
-        qf[nt][kk][0] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + tq * 4) : 0u;
-        qf[nt][kk][1] = tok < ql ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + 16 + tq * 4) : 0u;
+        qf[nt][kk][0] = tok < ntk ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + tq * 4) : 0u;
+        qf[nt][kk][1] = tok < ntk ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + 16 + tq * 4) : 0u;
       }
     }
   }
@@ -362,8 +370,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
       for (int e = 0; e < 4; e++) o[dt][nt][e] = 0.f;
   }
-  const int pbase = n - ql;  // position of token 0
-  const int tok_last = min(tok0 + NTW, ql) - 1;
+  const int tok_last = min(tok0 + NTW, ntk) - 1;
   // lane-dependent parts of the ldmatrix addresses
   const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_ch = g * 4 + (lane >> 4);
   const int v_row = (lane & 7) + (lane >> 4) * 8, v_ch = g * 4 + ((lane >> 3) & 1);
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       const int whi = min(j1, wlo + C::kMTiles * 16);
       const bool writer = (KS > 1) || sub == 0;
       for (int j = max(wlo, pbase); j < whi; j++) {
-        const int64_t t = (int64_t)qb + (j - pbase);
+        const int64_t t = (int64_t)qb + wk.i0 + (j - pbase);
         uint16_t k8, v8;
         fused_new_kv(a, t, g, lane, k8, v8, pos_err);
         const int r = j - tile_j;
@@ -408,7 +415,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       const int key_hi = tile_j + kTileKeys - 1;
       const int p_lo = pbase + tok0, p_hi = pbase + tok_last;
       const bool full = key_hi < j1 && key_hi <= p_lo &&
-                        (a.window == 0 || tile_j >= p_hi - a.window + 1) && (tok0 + NTW - 1 < ql);
+                        (a.window == 0 || tile_j >= p_hi - a.window + 1) && (tok0 + NTW - 1 < ntk);
 
       float sc[C::kMTiles][NTW][4];
 #pragma unroll
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
               const int j = tile_j + mt * 16 + gq + (e >> 1) * 8;
               const int tok = tok0 + nt;
               const int p = pbase + tok;
-              const bool okm = j < j1 && tok < ql && j <= p && (a.window == 0 || j >= p - a.window + 1);
+              const bool okm = j < j1 && tok < ntk && j <= p && (a.window == 0 || j >= p - a.window + 1);
               v = okm ? v : -INFINITY;
             }
             sc[mi][nt][e] = v;
@@ -568,14 +575,15 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   }
 
   const float vscale = a.scaled ? *a.v_scale : 1.0f;
-  const int rows = a.L * kNumQHeads;
-  float* obase = a.o_part + (int64_t)wk.slot * rows * kHeadDim;
-  float* lbase = a.lse_part + (int64_t)wk.slot * rows;
+  const int rows = a.S * kNumQHeads;  // rows of an output slot: the block's tokens x heads
+  const int64_t slot = (int64_t)wk.wbase + wk.chunk;
+  float* obase = a.o_part + slot * rows * kHeadDim;
+  float* lbase = a.lse_part + slot * rows;
 #pragma unroll
   for (int nt = 0; nt < NTW; nt++) {
     if (ks > 0) break;  // key shares were merged into ks == 0
     const int tok = tok0 + nt;
-    if (tok >= ql) continue;
+    if (tok >= ntk) continue;
 #pragma unroll
     for (int c = 0; c < 2; c++) {
       const int head = g * kGroup + 2 * tq + c;
@@ -611,15 +619,15 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       // through the barrier); for the last CTA the acquire orders the other
       // splits' partials before the merge's reads (the barrier below)
       int prev;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + b) : "memory");
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + wk.blk) : "memory");
       s_last = prev == wk.nchunks - 1;
     }
     named_bar_sync(1, NCW * 32);
     if (s_last) {
       const int64_t base_lse = (int64_t)wk.wbase * rows;
-      for (int rowi = tid >> 3; rowi < ql * kNumQHeads; rowi += NCW * 4) {  // 8 lanes per row
+      for (int rowi = tid >> 3; rowi < ntk * kNumQHeads; rowi += NCW * 4) {  // 8 lanes per row
         const int tok = rowi / kNumQHeads, h = rowi % kNumQHeads;
-        const int64_t t = (int64_t)qb + tok;
+        const int64_t t = (int64_t)qb + wk.i0 + tok;
         const int c0 = (tid & 7) * 8;
         float gg[8], ww[8];
         load_gate_weight(a.qkv, a.weight, (int)t, h, c0, gg, ww);
@@ -627,7 +635,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
                        a.o_part + (base_lse + rowi) * kHeadDim + c0, (int64_t)rows * kHeadDim, wk.nchunks, gg,
                        ww, a.eps, a.out + t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
       }
-      if (tid == 0) a.tickets[b] = 0;
+      if (tid == 0) a.tickets[wk.blk] = 0;
     }
   }
 }
@@ -660,29 +668,32 @@ int occupancy_variant() {
   return nb;
 }
 
+// The variant for query blocks of S tokens (S <= 16).
 cudaError_t launch_any(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
-  if (a.L == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>(a, num_work, pdl, s);
-  if (a.L <= 2) return launch_variant<1, 2, 2, false>(a, num_work, pdl, s);
-  if (a.L <= 4) return launch_variant<1, 2, 4, false>(a, num_work, pdl, s);
-  if (a.L <= 8) return launch_variant<1, 2, 8, false>(a, num_work, pdl, s);
+  if (a.S < 1 || a.S > 16) return cudaErrorInvalidValue;
+  if (a.S == 1) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>(a, num_work, pdl, s);
+  if (a.S <= 2) return launch_variant<1, 2, 2, false>(a, num_work, pdl, s);
+  if (a.S <= 4) return launch_variant<1, 2, 4, false>(a, num_work, pdl, s);
+  if (a.S <= 8) return launch_variant<1, 2, 8, false>(a, num_work, pdl, s);
   return launch_variant<1, 2, 16, false>(a, num_work, pdl, s);
 }
 
-int occupancy_any(int L) {
-  if (L == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>();
-  if (L <= 2) return occupancy_variant<1, 2, 2, false>();
-  if (L <= 4) return occupancy_variant<1, 2, 4, false>();
-  if (L <= 8) return occupancy_variant<1, 2, 8, false>();
+int occupancy_any(int S) {
+  if (S == 1) return occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, false>();
+  if (S <= 2) return occupancy_variant<1, 2, 2, false>();
+  if (S <= 4) return occupancy_variant<1, 2, 4, false>();
+  if (S <= 8) return occupancy_variant<1, 2, 8, false>();
   return occupancy_variant<1, 2, 16, false>();
 }
 
 }  // namespace
 
-// q_len 1: 2*KS consumer warps (2 KV heads x KS key shares), one n-tile of 8 heads
-// each; q_len 2..16: one consumer warp per KV head per pair of tokens.
+// Blocks of 1 token: 2*KS consumer warps (2 KV heads x KS key shares), one
+// n-tile of 8 heads each; blocks of 2..16 tokens: one consumer warp per KV head
+// per pair of tokens; on the tcgen05 kernel when the plan chose it.
 cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  if (a.tc && a.L >= 2 && a.L <= 8) return launch_decode_tc(a, num_work, pdl, s);
+  if (a.tc) return launch_decode_tc(a, num_work, pdl, s);
   return launch_any(a, num_work, pdl, s);
 }
 
@@ -690,15 +701,15 @@ cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStrea
 // three kernels are faster (one CTA per SM at the fused variant's registers,
 // and every split recomputing the block's new K/V rows).
 cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  if (a.L != 1) return cudaErrorInvalidValue;
+  if (a.L != 1 || a.S != 1) return cudaErrorInvalidValue;
   if (num_work == 0) return cudaSuccess;
   return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>(a, num_work, pdl, s);
 }
 
-int decode_ctas_per_sm(int L, bool tc) {
-  if (tc && L >= 2 && L <= 8) return decode_tc_ctas_per_sm();
-  const int a = occupancy_any(L);
-  if (L != 1) return a;
+int decode_ctas_per_sm(int S, bool tc) {
+  if (tc) return decode_tc_ctas_per_sm();
+  const int a = occupancy_any(S);
+  if (S != 1) return a;
   const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>();
   return a < b ? a : b;
 }

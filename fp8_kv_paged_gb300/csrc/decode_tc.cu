@@ -3,10 +3,12 @@
 // flash_attn_with_kvcache call of "012-attention-local-splits.py" with the
 // block's L queries, paged, causal within the block, window (window-1, 0).
 //
-// One CTA per work item (request b, chunk of its visible keys), as in
-// decode.cu; the CTA holds all 128 q rows of the request (L tokens x 16 heads,
-// rows g*64 + i*8 + hh for KV head g, token i, head g*8 + hh; rows of tokens
-// past q_len are zero and ignored) as ONE M = 128 operand:
+// One CTA per work item (query block of a request, chunk of its visible keys),
+// as in decode.cu; the CTA holds all 128 q rows of the block (up to 8 tokens x
+// 16 heads, rows g*64 + i*8 + hh for KV head g, token i of the block, head
+// g*8 + hh; rows of tokens past the block are zero and ignored) as ONE M = 128
+// operand (a verify block of q_len <= 8 is one block; longer extends are cut
+// into blocks of 8 consecutive tokens):
 //   S [128 x 64 keys]  = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
 //   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16,
 //                         P read from tensor memory)
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   auto s_free = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + 3 * kTcGroups + j); };
   const uint32_t mma_done = sb + kTcBar + 8 * (2 * kTcStages + 4 * kTcGroups);
 
+  // a fixed-capacity plan launches its capacity: CTAs past the live count return
+  if (a.live_work && (int)blockIdx.x >= *a.live_work) return;
   const WorkItem wk = a.work[blockIdx.x];  // plan data
   if (tid == 0) {
     for (int s = 0; s < kTcStages; s++) {
@@ -183,10 +187,15 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     if (qb < 0 || qb + ql > a.T) ql = 0;
     n = max(ql, min(n, a.max_pages * P));
   }
-  const int lo = a.window > 0 ? max(0, n - ql - a.window + 1) : 0;
+  // this block's tokens i0 .. i0 + ntk - 1 of the request, at positions pbase + i
+  const int ntk = max(0, min(a.S, ql - wk.i0));
+  if (ntk != wk.ntok || (wk.last && wk.i0 + ntk < ql)) bad_len = true;  // q lengths differ from the plan's
+  const int pbase = n - ql + wk.i0;
+  const int hi = pbase + ntk;  // keys < hi
+  const int lo = a.window > 0 ? max(0, pbase - a.window + 1) : 0;
   const int j0 = lo + wk.chunk * wk.chunk_keys;
-  const int j1 = min(n, j0 + wk.chunk_keys);
-  if (wk.chunk == wk.nchunks - 1 && j1 < n) bad_len = true;  // plan does not cover the keys
+  const int j1 = min(hi, j0 + wk.chunk_keys);
+  if (wk.chunk == wk.nchunks - 1 && j1 < hi) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
   const int jt = kTma ? (j0 & ~7) : j0;  // first key of tile 0 (keys below j0 are masked)
   const int ntiles = j1 > j0 ? (j1 - jt + kTcTileKeys - 1) / kTcTileKeys : 0;
@@ -398,14 +407,14 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   const int r = tid & (kTcRows - 1);  // q row
   const int g = r >> 6, ti = (r >> 3) & 7, hh = r & 7;
   const int head = g * kGroup + hh;
-  const bool live = ti < ql;
+  const bool live = ti < ntk;
   pdl_wait();  // q_fp8 is the prepare kernel's output
   pdl_launch_dependents();
   {
     // Q row r: the 64 E4M3 dims of (token ti, head) at K bytes [64g, 64g+64),
     // zeros elsewhere; group jw writes chunks [4 jw, 4 jw + 4) of the row
-    const uint4* src = reinterpret_cast<const uint4*>(a.q8 + ((int64_t)(qb + (live ? ti : 0)) * kNumQHeads + head) *
-                                                                 kHeadDim);
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.q8 + ((int64_t)(qb + wk.i0 + (live ? ti : 0)) * kNumQHeads + head) * kHeadDim);
 #pragma unroll
     for (int c = 4 * jw; c < 4 * jw + 4; c++) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   named_bar_sync(1, (kTcMmaWarp + 1) * 32);
 
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
-  const int pos = n - ql + ti;  // this row's query position
+  const int pos = pbase + ti;  // this row's query position
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t tS = t_lane + tc_col_s(jw);              // this row's S
   const uint32_t tO = t_lane + tc_col_o(jw) + 64 * g;      // this row's O half
@@ -566,9 +575,12 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     const float L = l * f0 + l1 * f1;
     const float vscale = a.scaled ? *a.v_scale : 1.0f;
     const float inv = L > 0.f ? vscale / L : 0.f;
-    const int rows = a.L * kNumQHeads;
+    const int rows = a.S * kNumQHeads;  // rows of an output slot: the block's tokens x heads
     const int row = ti * kNumQHeads + head;
-    float* orow = a.o_part + ((int64_t)wk.slot * rows + row) * kHeadDim;
+    // (the slot is read from the work item again here: kept live through the
+    // tile loop it cost the kernel about 30 registers)
+    const int64_t slot = (int64_t)__ldg(&a.work[blockIdx.x].wbase) + __ldg(&a.work[blockIdx.x].chunk);
+    float* orow = a.o_part + (slot * rows + row) * kHeadDim;
 #pragma unroll
     for (int h2 = 0; h2 < 2; h2++) {
       float o0[32], o1[32];
@@ -585,7 +597,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
         }
       }
     }
-    if (live) a.lse_part[(int64_t)wk.slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
+    if (live) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
   }
   tc_fence_before();
   named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // TMEM reads done: the MMA warp may free it
@@ -628,7 +640,7 @@ bool encode_cache_map(CUtensorMap* m, const uint8_t* base, int64_t rows) {
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
-  if (a.L < 2 || a.L > 8) return cudaErrorInvalidValue;
+  if (a.S < 1 || a.S > 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_work);
   cfg.blockDim = dim3(kTcThreads);

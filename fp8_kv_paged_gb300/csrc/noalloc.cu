@@ -66,7 +66,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   using namespace okc;
   if (!cfg || !seq_lens_host) return OKC_ERR_INVALID;
   const okc_attn_config& c = *cfg;
-  if (c.batch < 1 || c.q_len < 1 || c.q_len > 16 || c.window < 0 || c.max_pages < 1 ||
+  if (c.batch < 1 || c.q_len < 1 || c.q_len > kMaxQLen || c.window < 0 || c.max_pages < 1 ||
       c.num_pages < 1 || !(c.sm_scale > 0.f) || !(c.qk_scale_factor > 0.f) || !(c.kv_scale > 0.f) ||
       !std::isfinite(c.sm_scale) || !std::isfinite(c.qk_scale_factor) || !std::isfinite(c.kv_scale) ||
       !(eps >= 0.f) || !std::isfinite(eps) || (c.q_norm != OKC_QNORM_BF16 && c.q_norm != OKC_QNORM_FOLDED_SCALE))
@@ -93,18 +93,20 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return OKC_ERR_CUDA;
-  const bool use_tc = L >= 2 && L <= 8;  // the default plan's kernel choice
-  const int per_sm = cached_ctas_per_sm(dev, L, use_tc);
+  const bool use_tc = uses_tc(c, nullptr);  // the default plan's kernel choice
+  const int S = block_tokens(c, nullptr);
+  const int per_sm = cached_ctas_per_sm(dev, S, use_tc);
   if (per_sm <= 0) return OKC_ERR_CUDA;
   SplitResult split;
-  const okc_status st = make_splits(cfg, seq_lens_host, nullptr, sms * per_sm, &split);
+  const okc_status st = make_splits(cfg, seq_lens_host, nullptr, nullptr, sms * per_sm, &split);
   if (st != OKC_OK) return st;
   const int64_t W = (int64_t)split.work.size();
+  const int64_t NB = (int64_t)split.blocks.size();
   if (W > kMaxWork) return OKC_ERR_WORKSPACE;
-  // Scratch layout in the static array: work list | request table | LSE | partial outputs.
-  const int64_t rows = (int64_t)L * kNumQHeads;
+  // Scratch layout in the static array: work list | block table | LSE | partial outputs.
+  const int64_t rows = (int64_t)S * kNumQHeads;
   const size_t off_req = up256((size_t)W * sizeof(WorkItem));
-  const size_t off_lse = off_req + up256((size_t)B * sizeof(ReqInfo));
+  const size_t off_lse = off_req + up256((size_t)NB * sizeof(BlockInfo));
   const size_t off_o = off_lse + up256((size_t)W * rows * sizeof(float));
   const size_t need = off_o + (size_t)W * rows * kHeadDim * sizeof(float);
   if (need > kNoAllocScratchBytes) return OKC_ERR_WORKSPACE;
@@ -116,8 +118,8 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   // pageable sources are staged before cudaMemcpyAsync returns
   if (cudaMemcpyAsync(s8, split.work.data(), (size_t)W * sizeof(WorkItem), cudaMemcpyHostToDevice, str) !=
           cudaSuccess ||
-      cudaMemcpyAsync(s8 + off_req, split.req.data(), (size_t)B * sizeof(ReqInfo), cudaMemcpyHostToDevice, str) !=
-          cudaSuccess)
+      cudaMemcpyAsync(s8 + off_req, split.blocks.data(), (size_t)NB * sizeof(BlockInfo), cudaMemcpyHostToDevice,
+                      str) != cudaSuccess)
     return OKC_ERR_CUDA;
 
   int shift = 0;
@@ -134,18 +136,18 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   d.cu_seqlens_q = cu_seqlens_q;
   d.seq_lens = seq_lens;
   d.work = reinterpret_cast<const WorkItem*>(s8);
-  d.req = reinterpret_cast<const ReqInfo*>(s8 + off_req);
   d.o_part = reinterpret_cast<float*>(s8 + off_o);
   d.lse_part = reinterpret_cast<float*>(s8 + off_lse);
   d.err = nullptr;  // out-of-range accesses are still skipped, just not reported
   d.batch = B;
   d.L = L;
+  d.S = S;
   d.window = c.window;
   d.max_pages = c.max_pages;
   d.num_pages = c.num_pages;
   d.page_shift = shift;
   d.scaled = scaled;
-  d.T = B * L;
+  d.T = (int32_t)split.tokens;
   d.scale_log2 = softmax_scale_log2(c);
   if (launch_decode(d, (int)W, false, str) != cudaSuccess) return OKC_ERR_CUDA;
 
@@ -155,10 +157,11 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   m.qkv = static_cast<const uint16_t*>(qkv);
   m.weight = static_cast<const uint16_t*>(norm_weight);
   m.out = static_cast<uint16_t*>(out);
-  m.req = d.req;
+  m.blk = reinterpret_cast<const BlockInfo*>(s8 + off_req);
   m.err = nullptr;
-  m.T = B * L;
-  m.L = L;
+  m.nblocks = (int32_t)NB;
+  m.S = S;
+  m.T = (int32_t)split.tokens;
   m.eps = eps;
   if (launch_combine(m, false, str) != cudaSuccess) return OKC_ERR_CUDA;
   return OKC_OK;

@@ -13,7 +13,7 @@
 #include "okc_internal.h"
 
 using okc::make_splits;
-using okc::ReqInfo;
+using okc::BlockInfo;
 using okc::SplitResult;
 using okc::WorkItem;
 
@@ -26,7 +26,7 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 okc_status check_config(const okc_attn_config* c) {
   if (!c) return OKC_ERR_INVALID;
-  if (c->batch < 0 || c->q_len < 1 || c->q_len > 16) return OKC_ERR_INVALID;
+  if (c->batch < 0 || c->q_len < 1 || c->q_len > okc::kMaxQLen) return OKC_ERR_INVALID;
   if (c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return OKC_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads != 0) return OKC_ERR_INVALID;
   if (c->window < 0 || c->max_pages < 1 || c->num_pages < 1 || c->page_size < 1) return OKC_ERR_INVALID;
@@ -54,30 +54,51 @@ int page_shift(int P) {
 
 }  // namespace
 
-// Split every request's visible keys into work items. Visible keys of request b:
-// [lo, seq+L) with lo = max(0, seq - window + 1) on window layers (the union of
-// its L queries' windows). The split count follows the parallelism the batch
-// leaves idle: as many items as the GPU has resident CTA slots (SMs x CTAs per
-// SM, both read at run time), never below 128 keys per item unless the request
-// is shorter, so short or windowed requests get few splits and long ones many
-// (the H200 bound cdiv(132, B*Hkv) of "012-attention-local-splits.py" plays the
-// same role with a fixed SM count).
-okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const okc_plan_options* o,
-                       int slots, SplitResult* r) {
-  const int B = c->batch, L = c->q_len;
+// Split every query block's visible keys into work items. Request b's ql new
+// tokens sit at positions seq[b] .. seq[b] + ql - 1 and form ceil(ql / S)
+// blocks of S consecutive tokens (S from block_tokens). Block [i0, i0 + ntok)
+// sees keys [lo, hi): hi = seq + i0 + ntok, lo = max(0, seq + i0 - window + 1)
+// on window layers (the union of its queries' windows), else 0. The split count
+// follows the parallelism the batch leaves idle: as many items as the GPU has
+// resident CTA slots (SMs x CTAs per SM, both read at run time), never below
+// 128 keys per item unless the block is shorter, so short or windowed blocks
+// get few splits and long ones many (the H200 bound cdiv(132, B*Hkv) of
+// "012-attention-local-splits.py" plays the same role with a fixed SM count).
+okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const int32_t* q_lens,
+                            const okc_plan_options* o, int slots, SplitResult* r) {
+  const int B = c->batch, Lmax = c->q_len;
   if (o && o->chunk_keys != 0 && o->chunk_keys < 16) return OKC_ERR_INVALID;
-  std::vector<int64_t> nvis(B);
-  int64_t total = 0;
+  const int S = okc::block_tokens(*c, o);
+  r->S = S;
+  r->max_chunks = 0;
+  r->max_chunk_keys = 0;
+  // ---- the query blocks (units of the split): request, first token, tokens,
+  // first token of the step, key range end and visible keys
+  struct Unit {
+    int32_t b, i0, ntok, t0, last;
+    int64_t hi, nvis;
+  };
+  std::vector<Unit> units;
+  units.reserve((size_t)B * (size_t)((Lmax + S - 1) / S));
+  int64_t t0 = 0, total = 0;
   for (int b = 0; b < B; b++) {
-    if (seq[b] < 0) return OKC_ERR_INVALID;
-    const int64_t hi = (int64_t)seq[b] + L;
-    if (hi > (int64_t)c->max_pages * c->page_size) return OKC_ERR_INVALID;
-    const int64_t lo = c->window > 0 ? std::max<int64_t>(0, (int64_t)seq[b] - c->window + 1) : 0;
-    nvis[b] = hi - lo;
-    total += nvis[b];
+    const int ql = q_lens ? q_lens[b] : Lmax;
+    if (seq[b] < 0 || ql < 0 || ql > Lmax) return OKC_ERR_INVALID;
+    if ((int64_t)seq[b] + ql > (int64_t)c->max_pages * c->page_size) return OKC_ERR_INVALID;
+    for (int i0 = 0; i0 < ql; i0 += S) {
+      const int ntok = std::min(S, ql - i0);
+      const int64_t hi = (int64_t)seq[b] + i0 + ntok;
+      const int64_t lo = c->window > 0 ? std::max<int64_t>(0, (int64_t)seq[b] + i0 - c->window + 1) : 0;
+      units.push_back(Unit{b, i0, ntok, (int32_t)(t0 + i0), i0 + S >= ql ? 1 : 0, hi, hi - lo});
+      total += hi - lo;
+    }
+    t0 += ql;
   }
-  // Choose one key budget C for every request (a request's keys are then split
-  // into ceil(n_b / C) equal chunks). For m = 1..4 waves of the `slots` resident
+  r->tokens = t0;
+  const int U = (int)units.size();
+  if ((int64_t)units.size() > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
+  // Choose one key budget C for every block (a block's keys are then split
+  // into ceil(n_u / C) equal chunks). For m = 1..4 waves of the `slots` resident
   // CTA slots, take the smallest C whose items fit m waves and score it as
   //   max(largest item, ceil(items / slots) * mean item),
   // each item costing kItemCost keys on top of its own (start-up, the split's
@@ -85,21 +106,21 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
   // Skewed batches pick more waves of smaller items; uniform ones one wave.
   const int64_t min_chunk = 128, kItemCost = 128;
   int64_t nmax = 1;
-  for (int b = 0; b < B; b++) nmax = std::max(nmax, nvis[b]);
+  for (const Unit& u : units) nmax = std::max(nmax, u.nvis);
   // (key counts and budgets are below 2^31: 32-bit divisions)
   auto cdiv = [](int64_t a, int64_t b) { return (int64_t)(((uint32_t)a + (uint32_t)b - 1u) / (uint32_t)b); };
   // The search evaluates items(C) only at budgets C >= c_floor (the least any
-  // wave count below can pick), where a request of at most c_floor keys is one
-  // item: those are counted once. Requests of the largest size (on window
-  // layers every request whose context fills the window, on full layers a
-  // batch of equal contexts) are counted once times their number.
+  // wave count below can pick), where a block of at most c_floor keys is one
+  // item: those are counted once. Blocks of the largest size (on window
+  // layers every block whose context fills the window, on full layers a batch
+  // of equal contexts) are counted once times their number.
   const int64_t c_floor =
       slots > 0 ? std::max<int64_t>(min_chunk, (total + 4 * (int64_t)slots - 1) / (4 * (int64_t)slots)) : min_chunk;
   int64_t n_top = 0, n_small = 0, max_small = 0;
   std::vector<int64_t> rest;
-  rest.reserve((size_t)B);
-  for (int b = 0; b < B; b++) {
-    const int64_t v = nvis[b];
+  rest.reserve(units.size());
+  for (const Unit& u : units) {
+    const int64_t v = u.nvis;
     if (v == nmax) {
       n_top++;
     } else if (v <= c_floor) {
@@ -109,10 +130,10 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
       rest.push_back(v);
     }
   }
-  // items(C) = sum over requests of ceil(n_b / C) (every n_b >= 1): the
+  // items(C) = sum over blocks of ceil(n_u / C) (every n_u >= 1): the
   // quotient from one reciprocal per C, corrected to the exact integer (the
   // double estimate of a quotient below 2^31 is off by at most one), instead
-  // of a division per request
+  // of a division per block
   auto items = [&](int64_t C) {
     const double rc = 1.0 / (double)C;
     auto nch = [&](int64_t v) {
@@ -126,22 +147,22 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
     return w;
   };
   int64_t Cbud = std::max<int64_t>(min_chunk, nmax);
-  if (slots > 0 && B > 0) {
-    double best = -1.0, excess = 0.5 * B;
-    const int64_t cmax = std::max<int64_t>(min_chunk, nmax);  // items(cmax) = B
+  if (slots > 0 && U > 0) {
+    double best = -1.0, excess = 0.5 * U;
+    const int64_t cmax = std::max<int64_t>(min_chunk, nmax);  // items(cmax) = U
     for (int m = 1; m <= 4; m++) {
       // smallest C in [min_chunk, cmax] with items(C) <= cap (cmax when none).
-      // Since total / C <= items(C) <= total / C + B, that C is at least
-      // ceil(total / cap) and at most ceil(total / (cap - B)) when cap > B.
+      // Since total / C <= items(C) <= total / C + U, that C is at least
+      // ceil(total / cap) and at most ceil(total / (cap - U)) when cap > U.
       const int64_t cap = (int64_t)m * slots;
       int64_t lo_c = cmax, hi_c = cmax;
-      if (cap > B) {
+      if (cap > U) {
         lo_c = std::min(cmax, std::max(min_chunk, (total + cap - 1) / cap));
-        hi_c = std::min(cmax, std::max(lo_c, (total + cap - B - 1) / (cap - B)));
+        hi_c = std::min(cmax, std::max(lo_c, (total + cap - U - 1) / (cap - U)));
       }
       // Safeguarded search: probe where the model items(C) = total / C + e
       // puts items at cap (e: the excess over total / C seen at the last
-      // probe, between 0 and B), clamped into the bracket, and bisect after a
+      // probe, between 0 and U), clamped into the bracket, and bisect after a
       // probe that did not halve it. Every probe keeps the answer inside
       // [lo_c, hi_c] with items(hi_c) <= cap, so the result is the bisection's,
       // in a few probes instead of log2 of the bracket.
@@ -166,7 +187,7 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
       }
       const int64_t C = lo_c, W = w_hi >= 0 && hi_c == C ? w_hi : items(C);
       auto item_keys = [&](int64_t v) { return cdiv(v, std::max<int64_t>(1, cdiv(v, C))); };
-      int64_t biggest = std::max(max_small, n_top ? item_keys(nmax) : 0);  // a request of v <= C keys: v
+      int64_t biggest = std::max(max_small, n_top ? item_keys(nmax) : 0);  // a block of v <= C keys: v
       for (const int64_t v : rest) biggest = std::max(biggest, item_keys(v));
       const double mean = (double)(total + W * kItemCost) / (double)W;
       const double waves = (double)((W + slots - 1) / slots);
@@ -178,73 +199,81 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
       if (C == min_chunk) break;  // smaller items are not allowed
     }
   }
-  (void)total;
-  // q_len 2..8 decodes on the tcgen05 kernel, fed by TMA on pages of 8+ rows
-  const bool tc_tma = L >= 2 && L <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05)) && c->page_size >= 8;
+  // blocks of 2..8 tokens decode on the tcgen05 kernel, fed by TMA on pages of 8+ rows
+  const bool tc_tma = okc::uses_tc(*c, o) && c->page_size >= 8;
   const int64_t tma_pad = tc_tma ? 7 : 0;
-  r->req.assign(B, ReqInfo{0, 0, 0, 0});
+  r->blocks.assign((size_t)U, BlockInfo{0, 0, 0, 0});
+  std::vector<int32_t> chunk_of((size_t)U);
   int64_t wbase = 0;
-  int64_t prev_n = -1, chunk = 0, nch = 0;  // requests of equal size share their split
-  for (int b = 0; b < B; b++) {
-    if (nvis[b] != prev_n) {
-      prev_n = nvis[b];
+  int64_t prev_n = -1, chunk = 0, nch = 0;  // blocks of equal size share their split
+  for (int u = 0; u < U; u++) {
+    const int64_t nv = units[(size_t)u].nvis;
+    if (nv != prev_n) {
+      prev_n = nv;
       if (o && o->chunk_keys > 0) {
         chunk = o->chunk_keys;
       } else {
-        const int64_t k = std::max<int64_t>(1, cdiv(nvis[b], Cbud));
-        chunk = okc::split_chunk_keys(nvis[b], k, tma_pad);
+        const int64_t k = std::max<int64_t>(1, cdiv(nv, Cbud));
+        chunk = okc::split_chunk_keys(nv, k, tma_pad);
       }
-      nch = std::max<int64_t>(1, cdiv(nvis[b], chunk));
+      nch = std::max<int64_t>(1, cdiv(nv, chunk));
     }
     if (nch > (1 << 20) || wbase + nch > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
-    r->req[b] = ReqInfo{(int32_t)wbase, (int32_t)nch, (int32_t)chunk, 0};
+    r->blocks[(size_t)u] = BlockInfo{(int32_t)wbase, (int32_t)nch, units[(size_t)u].t0, units[(size_t)u].ntok};
+    chunk_of[(size_t)u] = (int32_t)chunk;
     r->max_chunks = std::max<int>(r->max_chunks, (int)nch);
+    r->max_chunk_keys = std::max<int64_t>(r->max_chunk_keys, chunk);
     wbase += nch;
   }
-  // Launch order: the largest items first (the last chunk of a request may be
-  // short), ties in slot order. A request's items before its last all hold
+  // Launch order: the largest items first (the last chunk of a block may be
+  // short), ties in slot order. A block's items before its last all hold
   // chunk_keys keys, so the order is a merge of two sorted runs: those items,
-  // request by request in (chunk_keys desc, request) order, and the last
-  // items in (keys desc, request) order. Sort words pack (2^31-1 - keys, b).
-  auto last_keys = [&](int b) {
-    const ReqInfo& q = r->req[b];
-    return nvis[b] - (int64_t)(q.nchunks - 1) * q.chunk_keys;
+  // block by block in (chunk_keys desc, block) order, and the last items in
+  // (keys desc, block) order. Sort words pack (2^31-1 - keys, u).
+  auto last_keys = [&](int u) {
+    const BlockInfo& q = r->blocks[(size_t)u];
+    return units[(size_t)u].nvis - (int64_t)(q.nchunks - 1) * chunk_of[(size_t)u];
   };
-  auto pack = [](int64_t keys, int b) { return ((uint64_t)(0x7FFFFFFF - keys) << 32) | (uint32_t)b; };
-  std::vector<uint64_t> run_full, run_last((size_t)B);
-  run_full.reserve((size_t)B);
-  for (int b = 0; b < B; b++) {
-    if (r->req[b].nchunks > 1) run_full.push_back(pack(r->req[b].chunk_keys, b));
-    run_last[(size_t)b] = pack(last_keys(b), b);
+  auto pack = [](int64_t keys, int u) { return ((uint64_t)(0x7FFFFFFF - keys) << 32) | (uint32_t)u; };
+  std::vector<uint64_t> run_full, run_last((size_t)U);
+  run_full.reserve((size_t)U);
+  for (int u = 0; u < U; u++) {
+    if (r->blocks[(size_t)u].nchunks > 1) run_full.push_back(pack(chunk_of[(size_t)u], u));
+    run_last[(size_t)u] = pack(last_keys(u), u);
   }
   std::sort(run_full.begin(), run_full.end());
   std::sort(run_last.begin(), run_last.end());
   r->work.resize((size_t)wbase);
   WorkItem* out = r->work.data();
+  auto item = [&](int u, int k, int64_t j0, int64_t j1) {
+    const Unit& x = units[(size_t)u];
+    const BlockInfo& q = r->blocks[(size_t)u];
+    return WorkItem{x.b, u, x.i0, x.ntok, k, (int32_t)j0, (int32_t)j1, chunk_of[(size_t)u], q.nchunks, q.wbase,
+                    x.t0, x.last};
+  };
   size_t il = 0;
   auto emit_last_before = [&](uint64_t key_word, int32_t slot) {  // last items ahead of (key, slot)
     while (il < run_last.size()) {
       const uint64_t w = run_last[il];
-      const int b = (int)(w & 0xFFFFFFFFu);
-      const ReqInfo& q = r->req[b];
+      const int u = (int)(w & 0xFFFFFFFFu);
+      const BlockInfo& q = r->blocks[(size_t)u];
       const int32_t ls = q.wbase + q.nchunks - 1;
       if ((w >> 32) > (key_word >> 32) || ((w >> 32) == (key_word >> 32) && ls > slot)) break;
-      const int64_t n = (int64_t)seq[b] + L, j0 = n - nvis[b] + (int64_t)(q.nchunks - 1) * q.chunk_keys;
-      *out++ = WorkItem{b, q.nchunks - 1, ls, (int32_t)j0, (int32_t)n, q.chunk_keys, q.nchunks, q.wbase};
+      const Unit& x = units[(size_t)u];
+      *out++ = item(u, q.nchunks - 1, x.hi - x.nvis + (int64_t)(q.nchunks - 1) * chunk_of[(size_t)u], x.hi);
       il++;
     }
   };
-  // A request's items before its last take slots wbase .. wbase + nchunks - 2,
-  // a range no other request's slot falls into, so the last items that go
-  // before any of them go before the first: one merge step per request.
+  // A block's items before its last take slots wbase .. wbase + nchunks - 2,
+  // a range no other block's slot falls into, so the last items that go
+  // before any of them go before the first: one merge step per block.
   for (const uint64_t w : run_full) {
-    const int b = (int)(w & 0xFFFFFFFFu);
-    const ReqInfo& q = r->req[b];
+    const int u = (int)(w & 0xFFFFFFFFu);
+    const BlockInfo& q = r->blocks[(size_t)u];
     emit_last_before(w, q.wbase);
-    int64_t j0 = (int64_t)seq[b] + L - nvis[b];  // these items hold chunk_keys keys each
-    for (int k = 0; k + 1 < q.nchunks; k++, j0 += q.chunk_keys)
-      *out++ = WorkItem{b, k, q.wbase + k, (int32_t)j0, (int32_t)(j0 + q.chunk_keys), q.chunk_keys, q.nchunks,
-                        q.wbase};
+    const int64_t ck = chunk_of[(size_t)u];
+    int64_t j0 = units[(size_t)u].hi - units[(size_t)u].nvis;  // these items hold chunk_keys keys each
+    for (int k = 0; k + 1 < q.nchunks; k++, j0 += ck) *out++ = item(u, k, j0, j0 + ck);
   }
   emit_last_before(~0ull, 0);
   return OKC_OK;
@@ -265,20 +294,20 @@ int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_
   const int flags = o ? o->flags : 0;
   if (flags & OKC_PLAN_STEP_THREE_LAUNCHES) return 3;
   if (flags & OKC_PLAN_STEP_ONE_LAUNCH) return 1;
-  int64_t max_chunk = 0;
-  for (const ReqInfo& q : s.req) max_chunk = std::max<int64_t>(max_chunk, q.chunk_keys);
   const int64_t W = (int64_t)s.work.size();
-  return (2 * W >= slots && (max_chunk <= 2048 || W > slots)) ? 1 : 3;
+  return (2 * W >= slots && (s.max_chunk_keys <= 2048 || W > slots)) ? 1 : 3;
 }
 
-// Buffer sizes for W work items (the workspace, q and the split partials).
-void sizes_for(const okc_attn_config* c, int64_t W, int max_chunks, okc_attn_sizes* z) {
-  const int64_t T = (int64_t)c->batch * c->q_len;
-  const int64_t rows = (int64_t)c->q_len * c->num_q_heads;
+// Buffer sizes of a step of W work items laid out in a work list of cap >= W
+// entries, NB query blocks of S tokens and T tokens (the workspace, q and the
+// split partials).
+void sizes_for(const okc_attn_config* c, int64_t W, int64_t cap, int64_t NB, int64_t T, int S, int max_chunks,
+               okc_attn_sizes* z) {
+  const int64_t rows = (int64_t)S * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
-  z->workspace_bytes = okc::kWsHeader + round_up(W * sizeof(WorkItem)) + round_up(c->batch * sizeof(ReqInfo)) +
-                      round_up(c->batch * sizeof(int32_t)) +  // + the one-launch step's arrival counters
-                      round_up(T * c->num_q_heads * c->head_dim);  // + q for the three-launch step
+  z->workspace_bytes = okc::kWsHeader + round_up(cap * sizeof(WorkItem)) + round_up(NB * sizeof(BlockInfo)) +
+                       round_up(NB * sizeof(int32_t)) +               // + the one-launch step's arrival counters
+                       round_up(T * c->num_q_heads * c->head_dim);  // + q for the three-launch step
   z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
   z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
   z->lse_partial_bytes = round_up(W * rows * sizeof(float));
@@ -288,46 +317,73 @@ void sizes_for(const okc_attn_config* c, int64_t W, int max_chunks, okc_attn_siz
   z->step_kernels = 3;
 }
 
-okc_status compute_sizes(const okc_attn_config* c, const SplitResult& s, okc_attn_sizes* z) {
-  sizes_for(c, (int64_t)s.work.size(), s.max_chunks, z);
-  return OKC_OK;
-}
-
 // Upper bounds of the split counts over every step whose requests each hold at
-// most max_context keys after the step. A request of n visible keys gets
+// most max_context keys after the step. A request has at most ceil(q_len / S)
+// query blocks, and a block sees at most min(max_context, window + S - 1)
+// keys (window layers) or max_context. A block of n visible keys gets
 // ceil(n / chunk_keys) items under a forced chunk size; under the heuristic
 // k = ceil(n / C) items for the budget C >= 128 (its chunk holds at least
 // ceil(n / k) keys), and the budget's work list either fits the m waves it was
-// chosen for (m <= 4: at most 4 x slots items) or is one item per request.
+// chosen for (m <= 4: at most 4 x slots items) or is one item per block.
 void split_bounds(const okc_attn_config* c, int64_t max_context, const okc_plan_options* o, int slots,
-                  int64_t* max_work, int64_t* max_chunks) {
-  const int64_t B = c->batch;
-  const int64_t nvis = c->window > 0 ? std::min<int64_t>(max_context, (int64_t)c->window + c->q_len - 1)
-                                     : max_context;
+                  int64_t* max_work, int64_t* max_chunks, int64_t* max_blocks) {
+  const int S = okc::block_tokens(*c, o);
+  const int64_t NB = (int64_t)c->batch * ((c->q_len + S - 1) / S);
+  const int64_t nvis = c->window > 0 ? std::min<int64_t>(max_context, (int64_t)c->window + S - 1) : max_context;
   const int64_t per = (o && o->chunk_keys > 0) ? o->chunk_keys : 128;
   const int64_t k = std::max<int64_t>(1, (nvis + per - 1) / per);
   *max_chunks = k;
-  *max_work = B * k;
-  if (!(o && o->chunk_keys > 0)) *max_work = std::min(*max_work, std::max<int64_t>(B, 4 * (int64_t)slots));
+  *max_blocks = NB;
+  *max_work = NB * k;
+  if (!(o && o->chunk_keys > 0)) *max_work = std::min(*max_work, std::max<int64_t>(NB, 4 * (int64_t)slots));
 }
 
-// Step 4 of a 2..8-token block runs on the tcgen05 kernel unless the plan says not to.
-bool use_tc(const okc_attn_config* c, const okc_plan_options* o) {
-  return c->q_len >= 2 && c->q_len <= 8 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
+// A plan with a fixed-capacity work list: okc_plan_options.max_context > 0.
+bool fixed_capacity(const okc_plan_options* o) { return o && o->max_context > 0; }
+
+// The sizes of a step under the options (the live split `s`; on a
+// fixed-capacity plan the work list laid out at the capacity for max_context,
+// returned in *cap_out), and its okc_attn_step form.
+okc_status plan_sizes_of(const okc_attn_config* c, const SplitResult& s, const okc_plan_options* o, int slots,
+                         okc_attn_sizes* z, int64_t* cap_out) {
+  const int64_t W = (int64_t)s.work.size();
+  int64_t cap = W;
+  if (fixed_capacity(o)) {
+    int64_t wb = 0, kb = 0, nb = 0;
+    split_bounds(c, o->max_context, o, slots, &wb, &kb, &nb);
+    if (W > wb) return OKC_ERR_WORKSPACE;  // (the bound holds for every step within max_context)
+    cap = wb;
+  }
+  sizes_for(c, W, cap, (int64_t)s.blocks.size(), s.tokens, s.S, s.max_chunks, z);
+  z->step_kernels = step_kernels(c, s, o, slots);
+  if (cap_out) *cap_out = fixed_capacity(o) ? cap : 0;
+  return OKC_OK;
+}
+
+// Steps a fixed-capacity plan serves: uniform q lengths, every request within max_context.
+okc_status check_fixed(const okc_attn_config* c, const int32_t* seq, const int32_t* q_lens,
+                       const okc_plan_options* o) {
+  if (!fixed_capacity(o)) return OKC_OK;
+  if (o->max_context < c->q_len || (int64_t)o->max_context > (int64_t)c->max_pages * c->page_size)
+    return OKC_ERR_INVALID;
+  if (q_lens) return OKC_ERR_UNSUPPORTED;
+  for (int b = 0; b < c->batch; b++)
+    if (seq[b] < 0 || (int64_t)seq[b] + c->q_len > o->max_context) return OKC_ERR_INVALID;
+  return OKC_OK;
 }
 
 }  // namespace
 
-// Resident decode CTAs per SM for (device, q_len, kernel family), queried once
-// per key: the query also raises the kernels' shared-memory limit on the device.
-int okc::cached_ctas_per_sm(int dev, int L, bool tc) {
+// Resident decode CTAs per SM for (device, block tokens, kernel family), queried
+// once per key: the query also raises the kernels' shared-memory limit on the device.
+int okc::cached_ctas_per_sm(int dev, int S, bool tc) {
   static std::mutex mu;
   static std::map<std::tuple<int, int, bool>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(dev, L, tc);
+  const auto key = std::make_tuple(dev, S, tc);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const int occ = okc::decode_ctas_per_sm(L, tc);
+  const int occ = okc::decode_ctas_per_sm(S, tc);
   if (occ > 0) cache[key] = occ;
   return occ;
 }
@@ -341,7 +397,7 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    if (per_sm == 0) per_sm = okc::cached_ctas_per_sm(dev, c->q_len, use_tc(c, o));
+    if (per_sm == 0) per_sm = okc::cached_ctas_per_sm(dev, okc::block_tokens(*c, o), okc::uses_tc(*c, o));
     if (per_sm <= 0) return -1;
   }
   if (sm_count_out) *sm_count_out = sms;
@@ -353,19 +409,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // the null checks are separate).
 bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0; }
 
-// The plan takes a split result: sizes, work list, request table, and the
-// workspace layout (error word | work list | request table | arrival counters | q).
+// The plan takes a split result: sizes, work list, block table, and the
+// workspace layout (header | work list | block table | arrival counters | q).
+// A fixed-capacity plan lays the work list out at its capacity, so the offsets
+// after it never move.
 void set_splits(okc_attn_plan_s* p, SplitResult& s, const okc_attn_sizes& z) {
   p->sizes = z;
   p->work.swap(s.work);
-  p->req.swap(s.req);
+  p->blocks.swap(s.blocks);
+  p->S = s.S;
+  const size_t cap = p->work_cap > 0 ? (size_t)p->work_cap : p->work.size();
   uint8_t* ws = static_cast<uint8_t*>(p->workspace);
   p->d_err = reinterpret_cast<unsigned*>(ws);
+  p->d_live = reinterpret_cast<int32_t*>(ws + okc::kWsCount);
   p->d_work = reinterpret_cast<WorkItem*>(ws + okc::kWsHeader);
-  p->d_req = reinterpret_cast<ReqInfo*>(ws + okc::kWsHeader + round_up(p->work.size() * sizeof(WorkItem)));
-  p->d_tickets =
-      reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_req) + round_up(p->req.size() * sizeof(ReqInfo)));
-  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(p->cfg.batch * sizeof(int32_t));
+  p->d_blk = reinterpret_cast<BlockInfo*>(ws + okc::kWsHeader + round_up(cap * sizeof(WorkItem)));
+  p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_blk) +
+                                            round_up(p->blocks.size() * sizeof(BlockInfo)));
+  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(p->blocks.size() * sizeof(int32_t));
 }
 
 // Bytes of the workspace head the plan uploads (everything before q).
@@ -373,16 +434,25 @@ size_t upload_bytes(const okc_attn_plan_s* p) {
   return static_cast<size_t>(p->d_q8 - static_cast<uint8_t*>(p->workspace));
 }
 
-// The work list and request table at their workspace offsets in a zeroed
-// host image of the head (the error word and arrival counters stay zero).
+// The live item count, the work list and the block table at their workspace
+// offsets in a zeroed host image of the head (the error word and the arrival
+// counters stay zero).
 void write_head(const okc_attn_plan_s* p, uint8_t* head) {
   const uint8_t* ws = static_cast<const uint8_t*>(p->workspace);
+  const int32_t live = (int32_t)p->work.size();
+  std::memcpy(head + okc::kWsCount, &live, sizeof live);
   if (!p->work.empty())
     std::memcpy(head + (reinterpret_cast<const uint8_t*>(p->d_work) - ws), p->work.data(),
                 p->work.size() * sizeof(WorkItem));
-  if (!p->req.empty())
-    std::memcpy(head + (reinterpret_cast<const uint8_t*>(p->d_req) - ws), p->req.data(),
-                p->req.size() * sizeof(ReqInfo));
+  if (!p->blocks.empty())
+    std::memcpy(head + (reinterpret_cast<const uint8_t*>(p->d_blk) - ws), p->blocks.data(),
+                p->blocks.size() * sizeof(BlockInfo));
+}
+
+// Work items the decode launches cover: the capacity on a fixed-capacity plan
+// (CTAs past the live count return at once), else the step's own count.
+int launch_items(const okc_attn_plan_s* p) {
+  return p->work_cap > 0 ? (int)p->work_cap : p->sizes.num_work;
 }
 
 // The device address of a page-locked, device-mapped host buffer, else NULL
@@ -426,19 +496,25 @@ const char* okc_status_string(okc_status s) {
   return "unknown status";
 }
 
-okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_lens_host,
-                               const okc_plan_options* opts, okc_attn_sizes* sizes) {
+okc_status okc_attn_plan_sizes_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                                      const int32_t* q_lens_host, const okc_plan_options* opts,
+                                      okc_attn_sizes* sizes) {
   okc_status st = check_config(cfg);
   if (st != OKC_OK) return st;
   if (!sizes || (cfg->batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
+  st = check_fixed(cfg, seq_lens_host, q_lens_host, opts);
+  if (st != OKC_OK) return st;
   const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
   if (slots < 0) return OKC_ERR_CUDA;
   SplitResult s;
-  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  st = make_splits(cfg, seq_lens_host, q_lens_host, opts, slots, &s);
   if (st != OKC_OK) return st;
-  st = compute_sizes(cfg, s, sizes);
-  sizes->step_kernels = step_kernels(cfg, s, opts, slots);
-  return st;
+  return plan_sizes_of(cfg, s, opts, slots, sizes, nullptr);
+}
+
+okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                               const okc_plan_options* opts, okc_attn_sizes* sizes) {
+  return okc_attn_plan_sizes_varlen(cfg, seq_lens_host, nullptr, opts, sizes);
 }
 
 okc_status okc_attn_plan_max_sizes(const okc_attn_config* cfg, int32_t max_context, const okc_plan_options* opts,
@@ -450,11 +526,17 @@ okc_status okc_attn_plan_max_sizes(const okc_attn_config* cfg, int32_t max_conte
   if (opts && opts->chunk_keys != 0 && opts->chunk_keys < 16) return OKC_ERR_INVALID;
   const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
   if (slots < 0) return OKC_ERR_CUDA;
-  int64_t W = 0, kmax = 0;
-  split_bounds(cfg, max_context, opts, slots, &W, &kmax);
-  if (cfg->batch == 0) W = kmax = 0;
+  int64_t W = 0, kmax = 0, NB = 0;
+  split_bounds(cfg, max_context, opts, slots, &W, &kmax, &NB);
+  if (cfg->batch == 0) W = kmax = NB = 0;
   if (kmax > (1 << 20) || W > ((int64_t)1 << 30)) return OKC_ERR_UNSUPPORTED;
-  sizes_for(cfg, W, (int)kmax, sizes);
+  int64_t cap = W;
+  if (fixed_capacity(opts)) {  // the work list of a fixed-capacity plan is laid out for its own max_context
+    int64_t wc = 0, kc = 0, nc = 0;
+    split_bounds(cfg, std::max<int64_t>(opts->max_context, cfg->q_len), opts, slots, &wc, &kc, &nc);
+    cap = cfg->batch > 0 ? std::max(W, wc) : 0;
+  }
+  sizes_for(cfg, W, cap, NB, (int64_t)cfg->batch * cfg->q_len, okc::block_tokens(*cfg, opts), (int)kmax, sizes);
   sizes->step_kernels = 0;  // depends on the lengths
   return OKC_OK;
 }
@@ -467,6 +549,29 @@ okc_status okc_attn_plan_workspace_size(const okc_attn_config* cfg, int32_t max_
   return st;
 }
 
+okc_status okc_attn_plan_items_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                                      const int32_t* q_lens_host, const okc_plan_options* opts, int32_t* items,
+                                      int32_t capacity, int32_t* count) {
+  okc_status st = check_config(cfg);
+  if (st != OKC_OK) return st;
+  if (!count || capacity < 0 || (capacity > 0 && !items) || (cfg->batch > 0 && !seq_lens_host))
+    return OKC_ERR_INVALID;
+  const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
+  if (slots < 0) return OKC_ERR_CUDA;
+  SplitResult s;
+  st = make_splits(cfg, seq_lens_host, q_lens_host, opts, slots, &s);
+  if (st != OKC_OK) return st;
+  *count = (int32_t)s.work.size();
+  if ((int64_t)s.work.size() > capacity) return capacity == 0 && !items ? OKC_OK : OKC_ERR_WORKSPACE;
+  for (size_t i = 0; i < s.work.size(); i++) {
+    items[4 * i] = s.work[i].b;
+    items[4 * i + 1] = s.work[i].i0;
+    items[4 * i + 2] = s.work[i].j0;
+    items[4 * i + 3] = s.work[i].j1;
+  }
+  return OKC_OK;
+}
+
 okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                                const okc_plan_options* opts, int32_t* items, int32_t capacity,
                                int32_t* count) {
@@ -477,7 +582,7 @@ okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_le
   const int slots = cfg->batch > 0 ? slots_for(cfg, opts, nullptr) : 1;
   if (slots < 0) return OKC_ERR_CUDA;
   SplitResult s;
-  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  st = make_splits(cfg, seq_lens_host, nullptr, opts, slots, &s);
   if (st != OKC_OK) return st;
   *count = (int32_t)s.work.size();
   if ((int64_t)s.work.size() > capacity) return capacity == 0 && !items ? OKC_OK : OKC_ERR_WORKSPACE;
@@ -489,40 +594,46 @@ okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_le
   return OKC_OK;
 }
 
-okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
-                         const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
-                         okc_stream stream, okc_attn_plan_t* plan_out) {
+okc_status okc_attn_plan_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host, const int32_t* q_lens_host,
+                                const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
+                                okc_stream stream, okc_attn_plan_t* plan_out) {
   okc_status st = check_config(cfg);
   if (st != OKC_OK) return st;
   if (!plan_out || (cfg->batch > 0 && !seq_lens_host) || !workspace) return OKC_ERR_INVALID;
   *plan_out = nullptr;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return OKC_ERR_WORKSPACE;
+  st = check_fixed(cfg, seq_lens_host, q_lens_host, opts);
+  if (st != OKC_OK) return st;
   int sms = 0;
   const int slots = slots_for(cfg, opts, &sms);
   if (slots < 0) return OKC_ERR_CUDA;
   SplitResult s;
-  st = make_splits(cfg, seq_lens_host, opts, slots, &s);
+  st = make_splits(cfg, seq_lens_host, q_lens_host, opts, slots, &s);
   if (st != OKC_OK) return st;
   okc_attn_sizes z;
-  compute_sizes(cfg, s, &z);
-  z.step_kernels = step_kernels(cfg, s, opts, slots);
+  int64_t cap = 0;
+  st = plan_sizes_of(cfg, s, opts, slots, &z, &cap);
+  if (st != OKC_OK) return st;
   if (workspace_bytes < z.workspace_bytes) return OKC_ERR_WORKSPACE;
 
   okc_attn_plan_s* p = new (std::nothrow) okc_attn_plan_s();
   if (!p) return OKC_ERR_INVALID;
   p->cfg = *cfg;
   if (opts) p->opts = *opts; else std::memset(&p->opts, 0, sizeof p->opts);
+  if (q_lens_host) p->q_lens.assign(q_lens_host, q_lens_host + cfg->batch);
   p->workspace = workspace;
   p->workspace_bytes = workspace_bytes;
   p->slots = slots;
+  p->work_cap = cap;
   cudaGetDevice(&p->device);
   p->sm_count = sms;
   p->pdl = !(p->opts.flags & OKC_PLAN_NO_PDL);
-  p->tc = use_tc(cfg, opts);
+  p->tc = okc::uses_tc(*cfg, opts);
   p->scale_log2 = okc::softmax_scale_log2(*cfg);
   set_splits(p, s, z);
-  // One upload of the workspace's head: the zeroed error word, the work list,
-  // the request table and the zeroed arrival counters, as laid out on the device.
+  // One upload of the workspace's head: the zeroed error word, the live item
+  // count, the work list, the block table and the zeroed arrival counters, as
+  // laid out on the device.
   const size_t up_bytes = upload_bytes(p);
   p->upload.assign(up_bytes, 0);
   write_head(p, p->upload.data());
@@ -536,34 +647,47 @@ okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_hos
   return OKC_OK;
 }
 
+okc_status okc_attn_plan(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                         const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
+                         okc_stream stream, okc_attn_plan_t* plan_out) {
+  return okc_attn_plan_varlen(cfg, seq_lens_host, nullptr, opts, workspace, workspace_bytes, stream, plan_out);
+}
+
 okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_lens_host, void* workspace,
                                 size_t workspace_bytes, okc_stream stream, okc_attn_plan_t* plan_out) {
   return okc_attn_plan(cfg, seq_lens_host, nullptr, workspace, workspace_bytes, stream, plan_out);
 }
 
-okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream) {
+okc_status okc_attn_plan_update_varlen(okc_attn_plan_t plan, const int32_t* seq_lens_host,
+                                       const int32_t* q_lens_host, okc_stream stream) {
   if (!plan || (plan->cfg.batch > 0 && !seq_lens_host)) return OKC_ERR_INVALID;
+  okc_status st = check_fixed(&plan->cfg, seq_lens_host, q_lens_host, &plan->opts);
+  if (st != OKC_OK) return st;
   // The new split is built in the spare lists (the ones the previous update
   // replaced: their capacity is reused); the plan's current lists, sizes and
   // workspace stay as they are until every step that can fail has passed.
   SplitResult s;
   s.work.swap(plan->spare_work);
-  s.req.swap(plan->spare_req);
+  s.blocks.swap(plan->spare_blocks);
   auto restore = [&](okc_status e) {
     s.work.swap(plan->spare_work);
-    s.req.swap(plan->spare_req);
+    s.blocks.swap(plan->spare_blocks);
     return e;
   };
-  okc_status st = make_splits(&plan->cfg, seq_lens_host, &plan->opts, plan->slots, &s);
+  st = make_splits(&plan->cfg, seq_lens_host, q_lens_host, &plan->opts, plan->slots, &s);
   if (st != OKC_OK) return restore(st);
   okc_attn_sizes z;
-  compute_sizes(&plan->cfg, s, &z);
-  z.step_kernels = step_kernels(&plan->cfg, s, &plan->opts, plan->slots);
-  // the staging buffer for the head (up to q: error word, work list, request
-  // table, arrival counters) is made ready before the plan changes
+  st = plan_sizes_of(&plan->cfg, s, &plan->opts, plan->slots, &z, nullptr);
+  if (st != OKC_OK) return restore(st);
+  // a fixed-capacity plan keeps the okc_attn_step form it was made with (a
+  // graph captured from it keeps its launches)
+  if (plan->work_cap > 0) z.step_kernels = plan->sizes.step_kernels;
+  // the staging buffer for the head (up to q: header, work list, block table,
+  // arrival counters) is made ready before the plan changes
   if (plan->workspace_bytes < z.workspace_bytes) return restore(OKC_ERR_WORKSPACE);
-  const size_t up_bytes = okc::kWsHeader + round_up(s.work.size() * sizeof(WorkItem)) +
-                          round_up(s.req.size() * sizeof(ReqInfo)) + round_up(plan->cfg.batch * sizeof(int32_t));
+  const size_t cap = plan->work_cap > 0 ? (size_t)plan->work_cap : s.work.size();
+  const size_t up_bytes = okc::kWsHeader + round_up(cap * sizeof(WorkItem)) + round_up(s.blocks.size() * sizeof(BlockInfo)) +
+                          round_up(s.blocks.size() * sizeof(int32_t));
   // the staging buffer may still feed the previous update's copy
   if (plan->pinned_done && cudaEventSynchronize(plan->pinned_done) != cudaSuccess) return restore(OKC_ERR_CUDA);
   if (plan->pinned_bytes < up_bytes) {
@@ -583,18 +707,28 @@ okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_ho
   }
   set_splits(plan, s, z);  // s now holds the replaced lists: they become the spares
   s.work.swap(plan->spare_work);
-  s.req.swap(plan->spare_req);
+  s.blocks.swap(plan->spare_blocks);
+  if (!q_lens_host)
+    plan->q_lens.clear();
+  else if (q_lens_host != plan->q_lens.data())
+    plan->q_lens.assign(q_lens_host, q_lens_host + plan->cfg.batch);
   uint8_t* head = static_cast<uint8_t*>(plan->pinned);
   std::memset(head, 0, up_bytes);
   write_head(plan, head);
-  // The upload starts past the header: the device error word keeps the bits
-  // earlier steps set until the caller reads or clears them.
+  // The upload starts past the error word: the device error word keeps the
+  // bits earlier steps set until the caller reads or clears them.
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(static_cast<uint8_t*>(plan->workspace) + okc::kWsHeader, head + okc::kWsHeader,
-                      up_bytes - okc::kWsHeader, cudaMemcpyHostToDevice, str) != cudaSuccess ||
+  if (cudaMemcpyAsync(static_cast<uint8_t*>(plan->workspace) + okc::kWsCount, head + okc::kWsCount,
+                      up_bytes - okc::kWsCount, cudaMemcpyHostToDevice, str) != cudaSuccess ||
       cudaEventRecord(plan->pinned_done, str) != cudaSuccess)
     return OKC_ERR_CUDA;
   return OKC_OK;
+}
+
+okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream) {
+  if (!plan) return OKC_ERR_INVALID;
+  return okc_attn_plan_update_varlen(plan, seq_lens_host, plan->q_lens.empty() ? nullptr : plan->q_lens.data(),
+                                     stream);
 }
 
 okc_status okc_attn_plan_destroy(okc_attn_plan_t plan) {
@@ -707,7 +841,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
                            float* o_partial, float* lse_partial, okc_stream stream) {
   if (!plan) return OKC_ERR_INVALID;
   const okc_attn_config& c = plan->cfg;
-  if (plan->sizes.num_work == 0) return OKC_OK;
+  if (launch_items(plan) == 0) return OKC_OK;
   if (!q_fp8 || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q ||
       !o_partial || !lse_partial)
     return OKC_ERR_INVALID;
@@ -729,12 +863,13 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
   a.cu_seqlens_q = cu_seqlens_q;
   a.seq_lens = seq_lens;
   a.work = plan->d_work;
-  a.req = plan->d_req;
+  a.live_work = plan->work_cap > 0 ? plan->d_live : nullptr;
   a.o_part = o_partial;
   a.lse_part = lse_partial;
   a.err = plan->d_err;
   a.batch = c.batch;
   a.L = c.q_len;
+  a.S = plan->S;
   a.window = c.window;
   a.max_pages = c.max_pages;
   a.num_pages = c.num_pages;
@@ -742,7 +877,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
   a.scaled = scaled;
   a.T = plan->sizes.num_tokens;
   a.scale_log2 = plan->scale_log2;  // the kernel multiplies in *k_scale when scaled
-  cudaError_t e = okc::launch_decode(a, plan->sizes.num_work, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = okc::launch_decode(a, launch_items(plan), plan->pdl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
 }
 
@@ -764,10 +899,11 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
   a.qkv = static_cast<const uint16_t*>(qkv);
   a.weight = static_cast<const uint16_t*>(norm_weight);
   a.out = static_cast<uint16_t*>(out);
-  a.req = plan->d_req;
+  a.blk = plan->d_blk;
   a.err = plan->d_err;
+  a.nblocks = (int32_t)plan->blocks.size();
+  a.S = plan->S;
   a.T = T;
-  a.L = plan->cfg.q_len;
   a.eps = eps;
   cudaError_t e = okc::launch_combine(a, plan->pdl, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
@@ -781,7 +917,7 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
                          float* lse_partial, void* out, okc_stream stream) {
   if (!plan) return OKC_ERR_INVALID;
   const okc_attn_config& c = plan->cfg;
-  if (plan->sizes.num_work == 0) return OKC_OK;
+  if (launch_items(plan) == 0) return OKC_OK;
   if (!qkv || !cache_loc || !k_cache || !v_cache || !page_table || !cache_seqlens || !cu_seqlens_q ||
       !o_partial || !lse_partial || !out)
     return OKC_ERR_INVALID;
@@ -809,12 +945,13 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.cu_seqlens_q = cu_seqlens_q;
   a.seq_lens = seq_lens;
   a.work = plan->d_work;
-  a.req = plan->d_req;
+  a.live_work = plan->work_cap > 0 ? plan->d_live : nullptr;
   a.o_part = o_partial;
   a.lse_part = lse_partial;
   a.err = plan->d_err;
   a.batch = c.batch;
   a.L = c.q_len;
+  a.S = plan->S;
   a.window = c.window;
   a.max_pages = c.max_pages;
   a.num_pages = c.num_pages;
@@ -839,7 +976,7 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.q_scale = c.qk_scale_factor;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   if (plan->sizes.step_kernels == 1) {
-    cudaError_t e = okc::launch_step_fused(a, plan->sizes.num_work, plan->pdl, str);
+    cudaError_t e = okc::launch_step_fused(a, launch_items(plan), plan->pdl, str);
     return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
   }
   // the three kernels, with q in the plan workspace

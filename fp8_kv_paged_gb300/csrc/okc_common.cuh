@@ -22,6 +22,7 @@ constexpr int kRowBytes = kNumKvHeads * kHeadDim;  // one cache row (both KV hea
 constexpr int kQkvWidth = (2 * kNumQHeads + 2 * kNumKvHeads) * kHeadDim;
 constexpr int kGateCol = (kNumQHeads + 2 * kNumKvHeads) * kHeadDim;
 constexpr int kRopePositionsMax = 1 << 21;
+constexpr int kMaxQLen = 1 << 16;  // new tokens of one request in one step
 constexpr float kRmsEps = 1.0e-5f;
 
 // ------------------------------------------------------------ launch control

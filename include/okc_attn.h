@@ -34,8 +34,11 @@
  *      k_cache    e4m3  [num_pages, page_size, Hkv, 64]  flat row = page*page_size + offset
  *      v_cache    e4m3  same as k_cache
  *      page_table int32 [B, max_pages]  physical page of each logical page (-1 unused)
- *      out        bf16  [B, L, Hq*64]
- *    with T = B*L tokens, token t = b*L + i at position seq_lens[b] + i.
+ *      out        bf16  [T, Hq*64]
+ *    with T tokens: the step's new tokens, request b's tokens at rows
+ *    cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and positions seq_lens[b] + i. A
+ *    decode or verify step has T = B*L (cu_seqlens_q = 0, L, 2L, ...); a
+ *    prefill/extend step (okc_attn_plan_varlen) q_lens[b] tokens per request.
  */
 #ifndef OKC_ATTN_H
 #define OKC_ATTN_H
@@ -69,13 +72,15 @@ typedef enum okc_status {
 /*
  * Mirrors the problem file's `class Config`. The library runs the per-GPU shape
  * of Muse Spark under TP8: num_q_heads = 16, num_kv_heads = 2, head_dim = 64
- * (anything else returns OKC_ERR_UNSUPPORTED), q_len in [1, 16], page_size a
- * power of two in [1, 256], max_pages * page_size <= 2^30 and batch * q_len <=
- * 2^26 (larger: OKC_ERR_UNSUPPORTED).
+ * (anything else returns OKC_ERR_UNSUPPORTED), q_len in [1, 65536], page_size
+ * a power of two in [1, 256], max_pages * page_size <= 2^30 and batch * q_len
+ * <= 2^26 (larger: OKC_ERR_UNSUPPORTED).
  */
 typedef struct okc_attn_config {
   int32_t batch;           /* B: requests in the step */
-  int32_t q_len;           /* L: 1 for decode, 8 for a speculative verify block (causal inside it) */
+  int32_t q_len;           /* L: 1 for decode, 8 for a speculative verify block (causal inside it),
+                              more for prefill/extend; with per-request q lengths the largest of them
+                              (the problem file's max_seqlen_q) */
   int32_t num_q_heads;     /* Hq */
   int32_t num_kv_heads;    /* Hkv; each serves Hq/Hkv query heads */
   int32_t head_dim;        /* 64 */
@@ -110,14 +115,24 @@ typedef struct okc_attn_config {
 typedef struct okc_plan_options {
   int32_t chunk_keys;      /* keys per split work item; 0 = the built-in heuristic, else >= 16 */
   int32_t flags;           /* OKC_PLAN_NO_PDL: launch the kernels without programmatic dependent launch;
-                              OKC_PLAN_NO_TCGEN05: q_len 2..8 decodes with the warp-level MMA kernel
-                              instead of the tcgen05 one;
+                              OKC_PLAN_NO_TCGEN05: q_len >= 2 decodes with the warp-level MMA kernel
+                              (blocks of up to 16 tokens) instead of the tcgen05 one;
                               OKC_PLAN_STEP_ONE_LAUNCH / OKC_PLAN_STEP_THREE_LAUNCHES: force the form
                               of okc_attn_step at q_len 1 (default: chosen by the plan) */
   int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
   int32_t sm_count;        /* SMs the split heuristic assumes; 0 = the current device's. With
                               ctas_per_sm also set, planning (okc_attn_plan_sizes,
                               okc_attn_plan_items) makes no CUDA call */
+  int32_t max_context;     /* 0: the work list is laid out for the plan's own step. > 0: a
+                              fixed-capacity plan for every step whose requests hold at most
+                              max_context tokens after it (uniform q_len only): the work list
+                              is laid out at the capacity okc_attn_plan_max_sizes gives for
+                              max_context, the decode launches cover that capacity and read
+                              the live item count from the workspace (CTAs past it return at
+                              once), and okc_attn_step keeps the form it was planned with. Every
+                              okc_attn_plan_update within max_context then keeps the launches a
+                              CUDA graph captured, so graphs replay correctly after any such
+                              update (scratch sized by okc_attn_plan_max_sizes). */
 } okc_plan_options;
 #define OKC_PLAN_NO_PDL 0x1
 #define OKC_PLAN_NO_TCGEN05 0x2
@@ -128,11 +143,13 @@ typedef struct okc_plan_options {
 typedef struct okc_attn_sizes {
   size_t workspace_bytes;    /* device workspace the plan is uploaded into (okc_attn_plan) */
   size_t q_fp8_bytes;        /* scratch: E4M3 q [T, Hq, 64], written by prepare, read by decode */
-  size_t o_partial_bytes;    /* scratch: f32 per-split outputs [num_work, L*Hq, 64] */
-  size_t lse_partial_bytes;  /* scratch: f32 per-split base-2 log-sum-exp [num_work, L*Hq] */
+  size_t o_partial_bytes;    /* scratch: f32 per-split outputs [num_work, S*Hq, 64], S the tokens
+                                of a query block: min(q_len, 8) on the tcgen05 kernel (q_len >= 2),
+                                min(q_len, 16) on the warp-level one */
+  size_t lse_partial_bytes;  /* scratch: f32 per-split base-2 log-sum-exp [num_work, S*Hq] */
   int32_t num_work;          /* split work items of this step */
-  int32_t num_tokens;        /* T = B*L */
-  int32_t max_chunks;        /* largest number of splits of one request */
+  int32_t num_tokens;        /* T: B*L, or the sum of the q lengths of a varlen plan */
+  int32_t max_chunks;        /* largest number of splits of one query block */
   int32_t step_kernels;      /* kernels okc_attn_step launches: 1 (one fused kernel, q_len 1 only)
                                 or 3 (prepare, decode, combine) */
 } okc_attn_sizes;
@@ -159,6 +176,35 @@ okc_status okc_attn_plan_sizes(const okc_attn_config* cfg, const int32_t* seq_le
 okc_status okc_attn_plan_items(const okc_attn_config* cfg, const int32_t* seq_lens_host,
                                const okc_plan_options* opts, int32_t* items, int32_t capacity,
                                int32_t* count);
+
+/*
+ * Prefill / extend: per-request q lengths (the problem file's `Inputs.cu_seqlens_q`
+ * with its `max_seqlen_q`). q_lens_host: int32 [B], the new tokens of each
+ * request in this step, each in [0, cfg->q_len] (cfg->q_len is their largest
+ * value; 0: the request takes no part); NULL = q_len each, which makes every
+ * call below the same as its form without q lengths. The step's T is the sum of
+ * the q lengths; request b's new tokens sit at positions seq_lens_host[b] + i,
+ * i < q_lens_host[b], each attending causally to every earlier key and to the
+ * block's earlier tokens (window: the window - 1 keys before it). A request's
+ * new tokens are cut into query blocks of S consecutive tokens (okc_attn_sizes)
+ * and every block's keys into split work items. The device inputs must agree:
+ * cu_seqlens_q = 0 then the running sums of q_lens_host, cache_seqlens[b] =
+ * seq_lens_host[b] + q_lens_host[b]; kernels that find other q lengths flag
+ * OKC_DEVERR_LENGTHS. okc_attn_plan_items_varlen writes 4 ints per item:
+ * request, first token of its block (within the request), first key, end key.
+ * okc_attn_plan_update_varlen re-plans in place with new q lengths (a
+ * fixed-capacity plan takes none: OKC_ERR_UNSUPPORTED); okc_attn_plan_update
+ * keeps the plan's q lengths.
+ */
+okc_status okc_attn_plan_sizes_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                                      const int32_t* q_lens_host, const okc_plan_options* opts,
+                                      okc_attn_sizes* sizes);
+okc_status okc_attn_plan_items_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host,
+                                      const int32_t* q_lens_host, const okc_plan_options* opts, int32_t* items,
+                                      int32_t capacity, int32_t* count);
+okc_status okc_attn_plan_varlen(const okc_attn_config* cfg, const int32_t* seq_lens_host, const int32_t* q_lens_host,
+                                const okc_plan_options* opts, void* workspace, size_t workspace_bytes,
+                                okc_stream stream, okc_attn_plan_t* plan_out);
 
 /*
  * Upper bounds of okc_attn_plan_sizes over every step of this config whose
@@ -216,12 +262,16 @@ okc_status okc_attn_plan_create(const okc_attn_config* cfg, const int32_t* seq_l
  * word is not part of the upload: bits set by earlier steps stay until
  * okc_attn_plan_clear_errors (or a new okc_attn_plan) clears them.
  * CUDA graphs: a launch captured in a graph keeps the grid size and the
- * workspace offsets of the plan as it was at capture. Replaying it after an
- * update is valid only while num_work is unchanged (the work list and request
- * table then keep their offsets); after an update that changed num_work,
- * capture again before replaying.
+ * workspace offsets of the plan as it was at capture. On a fixed-capacity plan
+ * (okc_plan_options.max_context) neither ever changes, so a graph captured
+ * once replays correctly after every update within max_context. On other
+ * plans, replaying after an update is valid only while num_work is unchanged
+ * (the work list and block table then keep their offsets); after an update
+ * that changed num_work, capture again before replaying.
  */
 okc_status okc_attn_plan_update(okc_attn_plan_t plan, const int32_t* seq_lens_host, okc_stream stream);
+okc_status okc_attn_plan_update_varlen(okc_attn_plan_t plan, const int32_t* seq_lens_host,
+                                       const int32_t* q_lens_host, okc_stream stream);
 
 okc_status okc_attn_plan_destroy(okc_attn_plan_t plan);
 /* The plan's sizes: the workspace it needs and the caller's scratch (q_fp8 and
@@ -274,17 +324,20 @@ okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t*
  * k/v descale when scaled). Query i of request b sits at position
  * cache_seqlens[b] - q_len_b + i and sees keys j with max(0, p-window+1) <= j <= p
  * (window 0: 0 <= j <= p); query head h reads KV head h / (Hq/Hkv). Each work item
- * of the plan covers a key range of one request for all its query rows and both
- * KV heads, and writes a normalized f32 partial output (already times v_scale)
- * and its base-2 log-sum-exp. q_len 2..8 runs on the tcgen05 kernel (M = 128
- * query rows per request, accumulators in tensor memory; on pages of 8 or more
- * rows its K/V tiles arrive by TMA through tensor maps the call encodes for
- * k_cache and v_cache, so page_size * num_pages rows must be addressable from
- * both base pointers) unless the plan was made with OKC_PLAN_NO_TCGEN05; q_len
- * 1 and 9..16 on the warp-level MMA kernel.
+ * of the plan covers a key range of one query block (the whole request for
+ * decode and verify steps; S consecutive tokens of a longer one) for all its
+ * query rows and both KV heads, and writes a normalized f32 partial output
+ * (already times v_scale) and its base-2 log-sum-exp. q_len >= 2 runs on the
+ * tcgen05 kernel (blocks of up to 8 tokens: M = 128 query rows, accumulators in
+ * tensor memory; on pages of 8 or more rows its K/V tiles arrive by TMA through
+ * tensor maps the call encodes for k_cache and v_cache, so page_size *
+ * num_pages rows must be addressable from both base pointers) unless the plan
+ * was made with OKC_PLAN_NO_TCGEN05 (then blocks of up to 16 tokens on the
+ * warp-level MMA kernel, which also runs q_len 1).
  *  q_fp8          from okc_prepare_qkv
  *  page_table     int32 [B, max_pages]
  *  cache_seqlens  int32 [B] = seq_lens + L; cu_seqlens_q int32 [B+1] = 0, L, 2L, ...
+ *                 (varlen plans: seq_lens + q_lens and the running sums of q_lens)
  *  seq_lens       int32 [B] (checked against cache_seqlens; may be NULL)
  *  o_partial/lse_partial  scratch, >= the plan's sizes
  */
@@ -300,7 +353,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
  * request's splits, ob = bf16(o), out = bf16(ob * rsqrt(mean(ob^2) + eps) * w *
  * sigmoid(gate)) with gate = qkv[t, (Hq+2Hkv)*64 + h*64 + c] read in place.
  *  norm_weight  bf16 [64] or NULL (NULL = the problem file's weight None)
- *  out          bf16 [B, L, Hq*64]
+ *  out          bf16 [T, Hq*64]
  */
 okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partial,
                                      const float* lse_partial, const void* qkv,
@@ -401,14 +454,19 @@ okc_status okc_selftest_bounded_wait(uint32_t* err, int32_t limit_us, okc_stream
  * takes no plan, workspace or scratch buffer: the work list, the per-request
  * table and the split partials live in one static device array of 8 MiB inside
  * the library, which every GPU that loads the library holds until the process
- * exits. It makes no device allocation (no cudaMalloc, cudaFree or other CUDA
- * allocating routine); its host-side work list is ordinary heap memory.
+ * exits. It calls no allocating routine (no cudaMalloc, cudaFree or other CUDA
+ * allocating routine); its host-side work list is ordinary heap memory. The
+ * array takes its device memory when the CUDA runtime loads the library's
+ * device code on a device: at the first call on that device under lazy module
+ * loading (the CUDA default), or when the library loads with
+ * CUDA_MODULE_LOADING=EAGER; later calls leave the device's free memory as it is.
  *
  * Arguments are those of okc_attn_plan (cfg, seq_lens_host), okc_attn_decode and
  * okc_attn_combine_normgate; q_fp8 must already hold okc_prepare_qkv's output.
  * The result equals the three-call path's `out` for the same inputs.
  * Limits: at most 2048 requests and 4096 split work items, and the partials
- * (work items x q_len*16 rows x 260 bytes, plus the tables) must fit in 8 MiB;
+ * (work items x S*16 rows x 260 bytes, S the plan's block tokens, plus the
+ * tables) must fit in 8 MiB;
  * larger steps return OKC_ERR_WORKSPACE before any GPU work. Device-side range
  * errors are skipped as in okc_attn_decode but not reported (there is no plan
  * error word).

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <random>
 #include <vector>
 static std::vector<unsigned char> g_array(8u << 20);
@@ -69,11 +70,14 @@ int main(int argc, char** argv) {
         (const int32_t*)dummy, nullptr, dummy, nullptr, 1e-5f, dummy, nullptr);
     // the plan's split for the same device
     okc::SplitResult want;
-    const bool tc = L >= 2 && L <= 8;
-    CHECK(okc::make_splits(&c, seq.data(), nullptr, 152 * (tc ? 1 : 3), &want) == OKC_OK);
-    const size_t W = want.work.size(), rows = (size_t)L * 16;
+    const bool tc = L >= 2;
+    CHECK(okc::make_splits(&c, seq.data(), nullptr, nullptr, 152 * (tc ? 1 : 3), &want) == OKC_OK);
+    const int S = tc ? std::min(L, 8) : 1;
+    CHECK(want.S == S);
+    const size_t W = want.work.size(), NB = want.blocks.size(), rows = (size_t)S * 16;
+    CHECK(NB == (size_t)B * ((L + S - 1) / S));
     const size_t off_req = (W * sizeof(okc::WorkItem) + 255) / 256 * 256;
-    const size_t off_lse = off_req + (B * sizeof(okc::ReqInfo) + 255) / 256 * 256;
+    const size_t off_lse = off_req + (NB * sizeof(okc::BlockInfo) + 255) / 256 * 256;
     const size_t off_o = off_lse + (W * rows * 4 + 255) / 256 * 256;
     const size_t need = off_o + W * rows * 64 * 4;
     const bool over = B > 2048 || W > 4096 || need > (8u << 20);
@@ -84,14 +88,14 @@ int main(int argc, char** argv) {
     }
     CHECK(st == OKC_OK);
     CHECK(g_copies.size() == 2 && g_copies[0].off == 0 && g_copies[0].n == W * sizeof(okc::WorkItem));
-    CHECK(g_copies[1].off == off_req && g_copies[1].n == B * sizeof(okc::ReqInfo));
+    CHECK(g_copies[1].off == off_req && g_copies[1].n == NB * sizeof(okc::BlockInfo));
     CHECK(memcmp(base, want.work.data(), g_copies[0].n) == 0);
-    CHECK(memcmp(base + off_req, want.req.data(), g_copies[1].n) == 0);
-    CHECK(g_launches == 2 && g_W == (int)W && g_dec.tc == (tc ? 1 : 0));
-    CHECK((const unsigned char*)g_dec.work == base && (const unsigned char*)g_dec.req == base + off_req);
+    CHECK(memcmp(base + off_req, want.blocks.data(), g_copies[1].n) == 0);
+    CHECK(g_launches == 2 && g_W == (int)W && g_dec.tc == (tc ? 1 : 0) && g_dec.S == S && g_comb.S == S);
+    CHECK((const unsigned char*)g_dec.work == base && (const unsigned char*)g_comb.blk == base + off_req);
     CHECK((const unsigned char*)g_dec.lse_part == base + off_lse && (const unsigned char*)g_dec.o_part == base + off_o);
-    CHECK(g_comb.o_part == g_dec.o_part && g_comb.lse_part == g_dec.lse_part && g_comb.req == g_dec.req);
-    CHECK(g_comb.T == B * L && g_dec.T == B * L);
+    CHECK(g_comb.o_part == g_dec.o_part && g_comb.lse_part == g_dec.lse_part && g_comb.nblocks == (int)NB);
+    CHECK(g_comb.T == B * L && g_dec.T == B * L && g_dec.live_work == nullptr);
     ok++;
   }
   if (ok == 0 || refused == 0) { printf("FAIL: %d run, %d refused\n", ok, refused); return 1; }

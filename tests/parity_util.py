@@ -38,7 +38,8 @@ def run_gpu(cfg: dict, inp: dict, opts: dict | None = None, dev_inp: dict | None
     d = dev_inp if dev_inp is not None else to_device(cfg, inp)
     if fused and not plan_form:
         opts = dict(opts or {}, flags=(opts or {}).get("flags", 0) | okc.PLAN_STEP_ONE_LAUNCH)
-    step = okc.AttnStep(cfg, inp["seq_lens"] if plan_seq is None else plan_seq, opts=opts)
+    step = okc.AttnStep(cfg, inp["seq_lens"] if plan_seq is None else plan_seq, opts=opts,
+                        q_lens=inp["q_lens"] if "q_lens" in cfg else None)
     out = step.run_fused(d, eps=inp["eps"]) if fused else step.run(d, eps=inp["eps"])
     torch.cuda.synchronize()
     T = inp["qkv"].shape[0]

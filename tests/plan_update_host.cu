@@ -65,16 +65,26 @@ int main(int argc, char** argv) {
   int cases = 0;
   const int iters = argc > 1 ? atoi(argv[1]) : 1000;
   for (int it = 0; it < iters; it++) {
-    const int L = std::vector<int>{1, 2, 8, 16}[g() % 4];
+    const int L = std::vector<int>{1, 2, 8, 16, 100}[g() % 5];
     const int P = std::vector<int>{1, 8, 64}[g() % 3];
     const int window = std::vector<int>{0, 64, 2048}[g() % 3];
     const int B = std::vector<int>{1, 3, 64, 300}[g() % 4];
     const int maxctx = 1 + g() % 60000;
     const int max_pages = (maxctx + L + P - 1) / P + 1;
     okc_attn_config c = {B, L, 16, 2, 64, P, window, max_pages, B * max_pages, 5e5f, 5.473f, 0.125f, 1.f};
-    okc_plan_options o = {0, 0, (int)(1 + g() % 3), 152};
+    okc_plan_options o = {0, 0, (int)(1 + g() % 3), 152, 0};
     if (g() % 4 == 0) o.chunk_keys = 16 + g() % 3000;
+    // kind 0: a plan for its own step; 1: a fixed-capacity plan (max_context);
+    // 2: per-request q lengths (varlen), new ones at every update
+    const int kind = g() % 3;
+    if (kind == 1) o.max_context = maxctx + L;
     auto lengths = [&](int hi) { std::vector<int32_t> v(B); for (auto& x : v) x = g() % (hi + 1); return v; };
+    auto qlens = [&]() { std::vector<int32_t> v(B); for (auto& x : v) x = g() % (L + 1); return v; };
+    std::vector<int32_t> ql = qlens();
+    auto qp = [&]() -> const int32_t* { return kind == 2 ? ql.data() : nullptr; };
+    auto update = [&](okc_attn_plan_t pl, const int32_t* sq) {
+      return kind == 2 ? okc_attn_plan_update_varlen(pl, sq, qp(), nullptr) : okc_attn_plan_update(pl, sq, nullptr);
+    };
     okc_attn_sizes bound;
     CHECK(okc_attn_plan_max_sizes(&c, maxctx + L, &o, &bound) == OKC_OK);
     // a plan in a workspace of the bound, and a fresh plan per step to compare with
@@ -83,9 +93,11 @@ int main(int argc, char** argv) {
     uint8_t* w2 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws2.data()) + 255) / 256 * 256);
     auto s0 = lengths(std::min(maxctx, 50));
     okc_attn_plan_t p = nullptr;
-    CHECK(okc_attn_plan(&c, s0.data(), &o, w, bound.workspace_bytes, nullptr, &p) == OKC_OK);
+    CHECK(okc_attn_plan_varlen(&c, s0.data(), qp(), &o, w, bound.workspace_bytes, nullptr, &p) == OKC_OK);
+    const size_t fixed_head = head_bytes(p);  // a fixed-capacity plan's offsets never move
     for (int step = 0; step < 6; step++) {
       auto s1 = lengths(maxctx);
+      if (kind == 2) ql = qlens();
       okc_attn_sizes before;
       okc_attn_plan_get_sizes(p, &before);
       std::vector<uint8_t> head_before(w, w + head_bytes(p));
@@ -93,7 +105,7 @@ int main(int argc, char** argv) {
       if (mode == 0) {  // a failed staging allocation leaves everything as it was
         g_fail_mallochost = 1;
         // force a (re)allocation: only the first update allocates, or a larger one
-        okc_status st = okc_attn_plan_update(p, s1.data(), nullptr);
+        okc_status st = update(p, s1.data());
         if (st == OKC_ERR_CUDA) {
           g_alloc_failures++;
           okc_attn_sizes after;
@@ -105,13 +117,15 @@ int main(int argc, char** argv) {
         g_fail_mallochost = 0;
       } else if (mode == 2) {  // the upload itself fails: reported, and the next update repairs the plan
         g_fail_memcpy = 1;
-        CHECK(okc_attn_plan_update(p, s1.data(), nullptr) == OKC_ERR_CUDA);
+        CHECK(update(p, s1.data()) == OKC_ERR_CUDA);
         g_fail_memcpy = 0;
         g_upload_failures++;
       } else if (mode == 1) {  // a length past the page table: refused, plan unchanged
         auto bad = s1;
-        bad[g() % B] = max_pages * P;  // + L > max_pages * P
-        CHECK(okc_attn_plan_update(p, bad.data(), nullptr) == OKC_ERR_INVALID);
+        const int i = (int)(g() % B);
+        bad[i] = max_pages * P;  // + its q length > max_pages * P
+        if (kind == 2 && ql[i] == 0) ql[i] = 1;
+        CHECK(update(p, bad.data()) == OKC_ERR_INVALID);
         okc_attn_sizes after;
         okc_attn_plan_get_sizes(p, &after);
         CHECK(memcmp(&before, &after, sizeof before) == 0);
@@ -120,17 +134,22 @@ int main(int argc, char** argv) {
       // bits the kernels set in the error word survive the update
       const uint32_t err_word = (uint32_t)g() | 1u;
       memcpy(w, &err_word, sizeof err_word);
-      CHECK(okc_attn_plan_update(p, s1.data(), nullptr) == OKC_OK);
+      CHECK(update(p, s1.data()) == OKC_OK);
       CHECK(memcmp(w, &err_word, sizeof err_word) == 0);
+      if (kind == 1) CHECK(head_bytes(p) == fixed_head);
       okc_attn_plan_t q = nullptr;
-      CHECK(okc_attn_plan(&c, s1.data(), &o, w2, bound.workspace_bytes, nullptr, &q) == OKC_OK);
+      CHECK(okc_attn_plan_varlen(&c, s1.data(), qp(), &o, w2, bound.workspace_bytes, nullptr, &q) == OKC_OK);
       okc_attn_sizes zp, zq;
       okc_attn_plan_get_sizes(p, &zp);
       okc_attn_plan_get_sizes(q, &zq);
+      if (kind == 1) zq.step_kernels = zp.step_kernels;  // a fixed-capacity plan keeps its form
       CHECK(memcmp(&zp, &zq, sizeof zp) == 0);
+      int32_t live = -1;
+      memcpy(&live, w + okc::kWsCount, sizeof live);
+      CHECK(live == zp.num_work);
       CHECK(head_bytes(p) == head_bytes(q));
-      // the uploaded heads are identical past the header (the fresh plan zeroed its error word)
-      CHECK(memcmp(w + okc::kWsHeader, w2 + okc::kWsHeader, head_bytes(p) - okc::kWsHeader) == 0);
+      // the uploaded heads are identical past the error word (the fresh plan zeroed its own)
+      CHECK(memcmp(w + okc::kWsCount, w2 + okc::kWsCount, head_bytes(p) - okc::kWsCount) == 0);
       memset(w, 0, sizeof err_word);
       CHECK(zp.workspace_bytes <= bound.workspace_bytes && zp.o_partial_bytes <= bound.o_partial_bytes &&
             zp.num_work <= bound.num_work);
@@ -139,6 +158,10 @@ int main(int argc, char** argv) {
     }
     // a workspace too small for the next step: refused, plan unchanged
     {
+      if (kind != 0) {  // (the refusal below is for plans sized to their own step)
+        okc_attn_plan_destroy(p);
+        continue;
+      }
       auto big = std::vector<int32_t>(B, maxctx);
       okc_attn_sizes zb;
       CHECK(okc_attn_plan_sizes(&c, big.data(), &o, &zb) == OKC_OK);

@@ -55,7 +55,8 @@ def _cfg(**kw):
     (dict(num_q_heads=32), okc.ERR_UNSUPPORTED),
     (dict(page_size=3), okc.ERR_UNSUPPORTED),
     (dict(q_len=0), okc.ERR_INVALID),
-    (dict(q_len=17), okc.ERR_INVALID),
+    (dict(q_len=65537), okc.ERR_INVALID),
+    (dict(q_norm=2), okc.ERR_INVALID),
     (dict(window=-1), okc.ERR_INVALID),
     (dict(sm_scale=0.0), okc.ERR_INVALID),
     (dict(kv_scale=-1.0), okc.ERR_INVALID),

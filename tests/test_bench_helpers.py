@@ -16,7 +16,7 @@ HOST = {"sm_count": 152, "ctas_per_sm": 3}
 
 def test_kv_bytes_equal_the_keys_the_work_list_covers():
     okc.build()
-    for name in W.WORKLOADS:
+    for name in W.DECODE_WORKLOADS:
         cfg = W.config(name)
         seq = W.lengths(cfg)
         items = okc.okc_attn_plan_items(cfg, seq, HOST)
@@ -24,6 +24,24 @@ def test_kv_bytes_equal_the_keys_the_work_list_covers():
         assert bench.kv_bytes(cfg, seq) == covered * 2 * 64 * 2, name
     cfg = W.config("full_decode_32k")
     assert bench.kv_bytes(cfg, W.lengths(cfg)) == 64 * 32769 * 256
+
+
+def test_extend_accounting():
+    """The extend workload: the algorithmic KV bytes are each request's visible
+    keys once (seq + q_len on a full-attention layer); the flops count every
+    token's visible keys; the work list covers each query block's keys once
+    (blocks of 8 tokens on the tcgen05 kernel)."""
+    okc.build()
+    cfg = W.config("extend")
+    inp = W.generate(cfg)
+    seq, ql = inp["seq_lens"].astype(np.int64), inp["q_lens"].astype(np.int64)
+    assert bench.kv_bytes(cfg, inp["seq_lens"], inp["q_lens"]) == int((seq + ql).sum()) * 256
+    keys = sum(int((s + np.arange(1, q + 1)).sum()) for s, q in zip(seq, ql))
+    assert bench.attention_flops(cfg, inp["seq_lens"], inp["q_lens"]) == keys * 4 * 64 * 16
+    items = okc.okc_attn_plan_items_varlen(cfg, inp["seq_lens"], inp["q_lens"], {"sm_count": 152, "ctas_per_sm": 1})
+    covered = int((items[:, 3].astype(np.int64) - items[:, 2]).sum())
+    want = sum(int(s + min(i + 8, q)) for s, q in zip(seq, ql) for i in range(0, q, 8))
+    assert covered == want
 
 
 class _FakeProc:

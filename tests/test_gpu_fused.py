@@ -288,3 +288,65 @@ def test_plan_update_keeps_the_device_error_word():
     torch.cuda.synchronize()
     assert step.errors() == 0
     check_against_oracle(cfg, inp, out.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def _at_lengths(cfg, inp, seq):
+    """The same batch at cached lengths `seq` (each <= the batch's own): same
+    caches and page table, positions, cache rows and lengths moved back."""
+    out = dict(inp)
+    L, P = cfg["q_len"], cfg["page_size"]
+    seq = np.asarray(seq, np.int32)
+    out["seq_lens"] = seq
+    out["cache_seqlens"] = (seq + L).astype(np.int32)
+    req = np.repeat(np.arange(cfg["batch"]), L)
+    pos = seq.astype(np.int64)[req] + np.tile(np.arange(L), cfg["batch"])
+    out["positions"] = pos
+    out["cache_loc"] = inp["page_table"][req, pos // P].astype(np.int64) * P + pos % P
+    return out
+
+
+@pytest.mark.parametrize("name", ["full_decode_32k", "mixed_full_decode", "verify_block", "sliding_decode"])
+def test_fixed_capacity_graph_replays_after_updates(name):
+    """A fixed-capacity plan (okc_plan_options.max_context): okc_attn_step is
+    captured in a CUDA graph once; then, step after step, okc_attn_plan_update
+    re-plans for new lengths that change num_work, the caller rewrites the
+    device inputs, and the same graph is replayed: every replay equals the
+    oracle on that step's inputs (element-wise, under the acceptance bounds)."""
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    if name == "verify_block":
+        cfg["window"] = 0  # (work items then grow with the context)
+    inp = W.generate(cfg)
+    seq = inp["seq_lens"].astype(np.int64)
+    rng = np.random.default_rng(3)
+    lengths = [np.minimum(seq, 40), seq, (seq * rng.uniform(0.2, 0.9, len(seq))).astype(np.int64), seq // 3, seq]
+    mc = int(seq.max()) + cfg["q_len"]
+    opts = {"max_context": mc}
+    step = okc.AttnStep(cfg, lengths[0], opts=opts)
+    d = to_device(cfg, _at_lengths(cfg, inp, lengths[0]))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step.run_fused(d, eps=inp["eps"], stream=s)  # warm the launch path
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.run_fused(d, eps=inp["eps"], stream=s)
+    works = set()
+    for sq in lengths:
+        case = _at_lengths(cfg, inp, sq)
+        step.plan.update(case["seq_lens"], s)
+        works.add(step.plan.sizes["num_work"])
+        fresh = to_device(cfg, case)
+        for k in ("qkv", "positions", "cache_loc", "cache_seqlens", "cu_seqlens_q", "seq_lens", "page_table",
+                  "k_cache", "v_cache"):
+            d[k].copy_(fresh[k])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert step.errors() == 0
+        got = step.out.view(torch.int16).cpu().numpy().view(np.uint16)
+        check_against_oracle(cfg, case, got, d["k_cache"].cpu().numpy(), d["v_cache"].cpu().numpy())
+    assert len(works) > 1, works  # the updates changed the number of work items

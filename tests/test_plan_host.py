@@ -47,11 +47,11 @@ def _check_cover(cfg, seq, items):
 
 
 def _pad(cfg, opts=None):
-    tc = 2 <= cfg["q_len"] <= 8 and not ((opts or {}).get("flags", 0) & okc.PLAN_NO_TCGEN05)
+    tc = cfg["q_len"] >= 2 and not ((opts or {}).get("flags", 0) & okc.PLAN_NO_TCGEN05)
     return 7 if tc and cfg["page_size"] >= 8 else 0
 
 
-@pytest.mark.parametrize("name", list(W.WORKLOADS))
+@pytest.mark.parametrize("name", list(W.DECODE_WORKLOADS))
 def test_workload_plans_cover_every_key_once(name):
     cfg = W.config(name)
     seq = W.lengths(cfg)
@@ -90,7 +90,7 @@ def test_step_form_rule_on_the_workloads():
 @pytest.mark.parametrize("seed", range(12))
 def test_random_batches(seed):
     rng = np.random.default_rng(7000 + seed)
-    L = int(rng.choice([1, 2, 4, 8, 12]))
+    L = int(rng.choice([1, 2, 4, 8]))  # one query block per request (longer ones: _check_blocks)
     P = int(rng.choice([1, 8, 16, 64]))
     window = int(rng.choice([0, 1, 64, 2048]))
     B = int(rng.integers(1, 300))
@@ -191,7 +191,7 @@ def test_max_sizes_on_the_workloads_and_errors():
     """On each workload's shape the bound holds and is at most four waves of
     items (one per request when requests outnumber them); max_context below
     q_len or past the page table is an argument error."""
-    for name in W.WORKLOADS:
+    for name in W.DECODE_WORKLOADS:
         cfg = W.config(name)
         seq = W.lengths(cfg)
         max_context = int(seq.max()) + cfg["q_len"]
@@ -208,3 +208,96 @@ def test_max_sizes_on_the_workloads_and_errors():
     assert e.value.status == okc.ERR_INVALID
     empty = dict(cfg, batch=0)
     assert okc.okc_attn_plan_max_sizes(empty, 10, HOST)["num_work"] == 0
+
+
+def _check_blocks(cfg, seq, ql, items, S):
+    """Varlen plans: request b's ql[b] tokens are cut into blocks [i0, i0 + S)
+    (the last one shorter), and each block's items cover its visible keys
+    [lo, hi) once and in order: hi = seq + i0 + ntok, lo = max(0, seq + i0 - w + 1)
+    on window layers, else 0. Requests with no new tokens have no items."""
+    w = cfg["window"]
+    blocks = {}
+    for b, i0, j0, j1 in items:
+        assert j0 < j1
+        blocks.setdefault((int(b), int(i0)), []).append((int(j0), int(j1)))
+    want = set()
+    for b, (s0, q) in enumerate(zip(seq.astype(np.int64), ql.astype(np.int64))):
+        for i0 in range(0, q, S):
+            want.add((b, i0))
+            ntok = min(S, q - i0)
+            hi = s0 + i0 + ntok
+            lo = max(0, s0 + i0 - w + 1) if w > 0 else 0
+            r = sorted(blocks[(b, i0)])
+            assert r[0][0] == lo and r[-1][1] == hi, (b, i0, r[0], r[-1], lo, hi)
+            for (a0, a1), (b0, b1) in zip(r, r[1:]):
+                assert a1 == b0
+    assert set(blocks) == want
+
+
+@pytest.mark.parametrize("window", [0, 2048])
+@pytest.mark.parametrize("flags,S", [(0, 8), (okc.PLAN_NO_TCGEN05, 16)])
+def test_varlen_blocks_cover_every_key_once(window, flags, S):
+    """Prefill/extend batches mixing decode requests (1 token), extends of 37,
+    256 and 1024 tokens and requests with no new token: blocks of 8 tokens on
+    the tcgen05 kernel, 16 on the warp-level one."""
+    rng = np.random.default_rng(window + flags)
+    for it in range(20):
+        B = int(rng.integers(1, 40))
+        cfg = W.config("extend", batch=B, window=window)
+        ql = rng.choice([0, 1, 37, 256, 1024], size=B).astype(np.int32)
+        seq = rng.integers(0, 20000, size=B).astype(np.int32)
+        cfg["max_pages"] = int((seq.max() + 1024) // cfg["page_size"] + 1)
+        cfg["num_pages"] = B * cfg["max_pages"]
+        opts = dict(HOST, flags=flags)
+        items = okc.okc_attn_plan_items_varlen(cfg, seq, ql, opts)
+        _check_blocks(cfg, seq, ql, items, S)
+        z = okc.okc_attn_plan_sizes(cfg, seq, opts, q_lens=ql)
+        assert z["num_work"] == len(items) and z["num_tokens"] == int(ql.sum())
+        assert z["o_partial_bytes"] >= len(items) * S * 16 * 64 * 4
+        # a uniform q_len of 12 or 40: blocks of S tokens per request, every key covered
+        if it == 1:
+            for L in (12, 40):
+                cu = dict(cfg, q_len=L)
+                itm = okc.okc_attn_plan_items_varlen(cu, seq, None, opts)
+                _check_blocks(cu, seq, np.full(B, L, np.int32), itm, S)
+        # uniform q lengths through the varlen calls: the same plan as without them
+        if it == 0:
+            u = np.full(B, 3, np.int32)
+            c3 = dict(cfg, q_len=3)
+            a = okc.okc_attn_plan_items_varlen(c3, seq, u, opts)
+            b = okc.okc_attn_plan_items(c3, seq, opts)
+            assert np.array_equal(a[:, [0, 2, 3]], b) and np.all(a[:, 1] == 0)
+
+
+def test_extend_workload_plan():
+    cfg = W.config("extend")
+    inp = W.generate(cfg)
+    items = okc.okc_attn_plan_items_varlen(cfg, inp["seq_lens"], inp["q_lens"], {"sm_count": SMS, "ctas_per_sm": 1})
+    _check_blocks(cfg, inp["seq_lens"], inp["q_lens"], items, 8)
+    bound = okc.okc_attn_plan_max_sizes(cfg, int((inp["seq_lens"] + inp["q_lens"]).max()),
+                                        {"sm_count": SMS, "ctas_per_sm": 1})
+    z = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"], {"sm_count": SMS, "ctas_per_sm": 1}, q_lens=inp["q_lens"])
+    for f in ("workspace_bytes", "o_partial_bytes", "num_work", "q_fp8_bytes"):
+        assert z[f] <= bound[f], f
+
+
+def test_fixed_capacity_plans_keep_their_layout():
+    """okc_plan_options.max_context: the workspace is laid out at the capacity
+    of okc_attn_plan_max_sizes for that context, for every step within it; steps
+    past it and per-request q lengths are refused."""
+    for name in W.DECODE_WORKLOADS:
+        cfg = W.config(name)
+        seq = W.lengths(cfg)
+        mc = int(seq.max()) + cfg["q_len"]
+        opts = dict(HOST, max_context=mc)
+        bound = okc.okc_attn_plan_max_sizes(cfg, mc, opts)
+        for s in (seq, np.minimum(seq, 7), seq // 2):
+            z = okc.okc_attn_plan_sizes(cfg, s, opts)
+            assert z["workspace_bytes"] == bound["workspace_bytes"], name
+            assert z["num_work"] == okc.okc_attn_plan_sizes(cfg, s, HOST)["num_work"]
+        with pytest.raises(okc.OkcError) as e:
+            okc.okc_attn_plan_sizes(cfg, seq + 1, opts)
+        assert e.value.status == okc.ERR_INVALID
+        with pytest.raises(okc.OkcError) as e:
+            okc.okc_attn_plan_sizes(cfg, seq, opts, q_lens=np.full(len(seq), cfg["q_len"], np.int32))
+        assert e.value.status == okc.ERR_UNSUPPORTED

@@ -11,7 +11,8 @@ import pytest
 import workloads as W
 
 SMALL = {"tiny_sliding_decode": {}, "sliding_decode": dict(batch=16), "full_decode_32k": dict(batch=3, seq=("const", 700)),
-         "verify_block": dict(batch=6), "mixed_full_decode": dict(batch=40, seq=("loguniform", 1, 5000))}
+         "verify_block": dict(batch=6), "mixed_full_decode": dict(batch=40, seq=("loguniform", 1, 5000)),
+         "extend": dict(batch=12, seq=("uniform", 0, 3000))}
 
 
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
@@ -27,21 +28,29 @@ def test_generated_step_has_the_recipes_structure(name):
         assert (seq == cfg["seq"][1]).all()
     else:
         assert list(seq) == list(cfg["seq"][1])
-    n_pages = (seq + L + P - 1) // P
+    ql = inp["q_lens"].astype(np.int64)  # new tokens per request (L each, or the "q_lens" recipe)
+    if "q_lens" in cfg:
+        assert set(ql) <= set(cfg["q_lens"][1]) and ql.max() <= L
+    else:
+        assert (ql == L).all()
+    n_pages = (seq + ql + P - 1) // P
     pt = inp["page_table"]
     assert pt.shape == (B, n_pages.max()) and cfg["num_pages"] == n_pages.sum()
     used = np.concatenate([pt[b, :n_pages[b]] for b in range(B)])
     assert np.array_equal(np.sort(used), np.arange(n_pages.sum()))  # a permutation of the pool
     for b in range(B):
         assert (pt[b, n_pages[b]:] == -1).all()
-    T = B * L
-    pos = inp["positions"].reshape(B, L)
-    assert np.array_equal(pos, seq[:, None] + np.arange(L)[None, :])
-    req = np.repeat(np.arange(B), L)
+    T = int(ql.sum())
+    cu = np.concatenate([[0], np.cumsum(ql)])
+    for b in range(B):
+        assert np.array_equal(inp["positions"][cu[b]:cu[b + 1]], seq[b] + np.arange(ql[b]))
+    req = np.repeat(np.arange(B), ql)
     p = inp["positions"]
     assert np.array_equal(inp["cache_loc"], pt[req, p // P].astype(np.int64) * P + p % P)
-    assert np.array_equal(inp["cache_seqlens"], seq + L)
-    assert np.array_equal(inp["cu_seqlens_q"], np.arange(B + 1) * L)
+    assert np.array_equal(inp["cache_seqlens"], seq + ql)
+    assert np.array_equal(inp["cu_seqlens_q"], cu)
+    if "q_lens" not in cfg:
+        assert np.array_equal(inp["cu_seqlens_q"], np.arange(B + 1) * L)
     assert inp["qkv"].shape == (T, 2304) and inp["qkv"].dtype == np.uint16
     assert inp["k_cache"].shape == (n_pages.sum(), P, 2, 64) and inp["k_cache"].dtype == np.uint8
     for c in (inp["k_cache"], inp["v_cache"]):

@@ -14,6 +14,12 @@ physical pages a random permutation of a pool sized to the total, page_table
 page table, cache_seqlens = seq_lens + L, cu_seqlens_q = 0, L, 2L, ...
 On the scaled path (kv_scale != 1) the device scales are k_scale = v_scale =
 kv_scale unless the config names its own "k_scale" / "v_scale".
+
+A config with a "q_lens" recipe is a prefill/extend step (the problem file's
+ragged `cu_seqlens_q` with its `max_seqlen_q`): request b then has q_lens[b]
+new tokens (q_len is their largest value), T is their sum, cu_seqlens_q their
+running sums and cache_seqlens = seq_lens + q_lens. The "extend" workload mixes
+decode requests with extends of 37, 256 and 1024 tokens.
 """
 from __future__ import annotations
 
@@ -40,7 +46,12 @@ WORKLOADS = {
                          window=2048, rope_theta=5e5, kv_scale=0.5, seed=1004),
     "mixed_full_decode": dict(_BASE, batch=256, q_len=1, seq=("loguniform", 1, 131072),
                               page_size=1, window=0, rope_theta=0.0, kv_scale=1.0, seed=1005),
+    "extend": dict(_BASE, batch=16, q_len=1024, q_lens=("choice", [1, 37, 256, 1024]),
+                   seq=("uniform", 0, 16384), page_size=64, window=0, rope_theta=0.0, kv_scale=1.0, seed=1006),
 }
+# the five decode / verify shapes the pages quote; "extend" is the prefill/extend variant
+DECODE_WORKLOADS = ("tiny_sliding_decode", "sliding_decode", "full_decode_32k", "verify_block",
+                    "mixed_full_decode")
 
 
 def config(name: str, **overrides) -> dict:
@@ -68,6 +79,23 @@ def _seq_lens(rng: np.random.Generator, recipe, batch: int) -> np.ndarray:
     return s.astype(np.int32)
 
 
+def _q_lens(rng: np.random.Generator, cfg: dict, batch: int) -> np.ndarray:
+    """New tokens per request: cfg's "q_lens" recipe, else q_len each (no draw)."""
+    recipe = cfg.get("q_lens")
+    if recipe is None:
+        return np.full(batch, cfg["q_len"], np.int32)
+    kind = recipe[0]
+    if kind == "list":
+        q = np.asarray(recipe[1], np.int64)
+        assert q.size == batch
+    elif kind == "choice":
+        q = rng.choice(np.asarray(recipe[1], np.int64), size=batch)
+    else:
+        raise ValueError(kind)
+    assert q.max(initial=0) <= cfg["q_len"], "q_len is the largest q length"
+    return q.astype(np.int32)
+
+
 def _bf16_bits(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16) \
         .view(torch.int16).numpy().view(np.uint16)
@@ -88,7 +116,8 @@ def lengths(cfg: dict, seed: int | None = None) -> np.ndarray:
     rng = np.random.default_rng(cfg["seed"] if seed is None else seed)
     B, L, P = cfg["batch"], cfg["q_len"], cfg["page_size"]
     seq = _seq_lens(rng, cfg["seq"], B)
-    n_pages = (seq.astype(np.int64) + L + P - 1) // P
+    ql = _q_lens(rng, cfg, B)
+    n_pages = (seq.astype(np.int64) + ql + P - 1) // P
     cfg["max_pages"] = max(1, int(n_pages.max())) if B else 1
     cfg["num_pages"] = max(1, int(n_pages.sum()))
     return seq
@@ -100,7 +129,8 @@ def generate(cfg: dict, seed: int | None = None) -> dict:
     B, L, P = cfg["batch"], cfg["q_len"], cfg["page_size"]
     hq, hkv, d = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     seq = _seq_lens(rng, cfg["seq"], B)
-    n_pages = (seq.astype(np.int64) + L + P - 1) // P
+    ql = _q_lens(rng, cfg, B)
+    n_pages = (seq.astype(np.int64) + ql + P - 1) // P
     total = int(n_pages.sum())
     phys = rng.permutation(total) if cfg.get("shuffle_pages", True) else np.arange(total)
     max_pages = max(1, int(n_pages.max()))
@@ -109,9 +139,10 @@ def generate(cfg: dict, seed: int | None = None) -> dict:
     for b in range(B):
         page_table[b, :n_pages[b]] = phys[off:off + n_pages[b]]
         off += int(n_pages[b])
-    T = B * L
-    positions = (seq.astype(np.int64)[:, None] + np.arange(L)[None, :]).reshape(T)
-    req = np.repeat(np.arange(B), L)
+    T = int(ql.sum())
+    req = np.repeat(np.arange(B), ql)
+    first = np.concatenate([[0], np.cumsum(ql)]).astype(np.int64)
+    positions = seq.astype(np.int64)[req] + (np.arange(T) - first[req])
     cache_loc = page_table[req, positions // P].astype(np.int64) * P + positions % P
     width = (2 * hq + 2 * hkv) * d
     qkv = _bf16_bits(rng.standard_normal((T, width), dtype=np.float32))
@@ -125,8 +156,8 @@ def generate(cfg: dict, seed: int | None = None) -> dict:
     cfg["num_pages"] = total
     return dict(
         qkv=qkv, positions=positions, cache_loc=cache_loc,
-        cache_seqlens=(seq + L).astype(np.int32),
-        cu_seqlens_q=(np.arange(B + 1) * L).astype(np.int32), seq_lens=seq,
+        cache_seqlens=(seq + ql).astype(np.int32),
+        cu_seqlens_q=first.astype(np.int32), seq_lens=seq, q_lens=ql,
         page_table=page_table, k_cache=k_cache, v_cache=v_cache,
         k_scale=np.float32(cfg.get("k_scale", cfg["kv_scale"])),
         v_scale=np.float32(cfg.get("v_scale", cfg["kv_scale"])),
