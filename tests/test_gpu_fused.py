@@ -325,7 +325,7 @@ def test_fixed_capacity_graph_replays_after_updates(name):
     mc = int(seq.max()) + cfg["q_len"]
     opts = {"max_context": mc}
     step = okc.AttnStep(cfg, lengths[0], opts=opts)
-    d = to_device(cfg, _at_lengths(cfg, inp, lengths[0]))
+    d = to_device(cfg, _at_lengths(cfg, inp, lengths[0]), rope_positions=mc)  # a table for every step
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
