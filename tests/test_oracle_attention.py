@@ -34,18 +34,23 @@ def _dense_reference(cfg, inp, q8, k_cache, v_cache):
     vc = v_cache.reshape(-1, HKV, D)
     out = np.zeros((q8.shape[0], HQ, D))
     lse = np.zeros((q8.shape[0], HQ))
+    # request b's new tokens: rows t0 .. t0 + ql - 1 (ql = L each unless q_lens says otherwise)
+    q_lens = inp.get("q_lens") if "q_lens" in cfg else None
+    t0 = 0
     for b in range(cfg["batch"]):
+        ql = L if q_lens is None else int(q_lens[b])
         n = int(inp["cache_seqlens"][b])
         rows = [inp["page_table"][b, j // P] * P + j % P for j in range(n)]
         K = oracle.e4m3_value(kc[rows]) * ks          # [n, Hkv, D]
         V = oracle.e4m3_value(vc[rows]) * vs
-        pos = n - L + np.arange(L)                    # query positions
+        pos = n - ql + np.arange(ql)                  # query positions
         j = np.arange(n)
         allowed = j[None, :] <= pos[:, None]
         if w > 0:
             allowed &= j[None, :] >= pos[:, None] - w + 1
-        for i in range(L):
-            t = b * L + i
+        t_first, t0 = t0, t0 + ql
+        for i in range(ql):
+            t = t_first + i
             Q = oracle.e4m3_value(q8[t])              # [Hq, D]
             for h in range(HQ):
                 g = h // (HQ // HKV)
@@ -71,6 +76,24 @@ def test_matches_dense_brute_force(L, P, window, seq, kv_scale, q_norm=0):
     if kv_scale != 1.0:
         inp["k_scale"] = np.float32(kv_scale)
         inp["v_scale"] = np.float32(kv_scale * 1.5)
+    k = inp["k_cache"].copy(); v = inp["v_cache"].copy()
+    q8, _ = oracle.prepare(cfg, inp, k, v)
+    o, lse, bad = oracle.attention(cfg, inp, q8, k, v, want_lse=True)
+    ref, ref_lse = _dense_reference(cfg, inp, q8, k, v)
+    assert bad == 0
+    assert np.max(np.abs(o - ref)) < 1e-12
+    assert np.max(np.abs(lse - ref_lse)) < 1e-10
+
+
+@pytest.mark.parametrize("window", [0, 4])
+def test_ragged_batch_matches_dense_brute_force(window):
+    """Per-request q lengths (ragged cu_seqlens_q, a request with none among
+    them): each request's tokens at rows cu_seqlens_q[b].., causal over its
+    own earlier keys; equal to the dense definition."""
+    cfg = W.config("tiny_sliding_decode", batch=4, q_len=6, q_lens=("list", [3, 0, 6, 1]), page_size=2,
+                   window=window, seq=("list", [5, 2, 0, 9]), rope_theta=5e5)
+    inp = W.generate(cfg)
+    assert list(inp["cu_seqlens_q"]) == [0, 3, 3, 9, 10]
     k = inp["k_cache"].copy(); v = inp["v_cache"].copy()
     q8, _ = oracle.prepare(cfg, inp, k, v)
     o, lse, bad = oracle.attention(cfg, inp, q8, k, v, want_lse=True)

@@ -48,6 +48,10 @@ MUTANTS = [
      [lambda: TA.test_matches_dense_brute_force(1, 4, 3, (6, 16), 0.5)]),
     ("sigmoid_sign", "1.0 / (1.0 + exp(-g))", "1.0 / (1.0 + exp(g))",
      [TA.test_normgate_saturated_gate_is_plain_rmsnorm]),
+    # (mistakes that stay inside the arrays: a mutant runs in the test's process)
+    ("ragged_rows_reversed", "const int64_t t = cu_seqlens_q[b] + i;",
+     "const int64_t t = cu_seqlens_q[b + 1] - 1 - i;",
+     [lambda: TA.test_ragged_batch_matches_dense_brute_force(0)]),
     # the scaled cache path ("012-attention-local-splits.py", `_prepare_qkv`, `if SCALED:`)
     ("k_divided_by_v_scale", "(key / k_scale)", "(key / v_scale)",
      [TP.test_scaled_cache_codes_from_the_definition]),
