@@ -58,10 +58,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("sliding_decode", "decode_kernel<fused step>"): 33.0816e6 + 8.96e3,
-    ("verify_block", "decode_tc_kernel"): 17.207808e6 + 0.0,
-    ("full_decode_32k", "decode_kernel"): 545.487872e6 + 3.411968e6,
-    ("mixed_full_decode", "decode_kernel<fused step>"): 803.03872e6 + 7.589632e6,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 803068416 + 6998272,
+    ("sliding_decode", "decode_kernel<fused step>"): 33095168 + 1536,
+    ("full_decode_32k", "decode_kernel"): 545486336 + 3203584,
+    ("verify_block", "decode_tc_kernel"): 17212416 + 0,
+    ("extend", "decode_tc_kernel"): 36406784 + 22272,
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0
