@@ -468,6 +468,8 @@ class Bench:
         if args.step_form != "plan":
             plan_opts["flags"] = okc.PLAN_STEP_ONE_LAUNCH if args.step_form == "one" else \
                 okc.PLAN_STEP_THREE_LAUNCHES
+        if args.early_gather:
+            plan_opts["flags"] = plan_opts.get("flags", 0) | okc.PLAN_EARLY_GATHER
         plan_opts = plan_opts or None
         step = okc.AttnStep(cfg, inp["seq_lens"], opts=plan_opts, q_lens=ql)
         fused = args.path == "fused"
@@ -582,6 +584,8 @@ def main():
                     help="keys per split work item (plan option; 0 = the plan's heuristic)")
     ap.add_argument("--step-form", default="plan", choices=["plan", "one", "three"],
                     help="okc_attn_step as one kernel or three (plan option; default: the plan's choice)")
+    ap.add_argument("--early-gather", action="store_true",
+                    help="plan flag OKC_PLAN_EARLY_GATHER (consecutive steps run on different input sets)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -23,6 +23,7 @@ __all__ = ["build", "load", "OkcError", "Plan", "okc_attn_plan", "okc_attn_plan_
            "okc_attn_decode_combine_noalloc", "okc_selftest_bounded_wait", "okc_attn_step", "okc_attn_step_host", "HostStepIO", "STEP_IO",
            "DEVERR_CACHE_LOC", "DEVERR_POSITION", "DEVERR_PAGE", "DEVERR_LENGTHS", "DEVERR_TIMEOUT",
            "PLAN_NO_PDL", "PLAN_NO_TCGEN05", "PLAN_STEP_ONE_LAUNCH", "PLAN_STEP_THREE_LAUNCHES",
+           "PLAN_EARLY_GATHER",
            "QNORM_BF16", "QNORM_FOLDED_SCALE",
            "EXPORTED_SYMBOLS"]
 
@@ -32,6 +33,7 @@ PLAN_NO_PDL = 0x1
 PLAN_NO_TCGEN05 = 0x2
 PLAN_STEP_ONE_LAUNCH = 0x4
 PLAN_STEP_THREE_LAUNCHES = 0x8
+PLAN_EARLY_GATHER = 0x10
 QNORM_BF16, QNORM_FOLDED_SCALE = 0, 1
 
 EXPORTED_SYMBOLS = [

@@ -201,9 +201,17 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   }
   const int b = wk.b;
 
-  if constexpr (FUSED) {  // the first kernel of the step: its predecessor may write any input
-    pdl_wait();
-    pdl_launch_dependents();
+  if constexpr (FUSED) {
+    // The first kernel of the step: its predecessor may write any input, so by
+    // default everything waits for it. Under OKC_PLAN_EARLY_GATHER the caller
+    // promises that the preceding kernels write neither the page table, the
+    // lengths, nor any cache row this step reads: then the lengths, the page ids
+    // and the already-cached keys are loaded before the wait, and only the
+    // consumers wait (q, the new K/V rows and every global write come after it).
+    if (!a.early) {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
     // the gate logits and norm weight the merge reads at the end: into L2 now
     // (the block's first token under the plan's q lengths)
     if (tid < 16) prefetch_l2(a.qkv + (int64_t)wk.t0 * kQkvWidth + kGateCol + tid * 64);
@@ -251,10 +259,12 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     if (qb < 0 || qb + ql > a.T) ql = 0;
     n = max(ql, min(n, a.max_pages * P));
   }
-  // this block's tokens i0 .. i0 + nt - 1 of the request, at positions pbase + tok
-  const int ntk = max(0, min(a.S, ql - wk.i0));
-  if (ntk != wk.ntok || (wk.last && wk.i0 + ntk < ql)) bad_len = true;  // q lengths differ from the plan's
-  const int pbase = n - ql + wk.i0;
+  // this block's tokens i0 .. i0 + ntk - 1 of the request, at positions pbase + tok
+  // (blocks of one token start at the request's first: i0 = 0)
+  const int i0 = (KS > 1) ? 0 : wk.i0;
+  const int ntk = max(0, min(a.S, ql - i0));
+  if (ntk != wk.ntok || (wk.last && i0 + ntk < ql)) bad_len = true;  // q lengths differ from the plan's
+  const int pbase = n - ql + i0;
   const int hi = pbase + ntk;                                           // keys < hi
   const int lo = a.window > 0 ? max(0, pbase - a.window + 1) : 0;     // first key any query sees
   const int j0 = lo + wk.chunk * wk.chunk_keys;
@@ -273,7 +283,11 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
     const int pmask = P - 1;
     const int newk = n - ql;  // keys >= newk are written by the prepare kernel (three-call path)
     const int rr = lane >> 3, ch = lane & 7;
-    bool dep = FUSED, bad_page = false;  // the fused step has waited already
+    // no wait before a tile: the three-call decode waits for the prepare kernel
+    // before a tile holding one of the step's new keys; the fused step computes
+    // those keys itself (the gathered row is replaced), having waited already or
+    // needing no wait (OKC_PLAN_EARLY_GATHER)
+    bool dep = FUSED, bad_page = false;
     auto issue = [&](int k, const int (&id)[kIds]) {
       const int s = k % kStages;
       const uint32_t sK = sbase + s * kStageSmem, sV = sK + kTileSmem;
@@ -339,10 +353,14 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   bool pos_err = false;
   uint32_t qf[NTW][2][2];
   if constexpr (FUSED) {
+    if (a.early) {  // qkv and the outputs: after the predecessor has finished
+      pdl_wait();
+      pdl_launch_dependents();
+    }
 #pragma unroll
     for (int nt = 0; nt < NTW; nt++) {
       const int tok = tok0 + nt;
-      fused_q_frag(a, (int64_t)qb + wk.i0 + (tok < ntk ? tok : 0), g * kGroup + gq, tq, tok < ntk, qf[nt], pos_err);
+      fused_q_frag(a, (int64_t)qb + i0 + (tok < ntk ? tok : 0), g * kGroup + gq, tq, tok < ntk, qf[nt], pos_err);
     }
   } else {
     pdl_wait();  // q_fp8 is the prepare kernel's output
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
     for (int nt = 0; nt < NTW; nt++) {
       const int tok = tok0 + nt;
-      const uint8_t* qrow = a.q8 + ((int64_t)(qb + wk.i0 + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
+      const uint8_t* qrow = a.q8 + ((int64_t)(qb + i0 + tok) * kNumQHeads + g * kGroup + gq) * kHeadDim;
 #pragma unroll
       for (int kk = 0; kk < 2; kk++) {
         qf[nt][kk][0] = tok < ntk ? *reinterpret_cast<const uint32_t*>(qrow + kk * 32 + tq * 4) : 0u;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       const int whi = min(j1, wlo + C::kMTiles * 16);
       const bool writer = (KS > 1) || sub == 0;
       for (int j = max(wlo, pbase); j < whi; j++) {
-        const int64_t t = (int64_t)qb + wk.i0 + (j - pbase);
+        const int64_t t = (int64_t)qb + i0 + (j - pbase);
         uint16_t k8, v8;
         fused_new_kv(a, t, g, lane, k8, v8, pos_err);
         const int r = j - tile_j;
@@ -619,7 +637,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       // through the barrier); for the last CTA the acquire orders the other
       // splits' partials before the merge's reads (the barrier below)
       int prev;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + wk.blk) : "memory");
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + b) : "memory");
       s_last = prev == wk.nchunks - 1;
     }
     named_bar_sync(1, NCW * 32);
@@ -627,7 +645,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
       const int64_t base_lse = (int64_t)wk.wbase * rows;
       for (int rowi = tid >> 3; rowi < ntk * kNumQHeads; rowi += NCW * 4) {  // 8 lanes per row
         const int tok = rowi / kNumQHeads, h = rowi % kNumQHeads;
-        const int64_t t = (int64_t)qb + wk.i0 + tok;
+        const int64_t t = (int64_t)qb + i0 + tok;
         const int c0 = (tid & 7) * 8;
         float gg[8], ww[8];
         load_gate_weight(a.qkv, a.weight, (int)t, h, c0, gg, ww);
@@ -635,7 +653,7 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
                        a.o_part + (base_lse + rowi) * kHeadDim + c0, (int64_t)rows * kHeadDim, wk.nchunks, gg,
                        ww, a.eps, a.out + t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
       }
-      if (tid == 0) a.tickets[wk.blk] = 0;
+      if (tid == 0) a.tickets[b] = 0;
     }
   }
 }

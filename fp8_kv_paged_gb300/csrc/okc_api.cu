@@ -306,7 +306,7 @@ void sizes_for(const okc_attn_config* c, int64_t W, int64_t cap, int64_t NB, int
   const int64_t rows = (int64_t)S * c->num_q_heads;
   std::memset(z, 0, sizeof *z);
   z->workspace_bytes = okc::kWsHeader + round_up(cap * sizeof(WorkItem)) + round_up(NB * sizeof(BlockInfo)) +
-                       round_up(NB * sizeof(int32_t)) +               // + the one-launch step's arrival counters
+                       round_up(c->batch * sizeof(int32_t)) +         // + the one-launch step's arrival counters
                        round_up(T * c->num_q_heads * c->head_dim);  // + q for the three-launch step
   z->q_fp8_bytes = round_up(T * c->num_q_heads * c->head_dim);
   z->o_partial_bytes = round_up(W * rows * c->head_dim * sizeof(float));
@@ -426,7 +426,9 @@ void set_splits(okc_attn_plan_s* p, SplitResult& s, const okc_attn_sizes& z) {
   p->d_blk = reinterpret_cast<BlockInfo*>(ws + okc::kWsHeader + round_up(cap * sizeof(WorkItem)));
   p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_blk) +
                                             round_up(p->blocks.size() * sizeof(BlockInfo)));
-  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up(p->blocks.size() * sizeof(int32_t));
+  // (one arrival counter per request: the one-kernel step runs blocks of one token,
+  // at most one per request)
+  p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up((size_t)p->cfg.batch * sizeof(int32_t));
 }
 
 // Bytes of the workspace head the plan uploads (everything before q).
@@ -687,7 +689,7 @@ okc_status okc_attn_plan_update_varlen(okc_attn_plan_t plan, const int32_t* seq_
   if (plan->workspace_bytes < z.workspace_bytes) return restore(OKC_ERR_WORKSPACE);
   const size_t cap = plan->work_cap > 0 ? (size_t)plan->work_cap : s.work.size();
   const size_t up_bytes = okc::kWsHeader + round_up(cap * sizeof(WorkItem)) + round_up(s.blocks.size() * sizeof(BlockInfo)) +
-                          round_up(s.blocks.size() * sizeof(int32_t));
+                          round_up((size_t)plan->cfg.batch * sizeof(int32_t));
   // the staging buffer may still feed the previous update's copy
   if (plan->pinned_done && cudaEventSynchronize(plan->pinned_done) != cudaSuccess) return restore(OKC_ERR_CUDA);
   if (plan->pinned_bytes < up_bytes) {
@@ -974,6 +976,7 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.eps = eps;
   a.q_fold = c.q_norm == OKC_QNORM_FOLDED_SCALE;
   a.q_scale = c.qk_scale_factor;
+  a.early = (plan->opts.flags & OKC_PLAN_EARLY_GATHER) && plan->pdl ? 1 : 0;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   if (plan->sizes.step_kernels == 1) {
     cudaError_t e = okc::launch_step_fused(a, launch_items(plan), plan->pdl, str);

@@ -90,13 +90,15 @@ struct DecodeArgs {
   int32_t rope_positions;
   int32_t rope;
   int64_t num_rows;         // num_pages * page_size
-  int32_t* tickets;         // [blocks] arrival counters, zero between launches
+  int32_t* tickets;         // [B] arrival counters (per request), zero between launches
   const uint16_t* weight;   // norm-gate weight bf16 [64] or null
   uint16_t* out;            // bf16 [T, Hq*64]
   float eps;
   int32_t tc;               // 1: blocks of 2..8 tokens run on the tcgen05 kernel (decode_tc.cu)
   int32_t q_fold;           // as PrepareArgs (the fused step derives q itself)
   float q_scale;
+  int32_t early;            // OKC_PLAN_EARLY_GATHER: the fused step loads lengths, page ids and
+                            // cached keys before the programmatic-dependency wait
 };
 
 struct CombineArgs {
@@ -137,7 +139,7 @@ struct okc_attn_plan_s {
   int32_t* d_live;     // the live work-item count in the header
   okc::WorkItem* d_work;
   okc::BlockInfo* d_blk;
-  int32_t* d_tickets;  // the fused step's per-block arrival counters
+  int32_t* d_tickets;  // the fused step's per-request arrival counters
   uint8_t* d_q8;       // q of okc_attn_step when it runs the three kernels
   bool tc;             // decode on the tcgen05 kernel (blocks of 2..8 tokens)
   int device;

@@ -118,7 +118,18 @@ typedef struct okc_plan_options {
                               OKC_PLAN_NO_TCGEN05: q_len >= 2 decodes with the warp-level MMA kernel
                               (blocks of up to 16 tokens) instead of the tcgen05 one;
                               OKC_PLAN_STEP_ONE_LAUNCH / OKC_PLAN_STEP_THREE_LAUNCHES: force the form
-                              of okc_attn_step at q_len 1 (default: chosen by the plan) */
+                              of okc_attn_step at q_len 1 (default: chosen by the plan);
+                              OKC_PLAN_EARLY_GATHER: the caller promises that the kernels launched
+                              before okc_attn_step on its stream write neither page_table, the
+                              length arrays, nor any K/V cache row the step reads (the QKV
+                              projection that precedes the block writes only qkv). The one-kernel
+                              step then loads the lengths and page ids and streams the cached keys
+                              while its predecessor still runs (programmatic dependent launch);
+                              q, the new K/V rows and every write wait for the predecessor as
+                              before. Results are unchanged. A step of the same layer that runs
+                              right after another one on the same caches breaks the promise (it
+                              reads the row the previous step writes): order them with a plain
+                              kernel boundary or leave the flag off. */
   int32_t ctas_per_sm;     /* occupancy the split heuristic assumes; 0 = derived from the kernel */
   int32_t sm_count;        /* SMs the split heuristic assumes; 0 = the current device's. With
                               ctas_per_sm also set, planning (okc_attn_plan_sizes,
@@ -138,6 +149,7 @@ typedef struct okc_plan_options {
 #define OKC_PLAN_NO_TCGEN05 0x2
 #define OKC_PLAN_STEP_ONE_LAUNCH 0x4
 #define OKC_PLAN_STEP_THREE_LAUNCHES 0x8
+#define OKC_PLAN_EARLY_GATHER 0x10
 
 /* Sizes of the buffers a plan needs. All byte counts are multiples of 256. */
 typedef struct okc_attn_sizes {

@@ -350,3 +350,48 @@ def test_fixed_capacity_graph_replays_after_updates(name):
         got = step.out.view(torch.int16).cpu().numpy().view(np.uint16)
         check_against_oracle(cfg, case, got, d["k_cache"].cpu().numpy(), d["v_cache"].cpu().numpy())
     assert len(works) > 1, works  # the updates changed the number of work items
+
+
+@pytest.mark.parametrize("name", ["sliding_decode", "mixed_full_decode", "tiny_sliding_decode"])
+def test_early_gather_steps_back_to_back(name):
+    """OKC_PLAN_EARLY_GATHER: six one-kernel steps captured back to back in one
+    CUDA graph, step i on input set i % 3 (three sets of the same lengths with
+    their own qkv and caches, so no step reads what the step before it writes):
+    each step overlaps its gather with its predecessor, and every output equals
+    the default plan's step on the same set bit for bit, and the oracle's."""
+    import fp8_kv_paged_gb300 as okc
+    import torch
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    cases = [inp]
+    for k in (1, 2):
+        other = W.generate(dict(cfg), seed=cfg["seed"] + 31 * k)
+        cases.append(dict(inp, qkv=other["qkv"], k_cache=np.roll(inp["k_cache"], 7 * k),
+                          v_cache=np.roll(inp["v_cache"], 5 * k)))
+    refs = [run_gpu(cfg, c, fused=True) for c in cases]  # default plan, one kernel, eager
+    flags = okc.PLAN_STEP_ONE_LAUNCH | okc.PLAN_EARLY_GATHER
+    step = okc.AttnStep(cfg, inp["seq_lens"], opts={"flags": flags})
+    sets = [to_device(cfg, c) for c in cases]
+    outs = [torch.empty_like(step.out) for _ in range(6)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step.run_fused(sets[0], eps=inp["eps"], stream=s)  # warm the launch path
+    s.synchronize()
+    sets = [to_device(cfg, c) for c in cases]  # fresh caches
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(6):
+            step.run_fused(sets[i % 3], eps=inp["eps"], out=outs[i], stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert step.errors() == 0
+    for i in range(6):
+        got = outs[i].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, refs[i % 3]["out"]), i
+    for j in range(3):
+        assert np.array_equal(sets[j]["k_cache"].cpu().numpy(), refs[j]["k_cache"])
+        assert np.array_equal(sets[j]["v_cache"].cpu().numpy(), refs[j]["v_cache"])
+    check_against_oracle(cfg, cases[1], outs[1].view(torch.int16).cpu().numpy().view(np.uint16),
+                         sets[1]["k_cache"].cpu().numpy(), sets[1]["v_cache"].cpu().numpy())
