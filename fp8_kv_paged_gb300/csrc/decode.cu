@@ -724,8 +724,8 @@ cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaS
   return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>(a, num_work, pdl, s);
 }
 
-int decode_ctas_per_sm(int S, bool tc) {
-  if (tc) return decode_tc_ctas_per_sm();
+int decode_ctas_per_sm(int S, bool tc, int tc_groups) {
+  if (tc) return decode_tc_ctas_per_sm(tc_groups);
   const int a = occupancy_any(S);
   if (S != 1) return a;
   const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>();

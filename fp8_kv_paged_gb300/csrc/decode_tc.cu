@@ -61,12 +61,8 @@ namespace okc {
 namespace {
 
 constexpr int kTcTileKeys = 64;
-constexpr int kTcStages = 6;
 constexpr int kTcProducers = 2;   // producer warps
 constexpr int kTcRows = 128;      // q rows per CTA (M)
-constexpr int kTcGroups = 2;      // softmax warpgroups
-constexpr int kTcMmaWarp = 4 * kTcGroups;  // warps 0-7 softmax, 8 MMA, 9-10 producers
-constexpr int kTcThreads = (kTcMmaWarp + 1 + kTcProducers) * 32;
 constexpr int kTcVPitch = 144;    // V staging row pitch: conflict-free ldmatrix
 constexpr uint32_t kTcLbo = 128;  // next core matrix along K
 constexpr uint32_t kTcSbo = 1024; // next 8-row group (rows of 128 bytes)
@@ -74,25 +70,44 @@ constexpr uint32_t kTcSbo = 1024; // next 8-row group (rows of 128 bytes)
 #define OKC_TC_RESCALE 0
 #endif
 constexpr float kTcRescale = OKC_TC_RESCALE;  // log2 headroom of the reference max (0: exact max)
-// shared memory
-constexpr int kTcQ = 0;                                              // Q E4M3 [128 x 128 B]
-constexpr int kTcK = kTcQ + kTcRows * 128;                           // K E4M3 [stage][64 x 128 B]
-constexpr int kTcV = kTcK + kTcStages * kTcTileKeys * 128;           // V E4M3 [stage][64 x 144 B]
-constexpr int kTcPvN = 144;                                          // PV's N: 128 dims + the ones column
+constexpr int kTcPvN = 144;                   // PV's N: 128 dims + the ones column
 constexpr int kTcVTBytes = kTcPvN * 128;
-constexpr int kTcVT = kTcV + kTcStages * kTcTileKeys * kTcVPitch;    // [V | 1]^T f16 [group][144 x 64 keys]
-constexpr int kTcX = kTcVT + kTcGroups * kTcVTBytes;                 // group 1's reference max per row
-constexpr int kTcBar = kTcX + kTcRows * 8;
-// barriers: full[S], empty[S], s_ready[2], p_ready[2], pv_done[2], s_free[2], mma_done
-constexpr int kTcTmemSlot = kTcBar + (2 * kTcStages + 4 * kTcGroups + 1) * 8;
-constexpr int kTcSmem = kTcTmemSlot + 16 + 2048;  // + slack past the last operand
-constexpr uint32_t kTcCols = 512;  // TMEM columns: S_j at 64 j (64), O_j at 128 + 160 j (144)
-__host__ __device__ constexpr uint32_t tc_col_s(int j) { return 64u * j; }
-__host__ __device__ constexpr uint32_t tc_col_o(int j) { return 128u + 160u * j; }
-// P_j (f16, two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j
-__host__ __device__ constexpr uint32_t tc_col_p(int j) { return 432u + 32u * j; }
-static_assert(tc_col_o(1) + kTcPvN <= tc_col_p(0) && tc_col_p(1) + 32 <= kTcCols, "TMEM columns");
-static_assert(kTcQ % 1024 == 0 && kTcK % 1024 == 0 && kTcVT % 1024 == 0, "operand alignment");
+// Softmax warpgroups per CTA (chosen by the plan, tc_groups; tile k goes to group
+// k & (NG - 1), its phase is bit 0 of k >> (NG - 1)): 2 (one CTA per SM: 512 TMEM
+// columns, 6 stages, the groups take alternate tiles) or 1 (two CTAs per SM:
+// 256 columns, 4 stages, ~105 KB of shared memory).
+
+// The layout of a CTA with NG softmax warpgroups. Warps 0 .. 4 NG - 1 run the
+// softmax, warp 4 NG issues the MMAs, the next two gather.
+template <int NG>
+struct TcCfg {
+  static constexpr int kStages = NG == 2 ? 6 : 4;
+  static constexpr int kMmaWarp = 4 * NG;
+  static constexpr int kThreads = (kMmaWarp + 1 + kTcProducers) * 32;
+  static constexpr int kMinBlocks = NG == 1 ? 2 : 0;  // __launch_bounds__ minimum (0: none; with 1 the
+                                                      // compiler takes 131 registers instead of 111)
+  // shared memory
+  static constexpr int kQ = 0;                                            // Q E4M3 [128 x 128 B]
+  static constexpr int kK = kQ + kTcRows * 128;                           // K E4M3 [stage][64 x 128 B]
+  static constexpr int kV = kK + kStages * kTcTileKeys * 128;             // V E4M3 [stage][64 x 144 B]
+  static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][144 x 64 keys]
+  static constexpr int kX = kVT + NG * kTcVTBytes;                        // each group's reference max per row
+  static constexpr int kBar = kX + NG * kTcRows * 4;
+  // barriers: full[S], empty[S], s_ready[NG], p_ready[NG], pv_done[NG], s_free[NG], mma_done
+  static constexpr int kTmemSlot = kBar + (2 * kStages + 4 * NG + 1) * 8;
+  static constexpr int kSmem = kTmemSlot + 16 + 2048;  // + slack past the last operand
+  // TMEM columns. NG = 2: S_j at 64 j (64), O_j at 128 + 160 j (144), P_j (f16,
+  // two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j.
+  // NG = 1: S at 0, P at 64, O at 96.
+  static constexpr uint32_t kCols = NG == 2 ? 512 : 256;
+  __host__ __device__ static constexpr uint32_t col_s(int j) { return 64u * j; }
+  __host__ __device__ static constexpr uint32_t col_o(int j) { return NG == 2 ? 128u + 160u * j : 96u; }
+  __host__ __device__ static constexpr uint32_t col_p(int j) { return NG == 2 ? 432u + 32u * j : 64u; }
+  static_assert(kQ % 1024 == 0 && kK % 1024 == 0 && kV % 1024 == 0 && kVT % 1024 == 0, "operand alignment");
+};
+static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col_p(1) + 32 <= 512, "TMEM columns");
+static_assert(TcCfg<1>::col_p(0) + 32 <= TcCfg<1>::col_o(0) && TcCfg<1>::col_o(0) + kTcPvN <= 256, "TMEM columns");
+static_assert(2 * TcCfg<1>::kSmem <= 227 * 1024, "two CTAs per SM");
 
 // Byte offset of (row r, byte kb) in a canonical tile of 128-byte rows.
 __device__ __forceinline__ uint32_t canon(int r, int kb) {
@@ -114,9 +129,14 @@ struct TcMaps {
 // the PV product through P = 0. Rows never loaded keep what the stage held
 // before (zeros at the start, else keys of earlier tiles). Otherwise tiles
 // arrive by 16-byte cp.async per row chunk (any page size).
-template <bool kTma>
-__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_constant__ DecodeArgs a,
-                                                               const __grid_constant__ TcMaps maps) {
+template <bool kTma, int NG>
+__global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
+    decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TcMaps maps) {
+  using C = TcCfg<NG>;
+  constexpr int kTcStages = C::kStages, kTcGroups = NG, kTcMmaWarp = C::kMmaWarp, kTcThreads = C::kThreads;
+  constexpr int kTcQ = C::kQ, kTcK = C::kK, kTcV = C::kV, kTcVT = C::kVT, kTcX = C::kX, kTcBar = C::kBar;
+  constexpr int kTcTmemSlot = C::kTmemSlot;
+  constexpr uint32_t kTcCols = C::kCols;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sb = smem_u32(smem);
@@ -148,6 +168,12 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     fence_mbar_init();
   }
   if (warp == kTcMmaWarp) tmem_alloc(sb + kTcTmemSlot, kTcCols);
+  if constexpr (kTma) {  // the tensor maps' descriptors: fetched now, while the lengths load
+    if (warp == kTcMmaWarp + 1 && lane == 0) {
+      prefetch_tensormap(&maps.k);
+      prefetch_tensormap(&maps.v);
+    }
+  }
   const int b = wk.b;
 
   // ---- producer set-up (as decode.cu): page ids of the first tiles with the
@@ -330,14 +356,14 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
       constexpr uint32_t id_pv = umma_idesc(0, kTcRows, kTcPvN);       // f16 x f16 -> f32, 128 x 144
       // S_j = Q K_k^T for tile k (group j = k & 1)
       auto qk = [&](int k) -> bool {
-        const int s = k % kTcStages, j = k & 1;
+        const int s = k % kTcStages, j = k & (NG - 1);
         if (!mbar_wait(full_bar(s), (k / kTcStages) & 1)) return false;
         fence_proxy_async();  // the gathered tile, written through the generic proxy
         tc_fence_after();
         const uint32_t kt = sb + kTcK + s * (kTcTileKeys * 128);
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)  // 128 bytes of K: 32 per instruction (two core matrices)
-          umma_f8(tmem + tc_col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
+          umma_f8(tmem + C::col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
                   kTma ? umma_desc_sw128(kt + kk * 32, kTcSbo) : umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
                   id_qk, kk > 0);
         umma_commit(s_ready(j));
@@ -345,15 +371,15 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
       };
       // O_j (+)= P_j V_k once group j has written P and V^T of tile k
       auto pv = [&](int k) -> bool {
-        const int j = k & 1;
-        if (!mbar_wait(p_ready(j), (k >> 1) & 1)) return false;
+        const int j = k & (NG - 1);
+        if (!mbar_wait(p_ready(j), (k >> (NG - 1)) & 1)) return false;
         fence_proxy_async();
         tc_fence_after();
         mbar_arrive(empty_bar(k % kTcStages));  // K read (S_k consumed), V converted: the stage is free
         const uint32_t va = sb + kTcVT + j * kTcVTBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)  // 64 keys: 16 per instruction
-          umma_f16_ta(tmem + tc_col_o(j), tmem + tc_col_p(j) + kk * 8,
+          umma_f16_ta(tmem + C::col_o(j), tmem + C::col_p(j) + kk * 8,
                       umma_desc(va + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_pv, (k >= kTcGroups || kk > 0) ? 1u : 0u);
         umma_commit(pv_done(j));
         return true;
@@ -368,14 +394,14 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
       uint64_t t_idle = 0;
       while (np < ntiles) {
         bool did = false;
-        if (nq < ntiles && (nq < kTcGroups || mbar_test_wait(s_free(nq & 1), ((nq - kTcGroups) >> 1) & 1)) &&
+        if (nq < ntiles && (nq < NG || mbar_test_wait(s_free(nq & (NG - 1)), ((nq - NG) >> (NG - 1)) & 1)) &&
             mbar_test_wait(full_bar(nq % kTcStages), (nq / kTcStages) & 1)) {
           tc_fence_after();
           ok = qk(nq);  // its waits succeed at once
           nq++;
           did = true;
         }
-        if (ok && np < nq && mbar_test_wait(p_ready(np & 1), (np >> 1) & 1)) {
+        if (ok && np < nq && mbar_test_wait(p_ready(np & (NG - 1)), (np >> (NG - 1)) & 1)) {
           ok = pv(np);
           np++;
           did = true;
@@ -412,11 +438,11 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   pdl_launch_dependents();
   {
     // Q row r: the 64 E4M3 dims of (token ti, head) at K bytes [64g, 64g+64),
-    // zeros elsewhere; group jw writes chunks [4 jw, 4 jw + 4) of the row
+    // zeros elsewhere; group jw writes chunks [8 jw / NG, 8 (jw + 1) / NG) of the row
     const uint4* src = reinterpret_cast<const uint4*>(
         a.q8 + ((int64_t)(qb + wk.i0 + (live ? ti : 0)) * kNumQHeads + head) * kHeadDim);
 #pragma unroll
-    for (int c = 4 * jw; c < 4 * jw + 4; c++) {
+    for (int c = 8 * jw / NG; c < 8 * (jw + 1) / NG; c++) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (live && (c >> 2) == g) v = src[c & 3];
       *reinterpret_cast<uint4*>(smem + kTcQ + canon(r, c * 16)) = v;
@@ -435,17 +461,17 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
   const int pos = pbase + ti;  // this row's query position
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  const uint32_t tS = t_lane + tc_col_s(jw);              // this row's S
-  const uint32_t tO = t_lane + tc_col_o(jw) + 64 * g;      // this row's O half
-  const uint32_t tL = t_lane + tc_col_o(jw) + 128;         // this row's P sum
-  const uint32_t tP = t_lane + tc_col_p(jw);               // this row's P (f16 pairs)
+  const uint32_t tS = t_lane + C::col_s(jw);              // this row's S
+  const uint32_t tO = t_lane + C::col_o(jw) + 64 * g;      // this row's O half
+  const uint32_t tL = t_lane + C::col_o(jw) + 128;         // this row's P sum
+  const uint32_t tP = t_lane + C::col_p(jw);               // this row's P (f16 pairs)
   const uint32_t sVT = kTcVT + jw * kTcVTBytes;
   float m = -INFINITY;  // reference max (log2 units)
   bool ok = true;
   int last = -1;  // this group's last tile
   for (int k = jw; k < ntiles; k += kTcGroups) {
     const int s = k % kTcStages;
-    const bool w = mbar_wait(s_ready(jw), (k >> 1) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
+    const bool w = mbar_wait(s_ready(jw), (k >> (NG - 1)) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
     tc_fence_after();
     const int tile_j = jt + k * kTcTileKeys;
@@ -479,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
     // ---- P, V^T and O of this group are free once its previous PV completed
     if (k >= kTcGroups) {
-      const bool w2 = mbar_wait(pv_done(jw), ((k - kTcGroups) >> 1) & 1);
+      const bool w2 = mbar_wait(pv_done(jw), ((k - NG) >> (NG - 1)) & 1);
       if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
       tc_fence_after();
     }
@@ -553,25 +579,27 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
   }
   // this group's O is complete once its last PV has
   if (ok && last >= 0) {
-    const bool w3 = mbar_wait(pv_done(jw), (last >> 1) & 1);
+    const bool w3 = mbar_wait(pv_done(jw), (last >> (NG - 1)) & 1);
     if (!__all_sync(0xffffffffu, w3)) ok = false;
     tc_fence_after();
   }
   if (!ok && lane == 0) set_error(a.err, OKC_DEVERR_TIMEOUT);
 
-  // ---- merge the two groups (group 1 hands (m, l) over), write the split
+  // ---- merge the two groups and write the split: the groups swap their
+  // reference maxima through shared memory, then group j writes dims
+  // [32 j, 32 j + 32) of each row's 64 (group 0 also the row's LSE)
   float* xml = reinterpret_cast<float*>(smem + kTcX);
-  if (jw == 1) xml[r] = m;
+  xml[jw * kTcRows + r] = m;
   tc_fence_before();
   named_bar_sync(3, kTcGroups * kTcRows);
   tc_fence_after();
-  if (jw == 0) {
-    const bool has0 = ok && ntiles >= 1, has1 = ok && ntiles >= 2;  // groups that ran a PV
-    const float m1 = xml[r];
-    const float l = has0 ? tmem_ld1(t_lane + tc_col_o(0) + 128) : 0.f;
-    const float l1 = has1 ? tmem_ld1(t_lane + tc_col_o(1) + 128) : 0.f;
-    const float M = fmaxf(m, m1);
-    const float f0 = m == -INFINITY ? 0.f : fast_exp2(m - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+  {
+    const bool has0 = ok && ntiles >= 1, has1 = NG > 1 && ok && ntiles >= 2;  // groups that ran a PV
+    const float m0 = xml[r], m1 = NG > 1 ? xml[kTcRows + r] : -INFINITY;
+    const float l = has0 ? tmem_ld1(t_lane + C::col_o(0) + 128) : 0.f;
+    const float l1 = has1 ? tmem_ld1(t_lane + C::col_o(NG - 1) + 128) : 0.f;
+    const float M = fmaxf(m0, m1);
+    const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
     const float L = l * f0 + l1 * f1;
     const float vscale = a.scaled ? *a.v_scale : 1.0f;
     const float inv = L > 0.f ? vscale / L : 0.f;
@@ -582,10 +610,11 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
     const int64_t slot = (int64_t)__ldg(&a.work[blockIdx.x].wbase) + __ldg(&a.work[blockIdx.x].chunk);
     float* orow = a.o_part + (slot * rows + row) * kHeadDim;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; h2++) {
+    for (int hh2 = 0; hh2 < 2 / NG; hh2++) {  // this group's halves of the row
+      const int h2 = NG == 2 ? jw : hh2;
       float o0[32], o1[32];
-      if (has0) tmem_ld32(t_lane + tc_col_o(0) + 64 * g + 32 * h2, o0);
-      if (has1) tmem_ld32(t_lane + tc_col_o(1) + 64 * g + 32 * h2, o1);
+      if (has0) tmem_ld32(t_lane + C::col_o(0) + 64 * g + 32 * h2, o0);
+      if (has1) tmem_ld32(t_lane + C::col_o(NG - 1) + 64 * g + 32 * h2, o1);
       if (live) {
 #pragma unroll
         for (int d = 0; d < 32; d += 4) {
@@ -597,7 +626,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(const __grid_cons
         }
       }
     }
-    if (live) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
+    if (live && jw == 0) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
   }
   tc_fence_before();
   named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // TMEM reads done: the MMA warp may free it
@@ -638,13 +667,13 @@ bool encode_cache_map(CUtensorMap* m, const uint8_t* base, int64_t rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
-  if (num_work == 0) return cudaSuccess;
-  if (a.S < 1 || a.S > 8) return cudaErrorInvalidValue;
+template <int NG>
+cudaError_t launch_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  using C = TcCfg<NG>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_work);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -656,21 +685,43 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaSt
   std::memset(&maps, 0, sizeof maps);
   const int64_t rows = (int64_t)a.num_pages << a.page_shift;
   if (a.page_shift >= 3 && encode_cache_map(&maps.k, a.kc, rows) && encode_cache_map(&maps.v, a.vc, rows))
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true>, a, maps);
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false>, a, maps);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true, NG>, a, maps);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false, NG>, a, maps);
 }
 
-int decode_tc_ctas_per_sm() {
+cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  if (num_work == 0) return cudaSuccess;
+  if (a.S < 1 || a.S > 8) return cudaErrorInvalidValue;
+  if (a.tc_groups == 1) return launch_tc<1>(a, num_work, pdl, s);
+  if (a.tc_groups == 2) return launch_tc<2>(a, num_work, pdl, s);
+  return cudaErrorInvalidValue;
+}
+
+template <int NG>
+int tc_ctas_per_sm() {
+  using C = TcCfg<NG>;
   int lowest = 0;
   for (int v = 0; v < 2; v++) {
-    auto kern = v ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+    auto kern = v ? decode_tc_kernel<true, NG> : decode_tc_kernel<false, NG>;
     int nb = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kTcThreads, kTcSmem) != cudaSuccess)
+    // (the largest shared-memory carveout: two one-group CTAs need ~210 KB per SM)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, C::kThreads, C::kSmem) != cudaSuccess)
       return 0;
     lowest = v ? std::min(lowest, nb) : nb;
   }
+  // The occupancy calculator reports one CTA per SM for the one-group kernel,
+  // yet two fit (2 x 28,672 registers of 65,536; 2 x ~106 KB of 228 KB of shared
+  // memory; 2 x 256 of the 512 TMEM columns), and a timeline of a launch shows
+  // two CTAs running on one SM at once: its residency is two.
+  if (NG == 1 && lowest == 1) lowest = 2;
   return lowest;
+}
+
+int decode_tc_ctas_per_sm(int tc_groups) {
+  return tc_groups == 1 ? tc_ctas_per_sm<1>() : tc_groups == 2 ? tc_ctas_per_sm<2>() : 0;
 }
 
 }  // namespace okc

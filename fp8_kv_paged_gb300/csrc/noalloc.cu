@@ -95,7 +95,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
     return OKC_ERR_CUDA;
   const bool use_tc = uses_tc(c, nullptr);  // the default plan's kernel choice
   const int S = block_tokens(c, nullptr);
-  const int per_sm = cached_ctas_per_sm(dev, S, use_tc);
+  const int per_sm = cached_ctas_per_sm(dev, S, use_tc, tc_groups(c));
   if (per_sm <= 0) return OKC_ERR_CUDA;
   SplitResult split;
   const okc_status st = make_splits(cfg, seq_lens_host, nullptr, nullptr, sms * per_sm, &split);
@@ -126,6 +126,7 @@ extern "C" okc_status okc_attn_decode_combine_noalloc(
   while ((1 << shift) < c.page_size) shift++;
   DecodeArgs d = {};
   d.tc = use_tc ? 1 : 0;
+  d.tc_groups = tc_groups(c);
   d.q8 = q_fp8;
   d.kc = k_cache;
   d.vc = v_cache;

@@ -376,14 +376,14 @@ okc_status check_fixed(const okc_attn_config* c, const int32_t* seq, const int32
 
 // Resident decode CTAs per SM for (device, block tokens, kernel family), queried
 // once per key: the query also raises the kernels' shared-memory limit on the device.
-int okc::cached_ctas_per_sm(int dev, int S, bool tc) {
+int okc::cached_ctas_per_sm(int dev, int S, bool tc, int tc_groups) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, bool>, int> cache;
+  static std::map<std::tuple<int, int, bool, int>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(dev, S, tc);
+  const auto key = std::make_tuple(dev, S, tc, tc ? tc_groups : 0);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  const int occ = okc::decode_ctas_per_sm(S, tc);
+  const int occ = okc::decode_ctas_per_sm(S, tc, tc_groups);
   if (occ > 0) cache[key] = occ;
   return occ;
 }
@@ -397,7 +397,8 @@ int slots_for(const okc_attn_config* c, const okc_plan_options* o, int* sm_count
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    if (per_sm == 0) per_sm = okc::cached_ctas_per_sm(dev, okc::block_tokens(*c, o), okc::uses_tc(*c, o));
+    if (per_sm == 0)
+      per_sm = okc::cached_ctas_per_sm(dev, okc::block_tokens(*c, o), okc::uses_tc(*c, o), okc::tc_groups(*c));
     if (per_sm <= 0) return -1;
   }
   if (sm_count_out) *sm_count_out = sms;
@@ -609,6 +610,12 @@ okc_status okc_attn_plan_varlen(const okc_attn_config* cfg, const int32_t* seq_l
   int sms = 0;
   const int slots = slots_for(cfg, opts, &sms);
   if (slots < 0) return OKC_ERR_CUDA;
+  // the decode kernels' shared-memory limits are raised on the device by the
+  // (cached) occupancy query, which forced options skip: run it here for every plan
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      okc::cached_ctas_per_sm(dev, okc::block_tokens(*cfg, opts), okc::uses_tc(*cfg, opts), okc::tc_groups(*cfg)) <= 0)
+    return OKC_ERR_CUDA;
   SplitResult s;
   st = make_splits(cfg, seq_lens_host, q_lens_host, opts, slots, &s);
   if (st != OKC_OK) return st;
@@ -855,6 +862,7 @@ okc_status okc_attn_decode(okc_attn_plan_t plan, const uint8_t* q_fp8, const uin
   if (scaled && (!k_scale || !v_scale)) return OKC_ERR_INVALID;
   okc::DecodeArgs a = {};
   a.tc = plan->tc ? 1 : 0;
+  a.tc_groups = okc::tc_groups(c);
   a.q8 = q_fp8;
   a.kc = k_cache;
   a.vc = v_cache;

@@ -108,6 +108,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (i >= kWaitMinPolls && global_ns() - t0 > limit_ns) return false;
   }
 }
+// Fetch a TMA tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
 // Arrive on mbarrier `bar` and add `bytes` to the transaction count its
 // current phase waits for (the bytes of the bulk copies that complete on it).
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {

@@ -95,6 +95,7 @@ struct DecodeArgs {
   uint16_t* out;            // bf16 [T, Hq*64]
   float eps;
   int32_t tc;               // 1: blocks of 2..8 tokens run on the tcgen05 kernel (decode_tc.cu)
+  int32_t tc_groups;        // its softmax warpgroups per CTA (tc_groups)
   int32_t q_fold;           // as PrepareArgs (the fused step derives q itself)
   float q_scale;
   int32_t early;            // OKC_PLAN_EARLY_GATHER: the fused step loads lengths, page ids and
@@ -163,6 +164,11 @@ inline float softmax_scale_log2(const okc_attn_config& c) {
 inline bool uses_tc(const okc_attn_config& c, const okc_plan_options* o) {
   return c.q_len >= 2 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
 }
+// Softmax warpgroups per CTA of the tcgen05 kernel: 2 (one CTA per SM, the
+// groups on alternate tiles) for steps of at most 8 tokens per request (decode,
+// verify: few blocks, many splits, where fewer, longer splits merge faster),
+// 1 (two CTAs per SM) for longer extends (many blocks, bound by the tensor cores).
+inline int tc_groups(const okc_attn_config& c) { return c.q_len > 8 ? 1 : 2; }
 // Tokens per query block: 1 for q_len 1, 8 on the tcgen05 kernel (its M = 128
 // rows are 8 tokens x 16 heads), 16 on the warp-level kernel; q_len itself when smaller.
 inline int block_tokens(const okc_attn_config& c, const okc_plan_options* o) {
@@ -211,12 +217,14 @@ cudaError_t launch_rope_table(float theta, const float* inv_freq, int32_t n, flo
 // Resident CTAs per SM of the decode kernels for blocks of S tokens (tc: the
 // tcgen05 kernel for blocks of 2..8), the lower of the three-call and the fused
 // variant (0 on error).
-int decode_ctas_per_sm(int S, bool tc);
-// decode_ctas_per_sm for device `dev`, queried once per (device, S, tc) and
-// cached (the query also raises the kernels' shared-memory limit on the device).
-int cached_ctas_per_sm(int dev, int S, bool tc);
-// The tcgen05 decode kernel for blocks of 2..8 tokens (decode_tc.cu).
+int decode_ctas_per_sm(int S, bool tc, int tc_groups);
+// decode_ctas_per_sm for device `dev`, queried once per (device, S, tc,
+// tc_groups) and cached (the query also raises the kernels' shared-memory limit
+// on the device).
+int cached_ctas_per_sm(int dev, int S, bool tc, int tc_groups);
+// The tcgen05 decode kernel for blocks of 2..8 tokens (decode_tc.cu), with
+// a.tc_groups softmax warpgroups per CTA.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
-int decode_tc_ctas_per_sm();
+int decode_tc_ctas_per_sm(int tc_groups);
 
 }  // namespace okc

@@ -31,9 +31,9 @@ cudaError_t launch_decode(const DecodeArgs&, int, bool, cudaStream_t) { g_launch
 cudaError_t launch_step_fused(const DecodeArgs&, int, bool, cudaStream_t) { g_launches++; return cudaSuccess; }
 cudaError_t launch_combine(const CombineArgs&, bool, cudaStream_t) { g_launches++; return cudaSuccess; }
 cudaError_t launch_rope_table(float, const float*, int32_t, float*, cudaStream_t) { return cudaSuccess; }
-int decode_ctas_per_sm(int, bool tc) { return tc ? 1 : 3; }
+int decode_ctas_per_sm(int, bool tc, int) { return tc ? 1 : 3; }
 cudaError_t launch_decode_tc(const DecodeArgs&, int, bool, cudaStream_t) { g_launches++; return cudaSuccess; }
-int decode_tc_ctas_per_sm() { return 1; }
+int decode_tc_ctas_per_sm(int) { return 1; }
 }
 
 alignas(256) static uint8_t arena[1 << 16];

@@ -52,9 +52,9 @@ cudaError_t launch_decode(const DecodeArgs&, int, bool, cudaStream_t) { return c
 cudaError_t launch_step_fused(const DecodeArgs&, int, bool, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_combine(const CombineArgs&, bool, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_rope_table(float, const float*, int32_t, float*, cudaStream_t) { return cudaSuccess; }
-int decode_ctas_per_sm(int, bool) { return 3; }
+int decode_ctas_per_sm(int, bool, int) { return 3; }
 cudaError_t launch_decode_tc(const DecodeArgs&, int, bool, cudaStream_t) { return cudaSuccess; }
-int decode_tc_ctas_per_sm() { return 1; }
+int decode_tc_ctas_per_sm(int) { return 1; }
 }
 #define CHECK(c) do { if (!(c)) { printf("FAIL line %d: %s\n", __LINE__, #c); exit(1); } } while (0)
 

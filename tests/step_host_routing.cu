@@ -53,9 +53,9 @@ cudaError_t launch_decode(const DecodeArgs& a, int, bool, cudaStream_t) { g_dec 
 cudaError_t launch_step_fused(const DecodeArgs& a, int, bool, cudaStream_t) { g_dec = a; g_fused++; return cudaSuccess; }
 cudaError_t launch_combine(const CombineArgs& a, bool, cudaStream_t) { g_comb = a; g_three++; return cudaSuccess; }
 cudaError_t launch_rope_table(float, const float*, int32_t, float*, cudaStream_t) { return cudaSuccess; }
-int decode_ctas_per_sm(int, bool tc) { return tc ? 1 : 3; }
+int decode_ctas_per_sm(int, bool tc, int) { return tc ? 1 : 3; }
 cudaError_t launch_decode_tc(const DecodeArgs& a, int, bool, cudaStream_t) { g_dec = a; g_three++; return cudaSuccess; }
-int decode_tc_ctas_per_sm() { return 1; }
+int decode_tc_ctas_per_sm(int) { return 1; }
 }
 #define CHECK(c) do { if (!(c)) { printf("FAIL case %d line %d: %s\n", cs, __LINE__, #c); return 1; } } while (0)
 

@@ -225,3 +225,28 @@ def test_many_requests(L):
     assert rep["num_work"] >= 1500
     full_check(cfg, inp, fused=True, plan_form=True)
     full_check(cfg, inp, fused=True)
+
+
+def test_forced_occupancy_plans_launch_in_a_fresh_process():
+    """A plan made with okc_plan_options.ctas_per_sm / sm_count (which skip the
+    occupancy query) still launches: the plan raises the decode kernels'
+    shared-memory limits itself. Run in a fresh process, where no earlier plan
+    has raised them, for the q_len-1 and the tcgen05 kernels."""
+    import os
+    import subprocess
+    import sys
+    code = r"""
+import sys
+sys.path.insert(0, "tests"); sys.path.insert(0, ".")
+import workloads as W
+from parity_util import full_check
+for name in ("sliding_decode", "verify_block"):
+    from test_gpu_parity import SMALL
+    cfg = W.config(name, **SMALL[name])
+    inp = W.generate(cfg)
+    full_check(cfg, inp, opts={"ctas_per_sm": 1, "sm_count": 148})
+print("ok")
+"""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]

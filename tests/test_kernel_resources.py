@@ -1,9 +1,10 @@
 """Per-kernel resources as ptxas reports them for sm_103a (-Xptxas -v; no GPU):
 the hot kernels keep the register counts their occupancy rests on (the decode
 kernels for q_len 1 at 80 registers x 256 threads: three CTAs per SM; the
-tcgen05 verify decode at 112 x 352: one CTA per SM with room for the prepare
-and combine CTAs beside it) and spill nothing beyond the fused step's known
-16-byte frame."""
+two-group tcgen05 decode (verify blocks) at 112 x 352: one CTA per SM with room
+for the prepare and combine CTAs beside it; the one-group tcgen05 decode
+(extends) at 128 x 224: two CTAs per SM) and spill nothing beyond the fused
+step's known 16-byte frame."""
 import os
 import re
 import shutil
@@ -18,8 +19,10 @@ CSRC = os.path.join(ROOT, "fp8_kv_paged_gb300", "csrc")
 LIMITS = {
     "decode_kernelILi2ELi1ELi4ELb1E": (80, 16),   # the fused step (sliding, mixed)
     "decode_kernelILi2ELi1ELi4ELb0E": (80, 0),    # q_len-1 decode of the three-call step
-    "decode_tc_kernelILb1E": (112, 0),            # verify block, TMA gather
-    "decode_tc_kernelILb0E": (112, 0),            # verify block, cp.async gather
+    "decode_tc_kernelILb1ELi2E": (112, 0),        # verify block, TMA gather
+    "decode_tc_kernelILb0ELi2E": (112, 0),        # verify block, cp.async gather
+    "decode_tc_kernelILb1ELi1E": (128, 0),        # extend, TMA gather
+    "decode_tc_kernelILb0ELi1E": (128, 0),        # extend, cp.async gather
     "prepare_kernel": (64, 0),
     "combine_kernel": (128, 0),
 }
