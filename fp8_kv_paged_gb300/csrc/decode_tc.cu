@@ -515,11 +515,11 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     if (k >= kTcGroups && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
       float ov[16];
 #pragma unroll
-      for (int h4 = 0; h4 < 4; h4++) {
+      for (int h4 = 0; h4 < 4; h4++) {  // (the stores complete at the sum's store below)
         tmem_ld16(tO + 16 * h4, ov);
 #pragma unroll
         for (int d = 0; d < 16; d++) ov[d] *= alpha;
-        tmem_st16(tO + 16 * h4, ov);
+        tmem_st16_async(tO + 16 * h4, ov);
       }
       tmem_st1(tL, tmem_ld1(tL) * alpha);
     }
