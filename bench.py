@@ -5,9 +5,10 @@ the largest workload that fits one GPU, the mixed full-attention decode batch:
 B=256, L=1, Hq=16, Hkv=2, d=64, seq_lens log-uniform in [1, 131072], page_size
 1, window 0 (no RoPE), kv_scale 1 (synthetic, seeded; about 0.73 GB of KV rows
 per step). The same line carries, under "workloads", the same measurements for
-the other four workloads (tiny sliding decode, sliding decode, full decode at
-32k, verify block); --workload picks another headline and --no-others drops
-the rest.
+the other workloads (tiny sliding decode, sliding decode, full decode at 32k,
+verify block, and the extend batch of ragged prefill/extend requests, whose
+roofline is the tensor peak); --workload picks another headline and
+--no-others drops the rest.
 
 The timed step is okc_attn_step in the form its plan chooses (one fused kernel
 or prepare, decode and combine: the entry's config.path says which). --path
@@ -28,9 +29,10 @@ page-locked and mapped), the step's calls and the output written back to host
 memory.
 
 cpu_baseline: the CPU oracle as it stands on a bounded sample of each workload
-(whole requests), single-threaded and on all host cores (one thread per core,
-each running the oracle's attention on its own share of the requests; ctypes
-calls release the interpreter lock), with the core count and CPU model.
+(a uniform sample of its query rows, token x head), single-threaded and on all
+host cores (one thread per core, each running the oracle's attention on its own
+share of the requests; ctypes calls release the interpreter lock), with the
+core count and CPU model.
 --impl reference times that oracle alone, on all host cores, as the reference
 arm. Multi-GPU: replicas only (each rank runs its own independent batch).
 """
@@ -58,11 +60,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("mixed_full_decode", "decode_kernel<fused step>"): 803068416 + 6998272,
-    ("sliding_decode", "decode_kernel<fused step>"): 33095168 + 1536,
-    ("full_decode_32k", "decode_kernel"): 545486336 + 3203584,
-    ("verify_block", "decode_tc_kernel"): 17212416 + 0,
-    ("extend", "decode_tc_kernel"): 36406784 + 22272,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 803062272 + 7515392,
+    ("sliding_decode", "decode_kernel<fused step>"): 33094656 + 1280,
+    ("full_decode_32k", "decode_kernel"): 545534720 + 3177472,
+    ("verify_block", "decode_tc_kernel"): 17209856 + 0,
+    ("extend", "decode_tc_kernel"): 36399104 + 43776,
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0

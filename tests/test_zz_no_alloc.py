@@ -91,6 +91,45 @@ def test_noalloc_call_takes_no_device_memory(cuda_lib):
         assert torch.equal(o, ref)
 
 
+def _bad_page_step(okc, cfg, inp, d):
+    """The three calls on inputs with an out-of-pool page id: they flag it."""
+    step = okc.AttnStep(cfg, inp["seq_lens"])
+    out = step.run(d, eps=inp["eps"]).clone()
+    torch.cuda.synchronize()
+    assert step.errors() == okc.DEVERR_PAGE
+    return step, out
+
+
+def test_noalloc_skips_a_bad_page_id(cuda_lib):
+    """The entry point has no error word, so it cannot report a page id past
+    the pool; its kernels still bound-check it and read nothing there. On the
+    q_len 1 kernel the key reads as zeros (as in the oracle): the output equals
+    the three calls' bit for bit and the oracle on every row. On the tcgen05
+    kernel (verify blocks, TMA loads) the skipped rows leave that request's
+    output void: every other request equals the three calls' output."""
+    okc = cuda_lib
+    cfg = W.config("sliding_decode", batch=4, seq=("uniform", 500, 900))
+    inp = W.generate(cfg)
+    inp = dict(inp, page_table=inp["page_table"].copy())
+    inp["page_table"][2, 10] = cfg["num_pages"] + 5
+    d = to_device(cfg, inp)
+    step, ref = _bad_page_step(okc, cfg, inp, d)
+    out = _noalloc(okc, cfg, inp, d, step.q_fp8)
+    assert torch.equal(out, ref)
+    check_against_oracle(cfg, inp, out.view(torch.int16).cpu().numpy().view(np.uint16))
+
+    vcfg = W.config("verify_block", batch=3, seq=("list", [300, 1000, 2500]))
+    vinp = W.generate(vcfg)
+    vinp = dict(vinp, page_table=vinp["page_table"].copy())
+    vinp["page_table"][1, 5] = vcfg["num_pages"] + 7
+    vd = to_device(vcfg, vinp)
+    vstep, vref = _bad_page_step(okc, vcfg, vinp, vd)
+    vout = _noalloc(okc, vcfg, vinp, vd, vstep.q_fp8)
+    L = vcfg["q_len"]
+    for b in (0, 2):
+        assert torch.equal(vout[b * L:(b + 1) * L], vref[b * L:(b + 1) * L]), b
+
+
 def test_noalloc_rejects_steps_beyond_its_scratch(cuda_lib):
     okc = cuda_lib
     # 200 requests x a 16-token block: 200 work items x 256 rows of partials
