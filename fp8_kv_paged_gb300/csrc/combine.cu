@@ -13,7 +13,13 @@ namespace okc {
 namespace {
 
 constexpr int kCombThreads = 8 * kNumQHeads;  // 128
+// Splits merged per round trip: 8 for blocks of one token (steps whose
+// requests have many splits); 4 for longer blocks (verify and extend steps: few
+// splits per block, many blocks), which keeps the kernel under 64 registers a
+// thread so that two of its CTAs fit beside a tcgen05 decode CTA on one SM (the
+// combine is launched under programmatic dependent launch while the decode runs).
 
+template <int kB>
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
   const int i = blockIdx.y;  // token of the block
   const int h = threadIdx.x >> 3;
@@ -30,7 +36,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(CombineArgs a) {
 
   const int rows = a.S * kNumQHeads;
   const int row = i * kNumQHeads + h;
-  merge_normgate(a.lse_part + (int64_t)bl.wbase * rows + row, rows,
+  merge_normgate<kB>(a.lse_part + (int64_t)bl.wbase * rows + row, rows,
                  a.o_part + ((int64_t)bl.wbase * rows + row) * kHeadDim + c0, (int64_t)rows * kHeadDim,
                  bl.nchunks, g, w, a.eps, a.out + (size_t)t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
 }
@@ -49,7 +55,7 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+  return a.S == 1 ? cudaLaunchKernelEx(&cfg, combine_kernel<8>, a) : cudaLaunchKernelEx(&cfg, combine_kernel<4>, a);
 }
 
 }  // namespace okc

@@ -22,11 +22,13 @@
 //
 // Warps: 0-3 and 4-7 are two softmax warpgroups that take alternate tiles
 // (thread r of a group owns q row r), 8 issues the MMAs (one thread) and owns
-// the TMEM allocation, 9-10 gather: on pages of 8 or more rows warp 9 issues
-// TMA tile loads (8-row boxes, 128-byte swizzle, read by the MMA through a
-// swizzled descriptor), else both warps run the cp.async producer of
-// decode.cu (K rows in the MMA's no-swizzle canonical layout, V rows in a
-// staging tile). Each group j has its own S, P and O in TMEM and its own V^T
+// the TMEM allocation, 9-10 gather (with one softmax group: warps 0-3, MMA 4,
+// gather 5-6): on pages of 8 or more rows each gather warp issues the TMA loads
+// of four of a tile's eight 8-row groups (8-row boxes, 128-byte swizzle, read
+// by the MMA through a swizzled descriptor; one warp's TMA issues are
+// serialised, so two issuing warps gather faster than one), else both run the
+// cp.async producer of decode.cu (K rows in the MMA's no-swizzle canonical
+// layout, V rows in a staging tile). Each group j has its own S, P and O in TMEM and its own V^T
 // tile in shared memory, so one group's softmax overlaps the other group's
 // MMAs. Per tile k of group j:
 //   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
@@ -61,7 +63,6 @@ namespace okc {
 namespace {
 
 constexpr int kTcTileKeys = 64;
-constexpr int kTcProducers = 2;   // producer warps
 constexpr int kTcRows = 128;      // q rows per CTA (M)
 constexpr int kTcVPitch = 144;    // V staging row pitch: conflict-free ldmatrix
 constexpr uint32_t kTcLbo = 128;  // next core matrix along K
@@ -78,12 +79,16 @@ constexpr int kTcVTBytes = kTcPvN * 128;
 // 256 columns, 4 stages, ~105 KB of shared memory).
 
 // The layout of a CTA with NG softmax warpgroups. Warps 0 .. 4 NG - 1 run the
-// softmax, warp 4 NG issues the MMAs, the next two gather.
+// softmax, warp 4 NG issues the MMAs, the next kProducers gather.
 template <int NG>
 struct TcCfg {
   static constexpr int kStages = NG == 2 ? 6 : 4;
   static constexpr int kMmaWarp = 4 * NG;
-  static constexpr int kThreads = (kMmaWarp + 1 + kTcProducers) * 32;
+  // gather warps: TMA issues from one warp are serialised, so each producer
+  // warp issues its share of a tile's boxes (a third or fourth warp gathered
+  // no faster, and a fourth held back the CTAs of the neighbouring kernels)
+  static constexpr int kProducers = 2;
+  static constexpr int kThreads = (kMmaWarp + 1 + kProducers) * 32;
   static constexpr int kMinBlocks = NG == 1 ? 2 : 0;  // __launch_bounds__ minimum (0: none; with 1 the
                                                       // compiler takes 131 registers instead of 111)
   // shared memory
@@ -134,6 +139,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<NG>;
   constexpr int kTcStages = C::kStages, kTcGroups = NG, kTcMmaWarp = C::kMmaWarp, kTcThreads = C::kThreads;
+  constexpr int kTcProducers = C::kProducers;
+  constexpr int kGroupsPW = 8 / kTcProducers;  // TMA: 8-row groups of a tile per producer warp
   constexpr int kTcQ = C::kQ, kTcK = C::kK, kTcV = C::kV, kTcVT = C::kVT, kTcX = C::kX, kTcBar = C::kBar;
   constexpr int kTcTmemSlot = C::kTmemSlot;
   constexpr uint32_t kTcCols = C::kCols;
@@ -153,9 +160,9 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   const WorkItem wk = a.work[blockIdx.x];  // plan data
   if (tid == 0) {
     for (int s = 0; s < kTcStages; s++) {
-      // TMA: one arrival with the tile's box bytes and one cp.async-tracked
-      // arrival per lane of the issuing warp; cp.async: one per producer lane
-      mbar_init(full_bar(s), kTma ? 1 + 32 : 32 * kTcProducers);
+      // TMA: per producer warp one arrival with its boxes' bytes and one
+      // cp.async-tracked arrival per lane; cp.async: one per producer lane
+      mbar_init(full_bar(s), kTma ? kTcProducers * (1 + 32) : 32 * kTcProducers);
       mbar_init(empty_bar(s), 1);                  // the MMA thread frees a stage
     }
     for (int j = 0; j < kTcGroups; j++) {
@@ -184,12 +191,13 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   static_assert(kKeysPW == 16 || kKeysPW == 32, "at most one page id per producer lane per tile");
   const int pw = warp - (kTcMmaWarp + 1), kbase = pw * kKeysPW;
   const int32_t* pt = a.page_table + (int64_t)b * a.max_pages;
-  // (TMA: producer warp 0 alone; its lane l < 8 loads the id of the tile's
-  // 8-row group l, tiles starting at the key range's start rounded down to 8)
+  // (TMA: lane l < kGroupsPW of producer warp pw loads the id of the tile's
+  // 8-row group pw kGroupsPW + l, tiles starting at the key range's start
+  // rounded down to 8)
   auto load_ids = [&](int& dst, int tile, int jb, int je) {
     if constexpr (kTma) {
-      const int j = (jb & ~7) + tile * kTcTileKeys + 8 * lane;
-      dst = (pw == 0 && lane < 8 && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
+      const int j = (jb & ~7) + tile * kTcTileKeys + 8 * (pw * kGroupsPW + lane);
+      dst = (lane < kGroupsPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
     } else {
       const int j = jb + tile * kTcTileKeys + kbase + lane;
       dst = (lane < kKeysPW && j < je) ? __ldg(pt + (j >> a.page_shift)) : -1;
@@ -246,10 +254,6 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     const int newk = n - ql;  // keys >= newk are written by the prepare kernel
     const int rr = lane >> 3, ch = lane & 7;
     bool dep = false, bad_page = false;
-    // (TMA: the first producer warp alone issues the loads; the block keeps the
-    // second, idle: without it the compiler takes 140 registers per thread
-    // instead of 112, and the step was slower)
-    if (kTma && pw != 0) return;
     auto issue = [&](int k, int id) {
       const int s = k % kTcStages;
       const uint32_t sK = sb + kTcK + s * (kTcTileKeys * 128), sV = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
@@ -259,11 +263,12 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         dep = true;
       }
       if constexpr (kTma) {
-        // lane l < 8: the 8 rows of keys tj + 8l .. +7 lie in one page
-        const int key = tj + 8 * lane;
-        int nrows = 0;  // rows of group l to load: 8, or up to the chunk's last key
+        // lane l < kGroupsPW: the 8 rows of group gi, keys tj + 8 gi .. +7, lie in one page
+        const int gi = pw * kGroupsPW + lane;
+        const int key = tj + 8 * gi;
+        int nrows = 0;  // rows of group gi to load: 8, or up to the chunk's last key
         int row = 0;
-        if (lane < 8 && key < j1) {
+        if (lane < kGroupsPW && key < j1) {
           if (id >= 0 && id < a.num_pages) {
             row = (id << a.page_shift) | (key & pmask);
             nrows = min(8, j1 - key);
@@ -275,15 +280,15 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(whole) * 2u * 1024u);
         __syncwarp();
         if (nrows == 8) {
-          tma_load_2d(sK + lane * 1024, &maps.k, 0, row, full_bar(s));
-          tma_load_2d(sV + lane * 1024, &maps.v, 0, row, full_bar(s));
+          tma_load_2d(sK + gi * 1024, &maps.k, 0, row, full_bar(s));
+          tma_load_2d(sV + gi * 1024, &maps.v, 0, row, full_bar(s));
         }
         // the group cut by the chunk's end (at most one): its rows by 16-byte
         // cp.async chunks into the same swizzled positions, all lanes
         const unsigned cut = __ballot_sync(0xffffffffu, nrows > 0 && nrows < 8);
         if (cut) {
-          const int gc = __ffs(cut) - 1;
-          const int crow = __shfl_sync(0xffffffffu, row, gc), cn = __shfl_sync(0xffffffffu, nrows, gc);
+          const int lc = __ffs(cut) - 1, gc = pw * kGroupsPW + lc;
+          const int crow = __shfl_sync(0xffffffffu, row, lc), cn = __shfl_sync(0xffffffffu, nrows, lc);
 #pragma unroll
           for (int h = 0; h < 2; h++) {
             const int cid = lane + 32 * h, r = cid >> 3, c = cid & 7;  // row r, chunk c of the group

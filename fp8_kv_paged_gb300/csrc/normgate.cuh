@@ -38,18 +38,20 @@ __device__ __forceinline__ void load_gate_weight(const uint16_t* qkv, const uint
   }
 }
 
-// Splits are visited in batches of kMergeBatch with every load of a batch in
-// flight (one round trip per batch). Online over batches: the running sums are
-// rescaled by 2^(M_old - M_new) when a batch raises the maximum; with at most
-// kMergeBatch splits this is the plain two-pass merge (M = max of all lse).
+// Splits are visited in batches of kB (8 by default) with every load of a
+// batch in flight (one round trip per batch; each split holds 9 registers).
+// Online over batches: the running sums are rescaled by 2^(M_old - M_new) when
+// a batch raises the maximum; with at most kB splits this is the plain
+// two-pass merge (M = max of all lse).
 constexpr int kMergeBatch = 8;
 
-__device__ __forceinline__ void merge_accumulate(const float (&ls)[kMergeBatch], const float4 (&x0)[kMergeBatch],
-                                                 const float4 (&x1)[kMergeBatch], float& M, float (&acc)[8],
+template <int kB>
+__device__ __forceinline__ void merge_accumulate(const float (&ls)[kB], const float4 (&x0)[kB],
+                                                 const float4 (&x1)[kB], float& M, float (&acc)[8],
                                                  float& wsum) {
   float bm = M;
 #pragma unroll
-  for (int u = 0; u < kMergeBatch; u++) bm = fmaxf(bm, ls[u]);
+  for (int u = 0; u < kB; u++) bm = fmaxf(bm, ls[u]);
   const float bmu = bm == -INFINITY ? 0.f : bm;
   if (M != -INFINITY && bm != M) {  // an earlier batch: rescale its sums to the new maximum
     const float sc = exp2f(M - bmu);
@@ -59,7 +61,7 @@ __device__ __forceinline__ void merge_accumulate(const float (&ls)[kMergeBatch],
   }
   M = bm;
 #pragma unroll
-  for (int u = 0; u < kMergeBatch; u++) {
+  for (int u = 0; u < kB; u++) {
     const float wt = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - bmu);
     wsum += wt;
     acc[0] += wt * x0[u].x; acc[1] += wt * x0[u].y; acc[2] += wt * x0[u].z; acc[3] += wt * x0[u].w;
@@ -101,11 +103,11 @@ __device__ __forceinline__ void normgate_store(const float (&acc)[8], float wsum
 // Splits in global memory. lse: the row's base-2 LSE of split 0, consecutive
 // splits `lse_stride` floats apart; op: this lane's 8 columns of split 0, splits
 // `o_stride` floats apart. Loads bypass L1 (partials written by other CTAs of
-// the same grid).
+// the same grid). kB: splits per batch.
+template <int kB = kMergeBatch>
 __device__ __forceinline__ void merge_normgate(const float* lse, int64_t lse_stride, const float* op,
                                                int64_t o_stride, int nchunks, const float (&g)[8],
                                                const float (&w)[8], float eps, uint16_t* dst) {
-  constexpr int kB = kMergeBatch;
   float M = -INFINITY;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;

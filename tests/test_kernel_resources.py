@@ -3,8 +3,9 @@ the hot kernels keep the register counts their occupancy rests on (the decode
 kernels for q_len 1 at 80 registers x 256 threads: three CTAs per SM; the
 two-group tcgen05 decode (verify blocks) at 112 x 352: one CTA per SM with room
 for the prepare and combine CTAs beside it; the one-group tcgen05 decode
-(extends) at 128 x 224: two CTAs per SM) and spill nothing beyond the fused
-step's known 16-byte frame."""
+(extends) at 128 x 224: two CTAs per SM; the combine for blocks of several
+tokens under 64 x 128, so that two of its CTAs fit beside a tcgen05 decode CTA)
+and spill nothing beyond the fused step's known 16-byte frame."""
 import os
 import re
 import shutil
@@ -25,6 +26,7 @@ LIMITS = {
     "decode_tc_kernelILb0ELi1E": (128, 0),        # extend, cp.async gather
     "prepare_kernel": (64, 0),
     "combine_kernel": (128, 0),
+    "combine_kernelILi4E": (64, 0),               # verify and extend steps (4 splits per round trip)
 }
 
 
