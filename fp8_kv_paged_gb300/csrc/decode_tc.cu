@@ -91,9 +91,13 @@ struct TcCfg {
   static constexpr int kThreads = (kMmaWarp + 1 + kProducers) * 32;
   static constexpr int kMinBlocks = NG == 1 ? 2 : 0;  // __launch_bounds__ minimum (0: none; with 1 the
                                                       // compiler takes 131 registers instead of 111)
+  // Q, the QK's A operand: in TMEM with two groups (the 32 columns the other
+  // operands leave free: the QK reads only K from shared memory), else in
   // shared memory
-  static constexpr int kQ = 0;                                            // Q E4M3 [128 x 128 B]
-  static constexpr int kK = kQ + kTcRows * 128;                           // K E4M3 [stage][64 x 128 B]
+  static constexpr bool kQTmem = NG == 2;
+  // shared memory
+  static constexpr int kQ = 0;                                            // Q E4M3 [128 x 128 B] (not kQTmem)
+  static constexpr int kK = kQ + (kQTmem ? 0 : kTcRows * 128);            // K E4M3 [stage][64 x 128 B]
   static constexpr int kV = kK + kStages * kTcTileKeys * 128;             // V E4M3 [stage][64 x 144 B]
   static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][144 x 64 keys]
   static constexpr int kX = kVT + NG * kTcVTBytes;                        // each group's reference max per row
@@ -108,9 +112,15 @@ struct TcCfg {
   __host__ __device__ static constexpr uint32_t col_s(int j) { return 64u * j; }
   __host__ __device__ static constexpr uint32_t col_o(int j) { return NG == 2 ? 128u + 160u * j : 96u; }
   __host__ __device__ static constexpr uint32_t col_p(int j) { return NG == 2 ? 432u + 32u * j : 64u; }
+  // kQTmem: Q's K bytes [32 kk, 32 kk + 32) (4 per column) at col_q(kk): the
+  // columns between O_0 and O_1 and after P_1
+  __host__ __device__ static constexpr uint32_t col_q(int kk) { return kk < 2 ? 272u + 8u * kk : 496u + 8u * (kk - 2); }
   static_assert(kQ % 1024 == 0 && kK % 1024 == 0 && kV % 1024 == 0 && kVT % 1024 == 0, "operand alignment");
 };
-static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col_p(1) + 32 <= 512, "TMEM columns");
+static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col_p(1) + 32 <= TcCfg<2>::col_q(2) &&
+                  TcCfg<2>::col_o(0) + kTcPvN <= TcCfg<2>::col_q(0) && TcCfg<2>::col_q(1) + 8 <= TcCfg<2>::col_o(1) &&
+                  TcCfg<2>::col_q(3) + 8 <= 512,
+              "TMEM columns");
 static_assert(TcCfg<1>::col_p(0) + 32 <= TcCfg<1>::col_o(0) && TcCfg<1>::col_o(0) + kTcPvN <= 256, "TMEM columns");
 static_assert(2 * TcCfg<1>::kSmem <= 227 * 1024, "two CTAs per SM");
 
@@ -355,7 +365,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
 
   if (warp == kTcMmaWarp) {
     // ================================================================ MMA issue
-    named_bar_sync(1, (kTcMmaWarp + 1) * 32);  // Q is in shared memory
+    named_bar_sync(1, (kTcMmaWarp + 1) * 32);  // Q is in TMEM or shared memory
+    tc_fence_after();
     if (lane == 0) {
       constexpr uint32_t id_qk = umma_idesc(0, kTcRows, kTcTileKeys);  // E4M3 x E4M3 -> f32, 128 x 64
       constexpr uint32_t id_pv = umma_idesc(0, kTcRows, kTcPvN);       // f16 x f16 -> f32, 128 x 144
@@ -367,10 +378,14 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         tc_fence_after();
         const uint32_t kt = sb + kTcK + s * (kTcTileKeys * 128);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++)  // 128 bytes of K: 32 per instruction (two core matrices)
-          umma_f8(tmem + C::col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
-                  kTma ? umma_desc_sw128(kt + kk * 32, kTcSbo) : umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo),
-                  id_qk, kk > 0);
+        for (int kk = 0; kk < 4; kk++) {  // 128 bytes of K: 32 per instruction (two core matrices)
+          const uint64_t kdesc =
+              kTma ? umma_desc_sw128(kt + kk * 32, kTcSbo) : umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo);
+          if constexpr (C::kQTmem)
+            umma_f8_ta(tmem + C::col_s(j), tmem + C::col_q(kk), kdesc, id_qk, kk > 0);
+          else
+            umma_f8(tmem + C::col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo), kdesc, id_qk, kk > 0);
+        }
         umma_commit(s_ready(j));
         return true;
       };
@@ -389,26 +404,27 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         umma_commit(pv_done(j));
         return true;
       };
-      // Issue order follows readiness: QK of tile t (S_j free: group j has read
-      // S of tile t-2; tile t landed) and PV of tile t (P_j written) are
+      // Issue order follows readiness: PV of tile t (P_j written) and QK of
+      // tile t (S_j free: group j has read S of tile t-2; tile t landed) are
       // polled without blocking and issued as soon as their inputs are ready,
-      // so a late tile never holds back a PV. Bounded: gives up after kWaitNs
-      // without progress.
+      // a ready PV first (its group waits on it to write the next P; the QKs
+      // run ahead), so a late tile never holds back a PV. Bounded: gives up
+      // after kWaitNs without progress.
       bool ok = true;
       int nq = 0, np = 0;  // next QK / PV to issue
       uint64_t t_idle = 0;
       while (np < ntiles) {
         bool did = false;
-        if (nq < ntiles && (nq < NG || mbar_test_wait(s_free(nq & (NG - 1)), ((nq - NG) >> (NG - 1)) & 1)) &&
+        if (np < nq && mbar_test_wait(p_ready(np & (NG - 1)), (np >> (NG - 1)) & 1)) {
+          ok = pv(np);  // its wait succeeds at once
+          np++;
+          did = true;
+        }
+        if (ok && nq < ntiles && (nq < NG || mbar_test_wait(s_free(nq & (NG - 1)), ((nq - NG) >> (NG - 1)) & 1)) &&
             mbar_test_wait(full_bar(nq % kTcStages), (nq / kTcStages) & 1)) {
           tc_fence_after();
           ok = qk(nq);  // its waits succeed at once
           nq++;
-          did = true;
-        }
-        if (ok && np < nq && mbar_test_wait(p_ready(np & (NG - 1)), (np >> (NG - 1)) & 1)) {
-          ok = pv(np);
-          np++;
           did = true;
         }
         if (!ok) break;
@@ -446,11 +462,26 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     // zeros elsewhere; group jw writes chunks [8 jw / NG, 8 (jw + 1) / NG) of the row
     const uint4* src = reinterpret_cast<const uint4*>(
         a.q8 + ((int64_t)(qb + wk.i0 + (live ? ti : 0)) * kNumQHeads + head) * kHeadDim);
+    if constexpr (C::kQTmem) {
+      // group jw: K bytes [64 jw, 64 jw + 64), 16 TMEM columns from col_q(2 jw)
+      float qv[16];
 #pragma unroll
-    for (int c = 8 * jw / NG; c < 8 * (jw + 1) / NG; c++) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (live && (c >> 2) == g) v = src[c & 3];
-      *reinterpret_cast<uint4*>(smem + kTcQ + canon(r, c * 16)) = v;
+      for (int c = 0; c < 4; c++) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (live && g == jw) v = src[c];
+        qv[4 * c] = __uint_as_float(v.x);
+        qv[4 * c + 1] = __uint_as_float(v.y);
+        qv[4 * c + 2] = __uint_as_float(v.z);
+        qv[4 * c + 3] = __uint_as_float(v.w);
+      }
+      tmem_st16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::col_q(2 * jw), qv);
+    } else {
+#pragma unroll
+      for (int c = 8 * jw / NG; c < 8 * (jw + 1) / NG; c++) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (live && (c >> 2) == g) v = src[c & 3];
+        *reinterpret_cast<uint4*>(smem + kTcQ + canon(r, c * 16)) = v;
+      }
     }
   }
   {
@@ -460,7 +491,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     const uint32_t one2 = rr2 == 128 ? 0x3C003C00u : 0u;  // f16 1.0 pairs
     *reinterpret_cast<uint4*>(smem + kTcVT + gj * kTcVTBytes + canon(rr2, c * 16)) = make_uint4(one2, one2, one2, one2);
   }
-  fence_proxy_async();
+  fence_proxy_async();  // shared-memory operands, for the MMAs
+  tc_fence_before();    // Q's TMEM stores (kQTmem), before the MMA thread reads them
   named_bar_sync(1, (kTcMmaWarp + 1) * 32);
 
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
