@@ -645,23 +645,42 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     // (the slot is read from the work item again here: kept live through the
     // tile loop it cost the kernel about 30 registers)
     const int64_t slot = (int64_t)__ldg(&a.work[blockIdx.x].wbase) + __ldg(&a.work[blockIdx.x].chunk);
-    float* orow = a.o_part + (slot * rows + row) * kHeadDim;
+    float* opart = a.o_part + slot * rows * kHeadDim;
+    // The split's partials leave through shared memory: each warp stages its
+    // 32 rows' half rows (32 floats at a 144-byte pitch: conflict-free float4
+    // writes and reads) in the K stages, idle now (every tile landed and was
+    // consumed, every MMA completed), then stores 4 half rows (four whole
+    // 128-byte lines) per instruction instead of one 16-byte piece of 32 rows.
+    constexpr int kStgPitch = 36;  // floats
+    static_assert(4 * NG * 32 * kStgPitch * 4 <= kTcStages * kTcTileKeys * 128, "staging fits the K stages");
+    float* stg = reinterpret_cast<float*>(smem + kTcK) + warp * 32 * kStgPitch;
 #pragma unroll
     for (int hh2 = 0; hh2 < 2 / NG; hh2++) {  // this group's halves of the row
       const int h2 = NG == 2 ? jw : hh2;
       float o0[32], o1[32];
       if (has0) tmem_ld32(t_lane + C::col_o(0) + 64 * g + 32 * h2, o0);
       if (has1) tmem_ld32(t_lane + C::col_o(NG - 1) + 64 * g + 32 * h2, o1);
-      if (live) {
 #pragma unroll
-        for (int d = 0; d < 32; d += 4) {
-          float v[4];
+      for (int d = 0; d < 32; d += 4) {
+        float v[4];
 #pragma unroll
-          for (int e = 0; e < 4; e++)
-            v[e] = ((has0 ? o0[d + e] * f0 : 0.f) + (has1 ? o1[d + e] * f1 : 0.f)) * inv;
-          *reinterpret_cast<float4*>(orow + 32 * h2 + d) = make_float4(v[0], v[1], v[2], v[3]);
+        for (int e = 0; e < 4; e++)
+          v[e] = ((has0 ? o0[d + e] * f0 : 0.f) + (has1 ? o1[d + e] * f1 : 0.f)) * inv;
+        *reinterpret_cast<float4*>(stg + lane * kStgPitch + d) = make_float4(v[0], v[1], v[2], v[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int lr = 4 * i + (lane >> 3);             // the warp's row lr: q row rq
+        const int rq = (warp & 3) * 32 + lr;
+        const int ti2 = (rq >> 3) & 7;
+        if (ti2 < ntk) {
+          const int row2 = ti2 * kNumQHeads + (rq >> 6) * kGroup + (rq & 7);
+          *reinterpret_cast<float4*>(opart + row2 * kHeadDim + 32 * h2 + 4 * (lane & 7)) =
+              *reinterpret_cast<const float4*>(stg + lr * kStgPitch + 4 * (lane & 7));
         }
       }
+      __syncwarp();  // the staging is rewritten by the next half
     }
     if (live && jw == 0) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
   }
