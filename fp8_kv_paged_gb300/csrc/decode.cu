@@ -267,8 +267,8 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   const int pbase = n - ql + i0;
   const int hi = pbase + ntk;                                           // keys < hi
   const int lo = a.window > 0 ? max(0, pbase - a.window + 1) : 0;     // first key any query sees
-  const int j0 = lo + wk.chunk * wk.chunk_keys;
-  const int j1 = min(hi, j0 + wk.chunk_keys);
+  const int j0 = lo + wk.koff;
+  const int j1 = min(hi, j0 + wk.cap);
   if (wk.chunk == wk.nchunks - 1 && j1 < hi) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
   const int ntiles = j1 > j0 ? (j1 - j0 + kTileKeys - 1) / kTileKeys : 0;

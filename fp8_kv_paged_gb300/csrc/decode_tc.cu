@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   const int pbase = n - ql + wk.i0;
   const int hi = pbase + ntk;  // keys < hi
   const int lo = a.window > 0 ? max(0, pbase - a.window + 1) : 0;
-  const int j0 = lo + wk.chunk * wk.chunk_keys;
-  const int j1 = min(hi, j0 + wk.chunk_keys);
+  const int j0 = lo + wk.koff;
+  const int j1 = min(hi, j0 + wk.cap);
   if (wk.chunk == wk.nchunks - 1 && j1 < hi) bad_len = true;  // plan does not cover the keys
   if (bad_len && tid == 0) set_error(a.err, OKC_DEVERR_LENGTHS);
   const int jt = kTma ? (j0 & ~7) : j0;  // first key of tile 0 (keys below j0 are masked)

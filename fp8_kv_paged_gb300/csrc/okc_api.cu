@@ -64,6 +64,97 @@ int page_shift(int P) {
 // 128 keys per item unless the block is shorter, so short or windowed blocks
 // get few splits and long ones many (the H200 bound cdiv(132, B*Hkv) of
 // "012-attention-local-splits.py" plays the same role with a fixed SM count).
+// The tail of a work list of more than one wave in finer items. Items start
+// in launch order as resident CTA slots free up, and equal items do not run at
+// equal speed (the CTAs on an SM share its bandwidth), so the items that
+// start last decide the step's end: the items that would start in the last
+// kTailPct percent of the work (each item counted with `item_cost` keys on top
+// of its own) are cut into up to kTailParts items of at least kTailMinKeys
+// keys each, at whole 64-key tiles from the item's start, within the list's
+// capacity `wcap`, and the tail is put back in largest-first order. A block's
+// items stay contiguous in slot order: slots, chunk numbers and counts are
+// renumbered by one prefix sum over the pieces per original slot, and a
+// block's last piece keeps the room its last item had for longer device
+// lengths.
+#ifndef OKC_TAIL_PCT
+#define OKC_TAIL_PCT 30
+#endif
+#ifndef OKC_TAIL_PARTS
+#define OKC_TAIL_PARTS 3
+#endif
+namespace {
+constexpr int kTailPct = OKC_TAIL_PCT, kTailParts = OKC_TAIL_PARTS;
+constexpr int64_t kTailMinKeys = 256;
+
+void split_tail(okc::SplitResult* r, int64_t wcap, int slots, int64_t item_cost) {
+  std::vector<WorkItem>& work = r->work;
+  const int64_t W = (int64_t)work.size();
+  if (kTailPct <= 0 || kTailParts < 2 || W <= slots || W >= wcap) return;
+  int64_t total = 0;
+  for (const WorkItem& w : work) total += (int64_t)(w.j1 - w.j0) + item_cost;
+  // pieces per original slot (the list holds slots 0 .. W-1 once each)
+  std::vector<int32_t> parts((size_t)W + 1, 1);
+  const int64_t start_tail = total - total * kTailPct / 100;
+  int64_t before = 0, added = 0;
+  for (const WorkItem& w : work) {
+    const int64_t n = (int64_t)(w.j1 - w.j0);
+    if (before >= start_tail) {
+      const int64_t p = std::min<int64_t>(kTailParts, n / std::max<int64_t>(kTailMinKeys, 64));
+      if (p >= 2 && W + added + p - 1 <= wcap) {
+        parts[(size_t)(w.wbase + w.chunk)] = (int32_t)p;
+        added += p - 1;
+      }
+    }
+    before += n + item_cost;
+  }
+  if (added == 0) return;
+  // first new slot of each original slot (exclusive prefix sum)
+  std::vector<int32_t> first((size_t)W + 1);
+  int32_t acc = 0;
+  for (int64_t s = 0; s < W; s++) {
+    first[(size_t)s] = acc;
+    acc += parts[(size_t)s];
+  }
+  first[(size_t)W] = acc;
+  for (okc::BlockInfo& q : r->blocks) {
+    const int32_t w0 = first[(size_t)q.wbase], w1 = first[(size_t)(q.wbase + q.nchunks)];
+    q.wbase = w0;
+    q.nchunks = w1 - w0;
+    r->max_chunks = std::max(r->max_chunks, (int)q.nchunks);
+  }
+  std::vector<WorkItem> out;
+  out.reserve((size_t)acc);
+  size_t tail_from = 0;  // the first piece of a split item (the tail starts there)
+  bool in_tail = false;
+  for (const WorkItem& w : work) {
+    const int32_t old_slot = w.wbase + w.chunk, p = parts[(size_t)old_slot];
+    const int32_t wbase = first[(size_t)w.wbase];
+    const int32_t nchunks = first[(size_t)(w.wbase + w.nchunks)] - wbase;
+    const int64_t n = (int64_t)(w.j1 - w.j0);
+    if (p > 1 && !in_tail) {
+      in_tail = true;
+      tail_from = out.size();
+    }
+    for (int32_t q = 0; q < p; q++) {
+      WorkItem x = w;
+      const int64_t a = n * q / p / 64 * 64, b = q + 1 < p ? n * (q + 1) / p / 64 * 64 : n;
+      x.j0 = w.j0 + (int32_t)a;
+      x.j1 = w.j0 + (int32_t)b;
+      x.koff = w.koff + (int32_t)a;
+      x.cap = q + 1 < p ? (int32_t)(b - a) : w.cap - (int32_t)a;  // the last piece keeps the item's end room
+      x.chunk = first[(size_t)old_slot] - wbase + q;
+      x.wbase = wbase;
+      x.nchunks = nchunks;
+      out.push_back(x);
+    }
+  }
+  // the tail largest first (ties: launch order)
+  std::stable_sort(out.begin() + (std::ptrdiff_t)tail_from, out.end(),
+                   [](const WorkItem& x, const WorkItem& y) { return x.j1 - x.j0 > y.j1 - y.j0; });
+  work.swap(out);
+}
+}  // namespace
+
 okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const int32_t* q_lens,
                             const okc_plan_options* o, int slots, SplitResult* r) {
   const int B = c->batch, Lmax = c->q_len;
@@ -248,8 +339,8 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
   auto item = [&](int u, int k, int64_t j0, int64_t j1) {
     const Unit& x = units[(size_t)u];
     const BlockInfo& q = r->blocks[(size_t)u];
-    return WorkItem{x.b, u, x.i0, x.ntok, k, (int32_t)j0, (int32_t)j1, chunk_of[(size_t)u], q.nchunks, q.wbase,
-                    x.t0, x.last};
+    return WorkItem{x.b, (int32_t)(j0 - (x.hi - x.nvis)), x.i0, x.ntok, k, (int32_t)j0, (int32_t)j1,
+                    chunk_of[(size_t)u], q.nchunks, q.wbase, x.t0, x.last};
   };
   size_t il = 0;
   auto emit_last_before = [&](uint64_t key_word, int32_t slot) {  // last items ahead of (key, slot)
@@ -276,6 +367,8 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
     for (int k = 0; k + 1 < q.nchunks; k++, j0 += ck) *out++ = item(u, k, j0, j0 + ck);
   }
   emit_last_before(~0ull, 0);
+  if (!(o && o->chunk_keys > 0) && S == 1 && slots > 0)
+    split_tail(r, (int64_t)std::max<int64_t>(U, 4 * (int64_t)slots), slots, kItemCost);
   return OKC_OK;
 }
 

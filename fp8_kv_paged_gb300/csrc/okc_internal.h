@@ -25,15 +25,18 @@ constexpr size_t kWsCount = 64;
 // request of ql new tokens has ceil(ql / S) blocks; decode and verify steps have
 // one block per request.
 //
-// One split work item: keys [j0, j1) (chunk `chunk` of the block's visible keys
-// under the plan's lengths; the kernel starts loading page ids with them and
-// checks them against the device lengths) for query block `blk`, tokens
-// [i0, i0 + ntok) of request b, token t0 of the step its first (under the plan's
-// q lengths); its output slot is wbase + chunk. chunk_keys, nchunks and wbase
-// repeat the block's split; `last` marks the request's last block.
+// One split work item: keys [j0, j1) (under the plan's lengths; the kernel
+// starts loading page ids with them) for query block tokens [i0, i0 + ntok) of
+// request b, token t0 of the step its first (under the plan's q lengths). The
+// kernel derives its keys from the device lengths: [lo + koff, min(hi, lo +
+// koff + cap)) for the block's visible range [lo, hi), and checks that the
+// block's items still cover it; cap is the item's key count, or more for a
+// block's last item (the room the plan's chunking leaves for longer device
+// lengths). Its output slot is wbase + chunk; nchunks and wbase repeat the
+// block's split; `last` marks the request's last block.
 struct WorkItem {
-  int32_t b, blk, i0, ntok;
-  int32_t chunk, j0, j1, chunk_keys;
+  int32_t b, koff, i0, ntok;
+  int32_t chunk, j0, j1, cap;
   int32_t nchunks, wbase, t0, last;
 };
 // Per query block: first output slot, number of splits, first token of the

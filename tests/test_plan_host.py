@@ -3,8 +3,9 @@ and the CTAs per SM, so planning makes no CUDA call): every request's visible
 keys are covered once, in order, by its work items; item sizes are whole
 64-key tiles (counting the TMA-fed tile start of the tcgen05 path); items
 launch largest first; the item count respects the waves the heuristic allows;
-the plan's sizes agree with its item list; and the step form follows the
-documented rule on the workloads' shapes."""
+a list of more than one wave ends in finer items; the plan's sizes agree with
+its item list; and the step form follows the documented rule on the
+workloads' shapes."""
 import numpy as np
 import pytest
 
@@ -38,7 +39,8 @@ def _check_cover(cfg, seq, items):
         assert 0 <= b < B and j0 < j1
         by_req[b].append((int(j0), int(j1)))
     for b in range(B):
-        r = sorted(by_req[b])
+        by_req[b].sort()  # in key order
+        r = by_req[b]
         assert r, f"request {b} has no work item"
         assert r[0][0] == lo[b] and r[-1][1] == hi[b]
         for (a0, a1), (b0, b1) in zip(r, r[1:]):
@@ -63,17 +65,36 @@ def test_workload_plans_cover_every_key_once(name):
     # launch order: the largest items first
     lens = items[:, 2] - items[:, 1]
     assert np.all(np.diff(lens) <= 0)
-    # every item but a request's last has the same size, whole 64-key tiles
+    # every item but a request's last holds whole 64-key tiles; within one
+    # wave of the resident slots every such item of a request has one size
     pad = _pad(cfg)
     for r in by_req:
         full = {j1 - j0 for j0, j1 in r[:-1]}
-        assert len(full) <= 1
-        if full:
-            c = full.pop()
+        for c in full:
             assert (c + pad) % 64 == 0, c
-            assert r[-1][1] - r[-1][0] <= c
+        if len(items) <= SMS * CTAS:
+            assert len(full) <= 1
+            if full:
+                assert r[-1][1] - r[-1][0] <= max(full)
     # at most four waves of the resident slots (or one item per request)
     assert len(items) <= max(len(seq), 4 * SMS * CTAS)
+
+
+def test_lists_of_more_than_one_wave_end_in_finer_items():
+    """The items that start last decide the step's end, so a q_len-1 list of
+    more than one wave of the resident slots ends in smaller items: the mixed
+    batch's last tenth of items is at most half the size of its first."""
+    cfg = W.config("mixed_full_decode")
+    seq = W.lengths(cfg)
+    items = okc.okc_attn_plan_items(cfg, seq, HOST)
+    assert len(items) > SMS * CTAS
+    lens = items[:, 2] - items[:, 1]
+    n = len(lens) // 10
+    assert lens[-n:].max() * 2 <= lens[:n].min(), (lens[:n].min(), lens[-n:].max())
+    # one wave: no item is cut finer than the budget's chunks
+    cfg1 = W.config("sliding_decode")
+    items1 = okc.okc_attn_plan_items(cfg1, W.lengths(cfg1), HOST)
+    assert len(items1) <= SMS * CTAS
 
 
 def test_step_form_rule_on_the_workloads():
