@@ -60,11 +60,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("mixed_full_decode", "decode_kernel<fused step>"): 803062272 + 7515392,
-    ("sliding_decode", "decode_kernel<fused step>"): 33094656 + 1280,
-    ("full_decode_32k", "decode_kernel"): 545534720 + 3177472,
-    ("verify_block", "decode_tc_kernel"): 17209856 + 0,
-    ("extend", "decode_tc_kernel"): 36399104 + 43776,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 803951360 + 7561472,
+    ("sliding_decode", "decode_kernel<fused step>"): 33093888 + 2304,
+    ("full_decode_32k", "decode_kernel"): 545479168 + 3285248,
+    ("verify_block", "decode_tc_kernel"): 17210112 + 0,
+    ("extend", "decode_tc_kernel"): 36403968 + 448256,
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0

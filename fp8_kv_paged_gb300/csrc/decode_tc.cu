@@ -129,6 +129,15 @@ __device__ __forceinline__ uint32_t canon(int r, int kb) {
   return (uint32_t)((r >> 3) * kTcSbo + (kb >> 4) * kTcLbo + (r & 7) * 16 + (kb & 15));
 }
 
+// Row of [V | 1]^T (= column of O) that holds output dim d (d < 128): within
+// each block of 16 dims, dims 4a + 2b + c sit at 8b + 2a + c, so that each
+// 8-row matrix the V conversion stores with stmatrix.trans lies in one core
+// matrix (conflict-free; in dim order it straddled two, 2-way conflicts). The
+// epilogue reads O's columns through the same map.
+__host__ __device__ constexpr int vt_pos(int d) {
+  return (d & ~15) | (((d >> 1) & 1) << 3) | (((d >> 2) & 3) << 1) | (d & 1);
+}
+
 // The K and V caches as 2-D byte tensors [num_rows, 128] for TMA tile loads of
 // 8 rows (one swizzle atom), used when a page holds a multiple of 8 rows.
 struct TcMaps {
@@ -598,13 +607,14 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
           hi4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] >> 16));      // dims +2, +3
         }
         // stored matrix jm (lanes 8jm..8jm+7 give its rows): {lo, hi} of block 2*half + (jm >> 1);
-        // its row cc holds dim 16 c16 + 4 (cc >> 1) + 2 (jm & 1) + (cc & 1) for the 8 keys
+        // its row cc holds dim 16 c16 + 4 (cc >> 1) + 2 (jm & 1) + (cc & 1) for the 8 keys,
+        // stored at row vt_pos(dim) = 16 c16 + 8 (jm & 1) + cc
         const int jm = lane >> 3, cc = lane & 7;
 #pragma unroll
         for (int half = 0; half < 2; half++) {
           const int c16 = cbase + half * 2 + (jm >> 1);
-          const int d = 16 * c16 + 4 * (cc >> 1) + 2 * (jm & 1) + (cc & 1);
-          stsm_x4_trans(sb + sVT + canon(d, a8 * 16), lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1],
+          const int pr = 16 * c16 + 8 * (jm & 1) + cc;
+          stsm_x4_trans(sb + sVT + canon(pr, a8 * 16), lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1],
                         hi4[half * 2 + 1]);
         }
       }
@@ -661,11 +671,11 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       if (has0) tmem_ld32(t_lane + C::col_o(0) + 64 * g + 32 * h2, o0);
       if (has1) tmem_ld32(t_lane + C::col_o(NG - 1) + 64 * g + 32 * h2, o1);
 #pragma unroll
-      for (int d = 0; d < 32; d += 4) {
+      for (int d = 0; d < 32; d += 4) {  // dims 32 h2 + d + e, O columns through vt_pos
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; e++)
-          v[e] = ((has0 ? o0[d + e] * f0 : 0.f) + (has1 ? o1[d + e] * f1 : 0.f)) * inv;
+          v[e] = ((has0 ? o0[vt_pos(d + e)] * f0 : 0.f) + (has1 ? o1[vt_pos(d + e)] * f1 : 0.f)) * inv;
         *reinterpret_cast<float4*>(stg + lane * kStgPitch + d) = make_float4(v[0], v[1], v[2], v[3]);
       }
       __syncwarp();
