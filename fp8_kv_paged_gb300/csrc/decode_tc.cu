@@ -538,26 +538,36 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (__all_sync(0xffffffffu, klo == 0 && khi == kTcTileKeys)) {  // every key valid for the warp's rows
 #pragma unroll
-      for (int c = 0; c < 32; c++) mx4[c & 3] = fmaxf(mx4[c & 3], fmaxf(s0[c], s1[c]));
+      for (int c = 0; c < 32; c++) mx4[c & 3] = fmax3(mx4[c & 3], s0[c], s1[c]);
     } else {
 #pragma unroll
       for (int c = 0; c < 32; c++) {
         s0[c] = (uint32_t)(c - klo) < kn ? s0[c] : -INFINITY;
         s1[c] = (uint32_t)(32 + c - klo) < kn ? s1[c] : -INFINITY;
-        mx4[c & 3] = fmaxf(mx4[c & 3], fmaxf(s0[c], s1[c]));
+        mx4[c & 3] = fmax3(mx4[c & 3], s0[c], s1[c]);
       }
     }
     // in log2 units (the scale is positive)
-    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+    const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]) * scale_log2;
+    // ---- reference max: moves when the row max passes it by more than 2^8
+    const float m_new = (m == -INFINITY || mx > m + kTcRescale) ? fmaxf(m, mx) : m;
+    const float alpha = m_new == m ? 1.f : (m == -INFINITY ? 0.f : fast_exp2(m - m_new));
+    m = m_new;
+    const float m_use = m == -INFINITY ? 0.f : m;
+    // ---- P row (f16), two keys per 32-bit word: p = 2^(s * scale - m) in f32,
+    // rounded to f16; computed before the wait below, which it does not need
+    uint32_t pw[32];
+#pragma unroll
+    for (int c = 0; c < 32; c++) {
+      const float x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32], x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+      pw[c] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
+    }
     // ---- P, V^T and O of this group are free once its previous PV completed
     if (k >= kTcGroups) {
       const bool w2 = mbar_wait(pv_done(jw), ((k - NG) >> (NG - 1)) & 1);
       if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
       tc_fence_after();
     }
-    // ---- reference max: moves when the row max passes it by more than 2^8
-    const float m_new = (m == -INFINITY || mx > m + kTcRescale) ? fmaxf(m, mx) : m;
-    const float alpha = m_new == m ? 1.f : (m == -INFINITY ? 0.f : fast_exp2(m - m_new));
     if (k >= kTcGroups && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
       float ov[16];
 #pragma unroll
@@ -569,19 +579,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       }
       tmem_st1(tL, tmem_ld1(tL) * alpha);
     }
-    m = m_new;
-    const float m_use = m == -INFINITY ? 0.f : m;
-    // ---- P row (f16) into this group's TMEM P columns (the PV's A operand),
-    // two keys per column: p = 2^(s * scale - m) in f32, rounded to f16
-    {
-      uint32_t pw[32];
-#pragma unroll
-      for (int c = 0; c < 32; c++) {
-        const float x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32], x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-        pw[c] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
-      }
-      tmem_st32u(tP, pw);
-    }
+    // ---- P into this group's TMEM P columns (the PV's A operand)
+    tmem_st32u(tP, pw);
     // ---- V tile E4M3 -> f16, transposed into this group's canonical B tile
     // (dims x keys). Warp w of the group converts key groups 2w, 2w+1 (8 keys
     // each) x 8 groups of 16 dims.

@@ -21,7 +21,7 @@ LIMITS = {
     "decode_kernelILi2ELi1ELi4ELb1E": (80, 16),   # the fused step (sliding, mixed)
     "decode_kernelILi2ELi1ELi4ELb0E": (80, 0),    # q_len-1 decode of the three-call step
     "decode_tc_kernelILb1ELi2E": (112, 0),        # verify block, TMA gather
-    "decode_tc_kernelILb0ELi2E": (112, 0),        # verify block, cp.async gather
+    "decode_tc_kernelILb0ELi2E": (120, 0),        # verify block on pages of < 8 rows, cp.async gather (allocated as 120)
     "decode_tc_kernelILb1ELi1E": (128, 0),        # extend, TMA gather
     "decode_tc_kernelILb0ELi1E": (128, 0),        # extend, cp.async gather
     "prepare_kernel": (64, 0),
