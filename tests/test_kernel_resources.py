@@ -1,8 +1,8 @@
 """Per-kernel resources as ptxas reports them for sm_103a (-Xptxas -v; no GPU):
 the hot kernels keep the register counts their occupancy rests on (the decode
 kernels for q_len 1 at 80 registers x 256 threads: three CTAs per SM; the
-two-group tcgen05 decode (verify blocks) at 112 x 352: one CTA per SM with room
-for the prepare and combine CTAs beside it; the one-group tcgen05 decode
+two-group tcgen05 decode (verify blocks) at 120 x 352 as allocated: one CTA per
+SM with room for a prepare and two combine CTAs beside it; the one-group tcgen05 decode
 (extends) at 128 x 224: two CTAs per SM; the combine for blocks of several
 tokens under 64 x 128, so that two of its CTAs fit beside a tcgen05 decode CTA)
 and spill nothing beyond the fused step's known 16-byte frame."""
@@ -20,7 +20,7 @@ CSRC = os.path.join(ROOT, "fp8_kv_paged_gb300", "csrc")
 LIMITS = {
     "decode_kernelILi2ELi1ELi4ELb1E": (80, 16),   # the fused step (sliding, mixed)
     "decode_kernelILi2ELi1ELi4ELb0E": (80, 0),    # q_len-1 decode of the three-call step
-    "decode_tc_kernelILb1ELi2E": (112, 0),        # verify block, TMA gather
+    "decode_tc_kernelILb1ELi2E": (120, 0),        # verify block, TMA gather (allocated as 120)
     "decode_tc_kernelILb0ELi2E": (120, 0),        # verify block on pages of < 8 rows, cp.async gather (allocated as 120)
     "decode_tc_kernelILb1ELi1E": (128, 0),        # extend, TMA gather
     "decode_tc_kernelILb0ELi1E": (128, 0),        # extend, cp.async gather
