@@ -52,6 +52,7 @@
 // and step 5 (the last CTA of each request merges the splits).
 #include "normgate.cuh"
 #include "okc_common.cuh"
+#include "fused_rows.cuh"
 #include "okc_internal.h"
 
 namespace okc {
@@ -133,41 +134,6 @@ __device__ __forceinline__ void fused_q_frag(const DecodeArgs& a, int64_t t, int
   for (int grp = 0; grp < 4; grp++)
     q[grp >> 1][grp & 1] = (uint32_t)f32x2_to_e4m3x2(y[grp * 4], y[grp * 4 + 1]) |
                            ((uint32_t)f32x2_to_e4m3x2(y[grp * 4 + 2], y[grp * 4 + 3]) << 16);
-}
-
-// The new key row of token t for KV head g: this lane's dims 2*lane, 2*lane+1 of
-// K (RMSNorm + RoPE, / k_scale on the scaled path) and of V (raw, / v_scale),
-// as two E4M3 pairs. All 32 lanes take part (the head's reduction).
-__device__ __forceinline__ void fused_new_kv(const DecodeArgs& a, int64_t t, int g, int lane, uint16_t& k8,
-                                             uint16_t& v8, bool& pos_err) {
-  const uint16_t* row = a.qkv + t * kQkvWidth;
-  const uint32_t kr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + g) * kHeadDim + 2 * lane);
-  const uint32_t vr = *reinterpret_cast<const uint32_t*>(row + (kNumQHeads + kNumKvHeads + g) * kHeadDim + 2 * lane);
-  const float x0 = bf16_bits_to_f32(kr & 0xFFFFu), x1 = bf16_bits_to_f32(kr >> 16);
-  const float xs[2] = {x0, x1};
-  const float inv = rms_inverse<32, 2>(xs, kRmsEps);
-  float y0 = bf16_round(__fmul_rn(x0, inv)), y1 = bf16_round(__fmul_rn(x1, inv));
-  if (a.rope) {
-    const int64_t pos = a.positions[t];
-    if (pos >= 0 && pos < a.rope_positions) {
-      const float c = a.rope_table[pos * kHeadDim + lane], sn = a.rope_table[pos * kHeadDim + kHeadDim / 2 + lane];
-      const float e = y0, o = y1;
-      y0 = bf16_round(__fsub_rn(__fmul_rn(e, c), __fmul_rn(o, sn)));
-      y1 = bf16_round(__fadd_rn(__fmul_rn(o, c), __fmul_rn(e, sn)));
-    } else {
-      pos_err = true;
-    }
-  }
-  float v0 = bf16_bits_to_f32(vr & 0xFFFFu), v1 = bf16_bits_to_f32(vr >> 16);
-  if (a.scaled) {
-    const float ks = *a.k_scale, vs = *a.v_scale;
-    y0 = bf16_round(__fdiv_rn(y0, ks));
-    y1 = bf16_round(__fdiv_rn(y1, ks));
-    v0 = bf16_round(__fdiv_rn(v0, vs));
-    v1 = bf16_round(__fdiv_rn(v1, vs));
-  }
-  k8 = f32x2_to_e4m3x2(y0, y1);
-  v8 = f32x2_to_e4m3x2(v0, v1);
 }
 
 template <int KS, int NTW, int NCW>

@@ -55,6 +55,8 @@
 #include <algorithm>
 #include <cstring>
 
+#include "fused_rows.cuh"
+#include "normgate.cuh"
 #include "okc_common.cuh"
 #include "okc_internal.h"
 
@@ -101,9 +103,13 @@ struct TcCfg {
   static constexpr int kV = kK + kStages * kTcTileKeys * 128;             // V E4M3 [stage][64 x 144 B]
   static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][144 x 64 keys]
   static constexpr int kX = kVT + NG * kTcVTBytes;                        // each group's reference max per row
-  static constexpr int kBar = kX + NG * kTcRows * 4;
-  // barriers: full[S], empty[S], s_ready[NG], p_ready[NG], pv_done[NG], s_free[NG], mma_done
-  static constexpr int kTmemSlot = kBar + (2 * kStages + 4 * NG + 1) * 8;
+  // the one-kernel step: the step's new K and V rows for this CTA's keys (at
+  // most 8 keys x K | V x 128 bytes), computed once and put into the tiles
+  static constexpr int kNew = kX + NG * kTcRows * 4;
+  static constexpr int kNewBytes = NG == 2 ? 8 * 2 * 128 : 0;
+  static constexpr int kBar = kNew + kNewBytes;
+  // barriers: full[S], empty[S], s_ready[NG], p_ready[NG], pv_done[NG], s_free[NG], mma_done, new_ready
+  static constexpr int kTmemSlot = kBar + (2 * kStages + 4 * NG + 2) * 8;
   static constexpr int kSmem = kTmemSlot + 16 + 2048;  // + slack past the last operand
   // TMEM columns. NG = 2: S_j at 64 j (64), O_j at 128 + 160 j (144), P_j (f16,
   // two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j.
@@ -153,10 +159,11 @@ struct TcMaps {
 // the PV product through P = 0. Rows never loaded keep what the stage held
 // before (zeros at the start, else keys of earlier tiles). Otherwise tiles
 // arrive by 16-byte cp.async per row chunk (any page size).
-template <bool kTma, int NG>
+template <bool kTma, int NG, bool FUSED>
 __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<NG>;
+  static_assert(!FUSED || NG == 2, "the one-kernel step runs blocks of at most 8 tokens with two softmax groups");
   constexpr int kTcStages = C::kStages, kTcGroups = NG, kTcMmaWarp = C::kMmaWarp, kTcThreads = C::kThreads;
   constexpr int kTcProducers = C::kProducers;
   constexpr int kGroupsPW = 8 / kTcProducers;  // TMA: 8-row groups of a tile per producer warp
@@ -173,6 +180,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   auto pv_done = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + 2 * kTcGroups + j); };
   auto s_free = [&](int j) { return sb + kTcBar + 8 * (2 * kTcStages + 3 * kTcGroups + j); };
   const uint32_t mma_done = sb + kTcBar + 8 * (2 * kTcStages + 4 * kTcGroups);
+  const uint32_t new_ready = mma_done + 8;  // the one-kernel step: the new K/V rows are in kNew
 
   // a fixed-capacity plan launches its capacity: CTAs past the live count return
   if (a.live_work && (int)blockIdx.x >= *a.live_work) return;
@@ -191,6 +199,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       mbar_init(s_free(j), kTcRows);
     }
     mbar_init(mma_done, 1);
+    mbar_init(new_ready, 32 * kTcProducers);
     fence_mbar_init();
   }
   if (warp == kTcMmaWarp) tmem_alloc(sb + kTcTmemSlot, kTcCols);
@@ -201,6 +210,13 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     }
   }
   const int b = wk.b;
+  // The one-kernel step reads only caller inputs that the preceding kernels may
+  // write: it waits for them first, unless the plan's OKC_PLAN_EARLY_GATHER
+  // promise lets it load lengths, page ids and cached keys before the wait
+  // (q, the new rows and every write still wait).
+  if constexpr (FUSED) {
+    if (!a.early) pdl_wait();
+  }
 
   // ---- producer set-up (as decode.cu): page ids of the first tiles with the
   // plan's key range while the device lengths load. Producer warp pw owns keys
@@ -270,15 +286,52 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       for (int t = 0; t < kTcStages; t++) load_ids(ids[t], t, j0, j1);
     }
     const int pmask = P - 1;
-    const int newk = n - ql;  // keys >= newk are written by the prepare kernel
+    const int newk = n - ql;  // keys >= newk are the step's new keys (written by the prepare kernel)
     const int rr = lane >> 3, ch = lane & 7;
-    bool dep = false, bad_page = false;
+    bool dep = false, bad_page = false, pos_err = false, new_ok = true;
+    // The one-kernel step: the new keys of this CTA's tiles, [max(jt, newk), j1),
+    // computed here (producer warp pw: KV head pw) into kNew; the keys of its
+    // own range [j0, j1) also written to the cache (keys below j0 belong to the
+    // previous chunk's CTA, which writes them; its tiles would read them from
+    // the cache while they are written). The block is the request's only one
+    // (q_len <= 8), so key newk + i is token i of the request.
+    static_assert(!FUSED || kTcProducers == kNumKvHeads, "one producer warp per KV head");
+    auto new_rows = [&]() {
+      pdl_wait();  // qkv, positions and cache_loc: caller inputs
+      const int jb = max(jt, newk), cnt = max(0, min(8, j1 - jb));
+      uint16_t k8[8], v8[8];
+      int64_t slot[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) slot[i] = (i < cnt && jb + i >= j0) ? a.cache_loc[qb + (jb + i - newk)] : -1;
+      fused_new_kv8(a, (int64_t)qb + (jb - newk), cnt, pw, lane, k8, v8, pos_err);
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        if (i >= cnt) break;
+        const int j = jb + i;
+        uint8_t* dst = smem + C::kNew + (j - newk) * 256 + pw * kHeadDim + 2 * lane;
+        *reinterpret_cast<uint16_t*>(dst) = k8[i];
+        *reinterpret_cast<uint16_t*>(dst + 128) = v8[i];
+        if (j >= j0) {
+          if (slot[i] >= 0 && slot[i] < a.num_rows) {
+            *reinterpret_cast<uint16_t*>(a.kc_w + slot[i] * kRowBytes + pw * kHeadDim + 2 * lane) = k8[i];
+            *reinterpret_cast<uint16_t*>(a.vc_w + slot[i] * kRowBytes + pw * kHeadDim + 2 * lane) = v8[i];
+          } else if (lane == 0) {
+            set_error(a.err, OKC_DEVERR_CACHE_LOC);
+          }
+        }
+      }
+      mbar_arrive(new_ready);                         // this warp's rows are in kNew
+      if (!mbar_wait(new_ready, 0)) new_ok = false;   // and the other warp's (bounded)
+    };
     auto issue = [&](int k, int id) {
       const int s = k % kTcStages;
       const uint32_t sK = sb + kTcK + s * (kTcTileKeys * 128), sV = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
       const int tj = jt + k * kTcTileKeys;
-      if (!dep && min(j1, tj + kTcTileKeys) > newk) {  // this tile holds a key prepare writes
-        pdl_wait();
+      if (!dep && min(j1, tj + kTcTileKeys) > newk) {  // this tile holds a new key
+        if constexpr (FUSED)
+          new_rows();
+        else
+          pdl_wait();  // written by the prepare kernel
         dep = true;
       }
       if constexpr (kTma) {
@@ -295,28 +348,44 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
             bad_page = true;
           }
         }
-        const unsigned whole = __ballot_sync(0xffffffffu, nrows == 8);
+        // (the one-kernel step: a group holding a new key is not loaded whole)
+        const bool plain = nrows == 8 && (!FUSED || key + 8 <= newk);
+        const unsigned whole = __ballot_sync(0xffffffffu, plain);
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(whole) * 2u * 1024u);
         __syncwarp();
-        if (nrows == 8) {
+        if (plain) {
           tma_load_2d(sK + gi * 1024, &maps.k, 0, row, full_bar(s));
           tma_load_2d(sV + gi * 1024, &maps.v, 0, row, full_bar(s));
         }
-        // the group cut by the chunk's end (at most one): its rows by 16-byte
-        // cp.async chunks into the same swizzled positions, all lanes
-        const unsigned cut = __ballot_sync(0xffffffffu, nrows > 0 && nrows < 8);
-        if (cut) {
-          const int lc = __ffs(cut) - 1, gc = pw * kGroupsPW + lc;
+        // the group cut by the chunk's end (at most one) and, in the one-kernel
+        // step, the groups holding new keys: their rows by 16-byte chunks into
+        // the same swizzled positions, all lanes; cached rows by cp.async, new
+        // rows from kNew
+        unsigned rest = __ballot_sync(0xffffffffu, nrows > 0 && !plain);
+        while (rest) {
+          const int lc = __ffs(rest) - 1, gc = pw * kGroupsPW + lc;
+          rest &= rest - 1;
           const int crow = __shfl_sync(0xffffffffu, row, lc), cn = __shfl_sync(0xffffffffu, nrows, lc);
+          const int ckey = tj + 8 * gc;
 #pragma unroll
           for (int h = 0; h < 2; h++) {
             const int cid = lane + 32 * h, r = cid >> 3, c = cid & 7;  // row r, chunk c of the group
             if (r < cn) {
               const uint32_t off = gc * 1024 + r * 128 + ((c ^ r) * 16);
-              cp_async_16(sK + off, a.kc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
-              cp_async_16(sV + off, a.vc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
+              if (!FUSED || ckey + r < newk) {
+                cp_async_16(sK + off, a.kc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
+                cp_async_16(sV + off, a.vc + (int64_t)(crow + r) * kRowBytes + c * 16, 16);
+              } else {
+                const uint8_t* src = smem + C::kNew + (ckey + r - newk) * 256 + c * 16;
+                *reinterpret_cast<uint4*>(smem + (sK - sb) + off) = *reinterpret_cast<const uint4*>(src);
+                *reinterpret_cast<uint4*>(smem + (sV - sb) + off) = *reinterpret_cast<const uint4*>(src + 128);
+              }
             }
           }
+        }
+        if constexpr (FUSED) {  // the stored rows: before the arrival, for the MMA (async proxy) too
+          __threadfence_block();
+          fence_proxy_async();
         }
         cp_async_mbar_arrive(full_bar(s));
       } else {
@@ -326,6 +395,13 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
           const int r = kbase + rl;
           const int pg = __shfl_sync(0xffffffffu, id, rl);
           const int j = tj + r;
+          if (FUSED && j < j1 && j >= newk) {  // a new key: from kNew (no copy, whose zero fill would race)
+            const uint8_t* src = smem + C::kNew + (j - newk) * 256 + ch * 16;
+            *reinterpret_cast<uint4*>(smem + (sK - sb) + canon(r, ch * 16)) = *reinterpret_cast<const uint4*>(src);
+            *reinterpret_cast<uint4*>(smem + (sV - sb) + r * kTcVPitch + ch * 16) =
+                *reinterpret_cast<const uint4*>(src + 128);
+            continue;
+          }
           int64_t row = 0;
           int bytes = 0;
           if (j < j1) {
@@ -339,6 +415,10 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
           cp_async_16(sK + canon(r, ch * 16), a.kc + row * kRowBytes + ch * 16, bytes);
           cp_async_16(sV + r * kTcVPitch + ch * 16, a.vc + row * kRowBytes + ch * 16, bytes);
         }
+        if constexpr (FUSED) {
+          __threadfence_block();
+          fence_proxy_async();
+        }
         cp_async_mbar_arrive(full_bar(s));
       }
     };
@@ -346,6 +426,14 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     for (int t = 0; t < kTcStages; t++) {
       if (t < ntiles) issue(t, ids[t]);
       load_ids(ids[t], t + kTcStages, j0, j1);
+    }
+    // the one-kernel step: the new rows of a later tile now, while the first
+    // tiles are consumed, not when that tile is issued
+    if constexpr (FUSED) {
+      if (!dep && ntiles > 0 && j1 > newk) {
+        new_rows();
+        dep = true;
+      }
     }
     bool ok = true;
     int issued = min(ntiles, kTcStages);  // tiles whose copies were issued
@@ -361,6 +449,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       }
     }
     if (bad_page && (kTma || ch == 0)) set_error(a.err, OKC_DEVERR_PAGE);
+    if (pos_err && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
+    if (!new_ok) ok = false;
     if constexpr (kTma) {
       // the CTA's shared memory must outlive the copies in flight: wait (bounded,
       // also after a timeout) until the last issued tile of every stage landed
@@ -464,8 +554,9 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   const int g = r >> 6, ti = (r >> 3) & 7, hh = r & 7;
   const int head = g * kGroup + hh;
   const bool live = ti < ntk;
-  pdl_wait();  // q_fp8 is the prepare kernel's output
+  pdl_wait();  // q_fp8 is the prepare kernel's output (the one-kernel step: qkv, a caller input)
   pdl_launch_dependents();
+  bool q_pos_err = false;
   {
     // Q row r: the 64 E4M3 dims of (token ti, head) at K bytes [64g, 64g+64),
     // zeros elsewhere; group jw writes chunks [8 jw / NG, 8 (jw + 1) / NG) of the row
@@ -474,14 +565,21 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     if constexpr (C::kQTmem) {
       // group jw: K bytes [64 jw, 64 jw + 64), 16 TMEM columns from col_q(2 jw)
       float qv[16];
+      if constexpr (FUSED) {  // the row from qkv (steps 1-3 of the block), by the group of its KV head
+        uint32_t qw[16];
+        fused_q_row(a, (int64_t)qb + wk.i0 + (live ? ti : 0), head, live && g == jw, qw, q_pos_err);
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (live && g == jw) v = src[c];
-        qv[4 * c] = __uint_as_float(v.x);
-        qv[4 * c + 1] = __uint_as_float(v.y);
-        qv[4 * c + 2] = __uint_as_float(v.z);
-        qv[4 * c + 3] = __uint_as_float(v.w);
+        for (int i = 0; i < 16; i++) qv[i] = __uint_as_float(qw[i]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (live && g == jw) v = src[c];
+          qv[4 * c] = __uint_as_float(v.x);
+          qv[4 * c + 1] = __uint_as_float(v.y);
+          qv[4 * c + 2] = __uint_as_float(v.z);
+          qv[4 * c + 3] = __uint_as_float(v.w);
+        }
       }
       tmem_st16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::col_q(2 * jw), qv);
     } else {
@@ -500,6 +598,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     const uint32_t one2 = rr2 == 128 ? 0x3C003C00u : 0u;  // f16 1.0 pairs
     *reinterpret_cast<uint4*>(smem + kTcVT + gj * kTcVTBytes + canon(rr2, c * 16)) = make_uint4(one2, one2, one2, one2);
   }
+  if (__any_sync(0xffffffffu, q_pos_err) && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
   fence_proxy_async();  // shared-memory operands, for the MMAs
   tc_fence_before();    // Q's TMEM stores (kQTmem), before the MMA thread reads them
   named_bar_sync(1, (kTcMmaWarp + 1) * 32);
@@ -695,6 +794,36 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   }
   tc_fence_before();
   named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // TMEM reads done: the MMA warp may free it
+  if constexpr (FUSED) {
+    // The block's last CTA merges every split and applies the norm-gate: once
+    // both groups' partials are written (barrier), one thread takes a ticket
+    // with an acquire-release atomic (publishing them); the CTA that draws the
+    // last ticket reads all partials (L2 loads) and resets the counter for the
+    // next launch. Nothing waits on another CTA.
+    volatile int& s_last = *reinterpret_cast<volatile int*>(smem + kTcX);  // (the maxima are read)
+    named_bar_sync(3, kTcGroups * kTcRows);
+    if (tid == 0) {
+      int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(prev) : "l"(a.tickets + b) : "memory");
+      s_last = prev == wk.nchunks - 1;
+    }
+    named_bar_sync(3, kTcGroups * kTcRows);
+    if (s_last) {
+      const int rows = a.S * kNumQHeads;
+      const int64_t base = (int64_t)wk.wbase * rows;
+      for (int rowi = tid >> 3; rowi < ntk * kNumQHeads; rowi += kTcGroups * kTcRows / 8) {  // 8 lanes per row
+        const int tok = rowi / kNumQHeads, h = rowi % kNumQHeads;
+        const int64_t t = (int64_t)qb + wk.i0 + tok;
+        const int c0 = (tid & 7) * 8;
+        float gg[8], ww[8];
+        load_gate_weight(a.qkv, a.weight, (int)t, h, c0, gg, ww);
+        merge_normgate<4>(a.lse_part + base + rowi, rows, a.o_part + (base + rowi) * kHeadDim + c0,
+                          (int64_t)rows * kHeadDim, wk.nchunks, gg, ww, a.eps,
+                          a.out + t * (kNumQHeads * kHeadDim) + h * kHeadDim + c0);
+      }
+      if (tid == 0) a.tickets[b] = 0;
+    }
+  }
 }
 
 }  // namespace
@@ -732,7 +861,7 @@ bool encode_cache_map(CUtensorMap* m, const uint8_t* base, int64_t rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NG>
+template <int NG, bool FUSED>
 cudaError_t launch_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   using C = TcCfg<NG>;
   cudaLaunchConfig_t cfg = {};
@@ -750,24 +879,33 @@ cudaError_t launch_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t 
   std::memset(&maps, 0, sizeof maps);
   const int64_t rows = (int64_t)a.num_pages << a.page_shift;
   if (a.page_shift >= 3 && encode_cache_map(&maps.k, a.kc, rows) && encode_cache_map(&maps.v, a.vc, rows))
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true, NG>, a, maps);
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false, NG>, a, maps);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<true, NG, FUSED>, a, maps);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<false, NG, FUSED>, a, maps);
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
   if (a.S < 1 || a.S > 8) return cudaErrorInvalidValue;
-  if (a.tc_groups == 1) return launch_tc<1>(a, num_work, pdl, s);
-  if (a.tc_groups == 2) return launch_tc<2>(a, num_work, pdl, s);
+  if (a.tc_groups == 1) return launch_tc<1, false>(a, num_work, pdl, s);
+  if (a.tc_groups == 2) return launch_tc<2, false>(a, num_work, pdl, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_step_fused_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
+  if (num_work == 0) return cudaSuccess;
+  if (a.L < 2 || a.L > 8 || a.S != a.L || a.tc_groups != 2) return cudaErrorInvalidValue;
+  return launch_tc<2, true>(a, num_work, pdl, s);
 }
 
 template <int NG>
 int tc_ctas_per_sm() {
   using C = TcCfg<NG>;
   int lowest = 0;
-  for (int v = 0; v < 2; v++) {
-    auto kern = v ? decode_tc_kernel<true, NG> : decode_tc_kernel<false, NG>;
+  // (every variant's shared-memory limit is raised here, the one-kernel step's too)
+  for (int v = 0; v < 4; v++) {
+    if (v >= 2 && NG != 2) break;
+    auto kern = v == 0 ? decode_tc_kernel<false, NG, false> : v == 1 ? decode_tc_kernel<true, NG, false>
+              : v == 2 ? decode_tc_kernel<false, NG, NG == 2> : decode_tc_kernel<true, NG, NG == 2>;
     int nb = 0;
     // (the largest shared-memory carveout: two one-group CTAs need ~210 KB per SM)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||

@@ -383,8 +383,13 @@ namespace {
 // for one wave of long chunks, where the separate merge overlaps the decode's
 // tail).
 int step_kernels(const okc_attn_config* c, const SplitResult& s, const okc_plan_options* o, int slots) {
-  if (c->q_len != 1) return 3;
   const int flags = o ? o->flags : 0;
+  if (c->q_len != 1) {
+    // blocks of 2..8 tokens on the tcgen05 kernel (one block per request): the
+    // one-kernel form when the options ask for it
+    const bool one = c->q_len <= 8 && okc::uses_tc(*c, o) && okc::tc_groups(*c) == 2 && s.S == c->q_len;
+    return one && (flags & OKC_PLAN_STEP_ONE_LAUNCH) && !(flags & OKC_PLAN_STEP_THREE_LAUNCHES) ? 1 : 3;
+  }
   if (flags & OKC_PLAN_STEP_THREE_LAUNCHES) return 3;
   if (flags & OKC_PLAN_STEP_ONE_LAUNCH) return 1;
   const int64_t W = (int64_t)s.work.size();
@@ -520,8 +525,8 @@ void set_splits(okc_attn_plan_s* p, SplitResult& s, const okc_attn_sizes& z) {
   p->d_blk = reinterpret_cast<BlockInfo*>(ws + okc::kWsHeader + round_up(cap * sizeof(WorkItem)));
   p->d_tickets = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(p->d_blk) +
                                             round_up(p->blocks.size() * sizeof(BlockInfo)));
-  // (one arrival counter per request: the one-kernel step runs blocks of one token,
-  // at most one per request)
+  // (one arrival counter per request: the one-kernel step runs at most one
+  // block per request)
   p->d_q8 = reinterpret_cast<uint8_t*>(p->d_tickets) + round_up((size_t)p->cfg.batch * sizeof(int32_t));
 }
 
@@ -1080,7 +1085,14 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.early = (plan->opts.flags & OKC_PLAN_EARLY_GATHER) && plan->pdl ? 1 : 0;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   if (plan->sizes.step_kernels == 1) {
-    cudaError_t e = okc::launch_step_fused(a, launch_items(plan), plan->pdl, str);
+    cudaError_t e;
+    if (plan->tc) {
+      a.tc = 1;
+      a.tc_groups = okc::tc_groups(c);
+      e = okc::launch_step_fused_tc(a, launch_items(plan), plan->pdl, str);
+    } else {
+      e = okc::launch_step_fused(a, launch_items(plan), plan->pdl, str);
+    }
     return e == cudaSuccess ? OKC_OK : OKC_ERR_CUDA;
   }
   // the three kernels, with q in the plan workspace

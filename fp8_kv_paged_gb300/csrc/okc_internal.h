@@ -228,6 +228,10 @@ int cached_ctas_per_sm(int dev, int S, bool tc, int tc_groups);
 // The tcgen05 decode kernel for blocks of 2..8 tokens (decode_tc.cu), with
 // a.tc_groups softmax warpgroups per CTA.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
+// The whole step in one launch for blocks of 2..8 tokens on the tcgen05 kernel
+// (q and the new K/V rows from qkv, attention, last-CTA merge and norm-gate);
+// requires L == S (one block per request) and two softmax groups.
+cudaError_t launch_step_fused_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
 int decode_tc_ctas_per_sm(int tc_groups);
 
 }  // namespace okc

@@ -38,6 +38,7 @@ namespace okc {
 cudaError_t launch_prepare(const PrepareArgs&, bool, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_decode(const DecodeArgs& a, int nw, bool, cudaStream_t) { g_dec = a; g_W = nw; g_launches++; return cudaSuccess; }
 cudaError_t launch_step_fused(const DecodeArgs&, int, bool, cudaStream_t) { return cudaSuccess; }
+cudaError_t launch_step_fused_tc(const DecodeArgs&, int, bool, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_combine(const CombineArgs& a, bool, cudaStream_t) { g_comb = a; g_launches++; return cudaSuccess; }
 cudaError_t launch_rope_table(float, const float*, int32_t, float*, cudaStream_t) { return cudaSuccess; }
 int decode_ctas_per_sm(int, bool tc, int) { return tc ? 1 : 3; }

@@ -78,7 +78,9 @@ def test_fused_repeated_launches_reuse_tickets():
 
 def test_step_form_chosen_by_the_plan():
     """q_len 1 steps that fill the GPU with short chunks run as one kernel; very
-    small batches, long chunks and verify blocks as three; the flags override."""
+    small batches, long chunks and verify blocks as three; the flags override
+    (verify blocks of up to 8 tokens on the tcgen05 kernel have a one-kernel
+    form too; longer blocks and the warp-level kernel do not)."""
     import fp8_kv_paged_gb300 as okc
     sliding = W.config("sliding_decode")
     seq = W.generate(sliding)["seq_lens"]
@@ -96,7 +98,13 @@ def test_step_form_chosen_by_the_plan():
     assert msz["step_kernels"] == 1 and msz["num_work"] > 456  # more than one wave
     verify = W.config("verify_block")
     vseq = W.generate(verify)["seq_lens"]
-    assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
+    assert okc.okc_attn_plan_sizes(verify, vseq)["step_kernels"] == 3
+    # blocks of 2..8 tokens on the tcgen05 kernel: one kernel when asked for
+    assert okc.okc_attn_plan_sizes(verify, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 1
+    warp = {"flags": okc.PLAN_STEP_ONE_LAUNCH | okc.PLAN_NO_TCGEN05}
+    assert okc.okc_attn_plan_sizes(verify, vseq, warp)["step_kernels"] == 3
+    longer = dict(verify, q_len=12)
+    assert okc.okc_attn_plan_sizes(longer, vseq, {"flags": okc.PLAN_STEP_ONE_LAUNCH})["step_kernels"] == 3
 
 
 def _host_tensor(a, memory):

@@ -39,9 +39,16 @@ def _adversarial_qkv(T, rng):
     return oracle.bf16_bits(np.clip(x, -3e38, 3e38))
 
 
-@pytest.mark.parametrize("rope,fused", [(0.0, False), (5e5, False), (5e5, True)])
-def test_rms_inverse_exact_on_adversarial_heads(rope, fused):
-    cfg = W.config("sliding_decode", batch=2048, seq=("uniform", 0, 40), rope_theta=rope, window=0)
+@pytest.mark.parametrize("rope,fused,L", [(0.0, False, 1), (5e5, False, 1), (5e5, True, 1), (5e5, True, 8)])
+def test_rms_inverse_exact_on_adversarial_heads(rope, fused, L):
+    """(L = 8 with fused: the one-kernel tcgen05 step, whose q rows are derived one
+    per thread inside the decode: its output equals the three calls' bit for bit,
+    whose q bytes equal the oracle's.)"""
+    if L == 1:
+        cfg = W.config("sliding_decode", batch=2048, seq=("uniform", 0, 40), rope_theta=rope, window=0)
+    else:
+        cfg = W.config("verify_block", batch=256, q_len=L, seq=("uniform", 0, 40), rope_theta=rope, window=0,
+                       kv_scale=1.0)
     inp = W.generate(cfg)
     inp["qkv"] = _adversarial_qkv(inp["qkv"].shape[0], np.random.default_rng(77))
     gpu = run_gpu(cfg, inp, fused=fused)
@@ -51,5 +58,10 @@ def test_rms_inverse_exact_on_adversarial_heads(rope, fused):
     loc = inp["cache_loc"]
     if not fused:
         assert np.array_equal(gpu["q8"], q8)
+    elif L > 1:
+        three = run_gpu(cfg, inp)
+        assert np.array_equal(three["q8"], q8)
+        assert gpu["sizes"]["step_kernels"] == 1
+        assert np.array_equal(gpu["out"], three["out"])
     assert np.array_equal(gpu["k_cache"].reshape(-1, 128)[loc], k.reshape(-1, 128)[loc])
     assert np.array_equal(gpu["v_cache"].reshape(-1, 128)[loc], v.reshape(-1, 128)[loc])
