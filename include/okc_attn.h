@@ -118,7 +118,9 @@ typedef struct okc_plan_options {
                               OKC_PLAN_NO_TCGEN05: q_len >= 2 decodes with the warp-level MMA kernel
                               (blocks of up to 16 tokens) instead of the tcgen05 one;
                               OKC_PLAN_STEP_ONE_LAUNCH / OKC_PLAN_STEP_THREE_LAUNCHES: force the form
-                              of okc_attn_step at q_len 1 (default: chosen by the plan);
+                              of okc_attn_step at q_len 1 (default: chosen by the plan); the one-
+                              kernel form also exists for blocks of 2..8 tokens on the tcgen05
+                              kernel (q_len <= 8) and is used only when this flag asks for it;
                               OKC_PLAN_EARLY_GATHER: the caller promises that the kernels launched
                               before okc_attn_step on its stream write neither page_table, the
                               length arrays, nor any K/V cache row the step reads (the QKV
@@ -383,10 +385,12 @@ okc_status okc_attn_combine_normgate(okc_attn_plan_t plan, const float* o_partia
  * request's splits and writes `out`. The plan chooses this one-kernel form for
  * q_len 1 when its work list fills at least half of the GPU's resident CTA
  * slots with chunks of at most 2048 keys or takes more than one wave of them
- * (sizes.step_kernels == 1, or forced by
- * OKC_PLAN_STEP_ONE_LAUNCH); otherwise, and always for q_len > 1, the call runs
- * the three kernels, keeping q in the plan workspace. Either way the results
- * equal the three calls' bit for bit.
+ * (sizes.step_kernels == 1, or forced by OKC_PLAN_STEP_ONE_LAUNCH). For
+ * q_len 2..8 on the tcgen05 kernel (one query block per request) the same form
+ * runs only under OKC_PLAN_STEP_ONE_LAUNCH (measured slower on the verify
+ * block than the three kernels). Otherwise, and always for q_len > 8 or the
+ * warp-level kernel, the call runs the three kernels, keeping q in the plan
+ * workspace. Either way the results equal the three calls' bit for bit.
  * Arguments: those of the three calls, minus q_fp8. cache_loc[t] must be the
  * page-table row of token t's position (the kernel uses the computed row
  * directly instead of reading it back).
