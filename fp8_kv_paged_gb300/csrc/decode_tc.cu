@@ -1,14 +1,15 @@
-// decode_tc.cu — step 4 for a speculative verify block (2 <= q_len <= 8) on the
-// 5th-generation tensor cores (tcgen05, accumulators in tensor memory): the
-// flash_attn_with_kvcache call of "012-attention-local-splits.py" with the
-// block's L queries, paged, causal within the block, window (window-1, 0).
+// decode_tc.cu — step 4 for query blocks of 2..8 tokens on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory): the
+// flash_attn_with_kvcache call of "012-attention-local-splits.py" with a
+// block's queries, paged, causal within the block, window (window-1, 0). It
+// serves the speculative verify block (q_len <= 8: one block per request) and
+// prefill/extend (requests cut into blocks of 8 consecutive tokens).
 //
 // One CTA per work item (query block of a request, chunk of its visible keys),
 // as in decode.cu; the CTA holds all 128 q rows of the block (up to 8 tokens x
 // 16 heads, rows g*64 + i*8 + hh for KV head g, token i of the block, head
 // g*8 + hh; rows of tokens past the block are zero and ignored) as ONE M = 128
-// operand (a verify block of q_len <= 8 is one block; longer extends are cut
-// into blocks of 8 consecutive tokens):
+// operand:
 //   S [128 x 64 keys]  = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
 //   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16,
 //                         P read from tensor memory)
@@ -20,36 +21,44 @@
 // hold both heads' 64 dims (the cache row as stored), so S = q . k_g exactly;
 // for PV every row gets both heads' 64 output dims and keeps its own half.
 //
-// Warps: 0-3 and 4-7 are two softmax warpgroups that take alternate tiles
-// (thread r of a group owns q row r), 8 issues the MMAs (one thread) and owns
-// the TMEM allocation, 9-10 gather (with one softmax group: warps 0-3, MMA 4,
-// gather 5-6): on pages of 8 or more rows each gather warp issues the TMA loads
-// of four of a tile's eight 8-row groups (8-row boxes, 128-byte swizzle, read
-// by the MMA through a swizzled descriptor; one warp's TMA issues are
-// serialised, so two issuing warps gather faster than one), else both run the
-// cp.async producer of decode.cu (K rows in the MMA's no-swizzle canonical
-// layout, V rows in a staging tile). Each group j has its own S, P and O in TMEM and its own V^T
+// Two forms (TcCfg<NG>, chosen by the plan): two softmax warpgroups taking
+// alternate tiles (one CTA per SM, 512 TMEM columns; Q is the QK's A operand in
+// TMEM, so the QK reads only K from shared memory) for steps of at most 8
+// tokens per request, and one (two CTAs per SM, 256 columns, Q in shared
+// memory) for longer extends. Warps: the softmax groups (thread r of a group
+// owns q row r), then one warp that issues the QK and PV MMAs (one thread, a
+// ready PV before the next QK) and owns the TMEM allocation, then two gather
+// warps: on pages of 8 or more rows each issues the TMA loads of four of a
+// tile's eight 8-row groups (8-row boxes, 128-byte swizzle, read by the MMA
+// through a swizzled descriptor; one warp's TMA issues are serialised, so two
+// issuing warps gather faster than one), else both run the cp.async producer
+// of decode.cu (K rows in the MMA's no-swizzle canonical layout, V rows in a
+// staging tile). Each group j has its own S, P and O in TMEM and its own V^T
 // tile in shared memory, so one group's softmax overlaps the other group's
 // MMAs. Per tile k of group j:
 //   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
 //   group j: wait s_ready_j -> S row from TMEM -> arrive(s_free_j) -> mask; row
-//            max; P = 2^(s - m) (f16 pairs) into TMEM (tcgen05.st); V tile E4M3 -> f16
-//            transposed (ldmatrix, exact conversion, stmatrix.trans)
-//            -> arrive(p_ready_j)
+//            max; P = 2^(s - m) (f16 pairs) in registers -> wait pv_done_j of
+//            its previous tile -> P into TMEM (tcgen05.st); V tile E4M3 -> f16
+//            transposed (ldmatrix, exact conversion, stmatrix.trans; V^T rows
+//            permuted within 16-dim blocks, vt_pos, so the stores hit no bank
+//            conflicts) -> arrive(p_ready_j)
 //   MMA:     wait p_ready_j -> free the stage -> O_j += P V -> commit(pv_done_j)
 // O accumulates in TMEM against a reference max m per row that moves when the
 // row's max grows past m + kTcRescale (log2 units; 0 by default: the exact
 // running max, P <= 1): then the row's O is rescaled in TMEM (tcgen05.ld / st)
-// before the next PV. At the end group 0 merges both groups' (m, l, O) and
-// writes O/l (times v_scale) and the base-2 LSE per row, as decode.cu does;
-// the combine kernel merges the splits.
+// before the next PV. At the end the groups merge their (m, l, O) and write
+// O/l (times v_scale) through shared memory (whole 128-byte lines) and the
+// base-2 LSE per row, as decode.cu does; the combine kernel merges the splits.
+// The one-kernel step (FUSED, two groups) also derives q and the step's new
+// K/V rows from qkv and merges the splits in the block's last CTA.
 //
-// Shared-memory operands Q, V^T (and K on the cp.async path) use the
-// no-swizzle K-major layout (8-row x 16-byte core matrices; core matrices 128
-// bytes apart along K, 8-row groups 1024 bytes apart for 128-byte rows); K on
-// the TMA path the 128-byte-swizzle K-major layout. Every wait is bounded
-// (mbar_wait); on a timeout the kernel flags OKC_DEVERR_TIMEOUT, waits for the
-// copies and MMAs it issued and frees its TMEM before it returns.
+// Shared-memory operands (Q of the one-group form, V^T, K on the cp.async
+// path) use the no-swizzle K-major layout (8-row x 16-byte core matrices; core
+// matrices 128 bytes apart along K, 8-row groups 1024 bytes apart for 128-byte
+// rows); K on the TMA path the 128-byte-swizzle K-major layout. Every wait is
+// bounded (mbar_wait); on a timeout the kernel flags OKC_DEVERR_TIMEOUT, waits
+// for the copies and MMAs it issued and frees its TMEM before it returns.
 #include <cuda.h>
 
 #include <algorithm>
