@@ -88,6 +88,19 @@ def kv_bytes(cfg, seq_lens, q_lens=None) -> int:
     return int(n.sum()) * cfg["num_kv_heads"] * cfg["head_dim"] * 2
 
 
+def page_table_bytes_read(cfg, seq_lens, q_lens=None) -> int:
+    """Bytes of page-table entries one step reads: for each request the pages
+    that hold its visible keys (the union over its new tokens' windows), 4
+    bytes each."""
+    ql = _q_lens(cfg, seq_lens, q_lens)
+    w, P = cfg["window"], cfg["page_size"]
+    hi = np.asarray(seq_lens, np.int64) + ql
+    n = np.minimum(hi, w + ql - 1) if w > 0 else hi
+    lo = hi - n
+    pages = np.where((ql > 0) & (n > 0), (hi - 1) // P - lo // P + 1, 0)
+    return int(pages.sum()) * 4
+
+
 def token_keys(cfg, seq_lens, q_lens=None) -> np.ndarray:
     """Per request: the sum over its new tokens of the keys each token sees."""
     ql = _q_lens(cfg, seq_lens, q_lens)
@@ -649,9 +662,11 @@ def run_e2e(cfg, inp, okc, torch, dev, stream, steps: int, fused: bool = True):
     op = torch.empty(max(16, sizes["o_partial_bytes"]) // 4, dtype=torch.float32, device=dev)
     lp = torch.empty(max(16, sizes["lse_partial_bytes"]) // 4, dtype=torch.float32, device=dev)
     out = torch.empty_like(out_host, device=dev)
-    # the step's inputs, and the plan's upload (the workspace up to its q scratch)
-    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names) + \
-        sizes["workspace_bytes"] - sizes["q_fp8_bytes"]
+    # the step's inputs (the page table: the entries the kernels read, the pages
+    # spanning each request's visible keys; every other input whole), and the
+    # plan's upload (the workspace up to its q scratch)
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in names if k != "page_table") + \
+        page_table_bytes_read(cfg, inp["seq_lens"], ql) + sizes["workspace_bytes"] - sizes["q_fp8_bytes"]
     d2h = out_host.numel() * 2
 
     io = okc.HostStepIO(dict(pinned, out=out_host), dict({k: dev_in[k] for k in names}, out=out))

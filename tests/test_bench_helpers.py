@@ -1,6 +1,7 @@
 """bench.py's accounting without a GPU: the algorithmic KV bytes of a step equal
 256 bytes per key the planner's work list covers (two independent accounts of
-the visible keys), the full-context workload's bytes are exact, and the clock
+the visible keys), the full-context workload's bytes are exact, the page-table
+bytes an end-to-end step reads are the pages the work list touches, and the clock
 sampler reads nvidia-smi's CSV rows into a median SM clock, the maximum clock
 and the active throttle reasons of the timed region."""
 import time
@@ -24,6 +25,24 @@ def test_kv_bytes_equal_the_keys_the_work_list_covers():
         assert bench.kv_bytes(cfg, seq) == covered * 2 * 64 * 2, name
     cfg = W.config("full_decode_32k")
     assert bench.kv_bytes(cfg, W.lengths(cfg)) == 64 * 32769 * 256
+
+
+def test_page_table_bytes_are_the_pages_the_work_list_touches():
+    """The end-to-end host-to-device count takes the page-table entries the step
+    reads: 4 bytes per distinct page holding a key of some work item."""
+    okc.build()
+    for name in W.DECODE_WORKLOADS:
+        cfg = W.config(name)
+        seq = W.lengths(cfg)
+        items = okc.okc_attn_plan_items(cfg, seq, HOST)
+        P = cfg["page_size"]
+        it = items[np.lexsort((items[:, 1], items[:, 0]))].astype(np.int64)
+        first, last = it[:, 1] // P, (it[:, 2] - 1) // P
+        count = int((last - first + 1).sum())
+        # a page shared by consecutive items of one request is counted once
+        same = (it[1:, 0] == it[:-1, 0]) & (first[1:] <= last[:-1])
+        count -= int((last[:-1][same] - first[1:][same] + 1).sum())
+        assert bench.page_table_bytes_read(cfg, seq) == 4 * count, name
 
 
 def test_extend_accounting():
