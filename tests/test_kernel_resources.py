@@ -2,7 +2,9 @@
 the hot kernels keep the register counts their occupancy rests on (the decode
 kernels for q_len 1 at 80 registers x 256 threads: three CTAs per SM; the
 two-group tcgen05 decode (verify blocks) at 120 x 352 as allocated: one CTA per
-SM with room for a prepare and two combine CTAs beside it; the one-group tcgen05 decode
+SM with room for a prepare and two combine CTAs beside it; its one-kernel step
+form, which also derives q and the new rows, within one CTA per SM (at most
+136 registers on TMA-fed tiles, 184 on cp.async-fed ones); the one-group tcgen05 decode
 (extends) at 128 x 224: two CTAs per SM; the combine for blocks of several
 tokens under 64 x 128, so that two of its CTAs fit beside a tcgen05 decode CTA)
 and spill nothing beyond the fused step's known 16-byte frame."""
@@ -20,10 +22,12 @@ CSRC = os.path.join(ROOT, "fp8_kv_paged_gb300", "csrc")
 LIMITS = {
     "decode_kernelILi2ELi1ELi4ELb1E": (80, 16),   # the fused step (sliding, mixed)
     "decode_kernelILi2ELi1ELi4ELb0E": (80, 0),    # q_len-1 decode of the three-call step
-    "decode_tc_kernelILb1ELi2E": (120, 0),        # verify block, TMA gather (allocated as 120)
-    "decode_tc_kernelILb0ELi2E": (120, 0),        # verify block on pages of < 8 rows, cp.async gather (allocated as 120)
-    "decode_tc_kernelILb1ELi1E": (128, 0),        # extend, TMA gather
-    "decode_tc_kernelILb0ELi1E": (128, 0),        # extend, cp.async gather
+    "decode_tc_kernelILb1ELi2ELb0E": (120, 0),    # verify block, TMA gather (allocated as 120)
+    "decode_tc_kernelILb0ELi2ELb0E": (120, 0),    # verify block on pages of < 8 rows, cp.async gather (allocated as 120)
+    "decode_tc_kernelILb1ELi2ELb1E": (136, 0),    # the verify block's one-kernel step, TMA gather
+    "decode_tc_kernelILb0ELi2ELb1E": (184, 0),    # the same on pages of < 8 rows (one CTA per SM: 184 x 352 fits)
+    "decode_tc_kernelILb1ELi1ELb0E": (128, 0),    # extend, TMA gather
+    "decode_tc_kernelILb0ELi1ELb0E": (128, 0),    # extend, cp.async gather
     "prepare_kernel": (64, 0),
     "combine_kernel": (128, 0),
     "combine_kernelILi4E": (64, 0),               # verify and extend steps (4 splits per round trip)
