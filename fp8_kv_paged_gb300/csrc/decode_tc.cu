@@ -83,18 +83,31 @@ constexpr uint32_t kTcSbo = 1024; // next 8-row group (rows of 128 bytes)
 #endif
 constexpr float kTcRescale = OKC_TC_RESCALE;  // log2 headroom of the reference max (0: exact max)
 constexpr int kTcPvN = 144;                   // PV's N: 128 dims + the ones column
-constexpr int kTcVTBytes = kTcPvN * 128;
-// Softmax warpgroups per CTA (chosen by the plan, tc_groups; tile k goes to group
-// k & (NG - 1), its phase is bit 0 of k >> (NG - 1)): 2 (one CTA per SM: 512 TMEM
-// columns, 6 stages, the groups take alternate tiles) or 1 (two CTAs per SM:
-// 256 columns, 4 stages, ~105 KB of shared memory).
+// The form of the kernel (chosen by the plan, tc_groups), NG:
+//  1: one softmax warpgroup (two CTAs per SM: 256 TMEM columns, 4 stages,
+//     ~105 KB of shared memory), blocks of 8 tokens x 16 heads;
+//  2: two warpgroups taking alternate tiles (tile k goes to group k & 1, its
+//     phase is bit 0 of k >> 1; one CTA per SM: 512 columns, 6 stages), blocks
+//     of up to 8 tokens x 16 heads;
+//  3: two warpgroups, one per KV head, both on every tile (one CTA per SM):
+//     blocks of 16 tokens, group j's 128 rows the block's 16 tokens x the 8 q
+//     heads of KV head j (row 8 i + hh: token i, head 8 j + hh), so the QK reads
+//     only head j's 64 K bytes (K = 64) and the PV only head j's 64 V dims
+//     (N = 64 + 16): half the tensor work per q row of the other forms, whose
+//     rows mix both heads, and one V conversion per tile for the block's 256 rows.
 
-// The layout of a CTA with NG softmax warpgroups. Warps 0 .. 4 NG - 1 run the
-// softmax, warp 4 NG issues the MMAs, the next kProducers gather.
+// The layout of a CTA of form NG. Warps 0 .. 4 kGroups - 1 run the softmax,
+// warp 4 kGroups issues the MMAs, the next kProducers gather.
 template <int NG>
 struct TcCfg {
-  static constexpr int kStages = NG == 2 ? 6 : 4;
-  static constexpr int kMmaWarp = 4 * NG;
+  static constexpr bool kPH = NG == 3;              // one group per KV head
+  static constexpr int kGroups = kPH ? 2 : NG;      // softmax warpgroups
+  static constexpr int kStep = kPH ? 1 : NG;        // group j's tiles: j (0 for kPH), + kStep, ...
+  static constexpr int kShift = kPH ? 0 : NG - 1;   // the phase of tile k: bit 0 of k >> kShift
+  static constexpr int kPvN = kPH ? 64 + 16 : kTcPvN;  // PV's N: the dims + the ones column (and zeros)
+  static constexpr int kVTBytes = kPvN * 128;       // [V | 1]^T f16 [kPvN x 64 keys]
+  static constexpr int kStages = NG == 1 ? 4 : 6;
+  static constexpr int kMmaWarp = 4 * kGroups;
   // gather warps: TMA issues from one warp are serialised, so each producer
   // warp issues its share of a tile's boxes (a third or fourth warp gathered
   // no faster, and a fourth held back the CTAs of the neighbouring kernels)
@@ -105,31 +118,39 @@ struct TcCfg {
   // Q, the QK's A operand: in TMEM with two groups (the 32 columns the other
   // operands leave free: the QK reads only K from shared memory), else in
   // shared memory
-  static constexpr bool kQTmem = NG == 2;
+  static constexpr bool kQTmem = NG != 1;
   // shared memory
   static constexpr int kQ = 0;                                            // Q E4M3 [128 x 128 B] (not kQTmem)
   static constexpr int kK = kQ + (kQTmem ? 0 : kTcRows * 128);            // K E4M3 [stage][64 x 128 B]
   static constexpr int kV = kK + kStages * kTcTileKeys * 128;             // V E4M3 [stage][64 x 144 B]
-  static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][144 x 64 keys]
-  static constexpr int kX = kVT + NG * kTcVTBytes;                        // each group's reference max per row
+  static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][kPvN x 64 keys]
+  static constexpr int kX = kVT + kGroups * kVTBytes;                     // each group's reference max per row
   // the one-kernel step: the step's new K and V rows for this CTA's keys (at
   // most 8 keys x K | V x 128 bytes), computed once and put into the tiles
-  static constexpr int kNew = kX + NG * kTcRows * 4;
+  static constexpr int kNew = kX + kGroups * kTcRows * 4;
   static constexpr int kNewBytes = NG == 2 ? 8 * 2 * 128 : 0;
   static constexpr int kBar = kNew + kNewBytes;
   // barriers: full[S], empty[S], s_ready[NG], p_ready[NG], pv_done[NG], s_free[NG], mma_done, new_ready
-  static constexpr int kTmemSlot = kBar + (2 * kStages + 4 * NG + 2) * 8;
+  static constexpr int kTmemSlot = kBar + (2 * kStages + 4 * kGroups + 2) * 8;
   static constexpr int kSmem = kTmemSlot + 16 + 2048;  // + slack past the last operand
   // TMEM columns. NG = 2: S_j at 64 j (64), O_j at 128 + 160 j (144), P_j (f16,
   // two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j.
+  // NG = 3: S_j at 64 j, O_j at 128 + 80 j (80), P_j at 288 + 32 j.
   // NG = 1: S at 0, P at 64, O at 96.
-  static constexpr uint32_t kCols = NG == 2 ? 512 : 256;
+  static constexpr uint32_t kCols = NG == 1 ? 256 : 512;
   __host__ __device__ static constexpr uint32_t col_s(int j) { return 64u * j; }
-  __host__ __device__ static constexpr uint32_t col_o(int j) { return NG == 2 ? 128u + 160u * j : 96u; }
-  __host__ __device__ static constexpr uint32_t col_p(int j) { return NG == 2 ? 432u + 32u * j : 64u; }
-  // kQTmem: Q's K bytes [32 kk, 32 kk + 32) (4 per column) at col_q(kk): the
-  // columns between O_0 and O_1 and after P_1
-  __host__ __device__ static constexpr uint32_t col_q(int kk) { return kk < 2 ? 272u + 8u * kk : 496u + 8u * (kk - 2); }
+  __host__ __device__ static constexpr uint32_t col_o(int j) {
+    return NG == 2 ? 128u + 160u * j : NG == 3 ? 128u + 80u * j : 96u;
+  }
+  __host__ __device__ static constexpr uint32_t col_p(int j) {
+    return NG == 2 ? 432u + 32u * j : NG == 3 ? 288u + 32u * j : 64u;
+  }
+  // kQTmem: Q's K bytes [32 kk, 32 kk + 32) (4 per column) at col_q(kk). NG = 2:
+  // the columns between O_0 and O_1 and after P_1; NG = 3: after P_1, group j's
+  // 64 bytes (its KV head's dims) as kk = 2 j, 2 j + 1
+  __host__ __device__ static constexpr uint32_t col_q(int kk) {
+    return NG == 3 ? 352u + 8u * kk : kk < 2 ? 272u + 8u * kk : 496u + 8u * (kk - 2);
+  }
   static_assert(kQ % 1024 == 0 && kK % 1024 == 0 && kV % 1024 == 0 && kVT % 1024 == 0, "operand alignment");
 };
 static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col_p(1) + 32 <= TcCfg<2>::col_q(2) &&
@@ -137,6 +158,9 @@ static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col
                   TcCfg<2>::col_q(3) + 8 <= 512,
               "TMEM columns");
 static_assert(TcCfg<1>::col_p(0) + 32 <= TcCfg<1>::col_o(0) && TcCfg<1>::col_o(0) + kTcPvN <= 256, "TMEM columns");
+static_assert(TcCfg<3>::col_s(1) + 64 <= TcCfg<3>::col_o(0) && TcCfg<3>::col_o(1) + TcCfg<3>::kPvN <= TcCfg<3>::col_p(0) &&
+                  TcCfg<3>::col_p(1) + 32 <= TcCfg<3>::col_q(0) && TcCfg<3>::col_q(3) + 8 <= 512,
+              "TMEM columns");
 static_assert(2 * TcCfg<1>::kSmem <= 227 * 1024, "two CTAs per SM");
 
 // Byte offset of (row r, byte kb) in a canonical tile of 128-byte rows.
@@ -173,7 +197,9 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<NG>;
   static_assert(!FUSED || NG == 2, "the one-kernel step runs blocks of at most 8 tokens with two softmax groups");
-  constexpr int kTcStages = C::kStages, kTcGroups = NG, kTcMmaWarp = C::kMmaWarp, kTcThreads = C::kThreads;
+  constexpr int kTcStages = C::kStages, kTcGroups = C::kGroups, kTcMmaWarp = C::kMmaWarp, kTcThreads = C::kThreads;
+  constexpr bool kPH = C::kPH;
+  constexpr int kStep = C::kStep, kShift = C::kShift;
   constexpr int kTcProducers = C::kProducers;
   constexpr int kGroupsPW = 8 / kTcProducers;  // TMA: 8-row groups of a tile per producer warp
   constexpr int kTcQ = C::kQ, kTcK = C::kK, kTcV = C::kV, kTcVT = C::kVT, kTcX = C::kX, kTcBar = C::kBar;
@@ -475,7 +501,74 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     // ================================================================ MMA issue
     named_bar_sync(1, (kTcMmaWarp + 1) * 32);  // Q is in TMEM or shared memory
     tc_fence_after();
-    if (lane == 0) {
+    if (kPH && lane == 0) {
+      // form 3, every tile k for both groups: S_j = Q_j K_k^T over KV head j's
+      // 64 K bytes, O_j (+)= P_j [V_k,j | 1]. Each is issued once its inputs
+      // are ready (polled, a ready PV first, as below); a stage is freed once
+      // both groups have consumed its tile (P written, their V dims converted).
+      constexpr uint32_t id_qk = umma_idesc(0, kTcRows, kTcTileKeys);  // E4M3 x E4M3 -> f32, 128 x 64
+      constexpr uint32_t id_pv = umma_idesc(0, kTcRows, C::kPvN);      // f16 x f16 -> f32, 128 x 80
+      auto qk = [&](int k, int j) {
+        const uint32_t kt = sb + kTcK + (k % kTcStages) * (kTcTileKeys * 128);
+#pragma unroll
+        for (int kk = 0; kk < 2; kk++) {  // head j's 64 bytes of K: 32 per instruction
+          const int kb = 2 * j + kk;
+          const uint64_t kdesc =
+              kTma ? umma_desc_sw128(kt + kb * 32, kTcSbo) : umma_desc(kt + kb * 2 * kTcLbo, kTcLbo, kTcSbo);
+          umma_f8_ta(tmem + C::col_s(j), tmem + C::col_q(kb), kdesc, id_qk, kk > 0);
+        }
+        umma_commit(s_ready(j));
+      };
+      auto pv = [&](int k, int j) {
+        const uint32_t va = sb + kTcVT + j * C::kVTBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++)  // 64 keys: 16 per instruction
+          umma_f16_ta(tmem + C::col_o(j), tmem + C::col_p(j) + kk * 8,
+                      umma_desc(va + kk * 2 * kTcLbo, kTcLbo, kTcSbo), id_pv, (k > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(pv_done(j));
+      };
+      bool ok = true;
+      int nq[2] = {0, 0}, np[2] = {0, 0}, freed = 0;  // next QK / PV per group, stages freed
+      uint64_t t_idle = 0;
+      while (np[0] < ntiles || np[1] < ntiles) {
+        bool did = false;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+          if (np[j] < nq[j] && mbar_test_wait(p_ready(j), np[j] & 1)) {
+            fence_proxy_async();  // V^T_j, written through the generic proxy
+            tc_fence_after();
+            pv(np[j], j);
+            np[j]++;
+            did = true;
+          }
+        }
+        for (; freed < min(np[0], np[1]); freed++) mbar_arrive(empty_bar(freed % kTcStages));
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+          const int k = nq[j];
+          if (k < ntiles && (k == 0 || mbar_test_wait(s_free(j), (k - 1) & 1)) &&
+              mbar_test_wait(full_bar(k % kTcStages), (k / kTcStages) & 1)) {
+            fence_proxy_async();  // the gathered tile, written through the generic proxy
+            tc_fence_after();
+            qk(k, j);
+            nq[j]++;
+            did = true;
+          }
+        }
+        if (did) {
+          t_idle = 0;
+        } else if (t_idle == 0) {
+          t_idle = global_ns();
+        } else if (global_ns() - t_idle > kWaitNs) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) set_error(a.err, OKC_DEVERR_TIMEOUT);
+      umma_commit(mma_done);  // arrives once every MMA issued above has completed
+      if (!mbar_wait(mma_done, 0)) set_error(a.err, OKC_DEVERR_TIMEOUT);
+    }
+    if (!kPH && lane == 0) {
       constexpr uint32_t id_qk = umma_idesc(0, kTcRows, kTcTileKeys);  // E4M3 x E4M3 -> f32, 128 x 64
       constexpr uint32_t id_pv = umma_idesc(0, kTcRows, kTcPvN);       // f16 x f16 -> f32, 128 x 144
       // S_j = Q K_k^T for tile k (group j = k & 1)
@@ -504,7 +597,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         fence_proxy_async();
         tc_fence_after();
         mbar_arrive(empty_bar(k % kTcStages));  // K read (S_k consumed), V converted: the stage is free
-        const uint32_t va = sb + kTcVT + j * kTcVTBytes;
+        const uint32_t va = sb + kTcVT + j * C::kVTBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)  // 64 keys: 16 per instruction
           umma_f16_ta(tmem + C::col_o(j), tmem + C::col_p(j) + kk * 8,
@@ -560,7 +653,8 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   // ================================================================== softmax
   const int jw = warp >> 2;  // this thread's group: tiles jw, jw + 2, ...
   const int r = tid & (kTcRows - 1);  // q row
-  const int g = r >> 6, ti = (r >> 3) & 7, hh = r & 7;
+  // KV head, token and head of row r (form 3: the group's KV head, 16 tokens)
+  const int g = kPH ? jw : r >> 6, ti = kPH ? r >> 3 : (r >> 3) & 7, hh = r & 7;
   const int head = g * kGroup + hh;
   const bool live = ti < ntk;
   pdl_wait();  // q_fp8 is the prepare kernel's output (the one-kernel step: qkv, a caller input)
@@ -601,11 +695,13 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     }
   }
   {
-    // rows 128..143 of both groups' [V | 1]^T: row 128 ones, the rest zeros
-    // (never rewritten; the V conversion writes rows 0..127)
-    const int gj = tid >> 7, rr2 = 128 + ((tid >> 3) & 15), c = tid & 7;
-    const uint32_t one2 = rr2 == 128 ? 0x3C003C00u : 0u;  // f16 1.0 pairs
-    *reinterpret_cast<uint4*>(smem + kTcVT + gj * kTcVTBytes + canon(rr2, c * 16)) = make_uint4(one2, one2, one2, one2);
+    // the last 16 rows of each group's [V | 1]^T (from row kPvN - 16, the
+    // first after the dims): that row ones, the rest zeros (never rewritten;
+    // the V conversion writes the dims' rows)
+    constexpr int kOnes = C::kPvN - 16;
+    const int gj = tid >> 7, rr2 = kOnes + ((tid >> 3) & 15), c = tid & 7;
+    const uint32_t one2 = rr2 == kOnes ? 0x3C003C00u : 0u;  // f16 1.0 pairs
+    *reinterpret_cast<uint4*>(smem + kTcVT + gj * C::kVTBytes + canon(rr2, c * 16)) = make_uint4(one2, one2, one2, one2);
   }
   if (__any_sync(0xffffffffu, q_pos_err) && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
   fence_proxy_async();  // shared-memory operands, for the MMAs
@@ -616,16 +712,16 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   const int pos = pbase + ti;  // this row's query position
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t tS = t_lane + C::col_s(jw);              // this row's S
-  const uint32_t tO = t_lane + C::col_o(jw) + 64 * g;      // this row's O half
-  const uint32_t tL = t_lane + C::col_o(jw) + 128;         // this row's P sum
+  const uint32_t tO = t_lane + C::col_o(jw) + (kPH ? 0 : 64 * g);  // this row's O dims
+  const uint32_t tL = t_lane + C::col_o(jw) + C::kPvN - 16;       // this row's P sum
   const uint32_t tP = t_lane + C::col_p(jw);               // this row's P (f16 pairs)
-  const uint32_t sVT = kTcVT + jw * kTcVTBytes;
+  const uint32_t sVT = kTcVT + jw * C::kVTBytes;
   float m = -INFINITY;  // reference max (log2 units)
   bool ok = true;
   int last = -1;  // this group's last tile
-  for (int k = jw; k < ntiles; k += kTcGroups) {
+  for (int k = kPH ? 0 : jw; k < ntiles; k += kStep) {
     const int s = k % kTcStages;
-    const bool w = mbar_wait(s_ready(jw), (k >> (NG - 1)) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
+    const bool w = mbar_wait(s_ready(jw), (k >> kShift) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
     tc_fence_after();
     const int tile_j = jt + k * kTcTileKeys;
@@ -671,12 +767,12 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       pw[c] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
     }
     // ---- P, V^T and O of this group are free once its previous PV completed
-    if (k >= kTcGroups) {
-      const bool w2 = mbar_wait(pv_done(jw), ((k - NG) >> (NG - 1)) & 1);
+    if (k >= kStep) {
+      const bool w2 = mbar_wait(pv_done(jw), ((k - kStep) >> kShift) & 1);
       if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
       tc_fence_after();
     }
-    if (k >= kTcGroups && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
+    if (k >= kStep && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale O rows (and sums) in TMEM
       float ov[16];
 #pragma unroll
       for (int h4 = 0; h4 < 4; h4++) {  // (the stores complete at the sum's store below)
@@ -691,14 +787,15 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     tmem_st32u(tP, pw);
     // ---- V tile E4M3 -> f16, transposed into this group's canonical B tile
     // (dims x keys). Warp w of the group converts key groups 2w, 2w+1 (8 keys
-    // each) x 8 groups of 16 dims.
+    // each) x 8 groups of 16 dims (form 3: the 4 groups of its KV head's dims).
     {
       const int wg = warp & 3;
       const uint32_t vs = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
+      constexpr int kIts = kPH ? 2 : 4;
 #pragma unroll 1
-      for (int it = 0; it < 4; it++) {
-        const int a8 = 2 * wg + (it >> 1);   // key group
-        const int cbase = (it & 1) * 4;      // first 16-dim group of this x4
+      for (int it = 0; it < kIts; it++) {
+        const int a8 = 2 * wg + (kPH ? it : it >> 1);  // key group
+        const int cbase = kPH ? 4 * jw : (it & 1) * 4;   // first 16-dim group of this x4
         uint32_t rg[4];
         // matrix mi = lane >> 3: keys a8*8 + (lane & 7), bytes 16 (cbase + mi) .. +15
         // (TMA: 8-row groups 1024 bytes apart, chunks XORed with the row mod 8)
@@ -719,7 +816,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         const int jm = lane >> 3, cc = lane & 7;
 #pragma unroll
         for (int half = 0; half < 2; half++) {
-          const int c16 = cbase + half * 2 + (jm >> 1);
+          const int c16 = cbase + half * 2 + (jm >> 1) - (kPH ? 4 * jw : 0);  // (of the group's dims)
           const int pr = 16 * c16 + 8 * (jm & 1) + cc;
           stsm_x4_trans(sb + sVT + canon(pr, a8 * 16), lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1],
                         hi4[half * 2 + 1]);
@@ -733,7 +830,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   }
   // this group's O is complete once its last PV has
   if (ok && last >= 0) {
-    const bool w3 = mbar_wait(pv_done(jw), (last >> (NG - 1)) & 1);
+    const bool w3 = mbar_wait(pv_done(jw), (last >> kShift) & 1);
     if (!__all_sync(0xffffffffu, w3)) ok = false;
     tc_fence_after();
   }
@@ -748,10 +845,11 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   named_bar_sync(3, kTcGroups * kTcRows);
   tc_fence_after();
   {
-    const bool has0 = ok && ntiles >= 1, has1 = NG > 1 && ok && ntiles >= 2;  // groups that ran a PV
-    const float m0 = xml[r], m1 = NG > 1 ? xml[kTcRows + r] : -INFINITY;
-    const float l = has0 ? tmem_ld1(t_lane + C::col_o(0) + 128) : 0.f;
-    const float l1 = has1 ? tmem_ld1(t_lane + C::col_o(NG - 1) + 128) : 0.f;
+    // groups that ran a PV for this row (form 3: this group alone holds it)
+    const bool has0 = ok && ntiles >= 1, has1 = NG == 2 && ok && ntiles >= 2;
+    const float m0 = kPH ? m : xml[r], m1 = NG == 2 ? xml[kTcRows + r] : -INFINITY;
+    const float l = has0 ? tmem_ld1(kPH ? tL : t_lane + C::col_o(0) + 128) : 0.f;
+    const float l1 = has1 ? tmem_ld1(t_lane + C::col_o(1) + 128) : 0.f;
     const float M = fmaxf(m0, m1);
     const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
     const float L = l * f0 + l1 * f1;
@@ -769,14 +867,14 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
     // consumed, every MMA completed), then stores 4 half rows (four whole
     // 128-byte lines) per instruction instead of one 16-byte piece of 32 rows.
     constexpr int kStgPitch = 36;  // floats
-    static_assert(4 * NG * 32 * kStgPitch * 4 <= kTcStages * kTcTileKeys * 128, "staging fits the K stages");
+    static_assert(4 * kTcGroups * 32 * kStgPitch * 4 <= kTcStages * kTcTileKeys * 128, "staging fits the K stages");
     float* stg = reinterpret_cast<float*>(smem + kTcK) + warp * 32 * kStgPitch;
 #pragma unroll
-    for (int hh2 = 0; hh2 < 2 / NG; hh2++) {  // this group's halves of the row
+    for (int hh2 = 0; hh2 < (NG == 2 ? 1 : 2); hh2++) {  // this group's halves of the row
       const int h2 = NG == 2 ? jw : hh2;
       float o0[32], o1[32];
-      if (has0) tmem_ld32(t_lane + C::col_o(0) + 64 * g + 32 * h2, o0);
-      if (has1) tmem_ld32(t_lane + C::col_o(NG - 1) + 64 * g + 32 * h2, o1);
+      if (has0) tmem_ld32(t_lane + (kPH ? C::col_o(jw) : C::col_o(0) + 64 * g) + 32 * h2, o0);
+      if (has1) tmem_ld32(t_lane + C::col_o(1) + 64 * g + 32 * h2, o1);
 #pragma unroll
       for (int d = 0; d < 32; d += 4) {  // dims 32 h2 + d + e, O columns through vt_pos
         float v[4];
@@ -790,16 +888,16 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
       for (int i = 0; i < 8; i++) {
         const int lr = 4 * i + (lane >> 3);             // the warp's row lr: q row rq
         const int rq = (warp & 3) * 32 + lr;
-        const int ti2 = (rq >> 3) & 7;
+        const int ti2 = kPH ? rq >> 3 : (rq >> 3) & 7;
         if (ti2 < ntk) {
-          const int row2 = ti2 * kNumQHeads + (rq >> 6) * kGroup + (rq & 7);
+          const int row2 = ti2 * kNumQHeads + (kPH ? jw : rq >> 6) * kGroup + (rq & 7);
           *reinterpret_cast<float4*>(opart + row2 * kHeadDim + 32 * h2 + 4 * (lane & 7)) =
               *reinterpret_cast<const float4*>(stg + lr * kStgPitch + 4 * (lane & 7));
         }
       }
       __syncwarp();  // the staging is rewritten by the next half
     }
-    if (live && jw == 0) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
+    if (live && (kPH || jw == 0)) a.lse_part[slot * rows + row] = L > 0.f ? M + log2f(L) : -INFINITY;
   }
   tc_fence_before();
   named_bar_sync(2, (kTcMmaWarp + 1) * 32);  // TMEM reads done: the MMA warp may free it
@@ -894,9 +992,10 @@ cudaError_t launch_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t 
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
-  if (a.S < 1 || a.S > 8) return cudaErrorInvalidValue;
+  if (a.S < 1 || a.S > (a.tc_groups == 3 ? 16 : 8)) return cudaErrorInvalidValue;
   if (a.tc_groups == 1) return launch_tc<1, false>(a, num_work, pdl, s);
   if (a.tc_groups == 2) return launch_tc<2, false>(a, num_work, pdl, s);
+  if (a.tc_groups == 3) return launch_tc<3, false>(a, num_work, pdl, s);
   return cudaErrorInvalidValue;
 }
 
@@ -933,7 +1032,8 @@ int tc_ctas_per_sm() {
 }
 
 int decode_tc_ctas_per_sm(int tc_groups) {
-  return tc_groups == 1 ? tc_ctas_per_sm<1>() : tc_groups == 2 ? tc_ctas_per_sm<2>() : 0;
+  return tc_groups == 1 ? tc_ctas_per_sm<1>() : tc_groups == 2 ? tc_ctas_per_sm<2>()
+       : tc_groups == 3 ? tc_ctas_per_sm<3>() : 0;
 }
 
 }  // namespace okc

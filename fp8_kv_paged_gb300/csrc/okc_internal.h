@@ -167,15 +167,19 @@ inline float softmax_scale_log2(const okc_attn_config& c) {
 inline bool uses_tc(const okc_attn_config& c, const okc_plan_options* o) {
   return c.q_len >= 2 && !(o && (o->flags & OKC_PLAN_NO_TCGEN05));
 }
-// Softmax warpgroups per CTA of the tcgen05 kernel: 2 (one CTA per SM, the
-// groups on alternate tiles) for steps of at most 8 tokens per request (decode,
-// verify: few blocks, many splits, where fewer, longer splits merge faster),
-// 1 (two CTAs per SM) for longer extends (many blocks, bound by the tensor cores).
-inline int tc_groups(const okc_attn_config& c) { return c.q_len > 8 ? 1 : 2; }
-// Tokens per query block: 1 for q_len 1, 8 on the tcgen05 kernel (its M = 128
-// rows are 8 tokens x 16 heads), 16 on the warp-level kernel; q_len itself when smaller.
+// The form of the tcgen05 kernel (decode_tc.cu): 2 (two softmax warpgroups on
+// alternate tiles, one CTA per SM, blocks of up to 8 tokens x 16 heads as the
+// M = 128 rows) for steps of at most 8 tokens per request (decode, verify: few
+// blocks, many splits, where fewer, longer splits merge faster), 3 (one
+// warpgroup per KV head, blocks of 16 tokens: each group's M = 128 rows are 16
+// tokens x its 8 heads, half the tensor work per row) for longer extends. (Form
+// 1, one warpgroup on blocks of 8 tokens at two CTAs per SM, is kept in the
+// kernel, not chosen.)
+inline int tc_groups(const okc_attn_config& c) { return c.q_len > 8 ? 3 : 2; }
+// Tokens per query block: 1 for q_len 1, 8 on the tcgen05 kernel's form 2,
+// 16 on its form 3 and on the warp-level kernel; q_len itself when smaller.
 inline int block_tokens(const okc_attn_config& c, const okc_plan_options* o) {
-  const int smax = uses_tc(c, o) ? 8 : 16;
+  const int smax = uses_tc(c, o) && c.q_len <= 8 ? 8 : 16;
   return c.q_len < smax ? c.q_len : smax;
 }
 

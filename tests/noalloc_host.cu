@@ -73,7 +73,7 @@ int main(int argc, char** argv) {
     okc::SplitResult want;
     const bool tc = L >= 2;
     CHECK(okc::make_splits(&c, seq.data(), nullptr, nullptr, 152 * (tc ? 1 : 3), &want) == OKC_OK);
-    const int S = tc ? std::min(L, 8) : 1;
+    const int S = tc ? std::min(L, 16) : 1;  // (q_len past 8: the per-KV-head form, blocks of up to 16)
     CHECK(want.S == S);
     const size_t W = want.work.size(), NB = want.blocks.size(), rows = (size_t)S * 16;
     CHECK(NB == (size_t)B * ((L + S - 1) / S));

@@ -49,7 +49,7 @@ def test_extend_accounting():
     """The extend workload: the algorithmic KV bytes are each request's visible
     keys once (seq + q_len on a full-attention layer); the flops count every
     token's visible keys; the work list covers each query block's keys once
-    (blocks of 8 tokens on the tcgen05 kernel)."""
+    (blocks of 16 tokens on the tcgen05 kernel)."""
     okc.build()
     cfg = W.config("extend")
     inp = W.generate(cfg)
@@ -59,7 +59,7 @@ def test_extend_accounting():
     assert bench.attention_flops(cfg, inp["seq_lens"], inp["q_lens"]) == keys * 4 * 64 * 16
     items = okc.okc_attn_plan_items_varlen(cfg, inp["seq_lens"], inp["q_lens"], {"sm_count": 152, "ctas_per_sm": 1})
     covered = int((items[:, 3].astype(np.int64) - items[:, 2]).sum())
-    want = sum(int(s + min(i + 8, q)) for s, q in zip(seq, ql) for i in range(0, q, 8))
+    want = sum(int(s + min(i + 16, q)) for s, q in zip(seq, ql) for i in range(0, q, 16))
     assert covered == want
 
 

@@ -256,11 +256,11 @@ def _check_blocks(cfg, seq, ql, items, S):
 
 
 @pytest.mark.parametrize("window", [0, 2048])
-@pytest.mark.parametrize("flags,S", [(0, 8), (okc.PLAN_NO_TCGEN05, 16)])
+@pytest.mark.parametrize("flags,S", [(0, 16), (okc.PLAN_NO_TCGEN05, 16)])
 def test_varlen_blocks_cover_every_key_once(window, flags, S):
     """Prefill/extend batches mixing decode requests (1 token), extends of 37,
-    256 and 1024 tokens and requests with no new token: blocks of 8 tokens on
-    the tcgen05 kernel, 16 on the warp-level one."""
+    256 and 1024 tokens and requests with no new token: blocks of 16 tokens on
+    the tcgen05 kernel (its per-KV-head form) and on the warp-level one."""
     rng = np.random.default_rng(window + flags)
     for it in range(20):
         B = int(rng.integers(1, 40))
@@ -294,7 +294,7 @@ def test_extend_workload_plan():
     cfg = W.config("extend")
     inp = W.generate(cfg)
     items = okc.okc_attn_plan_items_varlen(cfg, inp["seq_lens"], inp["q_lens"], {"sm_count": SMS, "ctas_per_sm": 1})
-    _check_blocks(cfg, inp["seq_lens"], inp["q_lens"], items, 8)
+    _check_blocks(cfg, inp["seq_lens"], inp["q_lens"], items, 16)
     bound = okc.okc_attn_plan_max_sizes(cfg, int((inp["seq_lens"] + inp["q_lens"]).max()),
                                         {"sm_count": SMS, "ctas_per_sm": 1})
     z = okc.okc_attn_plan_sizes(cfg, inp["seq_lens"], {"sm_count": SMS, "ctas_per_sm": 1}, q_lens=inp["q_lens"])
