@@ -1,41 +1,49 @@
-// decode_tc.cu — step 4 for query blocks of 2..8 tokens on the 5th-generation
+// decode_tc.cu — step 4 for query blocks of 2..16 tokens on the 5th-generation
 // tensor cores (tcgen05, accumulators in tensor memory): the
 // flash_attn_with_kvcache call of "012-attention-local-splits.py" with a
 // block's queries, paged, causal within the block, window (window-1, 0). It
 // serves the speculative verify block (q_len <= 8: one block per request) and
-// prefill/extend (requests cut into blocks of 8 consecutive tokens).
+// prefill/extend (requests cut into blocks of 16 consecutive tokens).
 //
 // One CTA per work item (query block of a request, chunk of its visible keys),
-// as in decode.cu; the CTA holds all 128 q rows of the block (up to 8 tokens x
-// 16 heads, rows g*64 + i*8 + hh for KV head g, token i of the block, head
-// g*8 + hh; rows of tokens past the block are zero and ignored) as ONE M = 128
-// operand:
-//   S [128 x 64 keys]  = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
-//   O [128 x 144]      += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in f16,
-//                         P read from tensor memory)
-// where column 128 of the B operand is all ones, so O's column 128 is the row
-// sum of P as the tensor core saw it (f16 P, f32 sums): the softmax
-// denominator, consistent with the numerator and kept by the same rescales.
-// GQA without splitting the MMA by KV head: a q row of KV head g carries its 64
-// dims at K positions [64g, 64g+64) and zeros elsewhere, against K rows that
-// hold both heads' 64 dims (the cache row as stored), so S = q . k_g exactly;
-// for PV every row gets both heads' 64 output dims and keeps its own half.
+// as in decode.cu, in one of two forms (TcCfg<NG>, chosen by the plan; one CTA
+// per SM, 512 TMEM columns):
+//  - form 2 (blocks of up to 8 tokens): the CTA holds all 128 q rows of the
+//    block (up to 8 tokens x 16 heads, rows g*64 + i*8 + hh for KV head g,
+//    token i of the block, head g*8 + hh; rows of tokens past the block are
+//    zero and ignored) as ONE M = 128 operand, and two softmax warpgroups take
+//    alternate tiles:
+//      S [128 x 64 keys] = Q [128 x 128] . K_tile^T   (kind::f8f6f4, E4M3 x E4M3)
+//      O [128 x 144]    += P [128 x 64] . [V_tile | 1] (kind::f16, P and V in
+//                          f16, P read from tensor memory)
+//    GQA without splitting the MMA by KV head: a q row of KV head g carries its
+//    64 dims at K positions [64g, 64g+64) and zeros elsewhere, against K rows
+//    that hold both heads' 64 dims (the cache row as stored), so S = q . k_g
+//    exactly; for PV every row gets both heads' 64 output dims and keeps its
+//    own half;
+//  - form 3 (blocks of up to 16 tokens): one softmax warpgroup per KV head j,
+//    both on every tile, group j's 128 rows the block's 16 tokens x the 8 q
+//    heads of KV head j (row 8 i + hh):
+//      S_j [128 x 64 keys] = Q_j [128 x 64] . K_tile,j^T  (head j's 64 K bytes)
+//      O_j [128 x 80]     += P_j [128 x 64] . [V_tile,j | 1]
+//    half the tensor work per q row of form 2, and each tile's V conversion
+//    split between the groups.
+// Column 64 (form 3) or 128 (form 2) of the PV's B operand is all ones, so
+// O's column there is the row sum of P as the tensor core saw it (f16 P, f32
+// sums): the softmax denominator, consistent with the numerator and kept by
+// the same rescales.
 //
-// Two forms (TcCfg<NG>, chosen by the plan): two softmax warpgroups taking
-// alternate tiles (one CTA per SM, 512 TMEM columns; Q is the QK's A operand in
-// TMEM, so the QK reads only K from shared memory) for steps of at most 8
-// tokens per request, and one (two CTAs per SM, 256 columns, Q in shared
-// memory) for longer extends. Warps: the softmax groups (thread r of a group
-// owns q row r), then one warp that issues the QK and PV MMAs (one thread, a
-// ready PV before the next QK) and owns the TMEM allocation, then two gather
-// warps: on pages of 8 or more rows each issues the TMA loads of four of a
-// tile's eight 8-row groups (8-row boxes, 128-byte swizzle, read by the MMA
-// through a swizzled descriptor; one warp's TMA issues are serialised, so two
-// issuing warps gather faster than one), else both run the cp.async producer
-// of decode.cu (K rows in the MMA's no-swizzle canonical layout, V rows in a
-// staging tile). Each group j has its own S, P and O in TMEM and its own V^T
-// tile in shared memory, so one group's softmax overlaps the other group's
-// MMAs. Per tile k of group j:
+// Q is the QK's A operand in TMEM, so the QK reads only K from shared memory.
+// Warps: the softmax groups (thread r of a group owns q row r), then one warp
+// that issues the QK and PV MMAs (one thread, a ready PV before the next QK)
+// and owns the TMEM allocation, then two gather warps: on pages of 8 or more
+// rows each issues the TMA loads of four of a tile's eight 8-row groups (8-row
+// boxes, 128-byte swizzle, read by the MMA through a swizzled descriptor; one
+// warp's TMA issues are serialised, so two issuing warps gather faster than
+// one), else both run the cp.async producer of decode.cu (K rows in the MMA's
+// no-swizzle canonical layout, V rows in a staging tile). Each group j has its
+// own S, P and O in TMEM and its own V^T tile in shared memory, so one group's
+// softmax overlaps the other group's MMAs. Per tile k of group j:
 //   MMA:     wait tile k -> S_j = Q K^T -> commit(s_ready_j)
 //   group j: wait s_ready_j -> S row from TMEM -> arrive(s_free_j) -> mask; row
 //            max; P = 2^(s - m) (f16 pairs) in registers -> wait pv_done_j of
@@ -43,22 +51,23 @@
 //            transposed (ldmatrix, exact conversion, stmatrix.trans; V^T rows
 //            permuted within 16-dim blocks, vt_pos, so the stores hit no bank
 //            conflicts) -> arrive(p_ready_j)
-//   MMA:     wait p_ready_j -> free the stage -> O_j += P V -> commit(pv_done_j)
+//   MMA:     wait p_ready_j -> free the stage (form 3: once both groups have
+//            consumed the tile) -> O_j += P V -> commit(pv_done_j)
 // O accumulates in TMEM against a reference max m per row that moves when the
 // row's max grows past m + kTcRescale (log2 units; 0 by default: the exact
 // running max, P <= 1): then the row's O is rescaled in TMEM (tcgen05.ld / st)
-// before the next PV. At the end the groups merge their (m, l, O) and write
-// O/l (times v_scale) through shared memory (whole 128-byte lines) and the
-// base-2 LSE per row, as decode.cu does; the combine kernel merges the splits.
-// The one-kernel step (FUSED, two groups) also derives q and the step's new
-// K/V rows from qkv and merges the splits in the block's last CTA.
+// before the next PV. At the end (form 2: the groups merge their (m, l, O))
+// the CTA writes O/l (times v_scale) through shared memory (whole 128-byte
+// lines) and the base-2 LSE per row, as decode.cu does; the combine kernel
+// merges the splits. The one-kernel step (FUSED, form 2) also derives q and the
+// step's new K/V rows from qkv and merges the splits in the block's last CTA.
 //
-// Shared-memory operands (Q of the one-group form, V^T, K on the cp.async
-// path) use the no-swizzle K-major layout (8-row x 16-byte core matrices; core
-// matrices 128 bytes apart along K, 8-row groups 1024 bytes apart for 128-byte
-// rows); K on the TMA path the 128-byte-swizzle K-major layout. Every wait is
-// bounded (mbar_wait); on a timeout the kernel flags OKC_DEVERR_TIMEOUT, waits
-// for the copies and MMAs it issued and frees its TMEM before it returns.
+// Shared-memory operands (V^T, K on the cp.async path) use the no-swizzle
+// K-major layout (8-row x 16-byte core matrices; core matrices 128 bytes apart
+// along K, 8-row groups 1024 bytes apart for 128-byte rows); K on the TMA path
+// the 128-byte-swizzle K-major layout. Every wait is bounded (mbar_wait); on a
+// timeout the kernel flags OKC_DEVERR_TIMEOUT, waits for the copies and MMAs
+// it issued and frees its TMEM before it returns.
 #include <cuda.h>
 
 #include <algorithm>
@@ -83,45 +92,40 @@ constexpr uint32_t kTcSbo = 1024; // next 8-row group (rows of 128 bytes)
 #endif
 constexpr float kTcRescale = OKC_TC_RESCALE;  // log2 headroom of the reference max (0: exact max)
 constexpr int kTcPvN = 144;                   // PV's N: 128 dims + the ones column
-// The form of the kernel (chosen by the plan, tc_groups), NG:
-//  1: one softmax warpgroup (two CTAs per SM: 256 TMEM columns, 4 stages,
-//     ~105 KB of shared memory), blocks of 8 tokens x 16 heads;
-//  2: two warpgroups taking alternate tiles (tile k goes to group k & 1, its
-//     phase is bit 0 of k >> 1; one CTA per SM: 512 columns, 6 stages), blocks
-//     of up to 8 tokens x 16 heads;
-//  3: two warpgroups, one per KV head, both on every tile (one CTA per SM):
-//     blocks of 16 tokens, group j's 128 rows the block's 16 tokens x the 8 q
+// The form of the kernel (chosen by the plan, tc_groups), NG; either runs one
+// CTA per SM (512 TMEM columns, 6 stages):
+//  2: two softmax warpgroups taking alternate tiles (tile k goes to group k & 1, its
+//     phase is bit 0 of k >> 1), blocks of up to 8 tokens x 16 heads;
+//  3: two warpgroups, one per KV head, both on every tile: blocks of up to 16
+//     tokens, group j's 128 rows the block's 16 tokens x the 8 q
 //     heads of KV head j (row 8 i + hh: token i, head 8 j + hh), so the QK reads
 //     only head j's 64 K bytes (K = 64) and the PV only head j's 64 V dims
-//     (N = 64 + 16): half the tensor work per q row of the other forms, whose
-//     rows mix both heads, and one V conversion per tile for the block's 256 rows.
+//     (N = 64 + 16): half the tensor work per q row of form 2, whose rows mix
+//     both heads, and one V conversion per tile for the block's 256 rows. (A
+//     one-group form at two CTAs per SM on blocks of 8 tokens ran extends 11 %
+//     slower.)
 
 // The layout of a CTA of form NG. Warps 0 .. 4 kGroups - 1 run the softmax,
 // warp 4 kGroups issues the MMAs, the next kProducers gather.
 template <int NG>
 struct TcCfg {
+  static_assert(NG == 2 || NG == 3, "forms 2 and 3");
   static constexpr bool kPH = NG == 3;              // one group per KV head
   static constexpr int kGroups = kPH ? 2 : NG;      // softmax warpgroups
   static constexpr int kStep = kPH ? 1 : NG;        // group j's tiles: j (0 for kPH), + kStep, ...
   static constexpr int kShift = kPH ? 0 : NG - 1;   // the phase of tile k: bit 0 of k >> kShift
   static constexpr int kPvN = kPH ? 64 + 16 : kTcPvN;  // PV's N: the dims + the ones column (and zeros)
   static constexpr int kVTBytes = kPvN * 128;       // [V | 1]^T f16 [kPvN x 64 keys]
-  static constexpr int kStages = NG == 1 ? 4 : 6;
+  static constexpr int kStages = 6;
   static constexpr int kMmaWarp = 4 * kGroups;
   // gather warps: TMA issues from one warp are serialised, so each producer
   // warp issues its share of a tile's boxes (a third or fourth warp gathered
   // no faster, and a fourth held back the CTAs of the neighbouring kernels)
   static constexpr int kProducers = 2;
   static constexpr int kThreads = (kMmaWarp + 1 + kProducers) * 32;
-  static constexpr int kMinBlocks = NG == 1 ? 2 : 0;  // __launch_bounds__ minimum (0: none; with 1 the
-                                                      // compiler takes 131 registers instead of 111)
-  // Q, the QK's A operand: in TMEM with two groups (the 32 columns the other
-  // operands leave free: the QK reads only K from shared memory), else in
-  // shared memory
-  static constexpr bool kQTmem = NG != 1;
-  // shared memory
-  static constexpr int kQ = 0;                                            // Q E4M3 [128 x 128 B] (not kQTmem)
-  static constexpr int kK = kQ + (kQTmem ? 0 : kTcRows * 128);            // K E4M3 [stage][64 x 128 B]
+  // shared memory (Q, the QK's A operand, is in TMEM: the QK reads only K
+  // from shared memory)
+  static constexpr int kK = 0;                                            // K E4M3 [stage][64 x 128 B]
   static constexpr int kV = kK + kStages * kTcTileKeys * 128;             // V E4M3 [stage][64 x 144 B]
   static constexpr int kVT = kV + kStages * kTcTileKeys * kTcVPitch;      // [V | 1]^T f16 [group][kPvN x 64 keys]
   static constexpr int kX = kVT + kGroups * kVTBytes;                     // each group's reference max per row
@@ -136,32 +140,25 @@ struct TcCfg {
   // TMEM columns. NG = 2: S_j at 64 j (64), O_j at 128 + 160 j (144), P_j (f16,
   // two per 32-bit column: the PV's A operand read from TMEM) at 432 + 32 j.
   // NG = 3: S_j at 64 j, O_j at 128 + 80 j (80), P_j at 288 + 32 j.
-  // NG = 1: S at 0, P at 64, O at 96.
-  static constexpr uint32_t kCols = NG == 1 ? 256 : 512;
+  static constexpr uint32_t kCols = 512;
   __host__ __device__ static constexpr uint32_t col_s(int j) { return 64u * j; }
-  __host__ __device__ static constexpr uint32_t col_o(int j) {
-    return NG == 2 ? 128u + 160u * j : NG == 3 ? 128u + 80u * j : 96u;
-  }
-  __host__ __device__ static constexpr uint32_t col_p(int j) {
-    return NG == 2 ? 432u + 32u * j : NG == 3 ? 288u + 32u * j : 64u;
-  }
-  // kQTmem: Q's K bytes [32 kk, 32 kk + 32) (4 per column) at col_q(kk). NG = 2:
+  __host__ __device__ static constexpr uint32_t col_o(int j) { return NG == 2 ? 128u + 160u * j : 128u + 80u * j; }
+  __host__ __device__ static constexpr uint32_t col_p(int j) { return NG == 2 ? 432u + 32u * j : 288u + 32u * j; }
+  // Q's K bytes [32 kk, 32 kk + 32) (4 per column) at col_q(kk). NG = 2:
   // the columns between O_0 and O_1 and after P_1; NG = 3: after P_1, group j's
   // 64 bytes (its KV head's dims) as kk = 2 j, 2 j + 1
   __host__ __device__ static constexpr uint32_t col_q(int kk) {
     return NG == 3 ? 352u + 8u * kk : kk < 2 ? 272u + 8u * kk : 496u + 8u * (kk - 2);
   }
-  static_assert(kQ % 1024 == 0 && kK % 1024 == 0 && kV % 1024 == 0 && kVT % 1024 == 0, "operand alignment");
+  static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kVT % 1024 == 0, "operand alignment");
 };
 static_assert(TcCfg<2>::col_o(1) + kTcPvN <= TcCfg<2>::col_p(0) && TcCfg<2>::col_p(1) + 32 <= TcCfg<2>::col_q(2) &&
                   TcCfg<2>::col_o(0) + kTcPvN <= TcCfg<2>::col_q(0) && TcCfg<2>::col_q(1) + 8 <= TcCfg<2>::col_o(1) &&
                   TcCfg<2>::col_q(3) + 8 <= 512,
               "TMEM columns");
-static_assert(TcCfg<1>::col_p(0) + 32 <= TcCfg<1>::col_o(0) && TcCfg<1>::col_o(0) + kTcPvN <= 256, "TMEM columns");
 static_assert(TcCfg<3>::col_s(1) + 64 <= TcCfg<3>::col_o(0) && TcCfg<3>::col_o(1) + TcCfg<3>::kPvN <= TcCfg<3>::col_p(0) &&
                   TcCfg<3>::col_p(1) + 32 <= TcCfg<3>::col_q(0) && TcCfg<3>::col_q(3) + 8 <= 512,
               "TMEM columns");
-static_assert(2 * TcCfg<1>::kSmem <= 227 * 1024, "two CTAs per SM");
 
 // Byte offset of (row r, byte kb) in a canonical tile of 128-byte rows.
 __device__ __forceinline__ uint32_t canon(int r, int kb) {
@@ -193,7 +190,7 @@ struct TcMaps {
 // before (zeros at the start, else keys of earlier tiles). Otherwise tiles
 // arrive by 16-byte cp.async per row chunk (any page size).
 template <bool kTma, int NG, bool FUSED>
-__global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
+__global__ void __launch_bounds__(TcCfg<NG>::kThreads)
     decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ TcMaps maps) {
   using C = TcCfg<NG>;
   static_assert(!FUSED || NG == 2, "the one-kernel step runs blocks of at most 8 tokens with two softmax groups");
@@ -202,7 +199,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   constexpr int kStep = C::kStep, kShift = C::kShift;
   constexpr int kTcProducers = C::kProducers;
   constexpr int kGroupsPW = 8 / kTcProducers;  // TMA: 8-row groups of a tile per producer warp
-  constexpr int kTcQ = C::kQ, kTcK = C::kK, kTcV = C::kV, kTcVT = C::kVT, kTcX = C::kX, kTcBar = C::kBar;
+  constexpr int kTcK = C::kK, kTcV = C::kV, kTcVT = C::kVT, kTcX = C::kX, kTcBar = C::kBar;
   constexpr int kTcTmemSlot = C::kTmemSlot;
   constexpr uint32_t kTcCols = C::kCols;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -582,10 +579,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         for (int kk = 0; kk < 4; kk++) {  // 128 bytes of K: 32 per instruction (two core matrices)
           const uint64_t kdesc =
               kTma ? umma_desc_sw128(kt + kk * 32, kTcSbo) : umma_desc(kt + kk * 2 * kTcLbo, kTcLbo, kTcSbo);
-          if constexpr (C::kQTmem)
-            umma_f8_ta(tmem + C::col_s(j), tmem + C::col_q(kk), kdesc, id_qk, kk > 0);
-          else
-            umma_f8(tmem + C::col_s(j), umma_desc(sb + kTcQ + kk * 2 * kTcLbo, kTcLbo, kTcSbo), kdesc, id_qk, kk > 0);
+          umma_f8_ta(tmem + C::col_s(j), tmem + C::col_q(kk), kdesc, id_qk, kk > 0);
         }
         umma_commit(s_ready(j));
         return true;
@@ -661,12 +655,12 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   pdl_launch_dependents();
   bool q_pos_err = false;
   {
-    // Q row r: the 64 E4M3 dims of (token ti, head) at K bytes [64g, 64g+64),
-    // zeros elsewhere; group jw writes chunks [8 jw / NG, 8 (jw + 1) / NG) of the row
+    // Q row r: the 64 E4M3 dims of (token ti, head). Form 2: at K bytes
+    // [64g, 64g+64), zeros elsewhere; group jw writes K bytes [64 jw, 64 jw +
+    // 64), 16 TMEM columns from col_q(2 jw). Form 3: the group's 64 K bytes.
     const uint4* src = reinterpret_cast<const uint4*>(
         a.q8 + ((int64_t)(qb + wk.i0 + (live ? ti : 0)) * kNumQHeads + head) * kHeadDim);
-    if constexpr (C::kQTmem) {
-      // group jw: K bytes [64 jw, 64 jw + 64), 16 TMEM columns from col_q(2 jw)
+    {
       float qv[16];
       if constexpr (FUSED) {  // the row from qkv (steps 1-3 of the block), by the group of its KV head
         uint32_t qw[16];
@@ -685,13 +679,6 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
         }
       }
       tmem_st16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::col_q(2 * jw), qv);
-    } else {
-#pragma unroll
-      for (int c = 8 * jw / NG; c < 8 * (jw + 1) / NG; c++) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (live && (c >> 2) == g) v = src[c & 3];
-        *reinterpret_cast<uint4*>(smem + kTcQ + canon(r, c * 16)) = v;
-      }
     }
   }
   {
@@ -705,7 +692,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads, TcCfg<NG>::kMinBlocks)
   }
   if (__any_sync(0xffffffffu, q_pos_err) && lane == 0) set_error(a.err, OKC_DEVERR_POSITION);
   fence_proxy_async();  // shared-memory operands, for the MMAs
-  tc_fence_before();    // Q's TMEM stores (kQTmem), before the MMA thread reads them
+  tc_fence_before();    // Q's TMEM stores, before the MMA thread reads them
   named_bar_sync(1, (kTcMmaWarp + 1) * 32);
 
   const float scale_log2 = a.scaled ? a.scale_log2 * __ldg(a.k_scale) : a.scale_log2;
@@ -993,7 +980,6 @@ cudaError_t launch_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (num_work == 0) return cudaSuccess;
   if (a.S < 1 || a.S > (a.tc_groups == 3 ? 16 : 8)) return cudaErrorInvalidValue;
-  if (a.tc_groups == 1) return launch_tc<1, false>(a, num_work, pdl, s);
   if (a.tc_groups == 2) return launch_tc<2, false>(a, num_work, pdl, s);
   if (a.tc_groups == 3) return launch_tc<3, false>(a, num_work, pdl, s);
   return cudaErrorInvalidValue;
@@ -1015,7 +1001,6 @@ int tc_ctas_per_sm() {
     auto kern = v == 0 ? decode_tc_kernel<false, NG, false> : v == 1 ? decode_tc_kernel<true, NG, false>
               : v == 2 ? decode_tc_kernel<false, NG, NG == 2> : decode_tc_kernel<true, NG, NG == 2>;
     int nb = 0;
-    // (the largest shared-memory carveout: two one-group CTAs need ~210 KB per SM)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
             cudaSuccess ||
@@ -1023,17 +1008,11 @@ int tc_ctas_per_sm() {
       return 0;
     lowest = v ? std::min(lowest, nb) : nb;
   }
-  // The occupancy calculator reports one CTA per SM for the one-group kernel,
-  // yet two fit (2 x 28,672 registers of 65,536; 2 x ~106 KB of 228 KB of shared
-  // memory; 2 x 256 of the 512 TMEM columns), and a timeline of a launch shows
-  // two CTAs running on one SM at once: its residency is two.
-  if (NG == 1 && lowest == 1) lowest = 2;
   return lowest;
 }
 
 int decode_tc_ctas_per_sm(int tc_groups) {
-  return tc_groups == 1 ? tc_ctas_per_sm<1>() : tc_groups == 2 ? tc_ctas_per_sm<2>()
-       : tc_groups == 3 ? tc_ctas_per_sm<3>() : 0;
+  return tc_groups == 2 ? tc_ctas_per_sm<2>() : tc_groups == 3 ? tc_ctas_per_sm<3>() : 0;
 }
 
 }  // namespace okc

@@ -172,9 +172,7 @@ inline bool uses_tc(const okc_attn_config& c, const okc_plan_options* o) {
 // M = 128 rows) for steps of at most 8 tokens per request (decode, verify: few
 // blocks, many splits, where fewer, longer splits merge faster), 3 (one
 // warpgroup per KV head, blocks of 16 tokens: each group's M = 128 rows are 16
-// tokens x its 8 heads, half the tensor work per row) for longer extends. (Form
-// 1, one warpgroup on blocks of 8 tokens at two CTAs per SM, is kept in the
-// kernel, not chosen.)
+// tokens x its 8 heads, half the tensor work per row) for longer extends.
 inline int tc_groups(const okc_attn_config& c) { return c.q_len > 8 ? 3 : 2; }
 // Tokens per query block: 1 for q_len 1, 8 on the tcgen05 kernel's form 2,
 // 16 on its form 3 and on the warp-level kernel; q_len itself when smaller.

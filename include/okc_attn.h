@@ -342,7 +342,8 @@ okc_status okc_prepare_qkv(okc_attn_plan_t plan, const void* qkv, const int64_t*
  * decode and verify steps; S consecutive tokens of a longer one) for all its
  * query rows and both KV heads, and writes a normalized f32 partial output
  * (already times v_scale) and its base-2 log-sum-exp. q_len >= 2 runs on the
- * tcgen05 kernel (blocks of up to 8 tokens: M = 128 query rows, accumulators in
+ * tcgen05 kernel (blocks of up to 8 tokens as M = 128 query rows, or past q_len 8
+ * blocks of up to 16 tokens with M = 128 rows per KV head; accumulators in
  * tensor memory; on pages of 8 or more rows its K/V tiles arrive by TMA through
  * tensor maps the call encodes for k_cache and v_cache, so page_size *
  * num_pages rows must be addressable from both base pointers) unless the plan

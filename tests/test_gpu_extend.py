@@ -2,7 +2,8 @@
 file's ragged cu_seqlens_q with its max_seqlen_q) on the same paged FP8 cache.
 Batches mix decode requests (1 token), extends of 37, 256 and 1024 tokens and
 requests with no new token, at window 2048 and 0, on 1-, 16- and 64-row pages;
-through the three calls (the tcgen05 decode on blocks of 8 tokens), through
+through the three calls (the tcgen05 decode on blocks of 16 tokens, one softmax
+warpgroup per KV head), through
 okc_attn_step, on the warp-level kernel (blocks of 16 tokens) and with forced
 split sizes; against the oracle on sampled query rows (every request's first
 and last token always in the sample). Uniform q lengths past 8 (several query
@@ -57,7 +58,7 @@ def test_ragged_extend_batches(q_lens, seq, window, P, rope, kvs):
     cfg = _extend_cfg(q_lens, seq, window, P, rope, kvs)
     inp = W.generate(cfg)
     mask = _rows_mask(inp, 0.2, seed=len(q_lens))
-    rep = full_check(cfg, inp, rows_mask=mask)  # three calls, tcgen05 decode, blocks of 8
+    rep = full_check(cfg, inp, rows_mask=mask)  # three calls, tcgen05 decode, blocks of 16
     assert rep["q8"]["match"] == 1.0
     full_check(cfg, inp, rows_mask=mask, fused=True, plan_form=True)  # okc_attn_step
     full_check(cfg, inp, rows_mask=mask, opts={"flags": okc.PLAN_NO_TCGEN05})  # warp-level MMA, blocks of 16

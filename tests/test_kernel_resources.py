@@ -4,8 +4,9 @@ kernels for q_len 1 at 80 registers x 256 threads: three CTAs per SM; the
 two-group tcgen05 decode (verify blocks) at 120 x 352 as allocated: one CTA per
 SM with room for a prepare and two combine CTAs beside it; its one-kernel step
 form, which also derives q and the new rows, within one CTA per SM (at most
-136 registers on TMA-fed tiles, 184 on cp.async-fed ones); the one-group tcgen05 decode
-(extends) at 128 x 224: two CTAs per SM; the combine for blocks of several
+136 registers on TMA-fed tiles, 184 on cp.async-fed ones); the per-KV-head
+tcgen05 decode (extends) at 120 x 352: one CTA per SM with room for two combine
+CTAs beside it; the combine for blocks of several
 tokens under 64 x 128, so that two of its CTAs fit beside a tcgen05 decode CTA)
 and spill nothing beyond the fused step's known 16-byte frame."""
 import os
@@ -26,8 +27,8 @@ LIMITS = {
     "decode_tc_kernelILb0ELi2ELb0E": (120, 0),    # verify block on pages of < 8 rows, cp.async gather (allocated as 120)
     "decode_tc_kernelILb1ELi2ELb1E": (136, 0),    # the verify block's one-kernel step, TMA gather
     "decode_tc_kernelILb0ELi2ELb1E": (184, 0),    # the same on pages of < 8 rows (one CTA per SM: 184 x 352 fits)
-    "decode_tc_kernelILb1ELi1ELb0E": (128, 0),    # extend, TMA gather
-    "decode_tc_kernelILb0ELi1ELb0E": (128, 0),    # extend, cp.async gather
+    "decode_tc_kernelILb1ELi3ELb0E": (120, 0),    # extend (one group per KV head), TMA gather
+    "decode_tc_kernelILb0ELi3ELb0E": (120, 0),    # extend, cp.async gather
     "prepare_kernel": (64, 0),
     "combine_kernel": (128, 0),
     "combine_kernelILi4E": (64, 0),               # verify and extend steps (4 splits per round trip)
