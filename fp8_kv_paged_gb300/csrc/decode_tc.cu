@@ -706,9 +706,37 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
   float m = -INFINITY;  // reference max (log2 units)
   bool ok = true;
   int last = -1;  // this group's last tile
+  // this row's valid keys [row_lo, row_hi): the chunk's range, the window and
+  // causality (empty for a dead row)
+  const int row_lo = live ? max(j0, a.window > 0 ? pos - a.window + 1 : 0) : 0;
+  const int row_hi = live ? min(j1, pos + 1) : 0;
+  // The V conversion's shared-memory addresses, the same for every tile but
+  // the stage's base: warp w of the group converts key groups 2w, 2w+1 (8 keys
+  // each) x 8 groups of 16 dims (form 3: the 4 groups of its KV head's dims),
+  // kIts ldmatrix.x4 loads and 2 kIts stmatrix.trans stores.
+  constexpr int kIts = kPH ? 2 : 4;
+  uint32_t v_ld[kIts], v_st[kIts][2];
+#pragma unroll
+  for (int it = 0; it < kIts; it++) {
+    const int a8 = 2 * (warp & 3) + (kPH ? it : it >> 1);  // key group
+    const int cbase = kPH ? 4 * jw : (it & 1) * 4;          // first 16-dim group of this x4
+    // matrix mi = lane >> 3: keys a8*8 + (lane & 7), bytes 16 (cbase + mi) .. +15
+    // (TMA: 8-row groups 1024 bytes apart, chunks XORed with the row mod 8)
+    v_ld[it] = kTma ? a8 * 1024 + (lane & 7) * 128 + (((cbase + (lane >> 3)) ^ (lane & 7)) * 16)
+                    : (a8 * 8 + (lane & 7)) * kTcVPitch + (cbase + (lane >> 3)) * 16;
+    // stored matrix jm (lanes 8jm..8jm+7 give its rows): {lo, hi} of block 2*half + (jm >> 1);
+    // its row cc holds dim 16 c16 + 4 (cc >> 1) + 2 (jm & 1) + (cc & 1) for the 8 keys,
+    // stored at row vt_pos(dim) = 16 c16 + 8 (jm & 1) + cc
+    const int jm = lane >> 3, cc = lane & 7;
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      const int c16 = cbase + half * 2 + (jm >> 1) - (kPH ? 4 * jw : 0);  // (of the group's dims)
+      v_st[it][half] = sb + sVT + canon(16 * c16 + 8 * (jm & 1) + cc, a8 * 16);
+    }
+  }
+  int s = kPH ? 0 : jw, sph = 0;  // tile k's stage and the phase bit of its fill
   for (int k = kPH ? 0 : jw; k < ntiles; k += kStep) {
-    const int s = k % kTcStages;
-    const bool w = mbar_wait(s_ready(jw), (k >> kShift) & 1) && mbar_wait(full_bar(s), (k / kTcStages) & 1);
+    const bool w = mbar_wait(s_ready(jw), (k >> kShift) & 1) && mbar_wait(full_bar(s), sph);
     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
     tc_fence_after();
     const int tile_j = jt + k * kTcTileKeys;
@@ -719,12 +747,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
     mbar_arrive(s_free(jw));  // S of this tile is in registers: the next QK may overwrite it
     // ---- mask: this row's valid keys of the tile are [klo, khi) (window,
     // causal, chunk end; none for a dead row); row max on the raw scores
-    int klo = 0, khi = 0;
-    if (live) {
-      klo = max(j0 - tile_j, a.window > 0 ? pos - a.window + 1 - tile_j : 0);
-      klo = max(0, klo);
-      khi = min(kTcTileKeys, min(j1, pos + 1) - tile_j);
-    }
+    const int klo = max(0, row_lo - tile_j), khi = min(kTcTileKeys, row_hi - tile_j);
     const uint32_t kn = khi > klo ? (uint32_t)(khi - klo) : 0u;
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (__all_sync(0xffffffffu, klo == 0 && khi == kTcTileKeys)) {  // every key valid for the warp's rows
@@ -773,23 +796,13 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
     // ---- P into this group's TMEM P columns (the PV's A operand)
     tmem_st32u(tP, pw);
     // ---- V tile E4M3 -> f16, transposed into this group's canonical B tile
-    // (dims x keys). Warp w of the group converts key groups 2w, 2w+1 (8 keys
-    // each) x 8 groups of 16 dims (form 3: the 4 groups of its KV head's dims).
+    // (dims x keys; the addresses above)
     {
-      const int wg = warp & 3;
       const uint32_t vs = sb + kTcV + s * (kTcTileKeys * kTcVPitch);
-      constexpr int kIts = kPH ? 2 : 4;
-#pragma unroll 1
+#pragma unroll
       for (int it = 0; it < kIts; it++) {
-        const int a8 = 2 * wg + (kPH ? it : it >> 1);  // key group
-        const int cbase = kPH ? 4 * jw : (it & 1) * 4;   // first 16-dim group of this x4
         uint32_t rg[4];
-        // matrix mi = lane >> 3: keys a8*8 + (lane & 7), bytes 16 (cbase + mi) .. +15
-        // (TMA: 8-row groups 1024 bytes apart, chunks XORed with the row mod 8)
-        if constexpr (kTma)
-          ldsm_x4(rg, vs + a8 * 1024 + (lane & 7) * 128 + (((cbase + (lane >> 3)) ^ (lane & 7)) * 16));
-        else
-          ldsm_x4(rg, vs + (a8 * 8 + (lane & 7)) * kTcVPitch + (cbase + (lane >> 3)) * 16);
+        ldsm_x4(rg, vs + v_ld[it]);
         // rg[mi]: key a8*8 + lane/4, dims 16 (cbase+mi) + 4 (lane%4) + {0,1,2,3}
         uint32_t lo4[4], hi4[4];
 #pragma unroll
@@ -797,23 +810,20 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
           lo4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] & 0xFFFFu));  // dims +0, +1
           hi4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] >> 16));      // dims +2, +3
         }
-        // stored matrix jm (lanes 8jm..8jm+7 give its rows): {lo, hi} of block 2*half + (jm >> 1);
-        // its row cc holds dim 16 c16 + 4 (cc >> 1) + 2 (jm & 1) + (cc & 1) for the 8 keys,
-        // stored at row vt_pos(dim) = 16 c16 + 8 (jm & 1) + cc
-        const int jm = lane >> 3, cc = lane & 7;
 #pragma unroll
-        for (int half = 0; half < 2; half++) {
-          const int c16 = cbase + half * 2 + (jm >> 1) - (kPH ? 4 * jw : 0);  // (of the group's dims)
-          const int pr = 16 * c16 + 8 * (jm & 1) + cc;
-          stsm_x4_trans(sb + sVT + canon(pr, a8 * 16), lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1],
-                        hi4[half * 2 + 1]);
-        }
+        for (int half = 0; half < 2; half++)
+          stsm_x4_trans(v_st[it][half], lo4[half * 2], hi4[half * 2], lo4[half * 2 + 1], hi4[half * 2 + 1]);
       }
     }
     fence_proxy_async();  // V^T, written through the generic proxy, for the MMA
     tc_fence_before();
     mbar_arrive(p_ready(jw));
     last = k;
+    s += kStep;  // the next tile's stage
+    if (s >= kTcStages) {
+      s -= kTcStages;
+      sph ^= 1;
+    }
   }
   // this group's O is complete once its last PV has
   if (ok && last >= 0) {
