@@ -774,7 +774,9 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
 #pragma unroll
     for (int c = 0; c < 32; c++) {
       const float x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32], x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-      pw[c] = pack_half2(fast_exp2(__fmaf_rn(x0, scale_log2, -m_use)), fast_exp2(__fmaf_rn(x1, scale_log2, -m_use)));
+      float e0, e1;
+      ffma2(x0, x1, scale_log2, -m_use, e0, e1);  // (two keys' s * scale - m per instruction)
+      pw[c] = pack_half2(fast_exp2(e0), fast_exp2(e1));
     }
     // ---- P, V^T and O of this group are free once its previous PV completed
     if (k >= kStep) {
@@ -788,7 +790,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
       for (int h4 = 0; h4 < 4; h4++) {  // (the stores complete at the sum's store below)
         tmem_ld16(tO + 16 * h4, ov);
 #pragma unroll
-        for (int d = 0; d < 16; d++) ov[d] *= alpha;
+        for (int d = 0; d < 16; d += 2) fmul2(ov[d], ov[d + 1], alpha, ov[d], ov[d + 1]);
         tmem_st16_async(tO + 16 * h4, ov);
       }
       tmem_st1(tL, tmem_ld1(tL) * alpha);

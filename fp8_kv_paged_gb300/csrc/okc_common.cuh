@@ -364,6 +364,21 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// Two float32 FMAs or products in one instruction (the f32x2 forms, sm_100
+// and later): (a0, a1) * b + c and (a0, a1) * b, each lane rounded once to
+// nearest, as __fmaf_rn and __fmul_rn.
+__device__ __forceinline__ void ffma2(float a0, float a1, float b, float c, float& y0, float& y1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mov.b64 rc, {%5, %5};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fmul2(float a0, float a1, float b, float& y0, float& y1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b));
+}
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
