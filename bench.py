@@ -63,8 +63,8 @@ NCU_TRAFFIC = {
     ("mixed_full_decode", "decode_kernel<fused step>"): 803951360 + 7561472,
     ("sliding_decode", "decode_kernel<fused step>"): 33093888 + 2304,
     ("full_decode_32k", "decode_kernel"): 545479168 + 3285248,
-    ("verify_block", "decode_tc_kernel"): 17210624 + 0,
-    ("extend", "decode_tc_kernel"): 36385536 + 496384,
+    ("verify_block", "decode_tc_kernel"): 17209856 + 0,
+    ("extend", "decode_tc_kernel"): 36384000 + 482560,
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0
