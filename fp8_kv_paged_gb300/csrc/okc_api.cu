@@ -290,7 +290,7 @@ okc_status okc::make_splits(const okc_attn_config* c, const int32_t* seq, const 
       if (C == min_chunk) break;  // smaller items are not allowed
     }
   }
-  // blocks of 2..8 tokens decode on the tcgen05 kernel, fed by TMA on pages of 8+ rows
+  // blocks of 2..16 tokens decode on the tcgen05 kernel, fed by TMA on pages of 8+ rows
   const bool tc_tma = okc::uses_tc(*c, o) && c->page_size >= 8;
   const int64_t tma_pad = tc_tma ? 7 : 0;
   r->blocks.assign((size_t)U, BlockInfo{0, 0, 0, 0});

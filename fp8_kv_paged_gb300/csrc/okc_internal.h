@@ -97,8 +97,8 @@ struct DecodeArgs {
   const uint16_t* weight;   // norm-gate weight bf16 [64] or null
   uint16_t* out;            // bf16 [T, Hq*64]
   float eps;
-  int32_t tc;               // 1: blocks of 2..8 tokens run on the tcgen05 kernel (decode_tc.cu)
-  int32_t tc_groups;        // its softmax warpgroups per CTA (tc_groups)
+  int32_t tc;               // 1: blocks of 2..16 tokens run on the tcgen05 kernel (decode_tc.cu)
+  int32_t tc_groups;        // its form (tc_groups: 2, or 3 for one softmax warpgroup per KV head)
   int32_t q_fold;           // as PrepareArgs (the fused step derives q itself)
   float q_scale;
   int32_t early;            // OKC_PLAN_EARLY_GATHER: the fused step loads lengths, page ids and
@@ -145,7 +145,7 @@ struct okc_attn_plan_s {
   okc::BlockInfo* d_blk;
   int32_t* d_tickets;  // the fused step's per-request arrival counters
   uint8_t* d_q8;       // q of okc_attn_step when it runs the three kernels
-  bool tc;             // decode on the tcgen05 kernel (blocks of 2..8 tokens)
+  bool tc;             // decode on the tcgen05 kernel (q_len >= 2: blocks of 2..16 tokens)
   int device;
   int sm_count;
   bool pdl;
@@ -227,8 +227,8 @@ int decode_ctas_per_sm(int S, bool tc, int tc_groups);
 // tc_groups) and cached (the query also raises the kernels' shared-memory limit
 // on the device).
 int cached_ctas_per_sm(int dev, int S, bool tc, int tc_groups);
-// The tcgen05 decode kernel for blocks of 2..8 tokens (decode_tc.cu), with
-// a.tc_groups softmax warpgroups per CTA.
+// The tcgen05 decode kernel for blocks of 2..16 tokens (decode_tc.cu) in form
+// a.tc_groups.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s);
 // The whole step in one launch for blocks of 2..8 tokens on the tcgen05 kernel
 // (q and the new K/V rows from qkv, attention, last-CTA merge and norm-gate);
