@@ -482,8 +482,15 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const uint32_t pr = __byte_perm(r[i], 0u, 0x3120);
-            ax[i] = e4m3x2_to_f16x2((uint16_t)(pr & 0xFFFFu));
-            ay[i] = e4m3x2_to_f16x2((uint16_t)(pr >> 16));
+            // (the same exact conversions; the fused step keeps the per-pair
+            // form, with which the mixed batch ran 2 % faster and the sliding
+            // batch 7 % slower than with the four-code form)
+            if constexpr (FUSED) {
+              ax[i] = e4m3x2_to_f16x2((uint16_t)(pr & 0xFFFFu));
+              ay[i] = e4m3x2_to_f16x2((uint16_t)(pr >> 16));
+            } else {
+              e4m3x4_to_f16x2x2(pr, ax[i], ay[i]);
+            }
           }
 #pragma unroll
           for (int nt = 0; nt < NTW; nt++) {

@@ -809,8 +809,7 @@ __global__ void __launch_bounds__(TcCfg<NG>::kThreads)
         uint32_t lo4[4], hi4[4];
 #pragma unroll
         for (int mi = 0; mi < 4; mi++) {
-          lo4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] & 0xFFFFu));  // dims +0, +1
-          hi4[mi] = e4m3x2_to_f16x2((uint16_t)(rg[mi] >> 16));      // dims +2, +3
+          e4m3x4_to_f16x2x2(rg[mi], lo4[mi], hi4[mi]);  // dims +0, +1 and +2, +3
         }
 #pragma unroll
         for (int half = 0; half < 2; half++)

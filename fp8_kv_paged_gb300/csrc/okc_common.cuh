@@ -342,6 +342,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
+// Four E4M3 codes (v, code i in byte i) -> two f16 pairs: lo holds codes 0, 1,
+// hi codes 2, 3 (the lower code in the lower half), exact; one cvt per pair
+// straight from the halves of v.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
 // Two floats -> two E4M3 codes, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return static_cast<uint16_t>(
