@@ -50,9 +50,11 @@
 // steps 1-3 (q from qkv in the consumers' fragment layout; the new token's K/V
 // row computed by the warp that owns its tile row and written to the cache)
 // and step 5 (the last CTA of each request merges the splits).
+#include <algorithm>
+
+#include "fused_rows.cuh"
 #include "normgate.cuh"
 #include "okc_common.cuh"
-#include "fused_rows.cuh"
 #include "okc_internal.h"
 
 namespace okc {
@@ -143,7 +145,10 @@ struct DecodeCfg {
 
 // FUSED false: the decode kernel of the three-call path (q from q_fp8, partials
 // out); true: the whole step (okc_attn_step), last-CTA merge through tickets.
-template <int KS, int NTW, int NCW, bool FUSED>
+// QCVT: the V conversion's form, four E4M3 codes per pair of cvt instructions
+// straight from the register halves, or the per-pair form (the same exact
+// values; which runs faster depends on the step, see launch_step_fused).
+template <int KS, int NTW, int NCW, bool FUSED, bool QCVT = !FUSED>
 __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_MINBLOCKS_L1 : 1)
     decode_kernel(DecodeArgs a) {
   using C = DecodeCfg<KS, NTW, NCW>;
@@ -482,14 +487,11 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const uint32_t pr = __byte_perm(r[i], 0u, 0x3120);
-            // (the same exact conversions; the fused step keeps the per-pair
-            // form, with which the mixed batch ran 2 % faster and the sliding
-            // batch 7 % slower than with the four-code form)
-            if constexpr (FUSED) {
+            if constexpr (QCVT) {
+              e4m3x4_to_f16x2x2(pr, ax[i], ay[i]);
+            } else {
               ax[i] = e4m3x2_to_f16x2((uint16_t)(pr & 0xFFFFu));
               ay[i] = e4m3x2_to_f16x2((uint16_t)(pr >> 16));
-            } else {
-              e4m3x4_to_f16x2x2(pr, ax[i], ay[i]);
             }
           }
 #pragma unroll
@@ -631,10 +633,10 @@ __global__ void __launch_bounds__((NCW + kProducers) * 32, KS > 1 ? OKC_DECODE_M
   }
 }
 
-template <int KS, int NTW, int NCW, bool FUSED>
+template <int KS, int NTW, int NCW, bool FUSED, bool QCVT = !FUSED>
 cudaError_t launch_variant(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   // the dynamic shared-memory limit was raised when the plan was made (occupancy query)
-  auto kern = decode_kernel<KS, NTW, NCW, FUSED>;
+  auto kern = decode_kernel<KS, NTW, NCW, FUSED, QCVT>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_work);
   cfg.blockDim = dim3((NCW + kProducers) * 32);
@@ -648,10 +650,10 @@ cudaError_t launch_variant(const DecodeArgs& a, int num_work, bool pdl, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int KS, int NTW, int NCW, bool FUSED>
+template <int KS, int NTW, int NCW, bool FUSED, bool QCVT = !FUSED>
 int occupancy_variant() {
   int nb = 0;
-  auto kern = decode_kernel<KS, NTW, NCW, FUSED>;
+  auto kern = decode_kernel<KS, NTW, NCW, FUSED, QCVT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, (NCW + kProducers) * 32, kSmemBytes) != cudaSuccess)
@@ -691,18 +693,24 @@ cudaError_t launch_decode(const DecodeArgs& a, int num_work, bool pdl, cudaStrea
 // The single-launch step is built for q_len 1 only: for a verify block the
 // three kernels are faster (one CTA per SM at the fused variant's registers,
 // and every split recomputing the block's new K/V rows).
+//
+// Its V conversion: the four-code form for steps of at most one wave of items
+// (the sliding batch: 15.6 -> 14.5 us per step), the per-pair form for longer
+// ones (the mixed batch: 162.9 us with the four-code form, 159.9 us without).
 cudaError_t launch_step_fused(const DecodeArgs& a, int num_work, bool pdl, cudaStream_t s) {
   if (a.L != 1 || a.S != 1) return cudaErrorInvalidValue;
   if (num_work == 0) return cudaSuccess;
-  return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>(a, num_work, pdl, s);
+  if (a.one_wave) return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true, true>(a, num_work, pdl, s);
+  return launch_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true, false>(a, num_work, pdl, s);
 }
 
 int decode_ctas_per_sm(int S, bool tc, int tc_groups) {
   if (tc) return decode_tc_ctas_per_sm(tc_groups);
   const int a = occupancy_any(S);
   if (S != 1) return a;
-  const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true>();
-  return a < b ? a : b;
+  const int b = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true, false>();
+  const int c = occupancy_variant<OKC_DECODE_KS_L1, 1, 2 * OKC_DECODE_KS_L1, true, true>();
+  return std::min(a, std::min(b, c));
 }
 
 }  // namespace okc

@@ -1083,6 +1083,7 @@ okc_status okc_attn_step(okc_attn_plan_t plan, const void* qkv, const int64_t* p
   a.q_fold = c.q_norm == OKC_QNORM_FOLDED_SCALE;
   a.q_scale = c.qk_scale_factor;
   a.early = (plan->opts.flags & OKC_PLAN_EARLY_GATHER) && plan->pdl ? 1 : 0;
+  a.one_wave = launch_items(plan) <= plan->slots ? 1 : 0;
   cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
   if (plan->sizes.step_kernels == 1) {
     cudaError_t e;

@@ -103,6 +103,7 @@ struct DecodeArgs {
   float q_scale;
   int32_t early;            // OKC_PLAN_EARLY_GATHER: the fused step loads lengths, page ids and
                             // cached keys before the programmatic-dependency wait
+  int32_t one_wave;         // the fused q_len-1 step: at most one wave of work items
 };
 
 struct CombineArgs {
