@@ -60,11 +60,11 @@ METRIC = "decode tokens/s and KV-stream HBM GB/s (fraction of GB300 peak) per st
 # capture of that kernel on that workload (dram__bytes_read.sum +
 # dram__bytes_write.sum); a kernel changed since its capture has no entry.
 NCU_TRAFFIC = {
-    ("mixed_full_decode", "decode_kernel<fused step>"): 803951360 + 7561472,
+    ("mixed_full_decode", "decode_kernel<fused step>"): 804015616 + 7570688,
     ("sliding_decode", "decode_kernel<fused step>"): 33093888 + 2304,
-    ("full_decode_32k", "decode_kernel"): 545479168 + 3285248,
-    ("verify_block", "decode_tc_kernel"): 17209856 + 0,
-    ("extend", "decode_tc_kernel"): 36384000 + 482560,
+    ("full_decode_32k", "decode_kernel"): 545539072 + 2930688,
+    ("verify_block", "decode_tc_kernel"): 17208832 + 0,
+    ("extend", "decode_tc_kernel"): 36384768 + 247296,
 }
 WORKLOAD = "mixed_full_decode"
 FALLBACK_HBM_GBS = 6800.0
